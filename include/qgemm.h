@@ -1,0 +1,159 @@
+/*
+ * qgemm.h -- C ABI of the B300 (sm_103a) quantized decode GEMM library.
+ *
+ * Computes the quantized linear layer
+ *     Y[M,N] = bf16( dequant( A_q[M,K] . W_q[N,K]^T ) )
+ * at decode token counts (M = 1..32, larger M also accepted) in the three
+ * formats of "Building a High-Performance and Portable vLLM Linear Backend
+ * with Helion" (discuss.pytorch.kr / PyTorch blog), section "Helion Linear
+ * Backend > Scope":
+ *   QG_FP8_DYNAMIC  E4M3 activations with one dynamic scale per token (row),
+ *                   E4M3 weights with one scale per output channel;
+ *   QG_W8A8_INT8    the same with symmetric int8 and an int32 accumulator;
+ *   QG_BLOCK_FP8    E4M3 with one activation scale per 1x128 group and one
+ *                   weight scale per 128x128 block;
+ * with the Standard, Split-K and Swap-AB algorithm variants of its section
+ * "Kernel Implementation", chosen per shape from a tuned table (sections
+ * "Per-shape Config Tuning" and "Hybrid Dispatch").
+ *
+ * Numerics (the page states no formulas; these are this library's readings):
+ *   scale s = amax / 448 (E4M3) or amax / 127 (int8) in IEEE fp32, s = 1 for
+ *   an all-zero row, group or block; q = round-to-nearest-even(x / s) with
+ *   one IEEE fp32 division, saturated to +-448 / [-127, 127];
+ *   FP8_Dynamic / INT8:  Y = bf16_rn((float(acc) * s_a[m]) * s_w[n]);
+ *   Block_FP8:           Y = bf16_rn(sum_kb s_a[m,kb] * s_w[n/128,kb] * acc_kb).
+ *
+ * Conventions for every entry point:
+ *   - returns a qg_status (0 = QG_OK); no exception crosses the ABI and
+ *     nothing aborts; on error qg_last_error() describes the failure;
+ *   - pointers named *_dev are device pointers owned by the caller; the
+ *     library never allocates, frees or synchronizes on the call path and
+ *     only enqueues kernels on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream), so the calls can be captured in a CUDA graph;
+ *   - all matrices are row-major with K contiguous; K % 16 == 0 (TMA rows
+ *     are 16-byte multiples); Block_FP8 also needs K % 128 == 0;
+ *     A_q / W_q / A / W base pointers 16-byte aligned; scales 4-byte aligned;
+ *   - kernel-side failures (a pipeline wait that exceeded its time bound) do
+ *     not trap: they set a device status word read by qg_device_error().
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { QG_FP8_DYNAMIC = 0, QG_W8A8_INT8 = 1, QG_BLOCK_FP8 = 2 } qg_format;
+
+/* Algorithm variants ("Kernel Implementation"): Standard puts tokens on the
+ * MMA M side; Swap-AB computes Y^T = W_q . A_q^T so the weight rows take the
+ * MMA M side (small M); the *_SPLITK forms also cut K into split_k ranges. */
+typedef enum { QG_STANDARD = 0, QG_SPLITK = 1, QG_SWAPAB = 2, QG_SWAPAB_SPLITK = 3 } qg_variant;
+
+typedef enum {
+  QG_OK = 0,
+  QG_ERR_INVALID_ARG = -1,        /* null pointer, bad enum, negative size ... */
+  QG_ERR_UNSUPPORTED_SHAPE = -2,  /* K % 16 (or % 128), split_k range, M too large for the variant */
+  QG_ERR_ALIGNMENT = -3,          /* a pointer or stride breaks the alignment rules above */
+  QG_ERR_WORKSPACE_TOO_SMALL = -4,
+  QG_ERR_NO_CONFIG = -5,          /* qg_select: shape absent from the table and defaults disallowed */
+  QG_ERR_CUDA = -6,               /* a CUDA runtime / driver call failed */
+  QG_ERR_DEVICE_TIMEOUT = -7,     /* reported by qg_device_error(): a kernel wait timed out */
+  QG_ERR_TABLE_PARSE = -8
+} qg_status;
+
+/* Dynamic activation quantization ("Scope": per-token for FP8_Dynamic and
+ * W8A8_INT8, 1x128 groups for Block_FP8).
+ *   A_dev    bf16 [M][lda] (lda >= K, lda % 8 == 0), read-only;
+ *   A_q_dev  [M][K] E4M3 codes (uint8) or int8, written;
+ *   s_a_dev  fp32 [M] (per token) or [M][K/128] (Block_FP8), written.
+ * M == 0 is a no-op. */
+QG_API int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_t lda, void* A_q_dev, float* s_a_dev,
+                 void* stream);
+
+/* Static weight quantization (offline setup, not on the decode path).
+ *   W_dev    fp32 [N][K], read-only;
+ *   W_q_dev  [N][K] E4M3 codes or int8, written;
+ *   s_w_dev  fp32 [N] (per output channel) or [ceil(N/128)][K/128]
+ *            (Block_FP8, 128x128 blocks; the last block row may be ragged). */
+QG_API int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q_dev, float* s_w_dev,
+                    void* stream);
+
+/* Workspace bytes qg_gemm_w8a8 needs for this shape and variant (0 when
+ * split_k == 1).  Layout: per-tile arrival counters (must be zero before the
+ * first use; the kernels leave them zero again), then the split partials. */
+QG_API size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k);
+
+/* Zero a workspace's counters (cudaMemsetAsync on `stream`). */
+QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* The quantized GEMM ("Kernel Implementation" plus the format's scaling).
+ *   A_q_dev, s_a_dev   from qg_quant_act (same fmt, M, K);
+ *   W_q_dev, s_w_dev   from qg_quant_weight (same fmt, N, K);
+ *   Y_dev              bf16 [M][ldy] (ldy >= N), fully overwritten;
+ *   variant, split_k   a qg_variant and the number of K ranges (1 ..
+ *                      ceil(K/128); must be 1 for the non-SPLITK variants);
+ *   config_id          shared-memory ring depth (0 = library default);
+ *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
+ *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
+ *                      exact integer accumulators (NULL to skip).
+ * Concurrent calls on different streams must use different workspaces. */
+QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
+                 const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
+                 int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream);
+
+/* Per-shape config lookup ("Per-shape Config Tuning"): the row of the loaded
+ * table for (fmt, N, K) and the smallest tuned token count >= M.  M larger
+ * than every tuned count ("Hybrid Dispatch": beyond the tuned range) and,
+ * when allowed, shapes missing from the table get the built-in default
+ * config.  Returns QG_ERR_NO_CONFIG for a missing shape otherwise. */
+QG_API int qg_select(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int* split_k, int* config_id);
+
+/* Load a tuned table (tab-separated "fmt N K M variant split_k config_id"
+ * rows, '#' comments), replacing the current one.  NULL reads $QG_TABLE. */
+QG_API int qg_load_table(const char* path);
+
+/* Allow (1) or forbid (0, the initial state) qg_select's built-in default
+ * config for shapes missing from the table. */
+QG_API int qg_set_allow_default(int allow);
+
+/* Launch flags: QG_LAUNCH_PDL enables programmatic dependent launch, so a
+ * GEMM starts streaming its (static) weights while the previous kernel in
+ * the stream finishes; W_q / s_w must then not be written by the kernels
+ * directly preceding the GEMM in that stream. */
+#define QG_LAUNCH_PDL 1
+QG_API int qg_set_launch_flags(int flags);
+
+/* Bound, in nanoseconds, of every pipeline wait inside the kernels (default
+ * 2e9).  0 restores the default. */
+QG_API int qg_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook: when nonzero, the next GEMM launches make their MMA thread wait
+ * on a barrier that nothing arrives on, so the bounded wait runs out and the
+ * kernel reports QG_ERR_DEVICE_TIMEOUT instead of computing. */
+QG_API int qg_set_force_timeout(int on);
+
+/* Synchronize the current device, then read and clear its status word:
+ * *code = 0 or the first qg_status a kernel reported. */
+QG_API int qg_device_error(int* code);
+
+/* Thread-local description of the last failure (never NULL). */
+QG_API const char* qg_last_error(void);
+
+/* Library version string. */
+QG_API const char* qg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

@@ -1,0 +1,502 @@
+// qgemm.cu -- C ABI of the quantized decode GEMM (see include/qgemm.h):
+// argument validation, TMA tensor-map encoding, variant dispatch, the tuned
+// config table and error reporting.  All arithmetic runs in the kernels of
+// quant.cuh, gemm_f8.cuh and gemm_i8.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/qgemm.h"
+#include "common.cuh"
+#include "gemm_f8.cuh"
+#include "gemm_i8.cuh"
+#include "quant.cuh"
+
+namespace {
+
+thread_local std::string g_err = "";
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(QG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+std::mutex g_mu;
+int g_launch_flags = 0;
+uint64_t g_wait_ns = 2000000000ull;
+int g_force_timeout = 0;
+bool g_allow_default = false;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 tensor map over rows x K bytes (row pitch `pitch` bytes), box of
+// 128 bytes x box_rows rows, 128-byte swizzle; rows past the end read zero.
+int make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int64_t pitch, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return QG_OK;
+}
+
+// -------------------------------------------------------------- launching
+struct DevInfo {
+  int sms = 0;
+  size_t smem_optin = 0;
+};
+DevInfo dev_info() {
+  static DevInfo cache[64];
+  int d = 0;
+  cudaGetDevice(&d);
+  if (d < 0 || d >= 64) d = 0;
+  if (cache[d].sms == 0) {
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, d) == cudaSuccess) {
+      cache[d].sms = p.multiProcessorCount;
+      cache[d].smem_optin = p.sharedMemPerBlockOptin;
+    } else {
+      cache[d].sms = 148;
+      cache[d].smem_optin = 232448;
+    }
+  }
+  return cache[d];
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int n = 0;
+  if (g_launch_flags & QG_LAUNCH_PDL) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+// ------------------------------------------------------------ GEMM shapes
+constexpr int kMaxStages = 16;
+
+struct Plan {
+  bool swap = false;
+  int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64
+  int n_tiles = 0, m_tiles = 0, kt = 0, splits = 1;
+};
+
+int64_t ws_counter_bytes(int64_t tiles) { return cdiv(tiles * 4, 256) * 256; }
+
+int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, Plan* p) {
+  p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK);
+  p->kt = static_cast<int>(cdiv(K, 128));
+  p->n_tiles = static_cast<int>(cdiv(N, 128));
+  if (p->swap) {
+    if (M > 64) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Swap-AB supports M <= 64 (got %lld)", (long long)M);
+    p->mpad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    p->m_tiles = 1;
+  } else {
+    p->m_tiles = static_cast<int>(cdiv(M, 128));
+    if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
+  }
+  const bool split_variant = (variant == QG_SPLITK || variant == QG_SWAPAB_SPLITK);
+  if (split_k < 1 || split_k > p->kt)
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "split_k=%d outside [1, ceil(K/128)=%d]", split_k, p->kt);
+  if (!split_variant && split_k != 1)
+    return fail(QG_ERR_INVALID_ARG, "split_k=%d needs a *_SPLITK variant", split_k);
+  if (split_k > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "split_k too large");
+  if (fmt == QG_W8A8_INT8 && !p->swap)
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "W8A8_INT8 runs the Swap-AB variants (M <= 64)");
+  p->splits = split_k;
+  return QG_OK;
+}
+
+int64_t workspace_bytes(const Plan& p, int64_t M, int64_t N) {
+  if (p.splits <= 1) return 0;
+  const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
+  return ws_counter_bytes(tiles) + static_cast<int64_t>(p.splits) * M * N * 4;
+}
+
+template <int FMT, bool SWAP, int MPAD>
+int run_f8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+           cudaStream_t stream) {
+  auto kernel = qg::gemm_f8_kernel<FMT, SWAP, MPAD>;
+  const size_t optin = dev_info().smem_optin;
+  int max_stages = kMaxStages;
+  while (max_stages > 2 && qg::gemm_f8_smem_bytes<SWAP, MPAD>(max_stages) > optin) --max_stages;
+  int stages = config_id > 0 ? config_id : max_stages;
+  if (stages > max_stages) stages = max_stages;
+  if (stages < 2) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
+  g.stages = stages;
+  const size_t smem = qg::gemm_f8_smem_bytes<SWAP, MPAD>(stages);
+  cudaError_t e = set_smem(kernel, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  dim3 grid(p.n_tiles, p.splits, SWAP ? 1 : p.m_tiles);
+  e = launch(kernel, grid, dim3(qg::kThreads), smem, stream, tmW, tmA, g);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+  return QG_OK;
+}
+
+template <bool SWAP, int MPAD>
+int run_f8_fmt(int fmt, const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g,
+               int config_id, cudaStream_t stream) {
+  if (fmt == QG_FP8_DYNAMIC) return run_f8<qg::kFmtFP8, SWAP, MPAD>(p, tmW, tmA, g, config_id, stream);
+  return run_f8<qg::kFmtBlock, SWAP, MPAD>(p, tmW, tmA, g, config_id, stream);
+}
+
+template <int MPAD>
+int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+           cudaStream_t stream) {
+  auto kernel = qg::gemm_i8_kernel<MPAD>;
+  const size_t optin = dev_info().smem_optin;
+  int max_stages = kMaxStages;
+  while (max_stages > 2 && qg::gemm_i8_smem_bytes<MPAD>(max_stages) > optin) --max_stages;
+  int stages = config_id > 0 ? config_id : max_stages;
+  if (stages > max_stages) stages = max_stages;
+  if (stages < 2) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
+  g.stages = stages;
+  const size_t smem = qg::gemm_i8_smem_bytes<MPAD>(stages);
+  cudaError_t e = set_smem(kernel, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  dim3 grid(p.n_tiles, p.splits, 1);
+  e = launch(kernel, grid, dim3(qg::kI8Threads), smem, stream, tmW, tmA, g);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+  return QG_OK;
+}
+
+// ------------------------------------------------------------------ table
+struct Key {
+  int fmt;
+  int64_t n, k;
+  int m;
+  bool operator<(const Key& o) const { return std::tie(fmt, n, k, m) < std::tie(o.fmt, o.n, o.k, o.m); }
+};
+struct Row {
+  int variant, split_k, config_id;
+};
+std::map<Key, Row> g_table;
+bool g_table_env_checked = false;
+
+// Built-in default config ("a default config for functional testing", section
+// "Toward a Practical Adoption Model"): Swap-AB for M <= 32 (M <= 64 for
+// INT8), Standard above; split K so that tiles x splits roughly fills the SMs,
+// with at least two 128-wide k-tiles per split.
+void default_config(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int* split_k, int* config_id) {
+  const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
+  const bool swap = (fmt == QG_W8A8_INT8) ? (M <= 64) : (M <= 32);
+  const int64_t tiles = cdiv(N, 128) * (swap ? 1 : cdiv(M, 128));
+  const int64_t kt = cdiv(K, 128);
+  int64_t s = sms / std::max<int64_t>(tiles, 1);
+  s = std::max<int64_t>(1, std::min<int64_t>(s, kt / 2));
+  if (s < 1) s = 1;
+  *variant = swap ? (s > 1 ? QG_SWAPAB_SPLITK : QG_SWAPAB) : (s > 1 ? QG_SPLITK : QG_STANDARD);
+  *split_k = static_cast<int>(s);
+  *config_id = 0;
+}
+
+int load_table_file(const char* path) {
+  FILE* f = fopen(path, "r");
+  if (!f) return fail(QG_ERR_TABLE_PARSE, "cannot open table '%s'", path);
+  std::map<Key, Row> t;
+  char line[512];
+  int lineno = 0;
+  while (fgets(line, sizeof(line), f)) {
+    ++lineno;
+    char* hash = strchr(line, '#');
+    if (hash) *hash = 0;
+    char* s = line;
+    while (*s == ' ' || *s == '\t' || *s == '\r' || *s == '\n') ++s;
+    if (!*s) continue;
+    int fmt, m, variant, split_k, config_id;
+    long long n, k;
+    if (sscanf(s, "%d %lld %lld %d %d %d %d", &fmt, &n, &k, &m, &variant, &split_k, &config_id) != 7 || fmt < 0 ||
+        fmt > 2 || n <= 0 || k <= 0 || m <= 0 || variant < 0 || variant > 3 || split_k < 1 || config_id < 0) {
+      fclose(f);
+      return fail(QG_ERR_TABLE_PARSE, "%s:%d: malformed row", path, lineno);
+    }
+    t[Key{fmt, n, k, m}] = Row{variant, split_k, config_id};
+  }
+  fclose(f);
+  g_table.swap(t);
+  return QG_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+extern "C" {
+
+const char* qg_last_error(void) { return g_err.c_str(); }
+const char* qg_version(void) { return "qgemm-b300 0.1 (sm_103a)"; }
+
+int qg_set_launch_flags(int flags) {
+  if (flags & ~QG_LAUNCH_PDL) return fail(QG_ERR_INVALID_ARG, "unknown launch flag bits 0x%x", flags);
+  g_launch_flags = flags;
+  return QG_OK;
+}
+int qg_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns = ns ? ns : 2000000000ull;
+  return QG_OK;
+}
+int qg_set_force_timeout(int on) {
+  g_force_timeout = on ? 1 : 0;
+  return QG_OK;
+}
+int qg_set_allow_default(int allow) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_allow_default = allow != 0;
+  return QG_OK;
+}
+
+int qg_device_error(int* code) {
+  if (!code) return fail(QG_ERR_INVALID_ARG, "code is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&v, qg::g_device_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read device status");
+  e = cudaMemcpyToSymbol(qg::g_device_status, &zero, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "clear device status");
+  *code = v;
+  return QG_OK;
+}
+
+int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_t lda, void* A_q_dev, float* s_a_dev,
+                 void* stream) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (M < 0 || K <= 0 || lda < K) return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld lda=%lld", (long long)M, (long long)K, (long long)lda);
+  if (M == 0) return QG_OK;
+  if (!A_dev || !A_q_dev || !s_a_dev) return fail(QG_ERR_INVALID_ARG, "null pointer");
+  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
+  if (lda % 8 || !aligned(A_dev, 16) || !aligned(A_q_dev, 16) || !aligned(s_a_dev, 4))
+    return fail(QG_ERR_ALIGNMENT, "A/A_q must be 16-byte aligned with lda %% 8 == 0");
+  if (M > 0x7FFFFFFF || K > 0x7FFFFFFF) return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(A_dev);
+  uint8_t* Q = static_cast<uint8_t*>(A_q_dev);
+  cudaError_t e;
+  if (fmt == QG_BLOCK_FP8) {
+    constexpr int W = 8;
+    const int64_t groups = M * (K / 128);
+    e = launch(qg::quant_groups_kernel<W>, dim3(static_cast<unsigned>(cdiv(groups, W))), dim3(W * 32), 0, s, A, lda,
+               static_cast<int>(M), static_cast<int>(K), Q, s_a_dev);
+  } else if (fmt == QG_FP8_DYNAMIC) {
+    e = launch(qg::quant_rows_kernel<__nv_bfloat16, qg::kFmtFP8, 512>, dim3(static_cast<unsigned>(M)), dim3(512), 0, s,
+               A, lda, static_cast<int>(K), Q, s_a_dev, 448.0f);
+  } else {
+    e = launch(qg::quant_rows_kernel<__nv_bfloat16, qg::kFmtINT8, 512>, dim3(static_cast<unsigned>(M)), dim3(512), 0,
+               s, A, lda, static_cast<int>(K), Q, s_a_dev, 127.0f);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "quant_act launch");
+  return QG_OK;
+}
+
+int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q_dev, float* s_w_dev, void* stream) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld", (long long)N, (long long)K);
+  if (!W_dev || !W_q_dev || !s_w_dev) return fail(QG_ERR_INVALID_ARG, "null pointer");
+  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
+  if (!aligned(W_dev, 16) || !aligned(W_q_dev, 16) || !aligned(s_w_dev, 4))
+    return fail(QG_ERR_ALIGNMENT, "W/W_q must be 16-byte aligned");
+  if (N > 0x7FFFFFFF || K > 0x7FFFFFFF || cdiv(N, 128) > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* Q = static_cast<uint8_t*>(W_q_dev);
+  cudaError_t e;
+  if (fmt == QG_BLOCK_FP8) {
+    e = launch(qg::quant_blocks_kernel, dim3(static_cast<unsigned>(K / 128), static_cast<unsigned>(cdiv(N, 128))),
+               dim3(256), 0, s, W_dev, static_cast<int>(N), static_cast<int>(K), Q, s_w_dev);
+  } else if (fmt == QG_FP8_DYNAMIC) {
+    e = launch(qg::quant_rows_kernel<float, qg::kFmtFP8, 256>, dim3(static_cast<unsigned>(N)), dim3(256), 0, s, W_dev,
+               K, static_cast<int>(K), Q, s_w_dev, 448.0f);
+  } else {
+    e = launch(qg::quant_rows_kernel<float, qg::kFmtINT8, 256>, dim3(static_cast<unsigned>(N)), dim3(256), 0, s, W_dev,
+               K, static_cast<int>(K), Q, s_w_dev, 127.0f);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "quant_weight launch");
+  return QG_OK;
+}
+
+size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k) {
+  Plan p;
+  if (fmt < 0 || fmt > 2 || M <= 0 || N <= 0 || K <= 0 || variant < 0 || variant > 3) return 0;
+  if (make_plan(fmt, M, N, K, variant, split_k, &p) != QG_OK) return 0;
+  return static_cast<size_t>(workspace_bytes(p, M, N));
+}
+
+int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream) {
+  if (!workspace_dev || ws_bytes == 0) return QG_OK;
+  cudaError_t e = cudaMemsetAsync(workspace_dev, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return QG_OK;
+}
+
+int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
+                 const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
+                 int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (variant < 0 || variant > 3) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
+  if (M < 0 || N <= 0 || K <= 0 || ldy < N)
+    return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld ldy=%lld", (long long)M, (long long)N, (long long)K, (long long)ldy);
+  if (config_id < 0 || config_id > kMaxStages) return fail(QG_ERR_INVALID_ARG, "config_id %d outside [0,%d]", config_id, kMaxStages);
+  if (M == 0) return QG_OK;
+  if (!A_q_dev || !s_a_dev || !W_q_dev || !s_w_dev || !Y_dev) return fail(QG_ERR_INVALID_ARG, "null pointer");
+  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
+  if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF || cdiv(N, 128) > 0x7FFFFFFF)
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+  if (!aligned(A_q_dev, 16) || !aligned(W_q_dev, 16) || !aligned(s_a_dev, 4) || !aligned(s_w_dev, 4) ||
+      !aligned(Y_dev, 2) || (debug_acc_dev && !aligned(debug_acc_dev, 4)))
+    return fail(QG_ERR_ALIGNMENT, "A_q/W_q need 16-byte alignment, scales 4, Y 2");
+  if (debug_acc_dev && fmt != QG_W8A8_INT8) return fail(QG_ERR_INVALID_ARG, "debug_acc is W8A8_INT8 only");
+  Plan p;
+  int rc = make_plan(fmt, M, N, K, variant, split_k, &p);
+  if (rc != QG_OK) return rc;
+  const int64_t need = workspace_bytes(p, M, N);
+  if (need > 0) {
+    if (!workspace_dev) return fail(QG_ERR_WORKSPACE_TOO_SMALL, "split_k=%d needs a %lld-byte workspace", split_k, (long long)need);
+    if (static_cast<int64_t>(ws_bytes) < need)
+      return fail(QG_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %lld needed", ws_bytes, (long long)need);
+    if (!aligned(workspace_dev, 256)) return fail(QG_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  }
+  CUtensorMap tmW, tmA;
+  rc = make_map(&tmW, W_q_dev, N, K, K, 128);
+  if (rc != QG_OK) return rc;
+  rc = make_map(&tmA, A_q_dev, M, K, K, p.swap ? static_cast<uint32_t>(p.mpad) : 128u);
+  if (rc != QG_OK) return rc;
+
+  qg::GemmArgs g = {};
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.ldy = ldy;
+  g.kt_total = p.kt;
+  g.splits = p.splits;
+  g.s_a = s_a_dev;
+  g.s_w = s_w_dev;
+  g.Y = static_cast<__nv_bfloat16*>(Y_dev);
+  if (need > 0) {
+    const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
+    g.ws_count = static_cast<int*>(workspace_dev);
+    g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
+  }
+  g.debug_acc = debug_acc_dev;
+  g.wait_ns = g_wait_ns;
+  g.force_timeout = g_force_timeout;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (fmt == QG_W8A8_INT8) {
+    if (p.mpad == 16) return run_i8<16>(p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return run_i8<32>(p, tmW, tmA, g, config_id, s);
+    return run_i8<64>(p, tmW, tmA, g, config_id, s);
+  }
+  if (p.swap) {
+    if (p.mpad == 16) return run_f8_fmt<true, 16>(fmt, p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return run_f8_fmt<true, 32>(fmt, p, tmW, tmA, g, config_id, s);
+    return run_f8_fmt<true, 64>(fmt, p, tmW, tmA, g, config_id, s);
+  }
+  return run_f8_fmt<false, 16>(fmt, p, tmW, tmA, g, config_id, s);
+}
+
+int qg_load_table(const char* path) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_table_env_checked = true;
+  if (!path) {
+    path = getenv("QG_TABLE");
+    if (!path) return fail(QG_ERR_INVALID_ARG, "no path given and $QG_TABLE unset");
+  }
+  return load_table_file(path);
+}
+
+int qg_select(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int* split_k, int* config_id) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (M <= 0 || N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "bad sizes");
+  if (!variant || !split_k || !config_id) return fail(QG_ERR_INVALID_ARG, "null output pointer");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_table_env_checked) {
+    g_table_env_checked = true;
+    const char* env = getenv("QG_TABLE");
+    if (env) {
+      int rc = load_table_file(env);
+      if (rc != QG_OK) return rc;
+    }
+  }
+  // smallest tuned token count >= M for this (fmt, N, K)
+  const Row* best = nullptr;
+  int max_m = 0;
+  for (auto it = g_table.lower_bound(Key{fmt, N, K, 0}); it != g_table.end(); ++it) {
+    if (it->first.fmt != fmt || it->first.n != N || it->first.k != K) break;
+    max_m = std::max(max_m, it->first.m);
+    if (it->first.m >= M && !best) best = &it->second;
+  }
+  if (best) {
+    *variant = best->variant;
+    *split_k = best->split_k;
+    *config_id = best->config_id;
+    return QG_OK;
+  }
+  if (max_m > 0 || g_allow_default) {  // beyond the tuned range, or defaults allowed
+    default_config(fmt, M, N, K, variant, split_k, config_id);
+    return QG_OK;
+  }
+  return fail(QG_ERR_NO_CONFIG, "no tuned config for fmt=%d N=%lld K=%lld M=%lld", fmt, (long long)N, (long long)K,
+              (long long)M);
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+// quant.cuh -- dynamic activation quantization and static weight
+// quantization for the three formats of "Building a High-Performance and
+// Portable vLLM Linear Backend with Helion", section "Helion Linear Backend >
+// Scope":
+//   FP8_Dynamic  per-token (row) E4M3, s = amax/448
+//   W8A8_INT8    per-token (row) symmetric int8, s = amax/127
+//   Block_FP8    E4M3 with one scale per 1x128 activation group and one per
+//                128x128 weight block
+// The page gives no formula; this code takes s = amax/QMAX in IEEE fp32
+// (s = 1 when amax == 0) and q = RNE-saturate(x / s) with one IEEE fp32
+// division, the same reading as the CPU oracle, so both agree bit for bit.
+#pragma once
+#include "common.cuh"
+#include <cuda_fp8.h>
+
+namespace qg {
+
+enum : int { kFmtFP8 = 0, kFmtINT8 = 1, kFmtBlock = 2 };
+
+__device__ __forceinline__ float scale_from_amax(float amax, float qmax) {
+  return amax > 0.0f ? __fdiv_rn(amax, qmax) : 1.0f;
+}
+
+// Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448);
+// `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ uint8_t int8_sym(float x) {
+  int v = __float2int_rn(x);  // round to nearest even
+  v = v > 127 ? 127 : (v < -127 ? -127 : v);
+  return static_cast<uint8_t>(static_cast<int8_t>(v));
+}
+
+// 8 consecutive inputs as fp32 (16-byte load for bf16, 2 x 16 bytes for f32).
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+template <int OUT>  // kFmtFP8 or kFmtINT8
+__device__ __forceinline__ uint2 encode8(const float (&x)[8], float s) {
+  uint32_t w[2];
+  if constexpr (OUT == kFmtFP8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint16_t lo = e4m3x2(__fdiv_rn(x[4 * h + 0], s), __fdiv_rn(x[4 * h + 1], s));
+      uint16_t hi = e4m3x2(__fdiv_rn(x[4 * h + 2], s), __fdiv_rn(x[4 * h + 3], s));
+      w[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t b0 = int8_sym(__fdiv_rn(x[4 * h + 0], s)), b1 = int8_sym(__fdiv_rn(x[4 * h + 1], s));
+      uint32_t b2 = int8_sym(__fdiv_rn(x[4 * h + 2], s)), b3 = int8_sym(__fdiv_rn(x[4 * h + 3], s));
+      w[h] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One CTA per row: per-row absmax over K (16-byte vector loads, warp-shuffle
+// then shared-memory reduction), one scale per row, then encode the row.
+// Rows: X[r * ldx + k], k < K (K % 8 == 0); Q[r * K + k]; s[r].
+template <typename InT, int OUT, int THREADS>
+__global__ void __launch_bounds__(THREADS) quant_rows_kernel(const InT* __restrict__ X, int64_t ldx, int K,
+                                                            uint8_t* __restrict__ Q, float* __restrict__ S,
+                                                            float qmax) {
+  // Let the next kernel (a GEMM that first streams its static weights) be
+  // scheduled now; this kernel's own inputs are read only after the wait.
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float red[THREADS / 32];
+  const int64_t r = blockIdx.x;
+  const InT* x = X + r * ldx;
+  float amax = 0.0f;
+  for (int k = threadIdx.x * 8; k < K; k += THREADS * 8) {
+    float v[8];
+    load8(x + k, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < THREADS / 32 ? red[threadIdx.x] : 0.0f;
+    v = warp_max(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float s = scale_from_amax(red[0], qmax);
+  if (threadIdx.x == 0) S[r] = s;
+  uint8_t* q = Q + r * static_cast<int64_t>(K);
+  for (int k = threadIdx.x * 8; k < K; k += THREADS * 8) {
+    float v[8];
+    load8(x + k, v);
+    *reinterpret_cast<uint2*>(q + k) = encode8<OUT>(v, s);
+  }
+}
+
+// Block_FP8 activations: one warp per 1x128 group (32 lanes x 4 values).
+// S is [rows][K/128] row-major.  K % 128 == 0.
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) quant_groups_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
+                                                                 int rows, int K, uint8_t* __restrict__ Q,
+                                                                 float* __restrict__ S) {
+  // Let the next kernel (a GEMM that first streams its static weights) be
+  // scheduled now; this kernel's own inputs are read only after the wait.
+  pdl_launch_dependents();
+  pdl_wait();
+  const int groups = K / 128;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+  if (gid >= static_cast<int64_t>(rows) * groups) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = gid / groups;
+  const int g = static_cast<int>(gid % groups);
+  const __nv_bfloat16* x = X + r * ldx + g * 128 + lane * 4;
+  uint2 u = *reinterpret_cast<const uint2*>(x);
+  float v[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                __uint_as_float(u.y & 0xFFFF0000u)};
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  amax = warp_max(amax);
+  const float s = scale_from_amax(amax, 448.0f);
+  if (lane == 0) S[r * groups + g] = s;
+  uint16_t lo = e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
+  uint16_t hi = e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
+  *reinterpret_cast<uint32_t*>(Q + r * static_cast<int64_t>(K) + g * 128 + lane * 4) =
+      static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Block_FP8 weights: one CTA of 256 threads per 128x128 block of W[N, K]
+// (fp32); the last block row may be ragged (N % 128 != 0).  K % 128 == 0.
+// S is [ceil(N/128)][K/128] row-major.
+__global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restrict__ W, int N, int K,
+                                                          uint8_t* __restrict__ Q, float* __restrict__ S) {
+  __shared__ float red[8];
+  const int kb = blockIdx.x, nb = blockIdx.y, kblocks = K / 128;
+  const int n0 = nb * 128, rows = min(128, N - n0);
+  // thread t covers rows t/16 + 16*j, columns (t%16)*8 .. +7
+  const int c = (threadIdx.x & 15) * 8;
+  float amax = 0.0f;
+  for (int rr = threadIdx.x >> 4; rr < rows; rr += 16) {
+    float v[8];
+    load8(W + static_cast<int64_t>(n0 + rr) * K + kb * 128 + c, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < 8 ? red[threadIdx.x] : 0.0f;
+    v = warp_max(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float s = scale_from_amax(red[0], 448.0f);
+  if (threadIdx.x == 0) S[nb * kblocks + kb] = s;
+  for (int rr = threadIdx.x >> 4; rr < rows; rr += 16) {
+    float v[8];
+    const int64_t off = static_cast<int64_t>(n0 + rr) * K + kb * 128 + c;
+    load8(W + off, v);
+    *reinterpret_cast<uint2*>(Q + off) = encode8<kFmtFP8>(v, s);
+  }
+}
+
+}  // namespace qg

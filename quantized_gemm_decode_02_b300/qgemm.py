@@ -1,0 +1,152 @@
+"""ctypes binding of libqgemm.so (include/qgemm.h), argument marshalling only.
+
+Every function keeps the C name and order of arguments; torch tensors are
+accepted where the C side takes device pointers, and ``stream`` defaults to
+torch's current stream.  All computation happens in the library's sm_103a
+kernels: importing this module fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemm.so")
+
+QG_FP8_DYNAMIC, QG_W8A8_INT8, QG_BLOCK_FP8 = 0, 1, 2
+QG_STANDARD, QG_SPLITK, QG_SWAPAB, QG_SWAPAB_SPLITK = 0, 1, 2, 3
+QG_OK = 0
+QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED_SHAPE, QG_ERR_ALIGNMENT = -1, -2, -3
+QG_ERR_WORKSPACE_TOO_SMALL, QG_ERR_NO_CONFIG, QG_ERR_CUDA = -4, -5, -6
+QG_ERR_DEVICE_TIMEOUT, QG_ERR_TABLE_PARSE = -7, -8
+QG_LAUNCH_PDL = 1
+
+FORMATS = {"FP8_Dynamic": QG_FP8_DYNAMIC, "W8A8_INT8": QG_W8A8_INT8, "Block_FP8": QG_BLOCK_FP8}
+VARIANTS = {"Standard": QG_STANDARD, "Split-K": QG_SPLITK, "Swap-AB": QG_SWAPAB, "Swap-AB+Split-K": QG_SWAPAB_SPLITK}
+
+EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
+           "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
+           "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
+
+
+class QGError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where} failed with status {code}: {msg}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libqgemm.so not built at {path}; run quantized_gemm_decode_02_b300/build.py")
+    lib = ctypes.CDLL(path)
+    P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.qg_quant_act.argtypes = [I, P, I64, I64, I64, P, P, P]
+    lib.qg_quant_weight.argtypes = [I, P, I64, I64, P, P, P]
+    lib.qg_workspace_bytes.argtypes = [I, I64, I64, I64, I, I]
+    lib.qg_workspace_bytes.restype = SZ
+    lib.qg_workspace_init.argtypes = [P, SZ, P]
+    lib.qg_gemm_w8a8.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
+    lib.qg_select.argtypes = [I, I64, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
+    lib.qg_load_table.argtypes = [ctypes.c_char_p]
+    lib.qg_set_allow_default.argtypes = [I]
+    lib.qg_set_launch_flags.argtypes = [I]
+    lib.qg_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.qg_set_force_timeout.argtypes = [I]
+    lib.qg_device_error.argtypes = [ctypes.POINTER(I)]
+    lib.qg_last_error.restype = ctypes.c_char_p
+    lib.qg_version.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = load_library()
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != QG_OK:
+        raise QGError(rc, where, _lib.qg_last_error().decode())
+    return rc
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def qg_quant_act(fmt, A, M, K, lda, A_q, s_a, stream=None) -> None:
+    _check(_lib.qg_quant_act(_fmt(fmt), _ptr(A), M, K, lda, _ptr(A_q), _ptr(s_a), _stream(stream)), "qg_quant_act")
+
+
+def qg_quant_weight(fmt, W, N, K, W_q, s_w, stream=None) -> None:
+    _check(_lib.qg_quant_weight(_fmt(fmt), _ptr(W), N, K, _ptr(W_q), _ptr(s_w), _stream(stream)), "qg_quant_weight")
+
+
+def qg_workspace_bytes(fmt, M, N, K, variant, split_k) -> int:
+    return int(_lib.qg_workspace_bytes(_fmt(fmt), M, N, K, variant, split_k))
+
+
+def qg_workspace_init(workspace, ws_bytes, stream=None) -> None:
+    _check(_lib.qg_workspace_init(_ptr(workspace), ws_bytes, _stream(stream)), "qg_workspace_init")
+
+
+def qg_gemm_w8a8(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, config_id=0, workspace=None,
+                 ws_bytes=0, debug_acc=None, stream=None) -> None:
+    _check(_lib.qg_gemm_w8a8(_fmt(fmt), M, N, K, _ptr(A_q), _ptr(s_a), _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant,
+                             split_k, config_id, _ptr(workspace), ws_bytes, _ptr(debug_acc), _stream(stream)),
+           "qg_gemm_w8a8")
+
+
+def qg_select(fmt, M, N, K) -> tuple[int, int, int]:
+    v, s, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.qg_select(_fmt(fmt), M, N, K, ctypes.byref(v), ctypes.byref(s), ctypes.byref(c)), "qg_select")
+    return v.value, s.value, c.value
+
+
+def qg_load_table(path) -> None:
+    _check(_lib.qg_load_table(None if path is None else os.fsencode(path)), "qg_load_table")
+
+
+def qg_set_allow_default(allow: bool) -> None:
+    _check(_lib.qg_set_allow_default(1 if allow else 0), "qg_set_allow_default")
+
+
+def qg_set_launch_flags(flags: int) -> None:
+    _check(_lib.qg_set_launch_flags(flags), "qg_set_launch_flags")
+
+
+def qg_set_wait_limit_ns(ns: int) -> None:
+    _check(_lib.qg_set_wait_limit_ns(ns), "qg_set_wait_limit_ns")
+
+
+def qg_set_force_timeout(on: bool) -> None:
+    _check(_lib.qg_set_force_timeout(1 if on else 0), "qg_set_force_timeout")
+
+
+def qg_device_error() -> int:
+    code = ctypes.c_int()
+    _check(_lib.qg_device_error(ctypes.byref(code)), "qg_device_error")
+    return code.value
+
+
+def qg_last_error() -> str:
+    return _lib.qg_last_error().decode()
+
+
+def qg_version() -> str:
+    return _lib.qg_version().decode()

@@ -8,6 +8,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_sessionstart(session):
+    # Build the sm_103a library (nvcc cross-compiles without a GPU) and the
+    # oracle before any test module imports them.
+    from quantized_gemm_decode_02_b300 import build as qbuild
+    qbuild.build()
+    from oracle import oracle as o
+    o.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (runs the sm_103a kernels)")
     config.addinivalue_line("markers", "slow: large oracle work (full-size sampled parity)")

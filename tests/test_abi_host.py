@@ -1,0 +1,169 @@
+"""Host-side checks of the C ABI (no GPU): the library loads and exports every
+symbol include/qgemm.h declares, argument validation returns the documented
+status codes before any device work, workspace sizing, and the per-shape
+config table ("Per-shape Config Tuning" / "Hybrid Dispatch" of "Building a
+High-Performance and Portable vLLM Linear Backend with Helion")."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemm.h")
+
+
+@pytest.fixture(scope="module")
+def q():
+    from quantized_gemm_decode_02_b300 import qgemm
+    return qgemm
+
+
+def header_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"QG_API\s+[\w\s\*]*?\b(qg_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_entry_points():
+    syms = header_symbols()
+    for s in ("qg_quant_act", "qg_quant_weight", "qg_gemm_w8a8", "qg_select", "qg_workspace_bytes",
+              "qg_load_table", "qg_last_error"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(q):
+    out = subprocess.run(["nm", "-D", "--defined-only", q.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (qg_\w+)", out))
+    missing = [s for s in header_symbols() if s not in exported]
+    assert not missing, missing
+    assert set(q.EXPORTS) == set(header_symbols())
+    lib = ctypes.CDLL(q.LIB_PATH)
+    for s in header_symbols():
+        assert getattr(lib, s) is not None
+
+
+def test_header_compiles_as_c():
+    src = '#include "qgemm.h"\nint main(void){ return QG_OK + QG_SWAPAB_SPLITK * 0; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-x", "c", "-",
+                        "-fsyntax-only"], input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def _raw(q):
+    return q._lib
+
+
+BAD16 = 0x10008  # 8-byte aligned only; never dereferenced (validation fails first)
+OK16 = 0x10000
+
+
+def test_quant_act_validation(q):
+    lib = _raw(q)
+    assert lib.qg_quant_act(7, OK16, 1, 128, 128, OK16, OK16, None) == q.QG_ERR_INVALID_ARG
+    assert lib.qg_quant_act(0, None, 1, 128, 128, OK16, OK16, None) == q.QG_ERR_INVALID_ARG
+    assert lib.qg_quant_act(0, OK16, 1, 120, 120, OK16, OK16, None) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert lib.qg_quant_act(2, OK16, 1, 144, 144, OK16, OK16, None) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert lib.qg_quant_act(0, BAD16, 1, 128, 128, OK16, OK16, None) == q.QG_ERR_ALIGNMENT
+    assert lib.qg_quant_act(0, OK16, 1, 128, 132, OK16, OK16, None) == q.QG_ERR_ALIGNMENT
+    assert lib.qg_quant_act(0, OK16, 1, 128, 64, OK16, OK16, None) == q.QG_ERR_INVALID_ARG
+    assert lib.qg_quant_act(0, None, 0, 128, 128, None, None, None) == q.QG_OK  # M == 0: no-op
+    assert "K" in q.qg_last_error() or q.qg_last_error() != ""
+
+
+def test_quant_weight_validation(q):
+    lib = _raw(q)
+    assert lib.qg_quant_weight(1, OK16, 0, 128, OK16, OK16, None) == q.QG_ERR_INVALID_ARG
+    assert lib.qg_quant_weight(1, OK16, 4, 40, OK16, OK16, None) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert lib.qg_quant_weight(1, BAD16, 4, 128, OK16, OK16, None) == q.QG_ERR_ALIGNMENT
+
+
+def _gemm(q, fmt=0, M=4, N=256, K=256, A=OK16, sa=OK16, W=OK16, sw=OK16, Y=OK16, ldy=None, variant=2, split=1,
+          cfg=0, ws=None, wsb=0, dbg=None):
+    return _raw(q).qg_gemm_w8a8(fmt, M, N, K, A, sa, W, sw, Y, N if ldy is None else ldy, variant, split, cfg, ws,
+                                wsb, dbg, None)
+
+
+def test_gemm_validation(q):
+    assert _gemm(q, fmt=5) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, variant=9) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, ldy=100) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, A=None) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, K=200) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(q, fmt=2, K=272) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(q, A=BAD16) == q.QG_ERR_ALIGNMENT
+    assert _gemm(q, W=BAD16) == q.QG_ERR_ALIGNMENT
+    assert _gemm(q, split=2) == q.QG_ERR_INVALID_ARG                    # split needs a *_SPLITK variant
+    assert _gemm(q, variant=3, split=3) == q.QG_ERR_UNSUPPORTED_SHAPE     # > ceil(K/128) = 2
+    assert _gemm(q, variant=3, split=0) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(q, variant=3, split=2) == q.QG_ERR_WORKSPACE_TOO_SMALL   # no workspace
+    assert _gemm(q, variant=3, split=2, ws=OK16, wsb=16) == q.QG_ERR_WORKSPACE_TOO_SMALL
+    assert _gemm(q, M=65, variant=2) == q.QG_ERR_UNSUPPORTED_SHAPE       # Swap-AB is M <= 64
+    assert _gemm(q, fmt=1, M=8, variant=0) == q.QG_ERR_UNSUPPORTED_SHAPE  # INT8 runs Swap-AB
+    assert _gemm(q, fmt=0, dbg=OK16) == q.QG_ERR_INVALID_ARG              # debug acc is INT8 only
+    assert _gemm(q, cfg=99) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, M=0) == q.QG_OK
+
+
+def test_workspace_bytes(q):
+    assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB, 1) == 0
+    # counters (2 tiles -> one 256-byte block) + splits * M * N * 4
+    assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB_SPLITK, 3) == 256 + 3 * 4 * 256 * 4
+    assert q.qg_workspace_bytes(1, 32, 4096, 2048, q.QG_SWAPAB_SPLITK, 4) == 256 + 4 * 32 * 4096 * 4
+    assert q.qg_workspace_bytes(0, 300, 256, 1024, q.QG_SPLITK, 2) == 256 + 2 * 300 * 256 * 4
+    assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB_SPLITK, 99) == 0  # invalid -> 0
+
+
+def test_launch_flag_and_limits(q):
+    assert _raw(q).qg_set_launch_flags(6) == q.QG_ERR_INVALID_ARG
+    q.qg_set_launch_flags(0)
+    q.qg_set_wait_limit_ns(0)
+
+
+def test_table_select(q, tmp_path):
+    t = tmp_path / "t.tsv"
+    t.write_text("# fmt N K M variant split config\n"
+                 "1\t2048\t2048\t1\t3\t8\t0\n"
+                 "1\t2048\t2048\t8\t3\t4\t6\n"
+                 "1\t2048\t2048\t32\t2\t1\t0\n")
+    q.qg_load_table(str(t))
+    q.qg_set_allow_default(False)
+    assert q.qg_select("W8A8_INT8", 1, 2048, 2048) == (3, 8, 0)
+    assert q.qg_select("W8A8_INT8", 2, 2048, 2048) == (3, 4, 6)    # next tuned M >= 2 is 8
+    assert q.qg_select("W8A8_INT8", 24, 2048, 2048) == (2, 1, 0)
+    v, s, c = q.qg_select("W8A8_INT8", 100, 2048, 2048)             # beyond the tuned range -> default
+    assert v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK, q.QG_STANDARD, q.QG_SPLITK) and s >= 1
+    with pytest.raises(q.QGError) as e:
+        q.qg_select("W8A8_INT8", 1, 4096, 2048)                     # missing shape
+    assert e.value.code == q.QG_ERR_NO_CONFIG
+    q.qg_set_allow_default(True)
+    v, s, c = q.qg_select("W8A8_INT8", 1, 4096, 2048)
+    assert v == q.QG_SWAPAB_SPLITK and 1 <= s <= 16
+    q.qg_set_allow_default(False)
+    bad = tmp_path / "bad.tsv"
+    bad.write_text("1 2048 2048 1 3\n")
+    with pytest.raises(q.QGError) as e:
+        q.qg_load_table(str(bad))
+    assert e.value.code == q.QG_ERR_TABLE_PARSE
+    with pytest.raises(q.QGError):
+        q.qg_load_table(str(tmp_path / "missing.tsv"))
+    empty = tmp_path / "empty.tsv"
+    empty.write_text("# nothing\n")
+    q.qg_load_table(str(empty))
+
+
+def test_default_config_fills_the_gpu(q):
+    q.qg_set_allow_default(True)
+    try:
+        for (M, N, K) in [(1, 2048, 2048), (32, 12288, 2048), (1, 5120, 25600), (32, 51200, 5120)]:
+            v, s, c = q.qg_select("FP8_Dynamic", M, N, K)
+            tiles = (N + 127) // 128
+            assert v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK)
+            assert s == 1 or tiles * s <= 148
+            assert s <= max(1, ((K + 127) // 128) // 2)
+        v, s, c = q.qg_select("FP8_Dynamic", 256, 4096, 4096)
+        assert v in (q.QG_STANDARD, q.QG_SPLITK)
+    finally:
+        q.qg_set_allow_default(False)

@@ -1,0 +1,192 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the CPU
+oracle on the same seeded inputs (quantizers bit-exact; INT8 accumulators
+bit-exact and Y within 1 bf16 ulp; FP8 within 8e-3 * s_a*s_w*sum|a_q*w_q|).
+
+Sizes here span several 128-row tiles, a ragged N tail, ragged K (FP8) and
+several 1024-K exactness segments (INT8), with M over the decode range."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gc():
+    import gpu_cases
+    return gpu_cases
+
+
+@pytest.fixture(scope="module")
+def q():
+    from quantized_gemm_decode_02_b300 import qgemm
+    return qgemm
+
+
+SW, SWS, ST, STS = 2, 3, 0, 1  # Swap-AB, Swap-AB+Split-K, Standard, Split-K
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 3), (ST, 1), (STS, 2)])
+def test_fp8_dynamic(orc, gc, M, variant, split):
+    gc.run_case(orc, "FP8_Dynamic", M, 424, 656, variant, split, seed=M)
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 24, 32])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 5), (ST, 1), (STS, 3)])
+def test_block_fp8(orc, gc, M, variant, split):
+    gc.run_case(orc, "Block_FP8", M, 392, 768, variant, split, seed=100 + M)
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 20, 32, 48])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 7)])
+def test_w8a8_int8(orc, gc, M, variant, split):
+    # K = 2304: 18 k-tiles -> three exact 1024-K segments at split 1
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=200 + M, outliers=True)
+
+
+def test_int8_accumulators_identical_across_variants(gc):
+    import seeded_inputs as si
+    M, N, K = 32, 256, 4096
+    A = si.activations(M, K, seed=5, outliers=True).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=5)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("W8A8_INT8", W)
+    Aq, sa = gc.quant_act_gpu("W8A8_INT8", A)
+    outs = [gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, v, s, debug=True) for v, s in
+            [(SW, 1), (SWS, 2), (SWS, 3), (SWS, 8), (SWS, 32)]]
+    torch.cuda.synchronize()
+    for Y, d in outs[1:]:
+        assert torch.equal(d, outs[0][1])
+        assert torch.equal(Y, outs[0][0])
+
+
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "Block_FP8", "W8A8_INT8"])
+def test_split_k_is_deterministic(gc, fmt):
+    import seeded_inputs as si
+    M, N, K = 16, 384, 2048
+    A = si.activations(M, K, seed=9).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=9)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu(fmt, W)
+    Aq, sa = gc.quant_act_gpu(fmt, A)
+    ys = [gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SWS, 5)[0] for _ in range(4)]
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
+def test_zero_rows_and_columns(orc, gc):
+    import seeded_inputs as si
+    for fmt in ("FP8_Dynamic", "W8A8_INT8", "Block_FP8"):
+        M, N, K = 6, 260, 512
+        A = si.activations(M, K, seed=3)
+        A[2] = 0
+        W = si.weights(N, K, seed=3)
+        W[7] = 0
+        W[130:140] = 0
+        Ad, Wd = A.to(gc.DEV), torch.from_numpy(W).to(gc.DEV)
+        Wq, sw = gc.quant_weight_gpu(fmt, Wd)
+        Aq, sa = gc.quant_act_gpu(fmt, Ad)
+        Y, dbg = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SWS, 2, debug=fmt == "W8A8_INT8")
+        torch.cuda.synchronize()
+        Yc = Y.float().cpu()
+        assert torch.all(Yc[2] == 0) and torch.all(Yc[:, 7] == 0)
+        oAq, osa, oWq, osw = gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
+        gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y, dbg)
+
+
+def test_output_stride_and_untouched_padding(gc):
+    import seeded_inputs as si
+    M, N, K, ldy = 9, 200, 384, 264
+    A = si.activations(M, K, seed=4).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=4)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("FP8_Dynamic", W)
+    Aq, sa = gc.quant_act_gpu("FP8_Dynamic", A)
+    big = torch.full((M, ldy), 123.0, dtype=torch.bfloat16, device=gc.DEV)
+    gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, SWS, 3, Y=big)
+    ref, _ = gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, SW, 1)
+    torch.cuda.synchronize()
+    assert torch.all(big[:, N:] == 123.0)
+    assert torch.allclose(big[:, :N].float(), ref.float(), rtol=1e-2, atol=1e-3)
+
+
+def test_m_zero_is_a_noop(q, gc):
+    d = torch.zeros(16, dtype=torch.uint8, device=gc.DEV)
+    f = torch.zeros(4, dtype=torch.float32, device=gc.DEV)
+    q.qg_quant_act("FP8_Dynamic", d, 0, 16, 16, d, f)
+    q.qg_gemm_w8a8("FP8_Dynamic", 0, 16, 16, d, f, d, f, d, 16, SW, 1)
+    torch.cuda.synchronize()
+
+
+def test_graph_capture_and_pdl_replay(orc, gc, q):
+    import seeded_inputs as si
+    fmt, M, N, K = "W8A8_INT8", 8, 512, 2048
+    A = si.activations(M, K, seed=12)
+    W = si.weights(N, K, seed=12)
+    Ad = A.to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu(fmt, torch.from_numpy(W).to(gc.DEV))
+    Aq = torch.empty((M, K), dtype=torch.uint8, device=gc.DEV)
+    sa = torch.empty((M,), dtype=torch.float32, device=gc.DEV)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=gc.DEV)
+    need = q.qg_workspace_bytes(fmt, M, N, K, SWS, 4)
+    ws = torch.zeros(need, dtype=torch.uint8, device=gc.DEV)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(3):
+                q.qg_quant_act(fmt, Ad, M, K, K, Aq, sa)
+                q.qg_gemm_w8a8(fmt, M, N, K, Aq, sa, Wq, sw, Y, N, SWS, 4, 0, ws, need)
+        for _ in range(3):
+            Y.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            oAq, osa, oWq, osw = gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
+            gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y)
+    finally:
+        q.qg_set_launch_flags(0)
+    assert q.qg_device_error() == 0
+
+
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])
+def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt):
+    import seeded_inputs as si
+    M, N, K = 4, 256, 1024
+    A = si.activations(M, K, seed=1)
+    W = si.weights(N, K, seed=1)
+    Ad, Wd = A.to(gc.DEV), torch.from_numpy(W).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu(fmt, Wd)
+    Aq, sa = gc.quant_act_gpu(fmt, Ad)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    q.qg_set_wait_limit_ns(2_000_000)  # 2 ms
+    q.qg_set_force_timeout(True)
+    try:
+        gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1)
+        assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
+    finally:
+        q.qg_set_force_timeout(False)
+        q.qg_set_wait_limit_ns(0)
+    assert q.qg_device_error() == 0
+    Y, dbg = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1, debug=fmt == "W8A8_INT8")
+    torch.cuda.synchronize()
+    oAq, osa, oWq, osw = gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
+    gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y, dbg)
+
+
+def test_quant_act_row_stride(orc, gc, q):
+    import seeded_inputs as si
+    M, K, lda = 5, 512, 640
+    big = si.activations(M, lda, seed=77)
+    A = big[:, :K].contiguous()
+    Ad = big.to(gc.DEV)
+    for fmt in ("FP8_Dynamic", "W8A8_INT8", "Block_FP8"):
+        Aq = torch.empty((M, K), dtype=torch.uint8, device=gc.DEV)
+        sa = torch.empty((M, K // 128) if fmt == "Block_FP8" else (M,), dtype=torch.float32, device=gc.DEV)
+        q.qg_quant_act(fmt, Ad, M, K, lda, Aq, sa)
+        torch.cuda.synchronize()
+        oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
+        assert np.array_equal(Aq.cpu().numpy().view(gc.oracle_dtype(fmt)), oAq)
+        assert np.array_equal(sa.cpu().numpy(), osa)
