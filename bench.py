@@ -1,0 +1,480 @@
+"""Benchmark of the quantized decode GEMM hot path on B300.
+
+Workload (default): W8A8_INT8 over the four Qwen3-1.7B linear layers
+(qkv K=2048 N=4096, o K=2048 N=2048, gate_up K=2048 N=12288, down K=6144
+N=2048) at every tuned decode token count M in {1,2,4,8,16,24,32}.  One step
+is one pass of the whole hot path over that batch: for each (M, layer) a
+dynamic per-token activation quantization (qg_quant_act) and the quantized
+GEMM (qg_gemm_w8a8) with the variant the tuned table selects (qg_select),
+28 + 28 kernels captured once into a CUDA graph with programmatic dependent
+launch and replayed.  Every (M, layer) pair owns distinct weights, so a step
+streams 352 MB of int8 weights (> 126 MB L2): no step finds its weights in L2.
+
+Metric: HBM GB/s = algorithmic bytes per step / step time (the kernels must
+move the weights, activations, scales and outputs once), plus µs per GEMM.
+
+Also reported: the roofline of the GEMM kernel (per-launch durations from
+timing events inside a second graph), an end-to-end figure through the C ABI
+with the activations copied from pinned host memory and the outputs copied
+back inside the timed region, SM clocks sampled during the timed region, and
+the CPU oracle timed on the host cores on a bounded sample (cpu_baseline).
+`--impl reference` times that oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+TABLE = os.path.join(ROOT, "quantized_gemm_decode_02_b300", "tables", "b300.tsv")
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+
+WORKLOADS = {
+    # name: (format, model, layers, token counts)
+    "int8_qwen3_1.7b": ("W8A8_INT8", "Qwen3-1.7B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
+    "fp8_qwen3_1.7b_o_m1": ("FP8_Dynamic", "Qwen3-1.7B", ("o",), (1,)),
+    "blockfp8_qwen3_8b": ("Block_FP8", "Qwen3-8B", ("qkv", "o", "gate_up", "down"), tuple(range(1, 33))),
+    "fp8_qwen3_32b": ("FP8_Dynamic", "Qwen3-32B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
+    "fp8_qwen3_8b": ("FP8_Dynamic", "Qwen3-8B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
+    "int8_qwen3_8b": ("W8A8_INT8", "Qwen3-8B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
+}
+DEFAULT_WORKLOAD = "int8_qwen3_1.7b"
+
+
+def gemm_bytes(fmt: str, M: int, N: int, K: int) -> int:
+    """Algorithmic bytes of one quantized GEMM: weights, quantized
+    activations, bf16 output and the scales, each moved once."""
+    if fmt == "Block_FP8":
+        return N * K + M * K + 2 * M * N + 4 * ((N + 127) // 128) * (K // 128) + 4 * M * (K // 128)
+    return N * K + M * K + 2 * M * N + 4 * N + 4 * M
+
+
+def quant_bytes(fmt: str, M: int, K: int) -> int:
+    """Algorithmic bytes of one activation quantization: bf16 in, codes and scales out."""
+    scales = M * (K // 128) if fmt == "Block_FP8" else M
+    return 2 * M * K + M * K + 4 * scales
+
+
+# ------------------------------------------------------------------ workload
+
+class Workload:
+    """Device buffers and the captured graphs for one workload."""
+
+    def __init__(self, name: str, device: str, seed: int = 0, pdl: bool = True):
+        from quantized_gemm_decode_02_b300 import qgemm as q
+        self.q = q
+        self.name = name
+        self.fmt, self.model, self.layers, self.ms = WORKLOADS[name]
+        self.device = device
+        self.pdl = pdl
+        shapes = si.QWEN3_LINEARS[self.model]
+        self.items = []  # (M, layer, N, K)
+        for M in self.ms:
+            for layer in self.layers:
+                K, N = shapes[layer]
+                self.items.append((M, layer, N, K))
+        if os.path.exists(TABLE):
+            q.qg_load_table(TABLE)
+        q.qg_set_allow_default(True)
+        fmt = self.fmt
+        # one contiguous activation buffer (bf16) and one output buffer (bf16),
+        # sliced per item at 256-byte boundaries, so e2e copies are single copies
+        def align(n):
+            return (n + 255) // 256 * 256
+        a_off, y_off, a_tot, y_tot = [], [], 0, 0
+        for (M, _, N, K) in self.items:
+            a_off.append(a_tot); a_tot += align(M * K * 2)
+            y_off.append(y_tot); y_tot += align(M * N * 2)
+        self.A_all = torch.empty(a_tot, dtype=torch.uint8, device=device)
+        self.Y_all = torch.empty(y_tot, dtype=torch.uint8, device=device)
+        self.recs = []
+        ws_need = 0
+        for i, (M, layer, N, K) in enumerate(self.items):
+            variant, split, cfg = q.qg_select(fmt, M, N, K)
+            need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
+            ws_need = max(ws_need, need)
+            A = self.A_all[a_off[i]:a_off[i] + M * K * 2].view(torch.bfloat16).view(M, K)
+            A.copy_(si.activations_device(M, K, seed=seed * 1000 + i, device=device,
+                                          outliers=(fmt == "Block_FP8")))
+            W = si.weights_device(N, K, seed=seed * 1000 + i, device=device)
+            Wq = torch.empty((N, K), dtype=torch.uint8, device=device)
+            if fmt == "Block_FP8":
+                sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device)
+                sa = torch.empty((M, K // 128), dtype=torch.float32, device=device)
+            else:
+                sw = torch.empty((N,), dtype=torch.float32, device=device)
+                sa = torch.empty((M,), dtype=torch.float32, device=device)
+            q.qg_quant_weight(fmt, W, N, K, Wq, sw)
+            del W
+            Aq = torch.empty((M, K), dtype=torch.uint8, device=device)
+            Y = self.Y_all[y_off[i]:y_off[i] + M * N * 2].view(torch.bfloat16).view(M, N)
+            self.recs.append(dict(M=M, layer=layer, N=N, K=K, A=A, Aq=Aq, sa=sa, Wq=Wq, sw=sw, Y=Y,
+                                  variant=variant, split=split, cfg=cfg, ws_need=need))
+        self.ws = torch.zeros(max(ws_need, 256), dtype=torch.uint8, device=device)
+        self.ws_bytes = ws_need
+        torch.cuda.synchronize()
+        self.bytes_gemm = sum(gemm_bytes(fmt, r["M"], r["N"], r["K"]) for r in self.recs)
+        self.bytes_quant = sum(quant_bytes(fmt, r["M"], r["K"]) for r in self.recs)
+        self.bytes_step = self.bytes_gemm + self.bytes_quant
+        self.weight_bytes = sum(r["N"] * r["K"] for r in self.recs)
+
+    def enqueue(self, stream, i: int, gemm_only: bool = False):
+        r = self.recs[i]
+        q = self.q
+        if not gemm_only:
+            q.qg_quant_act(self.fmt, r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
+        q.qg_gemm_w8a8(self.fmt, r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"], r["N"],
+                       r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes, None, stream=stream)
+
+    def capture_step(self, stream) -> torch.cuda.CUDAGraph:
+        """The whole step (quant + GEMM for every item) as one graph."""
+        self.q.qg_set_launch_flags(self.q.QG_LAUNCH_PDL if self.pdl else 0)
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(len(self.recs)):
+                    self.enqueue(stream, i)
+        finally:
+            self.q.qg_set_launch_flags(0)
+        return g
+
+    def capture_timed_kernels(self, stream):
+        """The same step with timing events around every GEMM launch (no PDL:
+        the events sit between kernels).  Returns (graph, event pairs)."""
+        g = torch.cuda.CUDAGraph()
+        evs = []
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(len(self.recs)):
+                r = self.recs[i]
+                self.q.qg_quant_act(self.fmt, r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
+                e0 = torch.cuda.Event(enable_timing=True, external=True)
+                e1 = torch.cuda.Event(enable_timing=True, external=True)
+                e0.record(stream)
+                self.enqueue(stream, i, gemm_only=True)
+                e1.record(stream)
+                evs.append((e0, e1))
+        return g, evs
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qg_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2])); smax.append(float(parts[3]))
+                power.append(float(parts[4]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[6:10]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------- cpu oracle
+
+def _oracle_items(name):
+    fmt, model, layers, ms = WORKLOADS[name]
+    shapes = si.QWEN3_LINEARS[model]
+    return fmt, [(M, *shapes[layer][::-1]) for M in ms for layer in layers]  # (M, N, K)
+
+
+def _oracle_pass(orc, name, cols, cache, cores):
+    """quant_act + GEMM in the oracle for every (M, layer) item, all token
+    rows, the first `cols` output columns.  Returns (seconds, bytes)."""
+    fmt, items = _oracle_items(name)
+    t_total, processed = 0.0, 0
+    for idx, (M, N, K) in enumerate(items):
+        nc = min(cols, N)
+        key = (N, K, nc)
+        if key not in cache:
+            cache[key] = orc.quant_weight(fmt, si.weights(nc, K, seed=idx))  # setup, not timed
+        Wq, sw = cache[key]
+        A = si.bf16_to_f32_numpy(si.activations(M, K, seed=idx))
+        t0 = time.perf_counter()
+        Aq, sa = orc.quant_act(fmt, A)
+        orc.gemm(fmt, Aq, sa, Wq, sw, threads=cores)
+        t_total += time.perf_counter() - t0
+        processed += gemm_bytes(fmt, M, nc, K) + quant_bytes(fmt, M, K)
+    return t_total, processed
+
+
+def cpu_oracle_leg(name: str, budget_s: float = 12.0) -> dict:
+    """Time the CPU oracle on a bounded sample of the workload: every
+    (M, layer) item, all token rows, the first `cols` output columns of each
+    layer (a multiple of 128), doubling `cols` until one pass takes at least
+    budget/2.  GB/s counts the algorithmic bytes of the sampled part with the
+    same accounting as the GPU path."""
+    from oracle import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    cols, cache = 128, {}
+    while True:
+        t, b = _oracle_pass(orc, name, cols, cache, cores)
+        if t >= budget_s / 2 or cols >= 8192:
+            break
+        cols *= 2
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{name}: all {len(_oracle_items(name)[1])} (M, layer) items, all token rows, the first "
+                      f"{cols} output columns per layer; quant_act + GEMM in the C oracle on {cores} threads "
+                      f"({t:.1f} s)"}
+
+
+# --------------------------------------------------------------------- main
+
+def load_peaks():
+    try:
+        with open(PEAKS) as fh:
+            p = json.load(fh)
+        return p.get("hbm_gbs", 6400.0), "measured"
+    except (OSError, ValueError):
+        return 6400.0, "fallback"
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float, device) -> float:
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, each step a bounded
+    sample of the workload sized so the whole run stays within ~2 minutes."""
+    if rank != 0:
+        return 0
+    from oracle import oracle as orc
+    orc.build()
+    name = args.workload
+    fmt, model, layers, ms = WORKLOADS[name]
+    cores = os.cpu_count() or 1
+    cache = {}
+    t16, _ = _oracle_pass(orc, name, 16, cache, cores)          # calibration
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    cols = 16
+    while cols < 8192 and t16 * (cols * 2) / 16 <= per_step:
+        cols *= 2
+    for _ in range(args.warmup):
+        _oracle_pass(orc, name, cols, cache, cores)
+    t_sum, b_sum = 0.0, 0
+    for _ in range(args.steps):
+        t, b = _oracle_pass(orc, name, cols, cache, cores)
+        t_sum += t
+        b_sum += b
+    value = b_sum / t_sum / 1e9
+    sample = (f"{name}: all {len(_oracle_items(name)[1])} (M, layer) items, all token rows, the first {cols} "
+              f"output columns per layer, per step; quant_act + GEMM in the C oracle on {cores} threads")
+    line = {"metric": "HBM GB/s (% of B300 peak) and us/GEMM at M=1..32 on Qwen3 linear shapes",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_sum / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8" if fmt == "W8A8_INT8" else "e4m3", "data": "synthetic",
+            "config": {"workload": name, "format": fmt, "model": model, "layers": list(layers), "M": list(ms)},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the compute path is the sm_103a library)")
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    wl = Workload(args.workload, device, seed=rank, pdl=not args.no_pdl)
+    stream = torch.cuda.Stream(device=device)
+    graph = wl.capture_step(stream)
+    timed_graph, evs = wl.capture_timed_kernels(stream)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays (one step each)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)  # let the sampler's first reading land
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_step = t_start.elapsed_time(t_end) / args.steps
+    ms_step = max_over_ranks(world, ms_step, device)
+    value = world * wl.bytes_step / (ms_step * 1e-3) / 1e9
+    assert wl.q.qg_device_error() == 0
+
+    # ---- per-launch GEMM durations (timing events inside a second graph)
+    reps = max(20, min(200, args.steps // 10))
+    per = np.zeros(len(wl.recs))
+    for _ in range(3):
+        timed_graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        timed_graph.replay()
+        torch.cuda.synchronize()
+        per += np.array([e0.elapsed_time(e1) for (e0, e1) in evs])
+    per_ms = per / reps
+    gemm_ms_total = float(per_ms.sum())
+    n_gemm = len(wl.recs)
+    avg_bytes = wl.bytes_gemm / n_gemm
+    avg_ms = gemm_ms_total / n_gemm
+    achieved = avg_bytes / (avg_ms * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+
+    # ---- end to end through the C ABI: pinned host activations in, outputs out
+    host_A = torch.empty(wl.A_all.numel(), dtype=torch.uint8, pin_memory=True)
+    host_A.copy_(wl.A_all.cpu())
+    host_Y = torch.empty(wl.Y_all.numel(), dtype=torch.uint8, pin_memory=True)
+    e2e_steps = max(10, args.e2e_steps)
+    for _ in range(5):
+        with torch.cuda.stream(stream):
+            wl.A_all.copy_(host_A, non_blocking=True)
+            graph.replay()
+            host_Y.copy_(wl.Y_all, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            wl.A_all.copy_(host_A, non_blocking=True)
+            graph.replay()
+            host_Y.copy_(wl.Y_all, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / e2e_steps, device)
+    e2e_val = world * wl.bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_leg(args.workload)
+
+    per_gemm = [{"M": r["M"], "layer": r["layer"], "N": r["N"], "K": r["K"], "variant": r["variant"],
+                 "split_k": r["split"], "us": round(float(per_ms[i]) * 1e3, 3),
+                 "GBps": round(gemm_bytes(wl.fmt, r["M"], r["N"], r["K"]) / (per_ms[i] * 1e-3) / 1e9, 1)}
+                for i, r in enumerate(wl.recs)]
+    if rank == 0:
+        line = {
+            "metric": "HBM GB/s (% of B300 peak) and us/GEMM at M=1..32 on Qwen3 linear shapes",
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8" if wl.fmt == "W8A8_INT8" else "e4m3", "data": "synthetic",
+            "config": {"workload": args.workload, "format": wl.fmt, "model": wl.model, "layers": list(wl.layers),
+                       "M": list(wl.ms), "gemms_per_step": n_gemm, "kernels_per_step": 2 * n_gemm,
+                       "bytes_per_step": wl.bytes_step, "weight_bytes_per_step": wl.weight_bytes,
+                       "l2": f"inputs larger than L2: {wl.weight_bytes / 1e6:.0f} MB of distinct weights per step",
+                       "graph": "one CUDA graph per step" + ("" if args.no_pdl else ", programmatic dependent launch"),
+                       "parallelism": f"replicas x{world}",
+                       "us_per_gemm": round(ms_step * 1e3 / n_gemm, 3),
+                       "pct_of_peak": round(100 * value / world / peak, 1)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": f"gemm ({wl.fmt})", "peak_kind": peak_kind,
+                         "avg_launch_us": round(avg_ms * 1e3, 3), "avg_bytes_per_launch": round(avg_bytes)},
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(wl.A_all.numel()),
+                    "d2h_bytes_per_step": int(wl.Y_all.numel()), "ms_per_step": round(e2e_ms, 6)},
+            "gpu_launches": 2 * n_gemm * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "per_gemm": per_gemm,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
