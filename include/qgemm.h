@@ -111,6 +111,33 @@ QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_
                  const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
                  int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream);
 
+/* Allocation-free form of qg_gemm_w8a8 (the pages have no counterpart; this
+ * is a convenience of this library).  It is for callers that cannot call
+ * cudaMalloc at all: code running inside a host framework or serving runtime
+ * that owns the device allocator and forbids outside allocations, plugins
+ * that receive only input and output buffers, or latency-critical paths that
+ * must never enter the allocator.  Such callers cannot provide the Split-K
+ * workspace that qg_gemm_w8a8 needs, so this entry point keeps the Split-K
+ * partials and tile counters in one static device array of
+ * QG_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that loads
+ * the library holds that array until the process exits.
+ *   Arguments: as qg_gemm_w8a8 without workspace_dev / ws_bytes.
+ *   Limit: a shape whose scratch (qg_workspace_bytes) exceeds
+ *   QG_NOALLOC_SCRATCH_BYTES is rejected with QG_ERR_WORKSPACE_TOO_SMALL;
+ *   use fewer splits, or qg_gemm_w8a8 with a caller workspace.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   with that device current (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.  It never calls cudaMalloc / cudaFree.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents; each call clears the tile counters (cudaMemsetAsync on
+ *   `stream`) before its kernel.  Calls whose kernels overlap on the GPU
+ *   (other streams, concurrent graph launches) race on the array and give
+ *   wrong results: serialize them. */
+#define QG_NOALLOC_SCRATCH_BYTES (4u << 20)
+QG_API int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
+                                const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
+                                int split_k, int config_id, int32_t* debug_acc_dev, void* stream);
+
 /* Per-shape config lookup ("Per-shape Config Tuning"): the row of the loaded
  * table for (fmt, N, K) and the smallest tuned token count >= M.  M larger
  * than every tuned count ("Hybrid Dispatch": beyond the tuned range) and,

@@ -278,6 +278,36 @@ int load_table_file(const char* path) {
 
 }  // namespace
 
+// Static device scratch of qg_gemm_w8a8_noalloc (Split-K counters and
+// partials for callers that cannot allocate).  In host code this name is only
+// a host-side stand-in: kernels get the device address looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QG_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(QG_ERR_INVALID_ARG, "device index %d unsupported", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return QG_OK;
+}
+
+}  // namespace
+
 // ====================================================================== ABI
 extern "C" {
 
@@ -452,6 +482,30 @@ int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, 
     return run_f8_fmt<true, 64>(fmt, p, tmW, tmA, g, config_id, s);
   }
   return run_f8_fmt<false, 16>(fmt, p, tmW, tmA, g, config_id, s);
+}
+
+int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
+                         const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
+                         int split_k, int config_id, int32_t* debug_acc_dev, void* stream) {
+  const size_t need = qg_workspace_bytes(fmt, M, N, K, variant, split_k);
+  if (need > QG_NOALLOC_SCRATCH_BYTES)
+    return fail(QG_ERR_WORKSPACE_TOO_SMALL,
+                "qg_gemm_w8a8_noalloc: this shape needs %zu bytes of Split-K scratch, more than the %u-byte static "
+                "array; use fewer splits or qg_gemm_w8a8 with a workspace",
+                need, static_cast<unsigned>(QG_NOALLOC_SCRATCH_BYTES));
+  void* ws = nullptr;
+  if (need > 0) {
+    int rc = noalloc_scratch(&ws);
+    if (rc != QG_OK) return rc;
+    Plan p;
+    rc = make_plan(fmt, M, N, K, variant, split_k, &p);
+    if (rc != QG_OK) return rc;
+    const int64_t counters = ws_counter_bytes(static_cast<int64_t>(p.n_tiles) * p.m_tiles);
+    cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(counters), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clear noalloc counters");
+  }
+  return qg_gemm_w8a8(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id, ws,
+                      need, debug_acc_dev, stream);
 }
 
 int qg_load_table(const char* path) {

@@ -26,7 +26,10 @@ QG_LAUNCH_PDL = 1
 FORMATS = {"FP8_Dynamic": QG_FP8_DYNAMIC, "W8A8_INT8": QG_W8A8_INT8, "Block_FP8": QG_BLOCK_FP8}
 VARIANTS = {"Standard": QG_STANDARD, "Split-K": QG_SPLITK, "Swap-AB": QG_SWAPAB, "Swap-AB+Split-K": QG_SWAPAB_SPLITK}
 
+QG_NOALLOC_SCRATCH_BYTES = 4 << 20
+
 EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
+           "qg_gemm_w8a8_noalloc",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
            "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
 
@@ -48,6 +51,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qg_workspace_bytes.restype = SZ
     lib.qg_workspace_init.argtypes = [P, SZ, P]
     lib.qg_gemm_w8a8.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
+    lib.qg_gemm_w8a8_noalloc.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, P]
     lib.qg_select.argtypes = [I, I64, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
     lib.qg_load_table.argtypes = [ctypes.c_char_p]
     lib.qg_set_allow_default.argtypes = [I]
@@ -110,6 +114,15 @@ def qg_gemm_w8a8(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, con
     _check(_lib.qg_gemm_w8a8(_fmt(fmt), M, N, K, _ptr(A_q), _ptr(s_a), _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant,
                              split_k, config_id, _ptr(workspace), ws_bytes, _ptr(debug_acc), _stream(stream)),
            "qg_gemm_w8a8")
+
+
+def qg_gemm_w8a8_noalloc(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, config_id=0, debug_acc=None,
+                         stream=None) -> None:
+    """qg_gemm_w8a8 without a caller workspace: Split-K scratch comes from the
+    library's static 4 MiB device array (for callers that cannot allocate)."""
+    _check(_lib.qg_gemm_w8a8_noalloc(_fmt(fmt), M, N, K, _ptr(A_q), _ptr(s_a), _ptr(W_q), _ptr(s_w), _ptr(Y), ldy,
+                                     variant, split_k, config_id, _ptr(debug_acc), _stream(stream)),
+           "qg_gemm_w8a8_noalloc")
 
 
 def qg_select(fmt, M, N, K) -> tuple[int, int, int]:
