@@ -7,14 +7,20 @@
 //   Swap-AB   D^T = W_q . A_q^T, so 128 weight rows take the MMA M side and
 //             the few tokens (padded to MPAD) the MMA N side;
 //   Split-K   K is cut into `splits` balanced ranges of whole 128-wide
-//             k-tiles, one CTA per (tile, range); partials go to a caller
-//             workspace and the last CTA to arrive on a tile sums them in the
-//             fixed order 0..splits-1 (deterministic, no atomics on data).
+//             k-tiles, one CTA per (tile, range), and the partial tiles are
+//             summed in the fixed order 0..splits-1 (deterministic).  For
+//             Swap-AB with at most 16 ranges the CTAs of one tile form a
+//             thread-block cluster and add their partials through distributed
+//             shared memory (no workspace); otherwise partials go to a caller
+//             workspace and the last CTA to arrive on a tile sums them.
 //
 // CTA = 6 warps: warp 0 issues TMA loads into a `stages`-deep shared-memory
 // ring (W tile 128x128 bytes + activation tile), warp 1 owns TMEM and issues
 // the MMAs from one thread, warps 2..5 (128 threads, one per TMEM lane) run
-// the epilogue.  Every mbarrier wait is bounded (see mbar_wait).
+// the epilogue.  Every mbarrier wait is bounded (see mbar_wait).  The Swap-AB
+// kernel is sized so that two CTAs fit on one SM: while one drains its
+// epilogue the other (or the next kernel's CTA, under programmatic dependent
+// launch) keeps the weight stream going.
 //
 // Block_FP8 (1x128 activation groups, 128x128 weight blocks): each 128-wide
 // k-tile is one scale group, so the MMA writes each k-tile's partial into its
@@ -26,17 +32,21 @@
 
 namespace qg {
 
+enum : int { kReduceNone = 0, kReduceCluster = 1, kReduceGlobal = 2 };
+constexpr int kMaxClusterSplits = 16;
+
 struct GemmArgs {
   int M, N, K;
   int64_t ldy;          // Y row stride (elements)
   int kt_total;         // ceil(K / 128)
   int splits;           // >= 1
   int stages;           // shared-memory ring depth
+  int reduce;           // kReduceNone / kReduceCluster / kReduceGlobal
   const float* s_a;     // [M] or [M][kt_total]
   const float* s_w;     // [N] or [ceil(N/128)][kt_total]
   __nv_bfloat16* Y;     // [M][ldy]
-  void* ws_part;        // [splits][M][N] fp32 (or int32) partials, when splits > 1
-  int* ws_count;        // one arrival counter per output tile, zero between launches
+  void* ws_part;        // kReduceGlobal: [splits][M][N] fp32 (or int32) partials
+  int* ws_count;        // kReduceGlobal: one arrival counter per output tile, zero between launches
   int32_t* debug_acc;   // [M][N] int32 accumulators (W8A8_INT8 only) or null
   uint64_t wait_ns;     // bound of every pipeline wait
   int force_timeout;    // test hook: the MMA thread first waits on a barrier nothing arrives on
@@ -79,29 +89,335 @@ __host__ __device__ constexpr size_t gemm_f8_smem_bytes(int stages) {
   return 1024 + static_cast<size_t>(stages) * TileShape<SWAP, MPAD>::kStageBytes + sizeof(Ctrl);
 }
 
-// Epilogue of one output element group, shared by the split and non-split paths.
 __device__ __forceinline__ void store_bf16(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-template <int FMT, bool SWAP, int MPAD>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
-  using TS = TileShape<SWAP, MPAD>;
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Split-K through distributed shared memory.  Every CTA of the cluster
+// (cluster rank == split index) holds its partial tile part[m][r]
+// (m < MPAD tokens, r < 128 weight rows) in its own shared memory.  CTA
+// `rank` owns rows [rank*R, rank*R + R), R = ceil(128 / S): for each of its
+// (m, r) with m < M it loads the S partials and adds them in the fixed order
+// 0..S-1, then calls store(m, r, sum).  The caller brackets this with
+// cluster_sync() (partials visible before; peers done reading after).
+template <typename T, typename Store>
+__device__ __forceinline__ void cluster_reduce_tile(const T* part, int rank, int S, int M, int tid, int nthreads,
+                                                    Store&& store) {
+  const int R = (kBN + S - 1) / S;
+  const int r0 = rank * R;
+  const int rn = min(kBN, r0 + R) - r0;
+  if (rn <= 0) return;
+  const uint32_t base = smem_u32(part);
+  for (int e = tid; e < rn * M; e += nthreads) {
+    const int r = r0 + e % rn, m = e / rn;
+    const uint32_t addr = base + static_cast<uint32_t>(m * kBN + r) * 4u;
+    T v[kMaxClusterSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxClusterSplits; ++s)
+      if (s < S) v[s] = ld_dsmem(dsmem_map(addr, static_cast<uint32_t>(s)), T{});
+    T sum = v[0];
+#pragma unroll
+    for (int s = 1; s < kMaxClusterSplits; ++s)
+      if (s < S) sum += v[s];
+    store(m, r, sum);
+  }
+}
+
+// ------------------------------------------------------------ Swap-AB --
+// One CTA per (128-row weight tile, K range).  D^T[128 x MPAD] in TMEM.
+template <int FMT, int MPAD>
+__global__ void __launch_bounds__(kThreads, 2)
+    gemm_f8_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
+  using TS = TileShape<true, MPAD>;
   constexpr bool BLOCK = (FMT == kFmtBlock);
-  constexpr int NBUF = BLOCK ? (SWAP ? 4 : 2) : 1;
-  // TMEM: Swap -> D^T is 128 lanes x MPAD cols per buffer. Standard -> D is
-  // 128 lanes x 128 cols per buffer, plus (Block) a 128-col running sum.
-  constexpr uint32_t kBufCols = TS::kMmaN;
-  constexpr uint32_t kTmemCols = pow2_cols(NBUF * kBufCols + ((BLOCK && !SWAP) ? kBN : 0));
-  static_assert(kTmemCols <= 512, "TMEM budget");
+  constexpr int NBUF = BLOCK ? 4 : 1;
+  constexpr uint32_t kTmemCols = pow2_cols(NBUF * MPAD);
+  static_assert(kTmemCols <= 256, "two CTAs per SM share the 512 TMEM columns");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + static_cast<size_t>(stages) * TS::kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x;
-  const int m_tile = SWAP ? 0 : blockIdx.z;
+  const int split = blockIdx.y;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
+  const int nk = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], 1);
+    }
+    mbar_init(&ctl->acc_full, 1);
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&ctl->tfull[b], 1);
+      mbar_init(&ctl->tempty[b], 128);
+    }
+    mbar_init(&ctl->never, 1);
+    ctl->last_flag = 0;
+    ctl->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmA);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  volatile int* abort_flag = &ctl->abort_flag;
+  float acc[MPAD];  // epilogue threads: weight row n of the tile x every token
+#pragma unroll
+  for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Starts at once (it needs no TMEM): the weights are static, so their
+    // first `pre` tiles are fetched before waiting on the kernel that
+    // produced the activations.
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+      const int w_row = n_tile * kBN;
+      const int pre = nk < stages ? nk : stages;
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
+        mbar_arrive_expect_tx(&ctl->full[i], TS::kStageBytes);
+        tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
+        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full[i], pol_a);
+      }
+      int issued = pre;
+      for (int i = pre; i < nk; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
+        if (!mbar_wait(&ctl->empty[s], ph ^ 1u, g.wait_ns) || *abort_flag) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + static_cast<size_t>(s) * TS::kStageBytes;
+        mbar_arrive_expect_tx(&ctl->full[s], TS::kStageBytes);
+        tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
+        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full[s], pol_a);
+        issued = i + 1;
+      }
+      // Every issued copy lands before this CTA may exit or reuse the ring.
+      for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+        mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+    }
+  } else {
+    if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tc_fence_before();
+    named_bar_sync(2, kThreads - 32);
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    if (warp == 1) {
+      // -------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc(128, MPAD, 0, 0);  // E4M3 x E4M3 -> F32
+        bool ok = true;
+        if (g.force_timeout) ok = mbar_wait(&ctl->never, 0, g.wait_ns);
+        for (int i = 0; ok && i < nk; ++i) {
+          const int s = i % stages;
+          const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
+          const int buf = BLOCK ? i % NBUF : 0;
+          if (BLOCK && i >= NBUF) {
+            if (!mbar_wait(&ctl->tempty[buf], static_cast<uint32_t>(i / NBUF - 1) & 1u, g.wait_ns)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!mbar_wait(&ctl->full[s], ph, g.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w_addr = smem_u32(smem + static_cast<size_t>(s) * TS::kStageBytes);
+          const uint32_t a_addr = w_addr + TS::kWBytes;
+          const uint32_t d = tmem + static_cast<uint32_t>(buf * MPAD);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk) {
+            const uint32_t accumulate = BLOCK ? (kk > 0) : (i > 0 || kk > 0);
+            mma_f8f6f4(d, sw128_kmajor_desc(w_addr + kk * 32), sw128_kmajor_desc(a_addr + kk * 32), idesc,
+                       accumulate);
+          }
+          tc_commit(&ctl->empty[s]);
+          if (BLOCK) tc_commit(&ctl->tfull[buf]);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          if (BLOCK)
+            for (int b = 0; b < NBUF; ++b) mbar_arrive(&ctl->tfull[b]);
+        }
+        // Completes once every MMA issued above has finished (also on abort).
+        tc_commit(&ctl->acc_full);
+      }
+    } else {
+      // ---------------------------------------------- epilogue: TMEM -> acc
+      pdl_wait();
+      const int q = warp & 3;  // TMEM lane quarter this warp may access
+      const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+      if constexpr (BLOCK) {
+        const int nb = n_tile;  // 128-row tile == weight block row
+        // lane l holds s_a of tokens l, l + 32, ... for the current k-tile
+        constexpr int kSaw = (MPAD + 31) / 32;
+        float sa_next[kSaw], sa_cur[kSaw];
+#pragma unroll
+        for (int j = 0; j < kSaw; ++j) {
+          const int t = lane + 32 * j;
+          sa_next[j] = t < g.M ? __ldg(g.s_a + static_cast<int64_t>(t) * g.kt_total + kb0) : 0.0f;
+        }
+        float sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
+        for (int i = 0; i < nk; ++i) {
+          const int buf = i % NBUF;
+#pragma unroll
+          for (int j = 0; j < kSaw; ++j) sa_cur[j] = sa_next[j];
+          const float sw_cur = sw_next;
+          if (i + 1 < nk) {
+#pragma unroll
+            for (int j = 0; j < kSaw; ++j) {
+              const int t = lane + 32 * j;
+              sa_next[j] = t < g.M ? __ldg(g.s_a + static_cast<int64_t>(t) * g.kt_total + kb0 + i + 1) : 0.0f;
+            }
+            sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
+          }
+          const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
+          if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          uint32_t v[MPAD];
+#pragma unroll
+          for (int c = 0; c < MPAD; c += 8) {
+            uint32_t t[8];
+            tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(buf * MPAD + c), t);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[c + j] = t[j];
+          }
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&ctl->tempty[buf]);
+#pragma unroll
+          for (int m = 0; m < MPAD; ++m) {
+            const float coef = __shfl_sync(0xffffffffu, sa_cur[m / 32], m & 31) * sw_cur;
+            acc[m] = fmaf(coef, __uint_as_float(v[m]), acc[m]);
+          }
+        }
+        // the MMA thread's final commit: all MMAs done before teardown
+        mbar_wait(&ctl->acc_full, 0, g.wait_ns);
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, g.wait_ns))) *abort_flag = 1;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < MPAD; c += 8) {
+          uint32_t t[8];
+          tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(c), t);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[c + j] = __uint_as_float(t[j]);
+        }
+        tmem_ld_wait();
+      }
+    }
+  }
+  // ------------------------------------------- all roles done: TMEM free
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(ctl->tmem_base, kTmemCols);
+  }
+  const bool abort = ctl->abort_flag != 0;  // stable after the barrier: uniform
+  const int row = (warp & 3) * 32 + lane;   // epilogue threads: weight row in the tile
+  const int n = n_tile * kBN + row;
+  const int et = threadIdx.x - 64;          // 0..127 for the epilogue warps
+  auto out = [&](int m, int nn, float sum) {
+    const float y = BLOCK ? sum : (sum * __ldg(g.s_a + m)) * __ldg(g.s_w + nn);
+    store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
+  };
+
+  if (g.reduce == kReduceCluster) {
+    // The ring is idle (every copy landed, every MMA finished): reuse it for
+    // this CTA's partial tile, [MPAD][128] fp32.
+    float* part = reinterpret_cast<float*>(smem);
+    if (warp >= 2) {
+#pragma unroll
+      for (int m = 0; m < MPAD; ++m) part[m * kBN + row] = acc[m];
+    }
+    cluster_sync();
+    if (warp >= 2 && !abort) {
+      cluster_reduce_tile(part, split, g.splits, g.M, et, 128, [&](int m, int r, float sum) {
+        const int nn = n_tile * kBN + r;
+        if (nn < g.N) out(m, nn, sum);
+      });
+    }
+    cluster_sync();
+  } else if (warp >= 2 && !abort) {
+    const bool n_ok = n < g.N;
+    if (g.reduce == kReduceNone) {
+      if (n_ok) {
+#pragma unroll
+        for (int m = 0; m < MPAD; ++m)
+          if (m < g.M) out(m, n, acc[m]);
+      }
+    } else {
+      float* part = static_cast<float*>(g.ws_part);
+      if (n_ok) {
+#pragma unroll
+        for (int m = 0; m < MPAD; ++m)
+          if (m < g.M) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = acc[m];
+      }
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (et == 0) {
+        const int old = atomicAdd(g.ws_count + n_tile, 1);
+        ctl->last_flag = (old == g.splits - 1);
+      }
+      named_bar_sync(1, 128);
+      if (ctl->last_flag) {
+        __threadfence();
+        if (n_ok) {
+          for (int m = 0; m < g.M; ++m) {
+            float sum = 0.0f;
+            for (int s = 0; s < g.splits; ++s) sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
+            out(m, n, sum);
+          }
+        }
+        if (et == 0) g.ws_count[n_tile] = 0;  // ready for the next launch
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------- Standard --
+// Tokens on the MMA M side: one CTA per (128-token tile, 128-row weight
+// tile, K range); D[128 tokens x 128 weight rows] in TMEM.  Serves M > 32
+// (and M <= 32 when the table picks it); Split-K uses the global workspace.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_f8_std_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
+  using TS = TileShape<false, 16>;
+  constexpr bool BLOCK = (FMT == kFmtBlock);
+  constexpr int NBUF = BLOCK ? 2 : 1;
+  // D is 128 lanes x 128 cols per buffer, plus (Block) a 128-col running sum.
+  constexpr uint32_t kBufCols = kBN;
+  constexpr uint32_t kTmemCols = pow2_cols(NBUF * kBufCols + (BLOCK ? kBN : 0));
+  static_assert(kTmemCols <= 512, "TMEM budget");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int stages = g.stages;
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + static_cast<size_t>(stages) * TS::kStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x;
+  const int m_tile = blockIdx.z;
   const int split = blockIdx.y;
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
@@ -141,8 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w_row = n_tile * kBN;
       const int a_row = m_tile * 128;
       const int pre = nk < stages ? nk : stages;
-      // The weights are static: their first `pre` tiles are fetched before
-      // waiting on the kernel that produced the activations.
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full[i], TS::kStageBytes);
@@ -167,14 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, a_row, &ctl->full[s], pol_a);
         issued = i + 1;
       }
-      // Every issued copy lands before this CTA may exit.
       for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
         mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(TS::kMmaM, TS::kMmaN, 0, 0);  // E4M3 x E4M3 -> F32
+      constexpr uint32_t idesc = make_idesc(128, kBN, 0, 0);  // E4M3 x E4M3 -> F32
       bool ok = true;
       if (g.force_timeout) ok = mbar_wait(&ctl->never, 0, g.wait_ns);
       for (int i = 0; ok && i < nk; ++i) {
@@ -182,241 +495,143 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
         const int buf = BLOCK ? i % NBUF : 0;
         if (BLOCK && i >= NBUF) {
-          if (!mbar_wait(&ctl->tempty[buf], static_cast<uint32_t>(i / NBUF - 1) & 1u, g.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&ctl->tempty[buf], static_cast<uint32_t>(i / NBUF - 1) & 1u, g.wait_ns)) {
+            ok = false;
+            break;
+          }
         }
-        if (!mbar_wait(&ctl->full[s], ph, g.wait_ns)) { ok = false; break; }
+        if (!mbar_wait(&ctl->full[s], ph, g.wait_ns)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t w_addr = smem_u32(smem + static_cast<size_t>(s) * TS::kStageBytes);
         const uint32_t a_addr = w_addr + TS::kWBytes;
-        const uint32_t a_op = SWAP ? w_addr : a_addr;   // MMA A operand (M side, 128 rows)
-        const uint32_t b_op = SWAP ? a_addr : w_addr;   // MMA B operand (N side)
         const uint32_t d = tmem + static_cast<uint32_t>(buf) * kBufCols;
 #pragma unroll
         for (int kk = 0; kk < kBK / 32; ++kk) {
           const uint32_t accumulate = BLOCK ? (kk > 0) : (i > 0 || kk > 0);
-          mma_f8f6f4(d, sw128_kmajor_desc(a_op + kk * 32), sw128_kmajor_desc(b_op + kk * 32), idesc, accumulate);
+          mma_f8f6f4(d, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(w_addr + kk * 32), idesc, accumulate);
         }
         tc_commit(&ctl->empty[s]);
         if (BLOCK) tc_commit(&ctl->tfull[buf]);
       }
       if (!ok) {
         *abort_flag = 1;
-        // release any waiting epilogue thread; it will see abort_flag
-        if (BLOCK) for (int b = 0; b < NBUF; ++b) mbar_arrive(&ctl->tfull[b]);
+        if (BLOCK)
+          for (int b = 0; b < NBUF; ++b) mbar_arrive(&ctl->tfull[b]);
       }
-      // Completes once every MMA issued above has finished (also on abort).
       tc_commit(&ctl->acc_full);
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // TMEM lane = token row m, columns = weight rows n.
     pdl_wait();
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int et = threadIdx.x - 64;  // 0..127
-    if constexpr (SWAP) {
-      const int n = n_tile * kBN + q * 32 + lane;
-      float acc[MPAD];
-      if constexpr (BLOCK) {
-#pragma unroll
-        for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
-        const int nb = n_tile;  // 128-row tile == weight block row
-        float sa_next = lane < g.M ? __ldg(g.s_a + static_cast<int64_t>(lane) * g.kt_total + kb0) : 0.0f;
-        float sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
-        for (int i = 0; i < nk; ++i) {
-          const int buf = i % NBUF;
-          const float sa_cur = sa_next, sw_cur = sw_next;
-          if (i + 1 < nk) {
-            sa_next = lane < g.M ? __ldg(g.s_a + static_cast<int64_t>(lane) * g.kt_total + kb0 + i + 1) : 0.0f;
-            sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
-          }
-          const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
-          if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          uint32_t v[MPAD];
-#pragma unroll
-          for (int c = 0; c < MPAD; c += 8) {
-            uint32_t t[8];
-            tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c), t);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[c + j] = t[j];
-          }
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&ctl->tempty[buf]);
-#pragma unroll
-          for (int m = 0; m < MPAD; ++m) {
-            const float coef = __shfl_sync(0xffffffffu, sa_cur, m) * sw_cur;
-            acc[m] = fmaf(coef, __uint_as_float(v[m]), acc[m]);
-          }
+    const int m = m_tile * 128 + q * 32 + lane;
+    const bool m_ok = m < g.M;
+    const uint32_t run_col = NBUF * kBufCols;  // Block: running sum columns
+    if constexpr (BLOCK) {
+      const int nb = n_tile;
+      for (int i = 0; i < nk; ++i) {
+        const int buf = i % NBUF;
+        const float sa = m_ok ? __ldg(g.s_a + static_cast<int64_t>(m) * g.kt_total + kb0 + i) : 0.0f;
+        const float coef = sa * __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i);
+        const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
+        if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
+          *abort_flag = 1;
+          break;
         }
-      } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, g.wait_ns))) *abort_flag = 1;
         tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kBN; c += 8) {
+          uint32_t p[8], r[8];
+          tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c), p);
+          if (i > 0) tmem_ld_x8(tmem + lane_base + run_col + c, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < MPAD; c += 8) {
-          uint32_t t[8];
-          tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(c), t);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[c + j] = __uint_as_float(t[j]);
+          for (int j = 0; j < 8; ++j) {
+            const float prev = i > 0 ? __uint_as_float(r[j]) : 0.0f;
+            r[j] = __float_as_uint(fmaf(coef, __uint_as_float(p[j]), prev));
+          }
+          tmem_st_x8(tmem + lane_base + run_col + c, r);
         }
-        tmem_ld_wait();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ctl->tempty[buf]);
       }
-      if (BLOCK) {
-        // the MMA thread's final commit: all MMAs done before teardown
-        mbar_wait(&ctl->acc_full, 0, g.wait_ns);
-      }
-      const bool abort = __any_sync(0xffffffffu, *abort_flag != 0);
-      const bool n_ok = n < g.N;
-      const float sw = (!BLOCK && n_ok) ? __ldg(g.s_w + n) : 1.0f;
-      if (!abort) {
-        if (g.splits == 1) {
-          if (n_ok) {
-#pragma unroll
-            for (int m = 0; m < MPAD; ++m)
-              if (m < g.M) {
-                const float y = BLOCK ? acc[m] : (acc[m] * __ldg(g.s_a + m)) * sw;
-                store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n, y);
-              }
-          }
-        } else {
-          float* part = static_cast<float*>(g.ws_part);
-          if (n_ok) {
-#pragma unroll
-            for (int m = 0; m < MPAD; ++m)
-              if (m < g.M) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = acc[m];
-          }
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (et == 0) {
-            const int old = atomicAdd(g.ws_count + n_tile, 1);
-            ctl->last_flag = (old == g.splits - 1);
-          }
-          named_bar_sync(1, 128);
-          if (ctl->last_flag) {
-            __threadfence();
-            if (n_ok) {
-#pragma unroll
-              for (int m = 0; m < MPAD; ++m)
-                if (m < g.M) {
-                  float sum = 0.0f;
-                  for (int s = 0; s < g.splits; ++s)
-                    sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
-                  const float y = BLOCK ? sum : (sum * __ldg(g.s_a + m)) * sw;
-                  store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n, y);
-                }
-            }
-            if (et == 0) g.ws_count[n_tile] = 0;  // ready for the next launch
-          }
-        }
-      }
+      mbar_wait(&ctl->acc_full, 0, g.wait_ns);
     } else {
-      // Standard: TMEM lane = token row m, columns = weight rows n.
-      const int m = m_tile * 128 + q * 32 + lane;
-      const bool m_ok = m < g.M;
-      const uint32_t run_col = NBUF * kBufCols;  // Block: running sum columns
-      if constexpr (BLOCK) {
-        const int nb = n_tile;
-        for (int i = 0; i < nk; ++i) {
-          const int buf = i % NBUF;
-          const float sa = m_ok ? __ldg(g.s_a + static_cast<int64_t>(m) * g.kt_total + kb0 + i) : 0.0f;
-          const float coef = sa * __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i);
-          const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
-          if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, g.wait_ns))) *abort_flag = 1;
+    }
+    tc_fence_after();
+    const bool abort = __any_sync(0xffffffffu, *abort_flag != 0);
+    const float sa = (!BLOCK && m_ok) ? __ldg(g.s_a + m) : 1.0f;
+    const uint32_t src_col = BLOCK ? run_col : 0;
+    float* part = static_cast<float*>(g.ws_part);
 #pragma unroll 1
-          for (int c = 0; c < kBN; c += 8) {
-            uint32_t p[8], r[8];
-            tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c), p);
-            if (i > 0) tmem_ld_x8(tmem + lane_base + run_col + c, r);
-            tmem_ld_wait();
+    for (int c = 0; c < kBN && !abort; c += 8) {
+      uint32_t t[8];
+      tmem_ld_x8(tmem + lane_base + src_col + c, t);
+      tmem_ld_wait();
+      const int n0 = n_tile * kBN + c;
+      if (!m_ok) continue;
+      if (g.splits == 1) {
+        if (n0 + 8 <= g.N) {
+          uint32_t packed[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float prev = i > 0 ? __uint_as_float(r[j]) : 0.0f;
-              r[j] = __float_as_uint(fmaf(coef, __uint_as_float(p[j]), prev));
+          for (int j = 0; j < 4; ++j) {
+            float y0 = __uint_as_float(t[2 * j]), y1 = __uint_as_float(t[2 * j + 1]);
+            if (!BLOCK) {
+              y0 = (y0 * sa) * __ldg(g.s_w + n0 + 2 * j);
+              y1 = (y1 * sa) * __ldg(g.s_w + n0 + 2 * j + 1);
             }
-            tmem_st_x8(tmem + lane_base + run_col + c, r);
+            __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+            packed[j] = *reinterpret_cast<uint32_t*>(&h);
           }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&ctl->tempty[buf]);
-        }
-        mbar_wait(&ctl->acc_full, 0, g.wait_ns);
-      } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, g.wait_ns))) *abort_flag = 1;
-      }
-      tc_fence_after();
-      const bool abort = __any_sync(0xffffffffu, *abort_flag != 0);
-      const float sa = (!BLOCK && m_ok) ? __ldg(g.s_a + m) : 1.0f;
-      const uint32_t src_col = BLOCK ? run_col : 0;
-      float* part = static_cast<float*>(g.ws_part);
-#pragma unroll 1
-      for (int c = 0; c < kBN && !abort; c += 8) {
-        uint32_t t[8];
-        tmem_ld_x8(tmem + lane_base + src_col + c, t);
-        tmem_ld_wait();
-        const int n0 = n_tile * kBN + c;
-        if (!m_ok) continue;
-        if (g.splits == 1) {
-          if (n0 + 8 <= g.N) {
-            uint32_t packed[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float y0 = __uint_as_float(t[2 * j]), y1 = __uint_as_float(t[2 * j + 1]);
-              if (!BLOCK) {
-                y0 = (y0 * sa) * __ldg(g.s_w + n0 + 2 * j);
-                y1 = (y1 * sa) * __ldg(g.s_w + n0 + 2 * j + 1);
-              }
-              __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
-              packed[j] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            __nv_bfloat16* dst = g.Y + static_cast<int64_t>(m) * g.ldy + n0;
-            if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-              *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) *reinterpret_cast<uint32_t*>(dst + 2 * j) = packed[j];
-            }
+          __nv_bfloat16* dst = g.Y + static_cast<int64_t>(m) * g.ldy + n0;
+          if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           } else {
-            for (int j = 0; j < 8 && n0 + j < g.N; ++j) {
-              float y = __uint_as_float(t[j]);
-              if (!BLOCK) y = (y * sa) * __ldg(g.s_w + n0 + j);
-              store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n0 + j, y);
-            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) *reinterpret_cast<uint32_t*>(dst + 2 * j) = packed[j];
           }
         } else {
-          for (int j = 0; j < 8 && n0 + j < g.N; ++j)
-            part[(static_cast<int64_t>(split) * g.M + m) * g.N + n0 + j] = __uint_as_float(t[j]);
-        }
-      }
-      if (g.splits > 1 && !abort) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        const int tile_id = m_tile * gridDim.x + n_tile;
-        if (et == 0) {
-          const int old = atomicAdd(g.ws_count + tile_id, 1);
-          ctl->last_flag = (old == g.splits - 1);
-        }
-        named_bar_sync(1, 128);
-        if (ctl->last_flag) {
-          __threadfence();
-          if (m_ok) {
-            for (int c = 0; c < kBN; ++c) {
-              const int n = n_tile * kBN + c;
-              if (n >= g.N) break;
-              float sum = 0.0f;
-              for (int s = 0; s < g.splits; ++s) sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
-              const float y = BLOCK ? sum : (sum * sa) * __ldg(g.s_w + n);
-              store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n, y);
-            }
+          for (int j = 0; j < 8 && n0 + j < g.N; ++j) {
+            float y = __uint_as_float(t[j]);
+            if (!BLOCK) y = (y * sa) * __ldg(g.s_w + n0 + j);
+            store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n0 + j, y);
           }
-          if (et == 0) g.ws_count[tile_id] = 0;
         }
+      } else {
+        for (int j = 0; j < 8 && n0 + j < g.N; ++j)
+          part[(static_cast<int64_t>(split) * g.M + m) * g.N + n0 + j] = __uint_as_float(t[j]);
+      }
+    }
+    if (g.splits > 1 && !abort) {
+      __threadfence();
+      named_bar_sync(1, 128);
+      const int tile_id = m_tile * gridDim.x + n_tile;
+      if (et == 0) {
+        const int old = atomicAdd(g.ws_count + tile_id, 1);
+        ctl->last_flag = (old == g.splits - 1);
+      }
+      named_bar_sync(1, 128);
+      if (ctl->last_flag) {
+        __threadfence();
+        if (m_ok) {
+          for (int c = 0; c < kBN; ++c) {
+            const int n = n_tile * kBN + c;
+            if (n >= g.N) break;
+            float sum = 0.0f;
+            for (int s = 0; s < g.splits; ++s) sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
+            const float y = BLOCK ? sum : (sum * sa) * __ldg(g.s_w + n);
+            store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n, y);
+          }
+        }
+        if (et == 0) g.ws_count[tile_id] = 0;
       }
     }
   }

@@ -11,25 +11,33 @@
 // over at most 1024 K stays below 2^24, so each 1024-K segment accumulates
 // exactly in fp32; segments are converted to int32 and summed in registers.
 //
-// Pipeline per CTA (one 128-row weight tile x one K range):
+// Pipeline per CTA (one 128-row weight tile x one K range), sized so that two
+// CTAs share an SM (at most 256 TMEM columns and ~113 KB of shared memory):
 //   warp 0      TMA: int8 W tile (128 x 128 B) + int8 activation tile into a
 //               `stages`-deep shared-memory ring;
-//   warps 2..5  converters, one thread per weight row (= TMEM lane): the
-//               weight row -> fp16 pairs -> tcgen05.st into a TMEM operand
-//               buffer (the MMA A operand lives in TMEM, so the widened
-//               weights never touch shared memory); the activation tile ->
-//               fp16 into a 128-byte-swizzled shared buffer (MMA B operand);
-//               they also drain finished accumulator segments into int32 and
-//               run the epilogue;
+//   warps 2..9  converters: warp w owns TMEM lane quarter w % 4 (weight rows
+//               32*(w%4) .. +31) and half (w-2)/4 of each 128-byte k-tile row;
+//               each thread widens its 64 weight bytes to fp16 and writes them
+//               with tcgen05.st into a TMEM operand buffer (the MMA A operand
+//               lives in TMEM, so the widened weights never touch shared
+//               memory); together they widen the activation tile into a
+//               128-byte-swizzled shared buffer (MMA B operand); they drain
+//               finished accumulator segments into int32 (warp w takes token
+//               half (w-2)/4) and run the epilogue;
 //   warp 1      one thread issues 8 MMAs (K = 16 each) per k-tile.
+// Split-K reduces through distributed shared memory across the cluster of
+// a tile's CTAs (up to 16 ranges) or through the caller workspace, exactly
+// as the FP8 kernel does, in int32.
 #pragma once
 #include "common.cuh"
 #include "gemm_f8.cuh"
 
 namespace qg {
 
-constexpr int kI8Threads = 192;
-constexpr int kI8OpBufs = 4;        // TMEM/shared operand buffers in flight
+constexpr int kI8ConvWarps = 8;
+constexpr int kI8ConvThreads = 32 * kI8ConvWarps;  // 256
+constexpr int kI8Threads = 64 + kI8ConvThreads;    // 320
+constexpr int kI8OpBufs = 3;        // TMEM/shared operand buffers in flight
 constexpr int kI8SegTiles = 8;      // k-tiles (of 128) per exact fp32 segment: 1024 K
 
 struct alignas(8) CtrlI8 {
@@ -54,6 +62,7 @@ struct I8Shape {
   static constexpr uint32_t kOpBBytes = MPAD * 256;        // fp16 activations: 2 swizzle atoms of 64 K
   static constexpr uint32_t kACols = 64;                   // 128 fp16 per row = 64 TMEM columns
   static constexpr uint32_t kDCols = MPAD;
+  static constexpr int kHalf = MPAD / 2;                   // tokens drained per converter warp
   static constexpr uint32_t kTmemCols = pow2_cols(kI8OpBufs * kACols + 2 * kDCols);
 };
 
@@ -84,11 +93,12 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t r, uint32_t c) {
 }
 
 template <int MPAD>
-__global__ void __launch_bounds__(kI8Threads, 1)
+__global__ void __launch_bounds__(kI8Threads, 2)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = I8Shape<MPAD>;
+  constexpr int kHalf = S::kHalf;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
   uint8_t* opb = smem + static_cast<size_t>(stages) * S::kStageBytes;  // fp16 activation buffers
   CtrlI8* ctl = reinterpret_cast<CtrlI8*>(opb + kI8OpBufs * S::kOpBBytes);
@@ -103,15 +113,15 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
-      mbar_init(&ctl->empty[i], 128);
+      mbar_init(&ctl->empty[i], kI8ConvWarps);
     }
     for (int b = 0; b < kI8OpBufs; ++b) {
-      mbar_init(&ctl->op_full[b], 128);
+      mbar_init(&ctl->op_full[b], kI8ConvWarps);
       mbar_init(&ctl->op_empty[b], 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&ctl->d_full[d], 1);
-      mbar_init(&ctl->d_empty[d], 128);
+      mbar_init(&ctl->d_empty[d], kI8ConvWarps);
     }
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->done, 1);
@@ -123,17 +133,19 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmA);
   }
-  if (warp == 1) tmem_alloc(&ctl->tmem_base, S::kTmemCols);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl->tmem_base;
   pdl_launch_dependents();
-  const uint32_t tmem_a = tmem;                                   // kI8OpBufs x 64 columns
-  const uint32_t tmem_d = tmem + kI8OpBufs * S::kACols;           // 2 x MPAD columns
   volatile int* abort_flag = &ctl->abort_flag;
+  // converter threads: weight row `row` of the tile x tokens [h*kHalf, h*kHalf + kHalf)
+  int32_t iacc[kHalf];
+#pragma unroll
+  for (int m = 0; m < kHalf; ++m) iacc[m] = 0;
+  const int cw = warp - 2;        // converter warp 0..7 (negative for warps 0, 1)
+  const int h = cw >> 2;          // K half of the weight row / token half of the accumulator
+  const uint32_t row = (warp & 3) * 32u + lane;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       const int w_row = n_tile * kBN;
@@ -165,169 +177,209 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
         mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(128, MPAD, 0, 0);  // F16 x F16 -> F32
+  } else {
+    if (warp == 1) tmem_alloc(&ctl->tmem_base, S::kTmemCols);
+    tc_fence_before();
+    named_bar_sync(2, kI8Threads - 32);
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t tmem_a = tmem;                                   // kI8OpBufs x 64 columns
+    const uint32_t tmem_d = tmem + kI8OpBufs * S::kACols;           // 2 x MPAD columns
+    if (warp == 1) {
+      // -------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc(128, MPAD, 0, 0);  // F16 x F16 -> F32
+        bool ok = true;
+        if (g.force_timeout) ok = mbar_wait(&ctl->never, 0, g.wait_ns);
+        for (int i = 0; ok && i < nk; ++i) {
+          const int seg = i / kI8SegTiles, d = seg & 1, buf = i % kI8OpBufs;
+          const bool seg_start = (i % kI8SegTiles) == 0;
+          if (seg_start && seg >= 2 &&
+              !mbar_wait(&ctl->d_empty[d], static_cast<uint32_t>((seg - 2) / 2) & 1u, g.wait_ns)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&ctl->op_full[buf], static_cast<uint32_t>(i / kI8OpBufs) & 1u, g.wait_ns) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_base = smem_u32(opb + buf * S::kOpBBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t b_addr = b_base + (kk >> 2) * (MPAD * 128) + (kk & 3) * 32;
+            mma_f16_ts(tmem_d + d * S::kDCols, tmem_a + buf * S::kACols + kk * 8, sw128_kmajor_desc(b_addr), idesc,
+                       (!seg_start || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&ctl->op_empty[buf]);
+          if ((i % kI8SegTiles) == kI8SegTiles - 1 || i == nk - 1) tc_commit(&ctl->d_full[d]);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          mbar_arrive(&ctl->d_full[0]);
+          mbar_arrive(&ctl->d_full[1]);
+        }
+        tc_commit(&ctl->done);  // all issued MMAs complete
+      }
+    } else {
+      // ------------------------------------------------------- converters
+      const uint32_t lane_base = ((warp & 3) * 32u) << 16;
+      const int ct = threadIdx.x - 64;  // 0..255
       bool ok = true;
-      if (g.force_timeout) ok = mbar_wait(&ctl->never, 0, g.wait_ns);
-      for (int i = 0; ok && i < nk; ++i) {
-        const int seg = i / kI8SegTiles, d = seg & 1, buf = i % kI8OpBufs;
-        const bool seg_start = (i % kI8SegTiles) == 0;
-        if (seg_start && seg >= 2 &&
-            !mbar_wait(&ctl->d_empty[d], static_cast<uint32_t>((seg - 2) / 2) & 1u, g.wait_ns)) { ok = false; break; }
-        if (!mbar_wait(&ctl->op_full[buf], static_cast<uint32_t>(i / kI8OpBufs) & 1u, g.wait_ns) || *abort_flag) {
+
+      auto drain = [&](int seg) -> bool {
+        const int d = seg & 1;
+        bool w = mbar_wait(&ctl->d_full[d], static_cast<uint32_t>(seg / 2) & 1u, g.wait_ns);
+        if (!__all_sync(0xffffffffu, w && !*abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 8) {
+          uint32_t t[8];
+          tmem_ld_x8(tmem_d + lane_base + d * S::kDCols + h * kHalf + c, t);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) iacc[c + j] += __float2int_rn(__uint_as_float(t[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->d_empty[d]);
+        return true;
+      };
+
+      pdl_wait();
+      for (int i = 0; i < nk; ++i) {
+        const int seg = i / kI8SegTiles, buf = i % kI8OpBufs, s = i % stages;
+        if ((i % kI8SegTiles) == 0 && seg >= 2 && !drain(seg - 2)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t b_base = smem_u32(opb + buf * S::kOpBBytes);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t b_addr = b_base + (kk >> 2) * (MPAD * 128) + (kk & 3) * 32;
-          mma_f16_ts(tmem_d + d * S::kDCols, tmem_a + buf * S::kACols + kk * 8, sw128_kmajor_desc(b_addr), idesc,
-                     (!seg_start || kk > 0) ? 1u : 0u);
+        bool w = mbar_wait(&ctl->full[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns);
+        if (i >= kI8OpBufs)
+          w = w && mbar_wait(&ctl->op_empty[buf], static_cast<uint32_t>(i / kI8OpBufs - 1) & 1u, g.wait_ns);
+        if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
+          ok = false;
+          break;
         }
-        tc_commit(&ctl->op_empty[buf]);
-        if ((i % kI8SegTiles) == kI8SegTiles - 1 || i == nk - 1) tc_commit(&ctl->d_full[d]);
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        mbar_arrive(&ctl->d_full[0]);
-        mbar_arrive(&ctl->d_full[1]);
-      }
-      tc_commit(&ctl->done);  // all issued MMAs complete
-    }
-  } else {
-    // ------------------------------------------------ converters + epilogue
-    const int q = warp & 3;
-    const int et = threadIdx.x - 64;           // 0..127
-    const uint32_t row = q * 32 + lane;        // weight row in tile == TMEM lane
-    const uint32_t lane_base = (q * 32u) << 16;
-    int32_t iacc[MPAD];
+        const uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
+        // this thread's 64 weight bytes -> fp16 -> TMEM operand buffer
 #pragma unroll
-    for (int m = 0; m < MPAD; ++m) iacc[m] = 0;
-    bool ok = true;
-
-    auto drain = [&](int seg) -> bool {
-      const int d = seg & 1;
-      bool w = mbar_wait(&ctl->d_full[d], static_cast<uint32_t>(seg / 2) & 1u, g.wait_ns);
-      if (!__all_sync(0xffffffffu, w && !*abort_flag)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < MPAD; c += 8) {
-        uint32_t t[8];
-        tmem_ld_x8(tmem_d + lane_base + d * S::kDCols + c, t);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) iacc[c + j] += __float2int_rn(__uint_as_float(t[j]));
-      }
-      tc_fence_before();
-      mbar_arrive(&ctl->d_empty[d]);
-      return true;
-    };
-
-    pdl_wait();
-    for (int i = 0; i < nk; ++i) {
-      const int seg = i / kI8SegTiles, buf = i % kI8OpBufs, s = i % stages;
-      if ((i % kI8SegTiles) == 0 && seg >= 2 && !drain(seg - 2)) { ok = false; break; }
-      bool w = mbar_wait(&ctl->full[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns);
-      if (i >= kI8OpBufs) w = w && mbar_wait(&ctl->op_empty[buf], static_cast<uint32_t>(i / kI8OpBufs - 1) & 1u, g.wait_ns);
-      if (!__all_sync(0xffffffffu, w && !*abort_flag)) { ok = false; break; }
-      const uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
-      // weight row -> fp16 -> TMEM operand buffer
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(st + sw128_chunk(row, c));
-        uint32_t o[8];
-        int8x4_to_f16x4(v.x, o[0], o[1]);
-        int8x4_to_f16x4(v.y, o[2], o[3]);
-        int8x4_to_f16x4(v.z, o[4], o[5]);
-        int8x4_to_f16x4(v.w, o[6], o[7]);
-        tmem_st_x8(tmem_a + lane_base + buf * S::kACols + c * 8, o);
-      }
-      // activation tile -> fp16, swizzled K-major B operand (2 atoms of 64 K)
-      uint8_t* ob = opb + buf * S::kOpBBytes;
-      for (int piece = et; piece < MPAD * 4; piece += 128) {
-        const uint32_t r = piece >> 2, p = piece & 3;   // row, 32-element quarter of the 128 K
-        const uint8_t* src = st + S::kWBytes;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p));
-        const uint4 v1 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p + 1));
-        uint32_t o[16];
-        int8x4_to_f16x4(v0.x, o[0], o[1]);
-        int8x4_to_f16x4(v0.y, o[2], o[3]);
-        int8x4_to_f16x4(v0.z, o[4], o[5]);
-        int8x4_to_f16x4(v0.w, o[6], o[7]);
-        int8x4_to_f16x4(v1.x, o[8], o[9]);
-        int8x4_to_f16x4(v1.y, o[10], o[11]);
-        int8x4_to_f16x4(v1.z, o[12], o[13]);
-        int8x4_to_f16x4(v1.w, o[14], o[15]);
-        uint8_t* atom = ob + (p >> 1) * (MPAD * 128);
-        const uint32_t c0 = (p & 1) * 4;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(atom + sw128_chunk(r, c0 + j)) =
-              make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-      }
-      tmem_st_wait();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      mbar_arrive(&ctl->op_full[buf]);
-      mbar_arrive(&ctl->empty[s]);
-    }
-    if (ok) {
-      for (int seg = nseg > 2 ? nseg - 2 : 0; seg < nseg; ++seg)
-        if (!drain(seg)) { ok = false; break; }
-    }
-    if (!ok) *abort_flag = 1;
-    mbar_wait(&ctl->done, 0, g.wait_ns);
-    const bool abort = *abort_flag != 0;
-
-    // ---------------------------------------------------------- epilogue
-    const int n = n_tile * kBN + static_cast<int>(row);
-    const bool n_ok = n < g.N;
-    if (!abort) {
-      const float sw = n_ok ? __ldg(g.s_w + n) : 0.0f;
-      auto finish = [&](int m, int32_t acc) {
-        if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m) * g.N + n] = acc;
-        const float y = (static_cast<float>(acc) * __ldg(g.s_a + m)) * sw;
-        store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + n, y);
-      };
-      if (g.splits == 1) {
-        if (n_ok) {
-#pragma unroll
-          for (int m = 0; m < MPAD; ++m)
-            if (m < g.M) finish(m, iacc[m]);
+        for (int c = 4 * h; c < 4 * h + 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(st + sw128_chunk(row, c));
+          uint32_t o[8];
+          int8x4_to_f16x4(v.x, o[0], o[1]);
+          int8x4_to_f16x4(v.y, o[2], o[3]);
+          int8x4_to_f16x4(v.z, o[4], o[5]);
+          int8x4_to_f16x4(v.w, o[6], o[7]);
+          tmem_st_x8(tmem_a + lane_base + buf * S::kACols + c * 8, o);
         }
-      } else {
-        int32_t* part = static_cast<int32_t*>(g.ws_part);
-        if (n_ok) {
+        // activation tile -> fp16, swizzled K-major B operand (2 atoms of 64 K)
+        uint8_t* ob = opb + buf * S::kOpBBytes;
+        for (int piece = ct; piece < MPAD * 4; piece += kI8ConvThreads) {
+          const uint32_t r = piece >> 2, p = piece & 3;  // row, 32-element quarter of the 128 K
+          const uint8_t* src = st + S::kWBytes;
+          const uint4 v0 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p + 1));
+          uint32_t o[16];
+          int8x4_to_f16x4(v0.x, o[0], o[1]);
+          int8x4_to_f16x4(v0.y, o[2], o[3]);
+          int8x4_to_f16x4(v0.z, o[4], o[5]);
+          int8x4_to_f16x4(v0.w, o[6], o[7]);
+          int8x4_to_f16x4(v1.x, o[8], o[9]);
+          int8x4_to_f16x4(v1.y, o[10], o[11]);
+          int8x4_to_f16x4(v1.z, o[12], o[13]);
+          int8x4_to_f16x4(v1.w, o[14], o[15]);
+          uint8_t* atom = ob + (p >> 1) * (MPAD * 128);
+          const uint32_t c0 = (p & 1) * 4;
 #pragma unroll
-          for (int m = 0; m < MPAD; ++m)
-            if (m < g.M) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = iacc[m];
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(atom + sw128_chunk(r, c0 + j)) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (et == 0) ctl->last_flag = (atomicAdd(g.ws_count + n_tile, 1) == g.splits - 1);
-        named_bar_sync(1, 128);
-        if (ctl->last_flag) {
-          __threadfence();
-          if (n_ok) {
-            for (int m = 0; m < g.M; ++m) {
-              int32_t sum = 0;
-              for (int s = 0; s < g.splits; ++s) sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
-              finish(m, sum);
-            }
+        tmem_st_wait();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctl->op_full[buf]);
+          mbar_arrive(&ctl->empty[s]);
+        }
+      }
+      if (ok) {
+        for (int seg = nseg > 2 ? nseg - 2 : 0; seg < nseg; ++seg)
+          if (!drain(seg)) {
+            ok = false;
+            break;
           }
-          if (et == 0) g.ws_count[n_tile] = 0;
-        }
       }
+      if (!ok) *abort_flag = 1;
+      mbar_wait(&ctl->done, 0, g.wait_ns);
     }
   }
+  // ------------------------------------------- all roles done: TMEM free
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, S::kTmemCols);
+    tmem_dealloc(ctl->tmem_base, S::kTmemCols);
+  }
+  const bool abort = ctl->abort_flag != 0;  // stable after the barrier: uniform
+  const int n = n_tile * kBN + static_cast<int>(row);
+  const int ct = threadIdx.x - 64;
+  auto finish = [&](int m, int nn, int32_t acc) {
+    if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m) * g.N + nn] = acc;
+    const float y = (static_cast<float>(acc) * __ldg(g.s_a + m)) * __ldg(g.s_w + nn);
+    store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
+  };
+
+  if (g.reduce == kReduceCluster) {
+    int32_t* part = reinterpret_cast<int32_t*>(smem);  // [MPAD][128] in the idle ring
+    if (warp >= 2) {
+#pragma unroll
+      for (int j = 0; j < kHalf; ++j) part[(h * kHalf + j) * kBN + row] = iacc[j];
+    }
+    cluster_sync();
+    if (warp >= 2 && !abort) {
+      cluster_reduce_tile(part, split, g.splits, g.M, ct, kI8ConvThreads, [&](int m, int r, int32_t sum) {
+        const int nn = n_tile * kBN + r;
+        if (nn < g.N) finish(m, nn, sum);
+      });
+    }
+    cluster_sync();
+  } else if (warp >= 2 && !abort) {
+    const bool n_ok = n < g.N;
+    if (g.reduce == kReduceNone) {
+      if (n_ok) {
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j)
+          if (h * kHalf + j < g.M) finish(h * kHalf + j, n, iacc[j]);
+      }
+    } else {
+      int32_t* part = static_cast<int32_t*>(g.ws_part);
+      if (n_ok) {
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j) {
+          const int m = h * kHalf + j;
+          if (m < g.M) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = iacc[j];
+        }
+      }
+      __threadfence();
+      named_bar_sync(1, kI8ConvThreads);
+      if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + n_tile, 1) == g.splits - 1);
+      named_bar_sync(1, kI8ConvThreads);
+      if (ctl->last_flag) {
+        __threadfence();
+        if (n_ok) {
+          for (int j = 0; j < kHalf; ++j) {
+            const int m = h * kHalf + j;
+            if (m >= g.M) break;
+            int32_t sum = 0;
+            for (int s = 0; s < g.splits; ++s) sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
+            finish(m, n, sum);
+          }
+        }
+        if (ct == 0) g.ws_count[n_tile] = 0;
+      }
+    }
   }
 }
 

@@ -86,7 +86,9 @@ int make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int64_t
 // -------------------------------------------------------------- launching
 struct DevInfo {
   int sms = 0;
-  size_t smem_optin = 0;
+  size_t smem_optin = 0;     // largest dynamic shared memory one CTA may opt into
+  size_t smem_per_sm = 0;    // shared memory of one SM
+  size_t smem_reserved = 0;  // shared memory the system reserves per CTA
 };
 DevInfo dev_info() {
   static DevInfo cache[64];
@@ -98,32 +100,57 @@ DevInfo dev_info() {
     if (cudaGetDeviceProperties(&p, d) == cudaSuccess) {
       cache[d].sms = p.multiProcessorCount;
       cache[d].smem_optin = p.sharedMemPerBlockOptin;
+      cache[d].smem_per_sm = p.sharedMemPerMultiprocessor;
+      cache[d].smem_reserved = p.reservedSharedMemPerBlock;
     } else {
       cache[d].sms = 148;
       cache[d].smem_optin = 232448;
+      cache[d].smem_per_sm = 233472;
+      cache[d].smem_reserved = 1024;
     }
   }
   return cache[d];
 }
 
+// Dynamic shared memory one CTA may use so that two CTAs share an SM.
+size_t two_per_sm_smem() {
+  const DevInfo d = dev_info();
+  return (d.smem_per_sm - 2 * d.smem_reserved) / 2;
+}
+
+// Launch with the library's launch flags; cluster_y > 1 groups that many
+// consecutive blockIdx.y into one thread-block cluster.
 template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                   Args&&... args) {
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           unsigned cluster_y, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int n = 0;
   if (g_launch_flags & QG_LAUNCH_PDL) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
+  if (cluster_y > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = cluster_y;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args&&... args) {
+  return launch_cluster(kernel, grid, block, smem, stream, 1u, std::forward<Args>(args)...);
 }
 
 template <typename K>
@@ -138,6 +165,7 @@ struct Plan {
   bool swap = false;
   int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64
   int n_tiles = 0, m_tiles = 0, kt = 0, splits = 1;
+  int reduce = qg::kReduceNone;  // how split partials are summed
 };
 
 int64_t ws_counter_bytes(int64_t tiles) { return cdiv(tiles * 4, 256) * 256; }
@@ -163,60 +191,88 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   if (fmt == QG_W8A8_INT8 && !p->swap)
     return fail(QG_ERR_UNSUPPORTED_SHAPE, "W8A8_INT8 runs the Swap-AB variants (M <= 64)");
   p->splits = split_k;
+  // Swap-AB splits of one tile reduce inside a thread-block cluster (no
+  // workspace) when there are at most 16 of them; otherwise through the
+  // caller workspace.
+  p->reduce = split_k == 1 ? qg::kReduceNone
+              : (p->swap && split_k <= qg::kMaxClusterSplits) ? qg::kReduceCluster
+                                                              : qg::kReduceGlobal;
   return QG_OK;
 }
 
 int64_t workspace_bytes(const Plan& p, int64_t M, int64_t N) {
-  if (p.splits <= 1) return 0;
+  if (p.reduce != qg::kReduceGlobal) return 0;
   const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
   return ws_counter_bytes(tiles) + static_cast<int64_t>(p.splits) * M * N * 4;
 }
 
-template <int FMT, bool SWAP, int MPAD>
-int run_f8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
-           cudaStream_t stream) {
-  auto kernel = qg::gemm_f8_kernel<FMT, SWAP, MPAD>;
-  const size_t optin = dev_info().smem_optin;
+// Ring depth: config_id > 0 asks for that many stages (capped by the opt-in
+// limit); 0 takes the deepest ring that still lets two CTAs share an SM.
+template <typename SmemFn>
+int pick_stages(int config_id, SmemFn smem_bytes, int* stages) {
+  const size_t optin = dev_info().smem_optin, two = two_per_sm_smem();
   int max_stages = kMaxStages;
-  while (max_stages > 2 && qg::gemm_f8_smem_bytes<SWAP, MPAD>(max_stages) > optin) --max_stages;
-  int stages = config_id > 0 ? config_id : max_stages;
-  if (stages > max_stages) stages = max_stages;
-  if (stages < 2) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
-  g.stages = stages;
-  const size_t smem = qg::gemm_f8_smem_bytes<SWAP, MPAD>(stages);
+  while (max_stages > 2 && smem_bytes(max_stages) > optin) --max_stages;
+  int def = max_stages;
+  while (def > 2 && smem_bytes(def) > two) --def;
+  int st = config_id > 0 ? config_id : def;
+  if (st > max_stages) st = max_stages;
+  if (st < 2) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
+  *stages = st;
+  return QG_OK;
+}
+
+template <typename Kernel>
+int launch_gemm(Kernel kernel, const Plan& p, dim3 grid, unsigned threads, size_t smem, const CUtensorMap& tmW,
+                const CUtensorMap& tmA, qg::GemmArgs& g, cudaStream_t stream) {
   cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-  dim3 grid(p.n_tiles, p.splits, SWAP ? 1 : p.m_tiles);
-  e = launch(kernel, grid, dim3(qg::kThreads), smem, stream, tmW, tmA, g);
+  unsigned cluster_y = 1;
+  if (p.reduce == qg::kReduceCluster) {
+    cluster_y = static_cast<unsigned>(p.splits);
+    if (cluster_y > 8) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+    }
+  }
+  g.reduce = p.reduce;
+  e = launch_cluster(kernel, grid, dim3(threads), smem, stream, cluster_y, tmW, tmA, g);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return QG_OK;
 }
 
-template <bool SWAP, int MPAD>
-int run_f8_fmt(int fmt, const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g,
-               int config_id, cudaStream_t stream) {
-  if (fmt == QG_FP8_DYNAMIC) return run_f8<qg::kFmtFP8, SWAP, MPAD>(p, tmW, tmA, g, config_id, stream);
-  return run_f8<qg::kFmtBlock, SWAP, MPAD>(p, tmW, tmA, g, config_id, stream);
+template <int FMT, int MPAD>
+int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                cudaStream_t stream) {
+  int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st); }, &g.stages);
+  if (rc != QG_OK) return rc;
+  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD>, p, dim3(p.n_tiles, p.splits, 1), qg::kThreads,
+                     qg::gemm_f8_smem_bytes<true, MPAD>(g.stages), tmW, tmA, g, stream);
+}
+
+template <int FMT>
+int run_f8_std(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+               cudaStream_t stream) {
+  int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_smem_bytes<false, 16>(st); }, &g.stages);
+  if (rc != QG_OK) return rc;
+  return launch_gemm(qg::gemm_f8_std_kernel<FMT>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kThreads,
+                     qg::gemm_f8_smem_bytes<false, 16>(g.stages), tmW, tmA, g, stream);
+}
+
+template <int MPAD>
+int run_f8_swap_fmt(int fmt, const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g,
+                    int config_id, cudaStream_t stream) {
+  if (fmt == QG_FP8_DYNAMIC) return run_f8_swap<qg::kFmtFP8, MPAD>(p, tmW, tmA, g, config_id, stream);
+  return run_f8_swap<qg::kFmtBlock, MPAD>(p, tmW, tmA, g, config_id, stream);
 }
 
 template <int MPAD>
 int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
            cudaStream_t stream) {
-  auto kernel = qg::gemm_i8_kernel<MPAD>;
-  const size_t optin = dev_info().smem_optin;
-  int max_stages = kMaxStages;
-  while (max_stages > 2 && qg::gemm_i8_smem_bytes<MPAD>(max_stages) > optin) --max_stages;
-  int stages = config_id > 0 ? config_id : max_stages;
-  if (stages > max_stages) stages = max_stages;
-  if (stages < 2) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
-  g.stages = stages;
-  const size_t smem = qg::gemm_i8_smem_bytes<MPAD>(stages);
-  cudaError_t e = set_smem(kernel, smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-  dim3 grid(p.n_tiles, p.splits, 1);
-  e = launch(kernel, grid, dim3(qg::kI8Threads), smem, stream, tmW, tmA, g);
-  if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
-  return QG_OK;
+  int rc = pick_stages(config_id, [](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st); }, &g.stages);
+  if (rc != QG_OK) return rc;
+  return launch_gemm(qg::gemm_i8_kernel<MPAD>, p, dim3(p.n_tiles, p.splits, 1), qg::kI8Threads,
+                     qg::gemm_i8_smem_bytes<MPAD>(g.stages), tmW, tmA, g, stream);
 }
 
 // ------------------------------------------------------------------ table
@@ -234,15 +290,17 @@ bool g_table_env_checked = false;
 
 // Built-in default config ("a default config for functional testing", section
 // "Toward a Practical Adoption Model"): Swap-AB for M <= 32 (M <= 64 for
-// INT8), Standard above; split K so that tiles x splits roughly fills the SMs,
-// with at least two 128-wide k-tiles per split.
+// INT8), Standard above; split K so that tiles x splits roughly fills the two
+// CTA slots of every SM, with at least two 128-wide k-tiles per split and (for
+// Swap-AB) no more splits than one cluster reduces.
 void default_config(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int* split_k, int* config_id) {
   const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
   const bool swap = (fmt == QG_W8A8_INT8) ? (M <= 64) : (M <= 32);
   const int64_t tiles = cdiv(N, 128) * (swap ? 1 : cdiv(M, 128));
   const int64_t kt = cdiv(K, 128);
-  int64_t s = sms / std::max<int64_t>(tiles, 1);
-  s = std::max<int64_t>(1, std::min<int64_t>(s, kt / 2));
+  int64_t s = (2 * static_cast<int64_t>(sms)) / std::max<int64_t>(tiles, 1);
+  s = std::min<int64_t>(s, kt / 2);
+  if (swap) s = std::min<int64_t>(s, qg::kMaxClusterSplits);
   if (s < 1) s = 1;
   *variant = swap ? (s > 1 ? QG_SWAPAB_SPLITK : QG_SWAPAB) : (s > 1 ? QG_SPLITK : QG_STANDARD);
   *split_k = static_cast<int>(s);
@@ -461,7 +519,7 @@ int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, 
   g.s_a = s_a_dev;
   g.s_w = s_w_dev;
   g.Y = static_cast<__nv_bfloat16*>(Y_dev);
-  if (need > 0) {
+  if (p.reduce == qg::kReduceGlobal) {
     const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
     g.ws_count = static_cast<int*>(workspace_dev);
     g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
@@ -477,11 +535,12 @@ int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, 
     return run_i8<64>(p, tmW, tmA, g, config_id, s);
   }
   if (p.swap) {
-    if (p.mpad == 16) return run_f8_fmt<true, 16>(fmt, p, tmW, tmA, g, config_id, s);
-    if (p.mpad == 32) return run_f8_fmt<true, 32>(fmt, p, tmW, tmA, g, config_id, s);
-    return run_f8_fmt<true, 64>(fmt, p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 16) return run_f8_swap_fmt<16>(fmt, p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return run_f8_swap_fmt<32>(fmt, p, tmW, tmA, g, config_id, s);
+    return run_f8_swap_fmt<64>(fmt, p, tmW, tmA, g, config_id, s);
   }
-  return run_f8_fmt<false, 16>(fmt, p, tmW, tmA, g, config_id, s);
+  if (fmt == QG_FP8_DYNAMIC) return run_f8_std<qg::kFmtFP8>(p, tmW, tmA, g, config_id, s);
+  return run_f8_std<qg::kFmtBlock>(p, tmW, tmA, g, config_id, s);
 }
 
 int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,

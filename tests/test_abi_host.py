@@ -98,8 +98,11 @@ def test_gemm_validation(q):
     assert _gemm(q, split=2) == q.QG_ERR_INVALID_ARG                    # split needs a *_SPLITK variant
     assert _gemm(q, variant=3, split=3) == q.QG_ERR_UNSUPPORTED_SHAPE     # > ceil(K/128) = 2
     assert _gemm(q, variant=3, split=0) == q.QG_ERR_UNSUPPORTED_SHAPE
-    assert _gemm(q, variant=3, split=2) == q.QG_ERR_WORKSPACE_TOO_SMALL   # no workspace
-    assert _gemm(q, variant=3, split=2, ws=OK16, wsb=16) == q.QG_ERR_WORKSPACE_TOO_SMALL
+    # Split-K through the workspace: Standard split-K, or Swap-AB with more
+    # than 16 ranges (up to 16 reduce inside a thread-block cluster)
+    assert _gemm(q, variant=1, split=2) == q.QG_ERR_WORKSPACE_TOO_SMALL   # no workspace
+    assert _gemm(q, variant=1, split=2, ws=OK16, wsb=16) == q.QG_ERR_WORKSPACE_TOO_SMALL
+    assert _gemm(q, K=4096, variant=3, split=20) == q.QG_ERR_WORKSPACE_TOO_SMALL
     assert _gemm(q, M=65, variant=2) == q.QG_ERR_UNSUPPORTED_SHAPE       # Swap-AB is M <= 64
     assert _gemm(q, fmt=1, M=8, variant=0) == q.QG_ERR_UNSUPPORTED_SHAPE  # INT8 runs Swap-AB
     assert _gemm(q, fmt=0, dbg=OK16) == q.QG_ERR_INVALID_ARG              # debug acc is INT8 only
@@ -109,9 +112,11 @@ def test_gemm_validation(q):
 
 def test_workspace_bytes(q):
     assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB, 1) == 0
-    # counters (2 tiles -> one 256-byte block) + splits * M * N * 4
-    assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB_SPLITK, 3) == 256 + 3 * 4 * 256 * 4
-    assert q.qg_workspace_bytes(1, 32, 4096, 2048, q.QG_SWAPAB_SPLITK, 4) == 256 + 4 * 32 * 4096 * 4
+    # Swap-AB with <= 16 ranges reduces in distributed shared memory: no workspace
+    assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB_SPLITK, 3) == 0
+    assert q.qg_workspace_bytes(1, 32, 4096, 2048, q.QG_SWAPAB_SPLITK, 16) == 0
+    # counters (tiles x 4 bytes, rounded up to 256) + splits * M * N * 4
+    assert q.qg_workspace_bytes(1, 32, 4096, 4096, q.QG_SWAPAB_SPLITK, 17) == 256 + 17 * 32 * 4096 * 4
     assert q.qg_workspace_bytes(0, 300, 256, 1024, q.QG_SPLITK, 2) == 256 + 2 * 300 * 256 * 4
     assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB_SPLITK, 99) == 0  # invalid -> 0
 
@@ -161,7 +166,8 @@ def test_default_config_fills_the_gpu(q):
             v, s, c = q.qg_select("FP8_Dynamic", M, N, K)
             tiles = (N + 127) // 128
             assert v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK)
-            assert s == 1 or tiles * s <= 148
+            assert s == 1 or tiles * s <= 2 * 148      # two CTA slots per SM
+            assert s <= 16                              # one cluster reduces the splits
             assert s <= max(1, ((K + 127) // 128) // 2)
         v, s, c = q.qg_select("FP8_Dynamic", 256, 4096, 4096)
         assert v in (q.QG_STANDARD, q.QG_SPLITK)

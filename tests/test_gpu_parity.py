@@ -47,6 +47,16 @@ def test_w8a8_int8(orc, gc, M, variant, split):
     gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=200 + M, outliers=True)
 
 
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])
+@pytest.mark.parametrize("split", [2, 8, 9, 13, 14, 16, 17])
+def test_split_k_cluster_and_workspace_reductions(orc, gc, fmt, split):
+    # 2..16 ranges reduce across a thread-block cluster (9..16: non-portable
+    # cluster sizes; 13 and 14 leave the last CTA few or no rows), 17 through
+    # the workspace.  K = 2304 (18 k-tiles), ragged N, M across 32.
+    M = 24 if fmt != "Block_FP8" else 19
+    gc.run_case(orc, fmt, M, 328, 2304, SWS, split, seed=300 + split)
+
+
 def test_int8_accumulators_identical_across_variants(gc):
     import seeded_inputs as si
     M, N, K = 32, 256, 4096

@@ -59,7 +59,10 @@ def _close(orc, gc, fmt, Aq, sa, Wq, sw, Y, Y_ref, dbg, dbg_ref):
 
 @pytest.mark.parametrize("fmt", ["W8A8_INT8", "FP8_Dynamic", "Block_FP8"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(orc, gc, q, fmt):
-    M, N, K, S = 16, 384, 2048, 4
+    # 20 K ranges: more than a thread-block cluster reduces, so the partials
+    # go through the scratch array (491,776 bytes of the 4 MiB)
+    M, N, K, S = 16, 384, 4096, 20
+    assert q.qg_workspace_bytes(fmt, M, N, K, q.QG_SWAPAB_SPLITK, S) > 0
     Aq, sa, Wq, sw = _inputs(gc, fmt, M, N, K, seed=31)
     is_int8 = fmt == "W8A8_INT8"
     Y_ref, dbg_ref = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, q.QG_SWAPAB_SPLITK, S, debug=is_int8)
@@ -85,7 +88,7 @@ def test_noalloc_without_split_k(orc, gc, q):
 
 
 def test_noalloc_rejects_scratch_beyond_the_array(gc, q):
-    M, N, K, S = 32, 12288, 2048, 16          # 16 * 32 * 12288 * 4 bytes = 24 MiB of partials
+    M, N, K, S = 32, 12288, 4096, 17          # 17 * 32 * 12288 * 4 bytes = 25.5 MiB of partials
     need = q.qg_workspace_bytes("FP8_Dynamic", M, N, K, q.QG_SWAPAB_SPLITK, S)
     assert need > q.QG_NOALLOC_SCRATCH_BYTES
     d = torch.zeros(16, dtype=torch.uint8, device=gc.DEV)
