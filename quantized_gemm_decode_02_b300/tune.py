@@ -1,0 +1,178 @@
+"""Offline per-shape config sweep: writes the table that qg_select reads.
+
+"Per-shape Config Tuning" of "Building a High-Performance and Portable vLLM
+Linear Backend with Helion" tunes every (model GEMM shape x num_tokens)
+separately, with the candidates benchmarked under CUDA graphs the way they
+will run ("Enable CUDA Graph for Autotuner Benchmarking").  This sweep keeps
+that method and replaces the page's LLM-seeded tree search with an exhaustive
+walk over a small grid: for every format, shape and tuned token count it
+times each candidate (variant, split_k, ring depth) as a CUDA graph of R
+launches over rotated weight copies (more than three L2 capacities, so the
+weights stream from HBM), with programmatic dependent launch on, and keeps
+the fastest.
+
+Rows already present in the output table are skipped, so an interrupted
+sweep resumes where it stopped.
+
+Usage:  python -m quantized_gemm_decode_02_b300.tune --out TABLE
+            [--formats FP8_Dynamic,W8A8_INT8,Block_FP8]
+            [--models Qwen3-1.7B,Qwen3-8B,Qwen3-32B] [--ms 1,2,4,8,16,24,32]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from quantized_gemm_decode_02_b300 import qgemm as q  # noqa: E402
+
+# Linear-layer shapes (K = in_features, N = out_features) of the Qwen3 models
+# whose GEMMs the pages tune.
+SHAPES = {
+    "Qwen3-1.7B": {"qkv": (2048, 4096), "o": (2048, 2048), "gate_up": (2048, 12288), "down": (6144, 2048)},
+    "Qwen3-8B": {"qkv": (4096, 6144), "o": (4096, 4096), "gate_up": (4096, 24576), "down": (12288, 4096)},
+    "Qwen3-32B": {"qkv": (5120, 10240), "o": (8192, 5120), "gate_up": (5120, 51200), "down": (25600, 5120)},
+}
+TUNED_M = (1, 2, 4, 8, 16, 24, 32)
+FMT_ID = {"FP8_Dynamic": 0, "W8A8_INT8": 1, "Block_FP8": 2}
+POOL_BYTES = 512 << 20
+
+
+def candidates(fmt: str, M: int, N: int, K: int, sms: int):
+    """(variant, split_k, config_id) candidates for one shape."""
+    tiles = (N + 127) // 128
+    kt = (K + 127) // 128
+    out = []
+    for cfg in (0, 12):                      # ring depth: two CTAs per SM, or one deep ring
+        out.append((q.QG_SWAPAB, 1, cfg))
+        for s in range(2, min(16, kt) + 1):  # Split-K reduced in a cluster
+            if tiles * s > 3 * sms or kt // s < 1:
+                continue
+            out.append((q.QG_SWAPAB_SPLITK, s, cfg))
+    return out
+
+
+class Bench:
+    """Device buffers shared by every candidate: a pool of random weight
+    bytes that launches take disjoint windows of, activations, scales, Y."""
+
+    def __init__(self, device):
+        self.device = device
+        g = torch.Generator(device=device)
+        g.manual_seed(1234)
+        # random bytes: valid int8 codes; as E4M3 they include NaN codes,
+        # which do not change the kernels' speed
+        self.pool = torch.randint(0, 256, (POOL_BYTES,), dtype=torch.uint8, device=device, generator=g)
+        self.Aq = torch.randint(0, 256, (64 * 32768,), dtype=torch.uint8, device=device, generator=g)
+        self.sa = torch.ones(64 * 256, dtype=torch.float32, device=device)
+        self.sw = torch.ones(65536 * 4, dtype=torch.float32, device=device)
+        self.Y = torch.empty(64 * 65536, dtype=torch.bfloat16, device=device)
+        self.ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.Stream(device=device)
+
+    def time_config(self, fmt, M, N, K, variant, split, cfg, min_bytes=3 * 126e6, reps=5):
+        """Microseconds per GEMM: median over `reps` replays of a graph of R
+        launches, each on its own window of the weight pool."""
+        wbytes = N * K
+        R = int(min(64, max(2, -(-min_bytes // wbytes))))
+        step = (wbytes + 255) // 256 * 256
+        if step * R > POOL_BYTES:
+            R = max(2, POOL_BYTES // step)
+        need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
+        q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=self.stream):
+                for r in range(R):
+                    W = self.pool[r * step:r * step + wbytes]
+                    q.qg_gemm_w8a8(fmt, M, N, K, self.Aq, self.sa, W, self.sw, self.Y, N, variant, split, cfg,
+                                   self.ws if need else None, need, None, stream=self.stream)
+        finally:
+            q.qg_set_launch_flags(0)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(reps):
+            with torch.cuda.stream(self.stream):
+                e0.record(self.stream)
+                graph.replay()
+                e1.record(self.stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / R)
+        del graph
+        return statistics.median(times)
+
+
+def read_table(path):
+    rows = {}
+    if os.path.exists(path):
+        for line in open(path):
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            f, n, k, m, v, s, c = (int(x) for x in line.split())
+            rows[(f, n, k, m)] = (v, s, c)
+    return rows
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", required=True)
+    ap.add_argument("--formats", default="FP8_Dynamic,W8A8_INT8,Block_FP8")
+    ap.add_argument("--models", default="Qwen3-1.7B,Qwen3-8B,Qwen3-32B")
+    ap.add_argument("--ms", default=",".join(str(m) for m in TUNED_M))
+    ap.add_argument("--log", default=None, help="JSON lines with every candidate's time")
+    args = ap.parse_args(argv)
+    device = "cuda:0"
+    torch.cuda.set_device(0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    bench = Bench(device)
+    done = read_table(args.out)
+    os.makedirs(os.path.dirname(os.path.abspath(args.out)), exist_ok=True)
+    new_file = not os.path.exists(args.out)
+    out = open(args.out, "a")
+    if new_file:
+        out.write("# fmt\tN\tK\tM\tvariant\tsplit_k\tconfig_id   (written by quantized_gemm_decode_02_b300/tune.py)\n")
+    log = open(args.log, "a") if args.log else None
+    t0 = time.time()
+    for fmt in args.formats.split(","):
+        fid = FMT_ID[fmt]
+        for model in args.models.split(","):
+            for layer, (K, N) in SHAPES[model].items():
+                for M in (int(m) for m in args.ms.split(",")):
+                    if (fid, N, K, M) in done:
+                        continue
+                    best = None
+                    for (v, s, c) in candidates(fmt, M, N, K, sms):
+                        us = bench.time_config(fmt, M, N, K, v, s, c)
+                        if log:
+                            log.write(json.dumps({"fmt": fmt, "model": model, "layer": layer, "M": M, "N": N, "K": K,
+                                                  "variant": v, "split_k": s, "config_id": c, "us": us}) + "\n")
+                        if best is None or us < best[0]:
+                            best = (us, v, s, c)
+                    us, v, s, c = best
+                    gbs = (N * K + M * K + 2 * M * N) / (us * 1e-6) / 1e9
+                    out.write(f"{fid}\t{N}\t{K}\t{M}\t{v}\t{s}\t{c}\t# {model} {layer} {us:.2f} us {gbs:.0f} GB/s\n")
+                    out.flush()
+                    print(f"{fmt:12s} {model:10s} {layer:8s} M={M:2d}: variant {v} split {s:2d} cfg {c:2d} "
+                          f"{us:7.2f} us {gbs:6.0f} GB/s  [{time.time() - t0:.0f} s]", flush=True)
+    out.close()
+    if log:
+        log.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
