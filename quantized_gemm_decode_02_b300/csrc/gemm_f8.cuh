@@ -42,6 +42,7 @@ struct GemmArgs {
   int splits;           // >= 1
   int stages;           // shared-memory ring depth
   int reduce;           // kReduceNone / kReduceCluster / kReduceGlobal
+  int recv_bytes;       // kReduceCluster: bytes of the shared-memory receive buffer (cluster_recv_bytes)
   const float* s_a;     // [M] or [M][kt_total]
   const float* s_w;     // [N] or [ceil(N/128)][kt_total]
   __nv_bfloat16* Y;     // [M][ldy]
@@ -69,9 +70,12 @@ struct alignas(8) Ctrl {
   uint64_t tfull[4];
   uint64_t tempty[4];
   uint64_t never;
+  uint64_t recv_bar;  // split-K: peers' partial rows have landed
   uint32_t tmem_base;
   int last_flag;
   int abort_flag;
+  float sa_s[64];   // per-token scales, staged for the epilogue
+  float sw_s[128];  // per-channel scales of the tile's rows
 };
 
 template <bool SWAP, int MPAD>
@@ -85,8 +89,8 @@ struct TileShape {
 };
 
 template <bool SWAP, int MPAD>
-__host__ __device__ constexpr size_t gemm_f8_smem_bytes(int stages) {
-  return 1024 + static_cast<size_t>(stages) * TileShape<SWAP, MPAD>::kStageBytes + sizeof(Ctrl);
+__host__ __device__ constexpr size_t gemm_f8_smem_bytes(int stages, int recv_bytes = 0) {
+  return 1024 + static_cast<size_t>(stages) * TileShape<SWAP, MPAD>::kStageBytes + recv_bytes + sizeof(Ctrl);
 }
 
 __device__ __forceinline__ void store_bf16(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
@@ -95,33 +99,70 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Split-K through distributed shared memory.  Every CTA of the cluster
-// (cluster rank == split index) holds its partial tile part[m][r]
-// (m < MPAD tokens, r < 128 weight rows) in its own shared memory.  CTA
-// `rank` owns rows [rank*R, rank*R + R), R = ceil(128 / S): for each of its
-// (m, r) with m < M it loads the S partials and adds them in the fixed order
-// 0..S-1, then calls store(m, r, sum).  The caller brackets this with
-// cluster_sync() (partials visible before; peers done reading after).
+// Split-K through distributed shared memory, push form.  The S CTAs of a
+// tile form one cluster (cluster rank == split index).  Row r of the tile is
+// owned by CTA r / R, R = ceil(128 / S).  Every CTA sends its partial of
+// each row to the row's owner with st.async, which lands in the owner's
+// receive buffer recv[s][j][mv] (s = sending rank, j = row - owner*R, mv = M
+// rounded up to 4) and completes bytes on the owner's mbarrier; the owner
+// waits for (S - 1) * rows * mv * 4 bytes, then adds the S partials of each
+// of its elements in the fixed order 0..S-1.  One one-way transfer and one
+// bounded wait; no CTA reads a peer, so none waits for its peers to finish.
+__host__ __device__ constexpr int cluster_rows_per_rank(int S) { return (kBN + S - 1) / S; }
+__host__ __device__ constexpr int cluster_mv(int M) { return (M + 3) & ~3; }
+__host__ __device__ constexpr int cluster_recv_bytes(int S, int M) {
+  return S * cluster_rows_per_rank(S) * cluster_mv(M) * 4;
+}
+__device__ __forceinline__ int cluster_rows_of(int rank, int S) {
+  const int R = cluster_rows_per_rank(S);
+  return max(0, min(kBN, rank * R + R) - rank * R);
+}
+
+// Send this thread's values v[0..N) of row `row` for tokens [m0, m0 + N)
+// (m0 and N multiples of 4) to the row's owner; values for the thread's own
+// rows are stored locally.
+template <typename T, int N>
+__device__ __forceinline__ void cluster_push_row(const T (&v)[N], int m0, int row, int rank, int S, int M,
+                                                 uint8_t* recv, uint64_t* recv_bar) {
+  const int R = cluster_rows_per_rank(S), mv = cluster_mv(M);
+  const int o = row / R, j = row - o * R;
+  const uint32_t base = smem_u32(recv), bar = smem_u32(recv_bar);
+#pragma unroll
+  for (int c = 0; c < N; c += 4) {
+    const int m = m0 + c;
+    if (m < mv) {
+      const uint32_t off = static_cast<uint32_t>(((rank * R + j) * mv + m) * 4);
+      const uint32_t w0 = reinterpret_cast<const uint32_t&>(v[c]);
+      const uint32_t w1 = reinterpret_cast<const uint32_t&>(v[c + 1]);
+      const uint32_t w2 = reinterpret_cast<const uint32_t&>(v[c + 2]);
+      const uint32_t w3 = reinterpret_cast<const uint32_t&>(v[c + 3]);
+      if (o == rank)
+        *reinterpret_cast<uint4*>(recv + off) = make_uint4(w0, w1, w2, w3);
+      else
+        st_async_v4(dsmem_map(base + off, static_cast<uint32_t>(o)), w0, w1, w2, w3,
+                    dsmem_map(bar, static_cast<uint32_t>(o)));
+    }
+  }
+}
+
+// Owner side, after the receive barrier completed: for each element (m, j)
+// of this CTA's rows, sum the S partials in order and call store(m, row, sum).
 template <typename T, typename Store>
-__device__ __forceinline__ void cluster_reduce_tile(const T* part, int rank, int S, int M, int tid, int nthreads,
-                                                    Store&& store) {
-  const int R = (kBN + S - 1) / S;
-  const int r0 = rank * R;
-  const int rn = min(kBN, r0 + R) - r0;
-  if (rn <= 0) return;
-  const uint32_t base = smem_u32(part);
+__device__ __forceinline__ void cluster_sum_rows(const uint8_t* recv, int rank, int S, int M, int tid, int nthreads,
+                                                 Store&& store) {
+  const int R = cluster_rows_per_rank(S), mv = cluster_mv(M), rn = cluster_rows_of(rank, S);
+  const T* buf = reinterpret_cast<const T*>(recv);
   for (int e = tid; e < rn * M; e += nthreads) {
-    const int r = r0 + e % rn, m = e / rn;
-    const uint32_t addr = base + static_cast<uint32_t>(m * kBN + r) * 4u;
+    const int m = e % M, j = e / M;
     T v[kMaxClusterSplits];
 #pragma unroll
     for (int s = 0; s < kMaxClusterSplits; ++s)
-      if (s < S) v[s] = ld_dsmem(dsmem_map(addr, static_cast<uint32_t>(s)), T{});
+      if (s < S) v[s] = buf[(s * R + j) * mv + m];
     T sum = v[0];
 #pragma unroll
     for (int s = 1; s < kMaxClusterSplits; ++s)
       if (s < S) sum += v[s];
-    store(m, r, sum);
+    store(m, rank * R + j, sum);
   }
 }
 
@@ -139,7 +180,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + static_cast<size_t>(stages) * TS::kStageBytes);
+  uint8_t* recv = smem + static_cast<size_t>(stages) * TS::kStageBytes;  // split-K receive buffer
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(recv + g.recv_bytes);
+  const bool clustered = g.reduce == kReduceCluster;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x;
@@ -159,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&ctl->tempty[b], 128);
     }
     mbar_init(&ctl->never, 1);
+    mbar_init(&ctl->recv_bar, 1);
     ctl->last_flag = 0;
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -168,6 +212,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tmap(&tmA);
   }
   __syncthreads();
+  if (clustered) {
+    // the receive barrier expects the peers' rows; every thread then marks
+    // this CTA's barriers initialized for the cluster (waited on before the
+    // first push, long after)
+    if (threadIdx.x == 0)
+      mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
+                                                                  cluster_mv(g.M) * 4));
+    cluster_arrive_relaxed();
+  }
   pdl_launch_dependents();
   volatile int* abort_flag = &ctl->abort_flag;
   float acc[MPAD];  // epilogue threads: weight row n of the tile x every token
@@ -263,6 +316,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       pdl_wait();
       const int q = warp & 3;  // TMEM lane quarter this warp may access
       const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+      if constexpr (!BLOCK) {
+        // scales for the epilogue, fetched while the main loop runs
+        const int et0 = threadIdx.x - 64, r = q * 32 + lane, nn = n_tile * kBN + r;
+        if (et0 < MPAD) ctl->sa_s[et0] = et0 < g.M ? __ldg(g.s_a + et0) : 0.0f;
+        ctl->sw_s[r] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
+      }
       if constexpr (BLOCK) {
         const int nb = n_tile;  // 128-row tile == weight block row
         // lane l holds s_a of tokens l, l + 32, ... for the current k-tile
@@ -337,34 +396,33 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int row = (warp & 3) * 32 + lane;   // epilogue threads: weight row in the tile
   const int n = n_tile * kBN + row;
   const int et = threadIdx.x - 64;          // 0..127 for the epilogue warps
-  auto out = [&](int m, int nn, float sum) {
-    const float y = BLOCK ? sum : (sum * __ldg(g.s_a + m)) * __ldg(g.s_w + nn);
+  // r: row of the tile (scales staged in shared memory); nn = n_tile*128 + r
+  auto out = [&](int m, int r, int nn, float sum) {
+    const float y = BLOCK ? sum : (sum * ctl->sa_s[m]) * ctl->sw_s[r];
     store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
   };
 
-  if (g.reduce == kReduceCluster) {
-    // The ring is idle (every copy landed, every MMA finished): reuse it for
-    // this CTA's partial tile, [MPAD][128] fp32.
-    float* part = reinterpret_cast<float*>(smem);
+  if (clustered) {
+    cluster_wait();  // every peer's receive barrier is initialized
     if (warp >= 2) {
-#pragma unroll
-      for (int m = 0; m < MPAD; ++m) part[m * kBN + row] = acc[m];
+      // rows go out even after an abort, so that every owner's wait completes
+      cluster_push_row(acc, 0, row, split, g.splits, g.M, recv, &ctl->recv_bar);
+      named_bar_sync(1, 128);  // this CTA's own rows, stored locally, are visible
+      const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
+      if (got && !abort) {
+        cluster_sum_rows<float>(recv, split, g.splits, g.M, et, 128, [&](int m, int r, float sum) {
+          const int nn = n_tile * kBN + r;
+          if (nn < g.N) out(m, r, nn, sum);
+        });
+      }
     }
-    cluster_sync();
-    if (warp >= 2 && !abort) {
-      cluster_reduce_tile(part, split, g.splits, g.M, et, 128, [&](int m, int r, float sum) {
-        const int nn = n_tile * kBN + r;
-        if (nn < g.N) out(m, nn, sum);
-      });
-    }
-    cluster_sync();
   } else if (warp >= 2 && !abort) {
     const bool n_ok = n < g.N;
     if (g.reduce == kReduceNone) {
       if (n_ok) {
 #pragma unroll
         for (int m = 0; m < MPAD; ++m)
-          if (m < g.M) out(m, n, acc[m]);
+          if (m < g.M) out(m, row, n, acc[m]);
       }
     } else {
       float* part = static_cast<float*>(g.ws_part);
@@ -386,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int m = 0; m < g.M; ++m) {
             float sum = 0.0f;
             for (int s = 0; s < g.splits; ++s) sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
-            out(m, n, sum);
+            out(m, row, n, sum);
           }
         }
         if (et == 0) g.ws_count[n_tile] = 0;  // ready for the next launch

@@ -15,16 +15,20 @@
 // CTAs share an SM (at most 256 TMEM columns and ~113 KB of shared memory):
 //   warp 0      TMA: int8 W tile (128 x 128 B) + int8 activation tile into a
 //               `stages`-deep shared-memory ring;
-//   warps 2..9  converters: warp w owns TMEM lane quarter w % 4 (weight rows
-//               32*(w%4) .. +31) and half (w-2)/4 of each 128-byte k-tile row;
-//               each thread widens its 64 weight bytes to fp16 and writes them
-//               with tcgen05.st into a TMEM operand buffer (the MMA A operand
-//               lives in TMEM, so the widened weights never touch shared
-//               memory); together they widen the activation tile into a
-//               128-byte-swizzled shared buffer (MMA B operand); they drain
-//               finished accumulator segments into int32 (warp w takes token
-//               half (w-2)/4) and run the epilogue;
+//   warps 2..9  weight converters: warp w owns TMEM lane quarter w % 4
+//               (weight rows 32*(w%4) .. +31) and half (w-2)/4 of each
+//               128-byte k-tile row; each thread widens its 64 weight bytes
+//               to fp16 and writes them with tcgen05.st into a TMEM operand
+//               buffer (the MMA A operand lives in TMEM, so the widened
+//               weights never touch shared memory); they drain finished
+//               accumulator segments into int32 (warp w takes token half
+//               (w-2)/4) and run the epilogue;
+//   warps 10,11 activation converters: widen the activation tile into a
+//               128-byte-swizzled shared buffer (MMA B operand);
 //   warp 1      one thread issues 8 MMAs (K = 16 each) per k-tile.
+// Weights and activations land on separate barriers, so the weight tiles
+// fetched before the activations exist (programmatic dependent launch) are
+// already widened into TMEM when the activations arrive.
 // Split-K reduces through distributed shared memory across the cluster of
 // a tile's CTAs (up to 16 ranges) or through the caller workspace, exactly
 // as the FP8 kernel does, in int32.
@@ -34,14 +38,17 @@
 
 namespace qg {
 
-constexpr int kI8ConvWarps = 8;
+constexpr int kI8ConvWarps = 8;                    // weight converters (warps 2..9)
 constexpr int kI8ConvThreads = 32 * kI8ConvWarps;  // 256
-constexpr int kI8Threads = 64 + kI8ConvThreads;    // 320
+constexpr int kI8AWarp = 2 + kI8ConvWarps;         // first activation converter (warp 10)
+constexpr int kI8AWarps = 2;                       // activation converters (warps 10, 11)
+constexpr int kI8Threads = 32 * (kI8AWarp + kI8AWarps);  // 384
 constexpr int kI8OpBufs = 3;        // TMEM/shared operand buffers in flight
 constexpr int kI8SegTiles = 8;      // k-tiles (of 128) per exact fp32 segment: 1024 K
 
 struct alignas(8) CtrlI8 {
-  uint64_t full[16];
+  uint64_t full[16];     // weight tile of the stage landed
+  uint64_t full_a[16];   // activation tile of the stage landed
   uint64_t empty[16];
   uint64_t op_full[kI8OpBufs];
   uint64_t op_empty[kI8OpBufs];
@@ -49,9 +56,12 @@ struct alignas(8) CtrlI8 {
   uint64_t d_empty[2];
   uint64_t never;
   uint64_t done;
+  uint64_t recv_bar;  // split-K: peers' partial rows have landed
   uint32_t tmem_base;
   int last_flag;
   int abort_flag;
+  float sa_s[64];   // per-token scales, staged for the epilogue
+  float sw_s[128];  // per-channel scales of the tile's rows
 };
 
 template <int MPAD>
@@ -67,9 +77,9 @@ struct I8Shape {
 };
 
 template <int MPAD>
-__host__ __device__ constexpr size_t gemm_i8_smem_bytes(int stages) {
+__host__ __device__ constexpr size_t gemm_i8_smem_bytes(int stages, int recv_bytes = 0) {
   return 1024 + static_cast<size_t>(stages) * I8Shape<MPAD>::kStageBytes +
-         static_cast<size_t>(kI8OpBufs) * I8Shape<MPAD>::kOpBBytes + sizeof(CtrlI8);
+         static_cast<size_t>(kI8OpBufs) * I8Shape<MPAD>::kOpBBytes + recv_bytes + sizeof(CtrlI8);
 }
 
 // 4 int8 (one 32-bit word, element 0 in the low byte) -> two fp16x2 words:
@@ -101,7 +111,9 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
   uint8_t* opb = smem + static_cast<size_t>(stages) * S::kStageBytes;  // fp16 activation buffers
-  CtrlI8* ctl = reinterpret_cast<CtrlI8*>(opb + kI8OpBufs * S::kOpBBytes);
+  uint8_t* recv = opb + kI8OpBufs * S::kOpBBytes;                        // split-K receive buffer
+  CtrlI8* ctl = reinterpret_cast<CtrlI8*>(recv + g.recv_bytes);
+  const bool clustered = g.reduce == kReduceCluster;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, split = blockIdx.y;
@@ -113,10 +125,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
-      mbar_init(&ctl->empty[i], kI8ConvWarps);
+      mbar_init(&ctl->full_a[i], 1);
+      mbar_init(&ctl->empty[i], kI8ConvWarps + kI8AWarps);
     }
     for (int b = 0; b < kI8OpBufs; ++b) {
-      mbar_init(&ctl->op_full[b], kI8ConvWarps);
+      mbar_init(&ctl->op_full[b], kI8ConvWarps + kI8AWarps);
       mbar_init(&ctl->op_empty[b], 1);
     }
     for (int d = 0; d < 2; ++d) {
@@ -125,6 +138,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     }
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->done, 1);
+    mbar_init(&ctl->recv_bar, 1);
     ctl->last_flag = 0;
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -134,6 +148,12 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     prefetch_tmap(&tmA);
   }
   __syncthreads();
+  if (clustered) {
+    if (threadIdx.x == 0)
+      mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
+                                                                  cluster_mv(g.M) * 4));
+    cluster_arrive_relaxed();
+  }
   pdl_launch_dependents();
   volatile int* abort_flag = &ctl->abort_flag;
   // converter threads: weight row `row` of the tile x tokens [h*kHalf, h*kHalf + kHalf)
@@ -152,13 +172,14 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       const int pre = nk < stages ? nk : stages;
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
-        mbar_arrive_expect_tx(&ctl->full[i], S::kStageBytes);
+        mbar_arrive_expect_tx(&ctl->full[i], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
-        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full[i], pol_a);
+        mbar_arrive_expect_tx(&ctl->full_a[i], S::kABytes);
+        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full_a[i], pol_a);
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -169,13 +190,17 @@ __global__ void __launch_bounds__(kI8Threads, 2)
           break;
         }
         uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
-        mbar_arrive_expect_tx(&ctl->full[s], S::kStageBytes);
+        mbar_arrive_expect_tx(&ctl->full[s], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
-        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full[s], pol_a);
+        mbar_arrive_expect_tx(&ctl->full_a[s], S::kABytes);
+        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full_a[s], pol_a);
         issued = i + 1;
       }
-      for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+      // every issued copy lands before the CTA may exit or reuse the ring
+      for (int j = issued > stages ? issued - stages : 0; j < issued; ++j) {
         mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+        mbar_wait(&ctl->full_a[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+      }
     }
   } else {
     if (warp == 1) tmem_alloc(&ctl->tmem_base, S::kTmemCols);
@@ -221,10 +246,62 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         }
         tc_commit(&ctl->done);  // all issued MMAs complete
       }
+    } else if (warp >= kI8AWarp) {
+      // -------------------------------------------- activation converters
+      pdl_wait();  // s_a is written by the kernel this one depends on
+      const int at = threadIdx.x - 32 * kI8AWarp;  // 0..63
+      if (at < MPAD) ctl->sa_s[at] = at < g.M ? __ldg(g.s_a + at) : 0.0f;
+      bool ok = true;
+      for (int i = 0; i < nk; ++i) {
+        const int buf = i % kI8OpBufs, s = i % stages;
+        bool w = mbar_wait(&ctl->full_a[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns);
+        if (i >= kI8OpBufs)
+          w = w && mbar_wait(&ctl->op_empty[buf], static_cast<uint32_t>(i / kI8OpBufs - 1) & 1u, g.wait_ns);
+        if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
+          ok = false;
+          break;
+        }
+        // activation tile -> fp16, swizzled K-major B operand (2 atoms of 64 K)
+        const uint8_t* src = smem + static_cast<size_t>(s) * S::kStageBytes + S::kWBytes;
+        uint8_t* ob = opb + buf * S::kOpBBytes;
+#pragma unroll
+        for (int piece = at; piece < MPAD * 4; piece += 32 * kI8AWarps) {
+          const uint32_t r = piece >> 2, p = piece & 3;  // row, 32-element quarter of the 128 K
+          const uint4 v0 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p + 1));
+          uint32_t o[16];
+          int8x4_to_f16x4(v0.x, o[0], o[1]);
+          int8x4_to_f16x4(v0.y, o[2], o[3]);
+          int8x4_to_f16x4(v0.z, o[4], o[5]);
+          int8x4_to_f16x4(v0.w, o[6], o[7]);
+          int8x4_to_f16x4(v1.x, o[8], o[9]);
+          int8x4_to_f16x4(v1.y, o[10], o[11]);
+          int8x4_to_f16x4(v1.z, o[12], o[13]);
+          int8x4_to_f16x4(v1.w, o[14], o[15]);
+          uint8_t* atom = ob + (p >> 1) * (MPAD * 128);
+          const uint32_t c0 = (p & 1) * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(atom + sw128_chunk(r, c0 + j)) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctl->op_full[buf]);
+          mbar_arrive(&ctl->empty[s]);
+        }
+      }
+      if (!ok) *abort_flag = 1;
     } else {
-      // ------------------------------------------------------- converters
+      // ------------------------------------------------- weight converters
+      // They read only the static weights, so they start before the
+      // activations exist (no dependency wait here).
       const uint32_t lane_base = ((warp & 3) * 32u) << 16;
-      const int ct = threadIdx.x - 64;  // 0..255
+      if (h == 0) {
+        const int nn = n_tile * kBN + static_cast<int>(row);
+        ctl->sw_s[row] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
+      }
       bool ok = true;
 
       auto drain = [&](int seg) -> bool {
@@ -246,7 +323,6 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         return true;
       };
 
-      pdl_wait();
       for (int i = 0; i < nk; ++i) {
         const int seg = i / kI8SegTiles, buf = i % kI8OpBufs, s = i % stages;
         if ((i % kI8SegTiles) == 0 && seg >= 2 && !drain(seg - 2)) {
@@ -272,31 +348,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
           int8x4_to_f16x4(v.w, o[6], o[7]);
           tmem_st_x8(tmem_a + lane_base + buf * S::kACols + c * 8, o);
         }
-        // activation tile -> fp16, swizzled K-major B operand (2 atoms of 64 K)
-        uint8_t* ob = opb + buf * S::kOpBBytes;
-        for (int piece = ct; piece < MPAD * 4; piece += kI8ConvThreads) {
-          const uint32_t r = piece >> 2, p = piece & 3;  // row, 32-element quarter of the 128 K
-          const uint8_t* src = st + S::kWBytes;
-          const uint4 v0 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p));
-          const uint4 v1 = *reinterpret_cast<const uint4*>(src + sw128_chunk(r, 2 * p + 1));
-          uint32_t o[16];
-          int8x4_to_f16x4(v0.x, o[0], o[1]);
-          int8x4_to_f16x4(v0.y, o[2], o[3]);
-          int8x4_to_f16x4(v0.z, o[4], o[5]);
-          int8x4_to_f16x4(v0.w, o[6], o[7]);
-          int8x4_to_f16x4(v1.x, o[8], o[9]);
-          int8x4_to_f16x4(v1.y, o[10], o[11]);
-          int8x4_to_f16x4(v1.z, o[12], o[13]);
-          int8x4_to_f16x4(v1.w, o[14], o[15]);
-          uint8_t* atom = ob + (p >> 1) * (MPAD * 128);
-          const uint32_t c0 = (p & 1) * 4;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(atom + sw128_chunk(r, c0 + j)) =
-                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
         tmem_st_wait();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -323,35 +375,38 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     tmem_dealloc(ctl->tmem_base, S::kTmemCols);
   }
   const bool abort = ctl->abort_flag != 0;  // stable after the barrier: uniform
+  pdl_wait();  // outputs are written only after the kernel this one depends on
   const int n = n_tile * kBN + static_cast<int>(row);
   const int ct = threadIdx.x - 64;
-  auto finish = [&](int m, int nn, int32_t acc) {
+  // r: row of the tile (scales staged in shared memory); nn = n_tile*128 + r
+  auto finish = [&](int m, int r, int nn, int32_t acc) {
     if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m) * g.N + nn] = acc;
-    const float y = (static_cast<float>(acc) * __ldg(g.s_a + m)) * __ldg(g.s_w + nn);
+    const float y = (static_cast<float>(acc) * ctl->sa_s[m]) * ctl->sw_s[r];
     store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
   };
 
-  if (g.reduce == kReduceCluster) {
-    int32_t* part = reinterpret_cast<int32_t*>(smem);  // [MPAD][128] in the idle ring
-    if (warp >= 2) {
-#pragma unroll
-      for (int j = 0; j < kHalf; ++j) part[(h * kHalf + j) * kBN + row] = iacc[j];
+  const bool holds_acc = warp >= 2 && warp < kI8AWarp;
+  if (clustered) {
+    cluster_wait();  // every peer's receive barrier is initialized
+    if (holds_acc) {
+      // rows go out even after an abort, so that every owner's wait completes
+      cluster_push_row(iacc, h * kHalf, static_cast<int>(row), split, g.splits, g.M, recv, &ctl->recv_bar);
+      named_bar_sync(1, kI8ConvThreads);  // this CTA's own rows, stored locally, are visible
+      const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
+      if (got && !abort) {
+        cluster_sum_rows<int32_t>(recv, split, g.splits, g.M, ct, kI8ConvThreads, [&](int m, int r, int32_t sum) {
+          const int nn = n_tile * kBN + r;
+          if (nn < g.N) finish(m, r, nn, sum);
+        });
+      }
     }
-    cluster_sync();
-    if (warp >= 2 && !abort) {
-      cluster_reduce_tile(part, split, g.splits, g.M, ct, kI8ConvThreads, [&](int m, int r, int32_t sum) {
-        const int nn = n_tile * kBN + r;
-        if (nn < g.N) finish(m, nn, sum);
-      });
-    }
-    cluster_sync();
-  } else if (warp >= 2 && !abort) {
+  } else if (holds_acc && !abort) {
     const bool n_ok = n < g.N;
     if (g.reduce == kReduceNone) {
       if (n_ok) {
 #pragma unroll
         for (int j = 0; j < kHalf; ++j)
-          if (h * kHalf + j < g.M) finish(h * kHalf + j, n, iacc[j]);
+          if (h * kHalf + j < g.M) finish(h * kHalf + j, static_cast<int>(row), n, iacc[j]);
       }
     } else {
       int32_t* part = static_cast<int32_t*>(g.ws_part);
@@ -374,7 +429,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
             if (m >= g.M) break;
             int32_t sum = 0;
             for (int s = 0; s < g.splits; ++s) sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
-            finish(m, n, sum);
+            finish(m, static_cast<int>(row), n, sum);
           }
         }
         if (ct == 0) g.ws_count[n_tile] = 0;

@@ -244,10 +244,11 @@ int launch_gemm(Kernel kernel, const Plan& p, dim3 grid, unsigned threads, size_
 template <int FMT, int MPAD>
 int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                 cudaStream_t stream) {
-  int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st); }, &g.stages);
+  const int rb = g.recv_bytes;
+  int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
   return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD>, p, dim3(p.n_tiles, p.splits, 1), qg::kThreads,
-                     qg::gemm_f8_smem_bytes<true, MPAD>(g.stages), tmW, tmA, g, stream);
+                     qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
 template <int FMT>
@@ -269,10 +270,11 @@ int run_f8_swap_fmt(int fmt, const Plan& p, const CUtensorMap& tmW, const CUtens
 template <int MPAD>
 int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
            cudaStream_t stream) {
-  int rc = pick_stages(config_id, [](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st); }, &g.stages);
+  const int rb = g.recv_bytes;
+  int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
   return launch_gemm(qg::gemm_i8_kernel<MPAD>, p, dim3(p.n_tiles, p.splits, 1), qg::kI8Threads,
-                     qg::gemm_i8_smem_bytes<MPAD>(g.stages), tmW, tmA, g, stream);
+                     qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
 // ------------------------------------------------------------------ table
@@ -524,6 +526,8 @@ int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, 
     g.ws_count = static_cast<int*>(workspace_dev);
     g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
   }
+  g.reduce = p.reduce;
+  g.recv_bytes = p.reduce == qg::kReduceCluster ? qg::cluster_recv_bytes(p.splits, static_cast<int>(M)) : 0;
   g.debug_acc = debug_acc_dev;
   g.wait_ns = g_wait_ns;
   g.force_timeout = g_force_timeout;

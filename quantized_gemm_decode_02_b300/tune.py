@@ -55,7 +55,7 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     for cfg in (0, 12):                      # ring depth: two CTAs per SM, or one deep ring
         out.append((q.QG_SWAPAB, 1, cfg))
         for s in range(2, min(16, kt) + 1):  # Split-K reduced in a cluster
-            if tiles * s > 3 * sms or kt // s < 1:
+            if tiles * s > 12 * sms or kt // s < 1:
                 continue
             out.append((q.QG_SWAPAB_SPLITK, s, cfg))
     return out
