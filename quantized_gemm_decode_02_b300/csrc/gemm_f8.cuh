@@ -167,7 +167,8 @@ __device__ __forceinline__ void cluster_sum_rows(const uint8_t* recv, int rank, 
 }
 
 // ------------------------------------------------------------ Swap-AB --
-// One CTA per (128-row weight tile, K range).  D^T[128 x MPAD] in TMEM.
+// One CTA per (128-row weight tile, K range, block of MPAD tokens).
+// D^T[128 x MPAD] in TMEM.
 template <int FMT, int MPAD>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_f8_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
@@ -187,6 +188,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x;
   const int split = blockIdx.y;
+  const int m_blk = blockIdx.z;               // token block: tokens [m_base, m_base + Mb)
+  const int m_base = m_blk * MPAD;
+  const int Mb = min(MPAD, g.M - m_base);
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
   const int nk = kb1 - kb0;
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // first push, long after)
     if (threadIdx.x == 0)
       mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
-                                                                  cluster_mv(g.M) * 4));
+                                                                  cluster_mv(Mb) * 4));
     cluster_arrive_relaxed();
   }
   pdl_launch_dependents();
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
-        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full[i], pol_a);
+        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[i], pol_a);
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint8_t* st = smem + static_cast<size_t>(s) * TS::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full[s], TS::kStageBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
-        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full[s], pol_a);
+        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[s], pol_a);
         issued = i + 1;
       }
       // Every issued copy lands before this CTA may exit or reuse the ring.
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if constexpr (!BLOCK) {
         // scales for the epilogue, fetched while the main loop runs
         const int et0 = threadIdx.x - 64, r = q * 32 + lane, nn = n_tile * kBN + r;
-        if (et0 < MPAD) ctl->sa_s[et0] = et0 < g.M ? __ldg(g.s_a + et0) : 0.0f;
+        if (et0 < MPAD) ctl->sa_s[et0] = et0 < Mb ? __ldg(g.s_a + m_base + et0) : 0.0f;
         ctl->sw_s[r] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
       }
       if constexpr (BLOCK) {
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int j = 0; j < kSaw; ++j) {
           const int t = lane + 32 * j;
-          sa_next[j] = t < g.M ? __ldg(g.s_a + static_cast<int64_t>(t) * g.kt_total + kb0) : 0.0f;
+          sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0) : 0.0f;
         }
         float sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
         for (int i = 0; i < nk; ++i) {
@@ -342,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < kSaw; ++j) {
               const int t = lane + 32 * j;
-              sa_next[j] = t < g.M ? __ldg(g.s_a + static_cast<int64_t>(t) * g.kt_total + kb0 + i + 1) : 0.0f;
+              sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i + 1)
+                                  : 0.0f;
             }
             sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
           }
@@ -396,21 +401,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int row = (warp & 3) * 32 + lane;   // epilogue threads: weight row in the tile
   const int n = n_tile * kBN + row;
   const int et = threadIdx.x - 64;          // 0..127 for the epilogue warps
-  // r: row of the tile (scales staged in shared memory); nn = n_tile*128 + r
+  // m: token of this block; r: row of the tile (scales staged in shared
+  // memory); nn = n_tile*128 + r
   auto out = [&](int m, int r, int nn, float sum) {
     const float y = BLOCK ? sum : (sum * ctl->sa_s[m]) * ctl->sw_s[r];
-    store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
+    store_bf16(g.Y + static_cast<int64_t>(m_base + m) * g.ldy + nn, y);
   };
 
   if (clustered) {
     cluster_wait();  // every peer's receive barrier is initialized
     if (warp >= 2) {
       // rows go out even after an abort, so that every owner's wait completes
-      cluster_push_row(acc, 0, row, split, g.splits, g.M, recv, &ctl->recv_bar);
+      cluster_push_row(acc, 0, row, split, g.splits, Mb, recv, &ctl->recv_bar);
       named_bar_sync(1, 128);  // this CTA's own rows, stored locally, are visible
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
       if (got && !abort) {
-        cluster_sum_rows<float>(recv, split, g.splits, g.M, et, 128, [&](int m, int r, float sum) {
+        cluster_sum_rows<float>(recv, split, g.splits, Mb, et, 128, [&](int m, int r, float sum) {
           const int nn = n_tile * kBN + r;
           if (nn < g.N) out(m, r, nn, sum);
         });
@@ -422,32 +428,34 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (n_ok) {
 #pragma unroll
         for (int m = 0; m < MPAD; ++m)
-          if (m < g.M) out(m, row, n, acc[m]);
+          if (m < Mb) out(m, row, n, acc[m]);
       }
     } else {
       float* part = static_cast<float*>(g.ws_part);
       if (n_ok) {
 #pragma unroll
         for (int m = 0; m < MPAD; ++m)
-          if (m < g.M) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = acc[m];
+          if (m < Mb) part[(static_cast<int64_t>(split) * g.M + m_base + m) * g.N + n] = acc[m];
       }
       __threadfence();
       named_bar_sync(1, 128);
+      const int tile_id = m_blk * gridDim.x + n_tile;
       if (et == 0) {
-        const int old = atomicAdd(g.ws_count + n_tile, 1);
+        const int old = atomicAdd(g.ws_count + tile_id, 1);
         ctl->last_flag = (old == g.splits - 1);
       }
       named_bar_sync(1, 128);
       if (ctl->last_flag) {
         __threadfence();
         if (n_ok) {
-          for (int m = 0; m < g.M; ++m) {
+          for (int m = 0; m < Mb; ++m) {
             float sum = 0.0f;
-            for (int s = 0; s < g.splits; ++s) sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
+            for (int s = 0; s < g.splits; ++s)
+              sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m_base + m) * g.N + n);
             out(m, row, n, sum);
           }
         }
-        if (et == 0) g.ws_count[n_tile] = 0;  // ready for the next launch
+        if (et == 0) g.ws_count[tile_id] = 0;  // ready for the next launch
       }
     }
   }

@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(kI8Threads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, split = blockIdx.y;
+  const int m_blk = blockIdx.z;               // token block: tokens [m_base, m_base + Mb)
+  const int m_base = m_blk * MPAD;
+  const int Mb = min(MPAD, g.M - m_base);
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
   const int nk = kb1 - kb0;
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   if (clustered) {
     if (threadIdx.x == 0)
       mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
-                                                                  cluster_mv(g.M) * 4));
+                                                                  cluster_mv(Mb) * 4));
     cluster_arrive_relaxed();
   }
   pdl_launch_dependents();
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full_a[i], S::kABytes);
-        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full_a[i], pol_a);
+        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[i], pol_a);
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         mbar_arrive_expect_tx(&ctl->full[s], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
         mbar_arrive_expect_tx(&ctl->full_a[s], S::kABytes);
-        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full_a[s], pol_a);
+        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[s], pol_a);
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit or reuse the ring
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       // -------------------------------------------- activation converters
       pdl_wait();  // s_a is written by the kernel this one depends on
       const int at = threadIdx.x - 32 * kI8AWarp;  // 0..63
-      if (at < MPAD) ctl->sa_s[at] = at < g.M ? __ldg(g.s_a + at) : 0.0f;
+      if (at < MPAD) ctl->sa_s[at] = at < Mb ? __ldg(g.s_a + m_base + at) : 0.0f;
       bool ok = true;
       for (int i = 0; i < nk; ++i) {
         const int buf = i % kI8OpBufs, s = i % stages;
@@ -378,11 +381,12 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   pdl_wait();  // outputs are written only after the kernel this one depends on
   const int n = n_tile * kBN + static_cast<int>(row);
   const int ct = threadIdx.x - 64;
-  // r: row of the tile (scales staged in shared memory); nn = n_tile*128 + r
+  // m: token of this block; r: row of the tile (scales staged in shared
+  // memory); nn = n_tile*128 + r
   auto finish = [&](int m, int r, int nn, int32_t acc) {
-    if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m) * g.N + nn] = acc;
+    if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m_base + m) * g.N + nn] = acc;
     const float y = (static_cast<float>(acc) * ctl->sa_s[m]) * ctl->sw_s[r];
-    store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
+    store_bf16(g.Y + static_cast<int64_t>(m_base + m) * g.ldy + nn, y);
   };
 
   const bool holds_acc = warp >= 2 && warp < kI8AWarp;
@@ -390,11 +394,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     cluster_wait();  // every peer's receive barrier is initialized
     if (holds_acc) {
       // rows go out even after an abort, so that every owner's wait completes
-      cluster_push_row(iacc, h * kHalf, static_cast<int>(row), split, g.splits, g.M, recv, &ctl->recv_bar);
+      cluster_push_row(iacc, h * kHalf, static_cast<int>(row), split, g.splits, Mb, recv, &ctl->recv_bar);
       named_bar_sync(1, kI8ConvThreads);  // this CTA's own rows, stored locally, are visible
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
       if (got && !abort) {
-        cluster_sum_rows<int32_t>(recv, split, g.splits, g.M, ct, kI8ConvThreads, [&](int m, int r, int32_t sum) {
+        cluster_sum_rows<int32_t>(recv, split, g.splits, Mb, ct, kI8ConvThreads, [&](int m, int r, int32_t sum) {
           const int nn = n_tile * kBN + r;
           if (nn < g.N) finish(m, r, nn, sum);
         });
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       if (n_ok) {
 #pragma unroll
         for (int j = 0; j < kHalf; ++j)
-          if (h * kHalf + j < g.M) finish(h * kHalf + j, static_cast<int>(row), n, iacc[j]);
+          if (h * kHalf + j < Mb) finish(h * kHalf + j, static_cast<int>(row), n, iacc[j]);
       }
     } else {
       int32_t* part = static_cast<int32_t*>(g.ws_part);
@@ -414,25 +418,27 @@ __global__ void __launch_bounds__(kI8Threads, 2)
 #pragma unroll
         for (int j = 0; j < kHalf; ++j) {
           const int m = h * kHalf + j;
-          if (m < g.M) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = iacc[j];
+          if (m < Mb) part[(static_cast<int64_t>(split) * g.M + m_base + m) * g.N + n] = iacc[j];
         }
       }
       __threadfence();
       named_bar_sync(1, kI8ConvThreads);
-      if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + n_tile, 1) == g.splits - 1);
+      const int tile_id = m_blk * gridDim.x + n_tile;
+      if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + tile_id, 1) == g.splits - 1);
       named_bar_sync(1, kI8ConvThreads);
       if (ctl->last_flag) {
         __threadfence();
         if (n_ok) {
           for (int j = 0; j < kHalf; ++j) {
             const int m = h * kHalf + j;
-            if (m >= g.M) break;
+            if (m >= Mb) break;
             int32_t sum = 0;
-            for (int s = 0; s < g.splits; ++s) sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
+            for (int s = 0; s < g.splits; ++s)
+              sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m_base + m) * g.N + n);
             finish(m, static_cast<int>(row), n, sum);
           }
         }
-        if (ct == 0) g.ws_count[n_tile] = 0;
+        if (ct == 0) g.ws_count[tile_id] = 0;
       }
     }
   }

@@ -175,9 +175,10 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   p->kt = static_cast<int>(cdiv(K, 128));
   p->n_tiles = static_cast<int>(cdiv(N, 128));
   if (p->swap) {
-    if (M > 64) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Swap-AB supports M <= 64 (got %lld)", (long long)M);
+    // tokens padded to the MMA N side; more than 64 tokens run as blocks of 64
     p->mpad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-    p->m_tiles = 1;
+    p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
+    if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else {
     p->m_tiles = static_cast<int>(cdiv(M, 128));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
@@ -189,7 +190,7 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
     return fail(QG_ERR_INVALID_ARG, "split_k=%d needs a *_SPLITK variant", split_k);
   if (split_k > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "split_k too large");
   if (fmt == QG_W8A8_INT8 && !p->swap)
-    return fail(QG_ERR_UNSUPPORTED_SHAPE, "W8A8_INT8 runs the Swap-AB variants (M <= 64)");
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "W8A8_INT8 runs the Swap-AB variants");
   p->splits = split_k;
   // Swap-AB splits of one tile reduce inside a thread-block cluster (no
   // workspace) when there are at most 16 of them; otherwise through the
@@ -247,7 +248,7 @@ int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, q
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD>, p, dim3(p.n_tiles, p.splits, 1), qg::kThreads,
+  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kThreads,
                      qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -273,7 +274,7 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_kernel<MPAD>, p, dim3(p.n_tiles, p.splits, 1), qg::kI8Threads,
+  return launch_gemm(qg::gemm_i8_kernel<MPAD>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kI8Threads,
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -291,14 +292,15 @@ std::map<Key, Row> g_table;
 bool g_table_env_checked = false;
 
 // Built-in default config ("a default config for functional testing", section
-// "Toward a Practical Adoption Model"): Swap-AB for M <= 32 (M <= 64 for
-// INT8), Standard above; split K so that tiles x splits roughly fills the two
-// CTA slots of every SM, with at least two 128-wide k-tiles per split and (for
-// Swap-AB) no more splits than one cluster reduces.
+// "Toward a Practical Adoption Model"): Swap-AB for M <= 32 (always for INT8,
+// in blocks of 64 tokens above 64), Standard above; split K so that tiles x
+// splits roughly fills the two CTA slots of every SM, with at least two
+// 128-wide k-tiles per split and (for Swap-AB) no more splits than one
+// cluster reduces.
 void default_config(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int* split_k, int* config_id) {
   const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
-  const bool swap = (fmt == QG_W8A8_INT8) ? (M <= 64) : (M <= 32);
-  const int64_t tiles = cdiv(N, 128) * (swap ? 1 : cdiv(M, 128));
+  const bool swap = (fmt == QG_W8A8_INT8) || (M <= 32);
+  const int64_t tiles = cdiv(N, 128) * (swap ? cdiv(M, M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : cdiv(M, 128));
   const int64_t kt = cdiv(K, 128);
   int64_t s = (2 * static_cast<int64_t>(sms)) / std::max<int64_t>(tiles, 1);
   s = std::min<int64_t>(s, kt / 2);
@@ -527,7 +529,9 @@ int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, 
     g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
   }
   g.reduce = p.reduce;
-  g.recv_bytes = p.reduce == qg::kReduceCluster ? qg::cluster_recv_bytes(p.splits, static_cast<int>(M)) : 0;
+  g.recv_bytes = p.reduce == qg::kReduceCluster
+                     ? qg::cluster_recv_bytes(p.splits, static_cast<int>(std::min<int64_t>(M, p.mpad)))
+                     : 0;
   g.debug_acc = debug_acc_dev;
   g.wait_ns = g_wait_ns;
   g.force_timeout = g_force_timeout;

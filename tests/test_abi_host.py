@@ -103,7 +103,6 @@ def test_gemm_validation(q):
     assert _gemm(q, variant=1, split=2) == q.QG_ERR_WORKSPACE_TOO_SMALL   # no workspace
     assert _gemm(q, variant=1, split=2, ws=OK16, wsb=16) == q.QG_ERR_WORKSPACE_TOO_SMALL
     assert _gemm(q, K=4096, variant=3, split=20) == q.QG_ERR_WORKSPACE_TOO_SMALL
-    assert _gemm(q, M=65, variant=2) == q.QG_ERR_UNSUPPORTED_SHAPE       # Swap-AB is M <= 64
     assert _gemm(q, fmt=1, M=8, variant=0) == q.QG_ERR_UNSUPPORTED_SHAPE  # INT8 runs Swap-AB
     assert _gemm(q, fmt=0, dbg=OK16) == q.QG_ERR_INVALID_ARG              # debug acc is INT8 only
     assert _gemm(q, cfg=99) == q.QG_ERR_INVALID_ARG
