@@ -1,17 +1,26 @@
 """Benchmark of the quantized decode GEMM hot path on B300.
 
-Workload (default): W8A8_INT8 over the four Qwen3-1.7B linear layers
-(qkv K=2048 N=4096, o K=2048 N=2048, gate_up K=2048 N=12288, down K=6144
-N=2048) at every tuned decode token count M in {1,2,4,8,16,24,32}.  One step
-is one pass of the whole hot path over that batch: for each (M, layer) a
-dynamic per-token activation quantization (qg_quant_act) and the quantized
-GEMM (qg_gemm_w8a8) with the variant the tuned table selects (qg_select),
-28 + 28 kernels captured once into a CUDA graph with programmatic dependent
-launch and replayed.  Every (M, layer) pair owns distinct weights, so a step
-streams 352 MB of int8 weights (> 126 MB L2): no step finds its weights in L2.
+Workload (default, `int8_qwen3_1.7b`): W8A8_INT8 over the four Qwen3-1.7B
+linear layers (qkv K=2048 N=4096, o K=2048 N=2048, gate_up K=2048 N=12288,
+down K=6144 N=2048) at every tuned decode token count M in
+{1,2,4,8,16,24,32}.  One step is one pass of the whole hot path over that
+batch: for each (M, layer) a dynamic per-token activation quantization
+(qg_quant_act) and the quantized GEMM (qg_gemm_w8a8) with the variant the
+tuned table selects (qg_select), 28 + 28 kernels captured once into a CUDA
+graph with programmatic dependent launch and replayed.  Every (M, layer) pair
+owns distinct weights, so a step streams 352 MB of int8 weights (> 126 MB
+L2): no step finds its weights in L2.
+
+Other workloads (--workload): Block_FP8 over the Qwen3-8B linears at M=1..32;
+FP8_Dynamic over the Qwen3-32B linears; FP8_Dynamic at M=1 on the Qwen3-1.7B
+o_proj shape; `layer_qwen3_8b`, all three formats on one Qwen3-8B layer's
+four linears chained in one graph at every M in 1..32; `large_m_qwen3_8b`,
+the same linears at M = 64..512 (compute-bound: TFLOP/s against the tensor
+peak of each format's MMA kind).
 
 Metric: HBM GB/s = algorithmic bytes per step / step time (the kernels must
-move the weights, activations, scales and outputs once), plus µs per GEMM.
+move the weights, activations, scales and outputs once), plus us per GEMM;
+TFLOP/s = 2*M*N*K per step / step time for the compute-bound workload.
 
 Also reported: the roofline of the GEMM kernel (per-launch durations from
 timing events inside a second graph), an end-to-end figure through the C ABI
@@ -41,16 +50,36 @@ import seeded_inputs as si  # noqa: E402
 TABLE = os.path.join(ROOT, "quantized_gemm_decode_02_b300", "tables", "b300.tsv")
 PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 
+LAYERS = ("qkv", "o", "gate_up", "down")
+FORMATS = ("FP8_Dynamic", "W8A8_INT8", "Block_FP8")
+
+
+def _items(fmts, model, layers, ms):
+    """(format, model, layer, M) in launch order: format, then token count,
+    then the layer's linears in forward order."""
+    return [(f, model, layer, M) for f in fmts for M in ms for layer in layers]
+
+
+# name: items, whether items share weights (one copy per (format, layer) and
+# token-count parity), roofline bound
 WORKLOADS = {
-    # name: (format, model, layers, token counts)
-    "int8_qwen3_1.7b": ("W8A8_INT8", "Qwen3-1.7B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
-    "fp8_qwen3_1.7b_o_m1": ("FP8_Dynamic", "Qwen3-1.7B", ("o",), (1,)),
-    "blockfp8_qwen3_8b": ("Block_FP8", "Qwen3-8B", ("qkv", "o", "gate_up", "down"), tuple(range(1, 33))),
-    "fp8_qwen3_32b": ("FP8_Dynamic", "Qwen3-32B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
-    "fp8_qwen3_8b": ("FP8_Dynamic", "Qwen3-8B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
-    "int8_qwen3_8b": ("W8A8_INT8", "Qwen3-8B", ("qkv", "o", "gate_up", "down"), si.TUNED_M),
+    "int8_qwen3_1.7b": dict(items=_items(["W8A8_INT8"], "Qwen3-1.7B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
+    "fp8_qwen3_1.7b_o_m1": dict(items=_items(["FP8_Dynamic"], "Qwen3-1.7B", ("o",), (1,)), shared=False, bound="hbm"),
+    "blockfp8_qwen3_8b": dict(items=_items(["Block_FP8"], "Qwen3-8B", LAYERS, range(1, 33)), shared=False,
+                              bound="hbm"),
+    "fp8_qwen3_32b": dict(items=_items(["FP8_Dynamic"], "Qwen3-32B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
+    "fp8_qwen3_8b": dict(items=_items(["FP8_Dynamic"], "Qwen3-8B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
+    "int8_qwen3_8b": dict(items=_items(["W8A8_INT8"], "Qwen3-8B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
+    # all three formats on one Qwen3-8B layer's four linears, chained in one
+    # graph, at every token count 1..32
+    "layer_qwen3_8b": dict(items=_items(FORMATS, "Qwen3-8B", LAYERS, range(1, 33)), shared=True, bound="hbm"),
+    # the compute-bound regime beyond the decode range
+    "large_m_qwen3_8b": dict(items=_items(FORMATS, "Qwen3-8B", LAYERS, (64, 128, 256, 384, 512)), shared=True,
+                             bound="tensor"),
 }
 DEFAULT_WORKLOAD = "int8_qwen3_1.7b"
+METRIC_HBM = "HBM GB/s (% of B300 peak) and us/GEMM at M=1..32 on Qwen3 linear shapes"
+METRIC_TENSOR = "TFLOP/s (% of B300 tensor peak) at M=64..512 on Qwen3 linear shapes"
 
 
 def gemm_bytes(fmt: str, M: int, N: int, K: int) -> int:
@@ -67,6 +96,12 @@ def quant_bytes(fmt: str, M: int, K: int) -> int:
     return 2 * M * K + M * K + 4 * scales
 
 
+def workload_dtype(items) -> str:
+    fmts = sorted({f for f, _, _, _ in items})
+    names = {"FP8_Dynamic": "e4m3", "Block_FP8": "e4m3", "W8A8_INT8": "int8"}
+    return "+".join(sorted({names[f] for f in fmts}))
+
+
 # ------------------------------------------------------------------ workload
 
 class Workload:
@@ -76,66 +111,76 @@ class Workload:
         from quantized_gemm_decode_02_b300 import qgemm as q
         self.q = q
         self.name = name
-        self.fmt, self.model, self.layers, self.ms = WORKLOADS[name]
+        spec = WORKLOADS[name]
+        self.bound = spec["bound"]
         self.device = device
         self.pdl = pdl
-        shapes = si.QWEN3_LINEARS[self.model]
-        self.items = []  # (M, layer, N, K)
-        for M in self.ms:
-            for layer in self.layers:
-                K, N = shapes[layer]
-                self.items.append((M, layer, N, K))
+        self.items = []  # (fmt, M, layer, N, K)
+        for fmt, model, layer, M in spec["items"]:
+            K, N = si.QWEN3_LINEARS[model][layer]
+            self.items.append((fmt, M, layer, N, K))
+        self.formats = sorted({it[0] for it in self.items})
+        self.models = sorted({m for _, m, _, _ in spec["items"]})
+        self.layers = list(dict.fromkeys(layer for _, _, layer, _ in spec["items"]))
+        self.ms = list(dict.fromkeys(M for _, _, _, M in spec["items"]))
         if os.path.exists(TABLE):
             q.qg_load_table(TABLE)
         q.qg_set_allow_default(True)
-        fmt = self.fmt
         # one contiguous activation buffer (bf16) and one output buffer (bf16),
         # sliced per item at 256-byte boundaries, so e2e copies are single copies
         def align(n):
             return (n + 255) // 256 * 256
         a_off, y_off, a_tot, y_tot = [], [], 0, 0
-        for (M, _, N, K) in self.items:
+        for (_, M, _, N, K) in self.items:
             a_off.append(a_tot); a_tot += align(M * K * 2)
             y_off.append(y_tot); y_tot += align(M * N * 2)
         self.A_all = torch.empty(a_tot, dtype=torch.uint8, device=device)
         self.Y_all = torch.empty(y_tot, dtype=torch.uint8, device=device)
         self.recs = []
         ws_need = 0
-        for i, (M, layer, N, K) in enumerate(self.items):
+        weights = {}
+        for i, (fmt, M, layer, N, K) in enumerate(self.items):
             variant, split, cfg = q.qg_select(fmt, M, N, K)
             need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
             ws_need = max(ws_need, need)
             A = self.A_all[a_off[i]:a_off[i] + M * K * 2].view(torch.bfloat16).view(M, K)
-            A.copy_(si.activations_device(M, K, seed=seed * 1000 + i, device=device,
-                                          outliers=(fmt == "Block_FP8")))
-            W = si.weights_device(N, K, seed=seed * 1000 + i, device=device)
-            Wq = torch.empty((N, K), dtype=torch.uint8, device=device)
-            if fmt == "Block_FP8":
-                sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device)
-                sa = torch.empty((M, K // 128), dtype=torch.float32, device=device)
-            else:
-                sw = torch.empty((N,), dtype=torch.float32, device=device)
-                sa = torch.empty((M,), dtype=torch.float32, device=device)
-            q.qg_quant_weight(fmt, W, N, K, Wq, sw)
-            del W
+            A.copy_(si.activations_device(M, K, seed=seed * 1000 + i, device=device, outliers=(fmt == "Block_FP8")))
+            # distinct weights per item, or (shared workloads) one copy per
+            # (format, layer) and token-count parity: consecutive uses of a
+            # copy are separated by the other linears' weights (> L2)
+            wkey = (fmt, layer, self.ms.index(M) % 2) if spec["shared"] else i
+            if wkey not in weights:
+                W = si.weights_device(N, K, seed=seed * 1000 + len(weights), device=device)
+                Wq = torch.empty((N, K), dtype=torch.uint8, device=device)
+                if fmt == "Block_FP8":
+                    sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device)
+                else:
+                    sw = torch.empty((N,), dtype=torch.float32, device=device)
+                q.qg_quant_weight(fmt, W, N, K, Wq, sw)
+                del W
+                weights[wkey] = (Wq, sw)
+            Wq, sw = weights[wkey]
+            sa = torch.empty((M, K // 128) if fmt == "Block_FP8" else (M,), dtype=torch.float32, device=device)
             Aq = torch.empty((M, K), dtype=torch.uint8, device=device)
             Y = self.Y_all[y_off[i]:y_off[i] + M * N * 2].view(torch.bfloat16).view(M, N)
-            self.recs.append(dict(M=M, layer=layer, N=N, K=K, A=A, Aq=Aq, sa=sa, Wq=Wq, sw=sw, Y=Y,
+            self.recs.append(dict(fmt=fmt, M=M, layer=layer, N=N, K=K, A=A, Aq=Aq, sa=sa, Wq=Wq, sw=sw, Y=Y,
                                   variant=variant, split=split, cfg=cfg, ws_need=need))
         self.ws = torch.zeros(max(ws_need, 256), dtype=torch.uint8, device=device)
         self.ws_bytes = ws_need
         torch.cuda.synchronize()
-        self.bytes_gemm = sum(gemm_bytes(fmt, r["M"], r["N"], r["K"]) for r in self.recs)
-        self.bytes_quant = sum(quant_bytes(fmt, r["M"], r["K"]) for r in self.recs)
+        self.bytes_gemm = sum(gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) for r in self.recs)
+        self.bytes_quant = sum(quant_bytes(r["fmt"], r["M"], r["K"]) for r in self.recs)
         self.bytes_step = self.bytes_gemm + self.bytes_quant
-        self.weight_bytes = sum(r["N"] * r["K"] for r in self.recs)
+        self.flops_step = sum(2 * r["M"] * r["N"] * r["K"] for r in self.recs)
+        self.weight_bytes = sum({id(r["Wq"]): r["N"] * r["K"] for r in self.recs}.values())
+        self.weight_bytes_streamed = sum(r["N"] * r["K"] for r in self.recs)
 
     def enqueue(self, stream, i: int, gemm_only: bool = False):
         r = self.recs[i]
         q = self.q
         if not gemm_only:
-            q.qg_quant_act(self.fmt, r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
-        q.qg_gemm_w8a8(self.fmt, r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"], r["N"],
+            q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
+        q.qg_gemm_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"], r["N"],
                        r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes, None, stream=stream)
 
     def capture_step(self, stream) -> torch.cuda.CUDAGraph:
@@ -158,7 +203,7 @@ class Workload:
         with torch.cuda.graph(g, stream=stream):
             for i in range(len(self.recs)):
                 r = self.recs[i]
-                self.q.qg_quant_act(self.fmt, r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
+                self.q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
                 e0 = torch.cuda.Event(enable_timing=True, external=True)
                 e1 = torch.cuda.Event(enable_timing=True, external=True)
                 e0.record(stream)
@@ -221,19 +266,21 @@ class ClockSampler:
 # --------------------------------------------------------------- cpu oracle
 
 def _oracle_items(name):
-    fmt, model, layers, ms = WORKLOADS[name]
-    shapes = si.QWEN3_LINEARS[model]
-    return fmt, [(M, *shapes[layer][::-1]) for M in ms for layer in layers]  # (M, N, K)
+    """(format, M, N, K) of every item of the workload."""
+    out = []
+    for fmt, model, layer, M in WORKLOADS[name]["items"]:
+        K, N = si.QWEN3_LINEARS[model][layer]
+        out.append((fmt, M, N, K))
+    return out
 
 
 def _oracle_pass(orc, name, cols, cache, cores):
-    """quant_act + GEMM in the oracle for every (M, layer) item, all token
-    rows, the first `cols` output columns.  Returns (seconds, bytes)."""
-    fmt, items = _oracle_items(name)
-    t_total, processed = 0.0, 0
-    for idx, (M, N, K) in enumerate(items):
+    """quant_act + GEMM in the oracle for every item, all token rows, the
+    first `cols` output columns.  Returns (seconds, bytes, flops)."""
+    t_total, processed, flops = 0.0, 0, 0
+    for idx, (fmt, M, N, K) in enumerate(_oracle_items(name)):
         nc = min(cols, N)
-        key = (N, K, nc)
+        key = (fmt, N, K, nc)
         if key not in cache:
             cache[key] = orc.quant_weight(fmt, si.weights(nc, K, seed=idx))  # setup, not timed
         Wq, sw = cache[key]
@@ -243,39 +290,60 @@ def _oracle_pass(orc, name, cols, cache, cores):
         orc.gemm(fmt, Aq, sa, Wq, sw, threads=cores)
         t_total += time.perf_counter() - t0
         processed += gemm_bytes(fmt, M, nc, K) + quant_bytes(fmt, M, K)
-    return t_total, processed
+        flops += 2 * M * nc * K
+    return t_total, processed, flops
+
+
+def _rate(bound, b, f, t):
+    return (b / t / 1e9, "GB/s") if bound == "hbm" else (f / t / 1e12, "TFLOP/s")
 
 
 def cpu_oracle_leg(name: str, budget_s: float = 12.0) -> dict:
-    """Time the CPU oracle on a bounded sample of the workload: every
-    (M, layer) item, all token rows, the first `cols` output columns of each
-    layer (a multiple of 128), doubling `cols` until one pass takes at least
-    budget/2.  GB/s counts the algorithmic bytes of the sampled part with the
+    """Time the CPU oracle on a bounded sample of the workload: every item,
+    all token rows, the first `cols` output columns of each layer (doubling
+    `cols` up to the full width while a pass stays short), then repeated
+    passes until `budget_s` seconds of oracle work are timed.  The rate
+    counts the algorithmic bytes (or flops) of the sampled part with the
     same accounting as the GPU path."""
     from oracle import oracle as orc
     orc.build()
     cores = os.cpu_count() or 1
-    cols, cache = 128, {}
+    n_max = max(n for _, _, n, _ in _oracle_items(name))
+    cols, cache = 16, {}
     while True:
-        t, b = _oracle_pass(orc, name, cols, cache, cores)
-        if t >= budget_s / 2 or cols >= 8192:
+        t, b, f = _oracle_pass(orc, name, cols, cache, cores)
+        if t >= budget_s / 4 or cols >= n_max:
             break
-        cols *= 2
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{name}: all {len(_oracle_items(name)[1])} (M, layer) items, all token rows, the first "
-                      f"{cols} output columns per layer; quant_act + GEMM in the C oracle on {cores} threads "
-                      f"({t:.1f} s)"}
+        cols = min(cols * 2, n_max)
+    passes = 1
+    while t < budget_s and passes < 64:
+        t1, b1, f1 = _oracle_pass(orc, name, cols, cache, cores)
+        t, b, f, passes = t + t1, b + b1, f + f1, passes + 1
+    v, unit = _rate(WORKLOADS[name]["bound"], b, f, t)
+    return {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"{name}: all {len(_oracle_items(name))} (format, M, layer) items, all token rows, the first "
+                      f"{cols} output columns per layer, {passes} passes; quant_act + GEMM in the C oracle on "
+                      f"{cores} threads ({t:.1f} s timed)"}
 
 
 # --------------------------------------------------------------------- main
 
 def load_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, kind): the measured copy and GEMM
+    peaks of this machine, else the fallback figures."""
     try:
         with open(PEAKS) as fh:
             p = json.load(fh)
-        return p.get("hbm_gbs", 6400.0), "measured"
+        return p.get("hbm_gbs", 6400.0), p.get("bf16_tflops", 1800.0), "measured"
     except (OSError, ValueError):
-        return 6400.0, "fallback"
+        return 6400.0, 1800.0, "fallback"
+
+
+def tensor_peak(fmt: str, bf16_tflops: float) -> float:
+    """Dense tensor peak of the MMA kind a format runs on: E4M3 runs
+    kind::f8f6f4 (nominally twice the bf16 rate), W8A8_INT8 runs kind::f16 on
+    widened operands (the bf16 rate)."""
+    return bf16_tflops * (2.0 if fmt in ("FP8_Dynamic", "Block_FP8") else 1.0)
 
 
 def dist_setup():
@@ -306,6 +374,14 @@ def max_over_ranks(world, v: float, device) -> float:
     return float(t.item())
 
 
+def _config(name, wl_items):
+    fmts = sorted({f for f, _, _, _ in wl_items})
+    models = sorted({m for _, m, _, _ in wl_items})
+    return {"workload": name, "formats": fmts, "models": models,
+            "layers": list(dict.fromkeys(layer for _, _, layer, _ in wl_items)),
+            "M": list(dict.fromkeys(M for _, _, _, M in wl_items))}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle as it stands, each step a bounded
     sample of the workload sized so the whole run stays within ~2 minutes."""
@@ -314,32 +390,33 @@ def run_reference(args, world, rank):
     from oracle import oracle as orc
     orc.build()
     name = args.workload
-    fmt, model, layers, ms = WORKLOADS[name]
+    spec = WORKLOADS[name]
     cores = os.cpu_count() or 1
     cache = {}
-    t16, _ = _oracle_pass(orc, name, 16, cache, cores)          # calibration
+    t16, _, _ = _oracle_pass(orc, name, 16, cache, cores)          # calibration
     per_step = 120.0 / max(1, args.steps + args.warmup)
     cols = 16
     while cols < 8192 and t16 * (cols * 2) / 16 <= per_step:
         cols *= 2
     for _ in range(args.warmup):
         _oracle_pass(orc, name, cols, cache, cores)
-    t_sum, b_sum = 0.0, 0
+    t_sum, b_sum, f_sum = 0.0, 0, 0
     for _ in range(args.steps):
-        t, b = _oracle_pass(orc, name, cols, cache, cores)
+        t, b, f = _oracle_pass(orc, name, cols, cache, cores)
         t_sum += t
         b_sum += b
-    value = b_sum / t_sum / 1e9
-    sample = (f"{name}: all {len(_oracle_items(name)[1])} (M, layer) items, all token rows, the first {cols} "
+        f_sum += f
+    value, unit = _rate(spec["bound"], b_sum, f_sum, t_sum)
+    sample = (f"{name}: all {len(_oracle_items(name))} (format, M, layer) items, all token rows, the first {cols} "
               f"output columns per layer, per step; quant_act + GEMM in the C oracle on {cores} threads")
-    line = {"metric": "HBM GB/s (% of B300 peak) and us/GEMM at M=1..32 on Qwen3 linear shapes",
-            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+    line = {"metric": METRIC_HBM if spec["bound"] == "hbm" else METRIC_TENSOR,
+            "value": value, "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_sum / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8" if fmt == "W8A8_INT8" else "e4m3", "data": "synthetic",
-            "config": {"workload": name, "format": fmt, "model": model, "layers": list(layers), "M": list(ms)},
+            "vs_baseline": None, "dtype": workload_dtype(spec["items"]), "data": "synthetic",
+            "config": _config(name, spec["items"]),
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -354,6 +431,9 @@ def main(argv=None):
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step's kernels directly instead of replaying the captured graph "
+                         "(for profilers that cannot follow graph nodes; not used for reported numbers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -369,6 +449,17 @@ def main(argv=None):
     graph = wl.capture_step(stream)
     timed_graph, evs = wl.capture_timed_kernels(stream)
     torch.cuda.synchronize()
+
+    if args.no_graph:
+        class _Direct:
+            """Stand-in for the step graph: enqueue the step's kernels."""
+            def replay(self_inner):
+                with torch.cuda.stream(stream):
+                    wl.q.qg_set_launch_flags(wl.q.QG_LAUNCH_PDL if wl.pdl else 0)
+                    for i in range(len(wl.recs)):
+                        wl.enqueue(stream, i)
+                    wl.q.qg_set_launch_flags(0)
+        graph = _Direct()
 
     # ---- timed region: K graph replays (one step each)
     for _ in range(args.warmup):
@@ -391,7 +482,12 @@ def main(argv=None):
     barrier(world)
     ms_step = t_start.elapsed_time(t_end) / args.steps
     ms_step = max_over_ranks(world, ms_step, device)
-    value = world * wl.bytes_step / (ms_step * 1e-3) / 1e9
+    hbm = wl.bound == "hbm"
+
+    def rate(b, f, ms):
+        return b / (ms * 1e-3) / 1e9 if hbm else f / (ms * 1e-3) / 1e12
+
+    value = world * rate(wl.bytes_step, wl.flops_step, ms_step)
     assert wl.q.qg_device_error() == 0
 
     # ---- per-launch GEMM durations (timing events inside a second graph)
@@ -405,12 +501,38 @@ def main(argv=None):
         torch.cuda.synchronize()
         per += np.array([e0.elapsed_time(e1) for (e0, e1) in evs])
     per_ms = per / reps
-    gemm_ms_total = float(per_ms.sum())
     n_gemm = len(wl.recs)
-    avg_bytes = wl.bytes_gemm / n_gemm
-    avg_ms = gemm_ms_total / n_gemm
-    achieved = avg_bytes / (avg_ms * 1e-3) / 1e9
-    peak, peak_kind = load_peaks()
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
+    # roofline of the GEMM kernel: algorithmic bytes (HBM-bound decode) or
+    # flops (compute-bound large M) per launch over the mean launch time
+    if hbm:
+        avg_units = wl.bytes_gemm / n_gemm
+        avg_ms = float(per_ms.sum()) / n_gemm
+        achieved = avg_units / (avg_ms * 1e-3) / 1e9
+        peak = hbm_peak
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "gemm (" + "+".join(wl.formats) + ")",
+                "peak_kind": peak_kind, "avg_launch_us": round(avg_ms * 1e3, 3),
+                "avg_bytes_per_launch": round(avg_units)}
+    else:
+        # the E4M3 GEMMs (the dominant kernels) against the kind::f8f6f4 peak;
+        # every format's own figure follows
+        by_fmt = {}
+        for fmt in wl.formats:
+            idx = [i for i, r in enumerate(wl.recs) if r["fmt"] == fmt]
+            fl = sum(2 * wl.recs[i]["M"] * wl.recs[i]["N"] * wl.recs[i]["K"] for i in idx)
+            t = float(per_ms[idx].sum())
+            ach = fl / (t * 1e-3) / 1e12
+            pk = tensor_peak(fmt, bf16_peak)
+            by_fmt[fmt] = {"achieved": round(ach, 1), "peak": round(pk, 1), "frac": round(ach / pk, 4)}
+        main_fmt = "FP8_Dynamic" if "FP8_Dynamic" in by_fmt else wl.formats[0]
+        fl_all = wl.flops_step
+        avg_ms = float(per_ms.sum()) / n_gemm
+        roof = {"bound": "tensor", "achieved": by_fmt[main_fmt]["achieved"], "peak": by_fmt[main_fmt]["peak"],
+                "unit": "TFLOP/s", "frac": by_fmt[main_fmt]["frac"], "traffic": None,
+                "kernel": f"gemm ({main_fmt})", "peak_kind": peak_kind + " bf16 x nominal kind ratio",
+                "by_format": by_fmt, "avg_launch_us": round(avg_ms * 1e3, 3),
+                "avg_flops_per_launch": round(fl_all / n_gemm)}
 
     # ---- end to end through the C ABI: pinned host activations in, outputs out
     host_A = torch.empty(wl.A_all.numel(), dtype=torch.uint8, pin_memory=True)
@@ -434,35 +556,41 @@ def main(argv=None):
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / e2e_steps, device)
-    e2e_val = world * wl.bytes_step / (e2e_ms * 1e-3) / 1e9
+    e2e_val = world * rate(wl.bytes_step, wl.flops_step, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_leg(args.workload)
 
-    per_gemm = [{"M": r["M"], "layer": r["layer"], "N": r["N"], "K": r["K"], "variant": r["variant"],
-                 "split_k": r["split"], "us": round(float(per_ms[i]) * 1e3, 3),
-                 "GBps": round(gemm_bytes(wl.fmt, r["M"], r["N"], r["K"]) / (per_ms[i] * 1e-3) / 1e9, 1)}
+    per_gemm = [{"fmt": r["fmt"], "M": r["M"], "layer": r["layer"], "N": r["N"], "K": r["K"],
+                 "variant": r["variant"], "split_k": r["split"], "us": round(float(per_ms[i]) * 1e3, 3),
+                 "GBps": round(gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) / (per_ms[i] * 1e-3) / 1e9, 1),
+                 "TFLOPs": round(2 * r["M"] * r["N"] * r["K"] / (per_ms[i] * 1e-3) / 1e12, 2)}
                 for i, r in enumerate(wl.recs)]
     if rank == 0:
+        unit = "GB/s" if hbm else "TFLOP/s"
+        cfg = _config(args.workload, WORKLOADS[args.workload]["items"])
+        cfg.update({
+            "gemms_per_step": n_gemm, "kernels_per_step": 2 * n_gemm,
+            "bytes_per_step": wl.bytes_step, "flops_per_step": wl.flops_step,
+            "weight_bytes_streamed_per_step": wl.weight_bytes_streamed,
+            "l2": (f"inputs larger than L2: {wl.weight_bytes_streamed / 1e6:.0f} MB of weights streamed per step "
+                   + ("(distinct weights per GEMM)" if not WORKLOADS[args.workload]["shared"] else
+                      f"({wl.weight_bytes / 1e6:.0f} MB distinct; a reuse is separated by > 126 MB of other "
+                      "weights)")),
+            "graph": "one CUDA graph per step" + ("" if args.no_pdl else ", programmatic dependent launch"),
+            "parallelism": f"replicas x{world}",
+            "us_per_gemm": round(ms_step * 1e3 / n_gemm, 3)})
+        if hbm:
+            cfg["pct_of_peak"] = round(100 * value / world / hbm_peak, 1)
         line = {
-            "metric": "HBM GB/s (% of B300 peak) and us/GEMM at M=1..32 on Qwen3 linear shapes",
-            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "metric": METRIC_HBM if hbm else METRIC_TENSOR,
+            "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8" if wl.fmt == "W8A8_INT8" else "e4m3", "data": "synthetic",
-            "config": {"workload": args.workload, "format": wl.fmt, "model": wl.model, "layers": list(wl.layers),
-                       "M": list(wl.ms), "gemms_per_step": n_gemm, "kernels_per_step": 2 * n_gemm,
-                       "bytes_per_step": wl.bytes_step, "weight_bytes_per_step": wl.weight_bytes,
-                       "l2": f"inputs larger than L2: {wl.weight_bytes / 1e6:.0f} MB of distinct weights per step",
-                       "graph": "one CUDA graph per step" + ("" if args.no_pdl else ", programmatic dependent launch"),
-                       "parallelism": f"replicas x{world}",
-                       "us_per_gemm": round(ms_step * 1e3 / n_gemm, 3),
-                       "pct_of_peak": round(100 * value / world / peak, 1)},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": f"gemm ({wl.fmt})", "peak_kind": peak_kind,
-                         "avg_launch_us": round(avg_ms * 1e3, 3), "avg_bytes_per_launch": round(avg_bytes)},
-            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(wl.A_all.numel()),
+            "dtype": workload_dtype(WORKLOADS[args.workload]["items"]), "data": "synthetic",
+            "config": cfg,
+            "roofline": roof,
+            "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": int(wl.A_all.numel()),
                     "d2h_bytes_per_step": int(wl.Y_all.numel()), "ms_per_step": round(e2e_ms, 6)},
             "gpu_launches": 2 * n_gemm * args.steps,
             "clocks": clk,

@@ -17,6 +17,8 @@ sweep resumes where it stopped.
 Usage:  python -m quantized_gemm_decode_02_b300.tune --out TABLE
             [--formats FP8_Dynamic,W8A8_INT8,Block_FP8]
             [--models Qwen3-1.7B,Qwen3-8B,Qwen3-32B] [--ms 1,2,4,8,16,24,32]
+The decode table covers the tuned token counts; a second pass with
+--ms 64,128,256,384,512 adds rows for the compute-bound regime.
 """
 from __future__ import annotations
 
@@ -48,16 +50,29 @@ POOL_BYTES = 512 << 20
 
 
 def candidates(fmt: str, M: int, N: int, K: int, sms: int):
-    """(variant, split_k, config_id) candidates for one shape."""
-    tiles = (N + 127) // 128
+    """(variant, split_k, config_id) candidates for one shape: Swap-AB with
+    and without Split-K (reduced in a cluster, up to 16 ranges) for every M
+    (in blocks of 64 tokens above 64); above 32 tokens also the Standard
+    variant of the E4M3 formats.  Ring depth: 0 = two CTAs per SM, 12 = one
+    deep ring per SM (6 for Standard, whose stages are twice as large)."""
+    n_tiles = (N + 127) // 128
     kt = (K + 127) // 128
+    mpad = 16 if M <= 16 else (32 if M <= 32 else 64)
+    tiles = n_tiles * -(-M // mpad)
     out = []
-    for cfg in (0, 12):                      # ring depth: two CTAs per SM, or one deep ring
+    for cfg in (0, 12):
         out.append((q.QG_SWAPAB, 1, cfg))
-        for s in range(2, min(16, kt) + 1):  # Split-K reduced in a cluster
+        for s in range(2, min(16, kt) + 1):
             if tiles * s > 12 * sms or kt // s < 1:
                 continue
             out.append((q.QG_SWAPAB_SPLITK, s, cfg))
+    if M > 32 and fmt != "W8A8_INT8":
+        std_tiles = n_tiles * -(-M // 128)
+        for cfg in (0, 6):
+            out.append((q.QG_STANDARD, 1, cfg))
+            for s in (2, 3, 4, 6, 8):
+                if s <= kt and std_tiles * s <= 4 * sms:
+                    out.append((q.QG_SPLITK, s, cfg))
     return out
 
 
