@@ -107,10 +107,11 @@ def workload_dtype(items) -> str:
 class Workload:
     """Device buffers and the captured graphs for one workload."""
 
-    def __init__(self, name: str, device: str, seed: int = 0, pdl: bool = True):
+    def __init__(self, name: str, device: str, seed: int = 0, pdl: bool = True, fused: bool = False):
         from quantized_gemm_decode_02_b300 import qgemm as q
         self.q = q
         self.name = name
+        self.fused = fused
         spec = WORKLOADS[name]
         self.bound = spec["bound"]
         self.device = device
@@ -175,11 +176,27 @@ class Workload:
         self.weight_bytes = sum({id(r["Wq"]): r["N"] * r["K"] for r in self.recs}.values())
         self.weight_bytes_streamed = sum(r["N"] * r["K"] for r in self.recs)
 
-    def enqueue(self, stream, i: int, gemm_only: bool = False):
+    def fused_item(self, i: int) -> bool:
+        """Whether item i runs as one kernel (activation quantization inside
+        the GEMM): FP8_Dynamic / W8A8_INT8 with the Swap-AB variants."""
+        r = self.recs[i]
+        return self.fused and r["fmt"] != "Block_FP8" and r["variant"] in (self.q.QG_SWAPAB, self.q.QG_SWAPAB_SPLITK)
+
+    def kernels(self, i: int) -> int:
+        return 1 if self.fused_item(i) else 2
+
+    def enqueue(self, stream, i: int):
+        """One linear layer: activation quantization + GEMM (one kernel when
+        fused, else qg_quant_act then qg_gemm_w8a8)."""
         r = self.recs[i]
         q = self.q
-        if not gemm_only:
-            q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
+        if self.fused:
+            fz = self.fused_item(i)
+            q.qg_linear_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["A"], r["K"], r["Wq"], r["sw"], r["Y"], r["N"],
+                             r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes,
+                             None if fz else r["Aq"], None if fz else r["sa"], None, stream=stream)
+            return
+        q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
         q.qg_gemm_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"], r["N"],
                        r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes, None, stream=stream)
 
@@ -196,18 +213,17 @@ class Workload:
         return g
 
     def capture_timed_kernels(self, stream):
-        """The same step with timing events around every GEMM launch (no PDL:
-        the events sit between kernels).  Returns (graph, event pairs)."""
+        """The same step with timing events around every linear layer (its
+        quantization and GEMM; no PDL: the events sit between kernels).
+        Returns (graph, event pairs)."""
         g = torch.cuda.CUDAGraph()
         evs = []
         with torch.cuda.graph(g, stream=stream):
             for i in range(len(self.recs)):
-                r = self.recs[i]
-                self.q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
                 e0 = torch.cuda.Event(enable_timing=True, external=True)
                 e1 = torch.cuda.Event(enable_timing=True, external=True)
                 e0.record(stream)
-                self.enqueue(stream, i, gemm_only=True)
+                self.enqueue(stream, i)
                 e1.record(stream)
                 evs.append((e0, e1))
         return g, evs
@@ -429,6 +445,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="quantize activations inside the GEMM kernel (qg_linear_w8a8) instead of in their own "
+                         "kernel (qg_quant_act + qg_gemm_w8a8); measured slower on B300, so not the default")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-graph", action="store_true",
@@ -444,7 +463,7 @@ def main(argv=None):
         raise SystemExit("bench.py needs a CUDA device (the compute path is the sm_103a library)")
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    wl = Workload(args.workload, device, seed=rank, pdl=not args.no_pdl)
+    wl = Workload(args.workload, device, seed=rank, pdl=not args.no_pdl, fused=args.fused)
     stream = torch.cuda.Stream(device=device)
     graph = wl.capture_step(stream)
     timed_graph, evs = wl.capture_timed_kernels(stream)
@@ -503,17 +522,21 @@ def main(argv=None):
     per_ms = per / reps
     n_gemm = len(wl.recs)
     hbm_peak, bf16_peak, peak_kind = load_peaks()
-    # roofline of the GEMM kernel: algorithmic bytes (HBM-bound decode) or
-    # flops (compute-bound large M) per launch over the mean launch time
+    n_kernels = sum(wl.kernels(i) for i in range(n_gemm))
+    # roofline of the linear layer (its GEMM kernel, with the activation
+    # quantization fused in or in its own kernel before it): algorithmic
+    # bytes (HBM-bound decode) or flops (compute-bound large M) per layer
+    # over the mean time of a layer
     if hbm:
-        avg_units = wl.bytes_gemm / n_gemm
+        avg_units = wl.bytes_step / n_gemm
         avg_ms = float(per_ms.sum()) / n_gemm
         achieved = avg_units / (avg_ms * 1e-3) / 1e9
         peak = hbm_peak
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "gemm (" + "+".join(wl.formats) + ")",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": ("fused quantize+gemm" if wl.fused else "quant_act + gemm") + " (" + "+".join(wl.formats) + ")",
                 "peak_kind": peak_kind, "avg_launch_us": round(avg_ms * 1e3, 3),
-                "avg_bytes_per_launch": round(avg_units)}
+                "avg_bytes_per_launch": round(avg_units), "kernels_per_layer": round(n_kernels / n_gemm, 3)}
     else:
         # the E4M3 GEMMs (the dominant kernels) against the kind::f8f6f4 peak;
         # every format's own figure follows
@@ -571,7 +594,9 @@ def main(argv=None):
         unit = "GB/s" if hbm else "TFLOP/s"
         cfg = _config(args.workload, WORKLOADS[args.workload]["items"])
         cfg.update({
-            "gemms_per_step": n_gemm, "kernels_per_step": 2 * n_gemm,
+            "gemms_per_step": n_gemm, "kernels_per_step": n_kernels,
+            "activation_quantization": "fused into the GEMM kernel (qg_linear_w8a8) where one kernel does both"
+                                       if wl.fused else "own kernel (qg_quant_act)",
             "bytes_per_step": wl.bytes_step, "flops_per_step": wl.flops_step,
             "weight_bytes_streamed_per_step": wl.weight_bytes_streamed,
             "l2": (f"inputs larger than L2: {wl.weight_bytes_streamed / 1e6:.0f} MB of weights streamed per step "
@@ -592,7 +617,7 @@ def main(argv=None):
             "roofline": roof,
             "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": int(wl.A_all.numel()),
                     "d2h_bytes_per_step": int(wl.Y_all.numel()), "ms_per_step": round(e2e_ms, 6)},
-            "gpu_launches": 2 * n_gemm * args.steps,
+            "gpu_launches": n_kernels * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
             "per_gemm": per_gemm,

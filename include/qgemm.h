@@ -111,6 +111,28 @@ QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_
                  const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
                  int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream);
 
+/* The whole quantized linear layer in one call: dynamic activation
+ * quantization ("Scope": per token, or per 1x128 group for Block_FP8)
+ * followed by the quantized GEMM ("Kernel Implementation"), i.e.
+ * qg_quant_act then qg_gemm_w8a8 with the same results bit for bit.  For
+ * FP8_Dynamic and W8A8_INT8 with the Swap-AB variants both steps run in ONE
+ * kernel: each CTA quantizes the slice of the activations its K range needs,
+ * the CTAs of a Split-K cluster agree on every token's maximum over the
+ * whole row through distributed shared memory, and no quantized activation
+ * tensor is written unless asked for.  Block_FP8 and the Standard variants
+ * run the two kernels in sequence.
+ *   A_dev      bf16 [M][lda] activations (lda >= K, lda % 8 == 0, 16-byte
+ *              aligned), read-only;
+ *   W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id, workspace,
+ *   ws_bytes, debug_acc_dev   as qg_gemm_w8a8;
+ *   A_q_dev, s_a_dev  [M][K] codes and the scales (layouts of qg_quant_act):
+ *              optional outputs in the fused case (NULL to skip), required
+ *              buffers for Block_FP8 and the Standard variants. */
+QG_API int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, int64_t lda,
+                          const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
+                          int split_k, int config_id, void* workspace_dev, size_t ws_bytes, void* A_q_dev,
+                          float* s_a_dev, int32_t* debug_acc_dev, void* stream);
+
 /* Allocation-free form of qg_gemm_w8a8 (the pages have no counterpart; this
  * is a convenience of this library).  It is for callers that cannot call
  * cudaMalloc at all: code running inside a host framework or serving runtime

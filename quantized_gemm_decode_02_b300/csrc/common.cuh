@@ -137,6 +137,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile
+// (the layout sw128_kmajor_desc describes).
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t r, uint32_t c) {
+  return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
+}
+
 // Instruction descriptor: dense, D = f32, K-major A and B, shape M x N.
 // a_fmt/b_fmt: kind::f8f6f4 -> 0 = E4M3; kind::f16 -> 0 = F16, 1 = BF16.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t m, uint32_t n, uint32_t a_fmt, uint32_t b_fmt) {
@@ -204,6 +210,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t
                                             uint32_t cbar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(caddr),
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
+               : "memory");
+}
+// 4 bytes from a register into a peer CTA's shared memory (see st_async_v4).
+__device__ __forceinline__ void st_async_b32(uint32_t caddr, uint32_t a, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr), "r"(a),
+               "r"(cbar)
                : "memory");
 }
 // Bounded wait with cluster-scope acquire (for data peers wrote with st.async).

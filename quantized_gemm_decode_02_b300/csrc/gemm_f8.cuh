@@ -49,6 +49,12 @@ struct GemmArgs {
   void* ws_part;        // kReduceGlobal: [splits][M][N] fp32 (or int32) partials
   int* ws_count;        // kReduceGlobal: one arrival counter per output tile, zero between launches
   int32_t* debug_acc;   // [M][N] int32 accumulators (W8A8_INT8 only) or null
+  // fused activation quantization (qg_linear_w8a8): the kernel reads bf16
+  // activations and quantizes them itself; A_q / s_a are optional copies
+  const __nv_bfloat16* A;  // [M][lda] bf16
+  int64_t lda;
+  uint8_t* a_q_out;        // [M][K] codes, or null
+  float* s_a_out;          // per-token scales, or null
   uint64_t wait_ns;     // bound of every pipeline wait
   int force_timeout;    // test hook: the MMA thread first waits on a barrier nothing arrives on
 };
@@ -71,11 +77,14 @@ struct alignas(8) Ctrl {
   uint64_t tempty[4];
   uint64_t never;
   uint64_t recv_bar;  // split-K: peers' partial rows have landed
+  uint64_t amax_bar;  // fused quantization: peers' partial row maxima have landed
+  uint64_t full_a[16];  // fused quantization: the stage's activation tile is written
   uint32_t tmem_base;
   int last_flag;
   int abort_flag;
   float sa_s[64];   // per-token scales, staged for the epilogue
   float sw_s[128];  // per-channel scales of the tile's rows
+  float amax_s[kMaxClusterSplits * 64];  // fused quantization: [source rank][token] partial row maxima
 };
 
 template <bool SWAP, int MPAD>
@@ -166,14 +175,88 @@ __device__ __forceinline__ void cluster_sum_rows(const uint8_t* recv, int rank, 
   }
 }
 
+// Fused activation quantization, part 1: the scale of every token of this
+// CTA's block (the per-token formats, "Scope": one scale per token over the
+// whole row).  `nthr` threads (index t, a multiple of 32) take the maximum
+// |A| of each token over this CTA's K range [k0, k1); with Split-K in a
+// cluster each CTA pushes its partial maxima to every peer (st.async into
+// amax_s[src][token]) and waits for theirs, so every CTA holds the row
+// maximum over all of K; then s = amax / qmax (IEEE, 1 for an all-zero row)
+// goes to sa_s.  With Split-K through the workspace, [k0, k1) must be the
+// whole row.  Ends with a barrier among the nthr threads.
+__device__ __forceinline__ void fused_token_scales(const GemmArgs& g, int m_base, int Mb, int k0, int k1,
+                                                   bool clustered, int rank, float qmax, float* amax_s, float* sa_s,
+                                                   uint64_t* amax_bar, int t, int nthr, int bar_id,
+                                                   bool write_scales) {
+  const int warps = nthr / 32, w = t >> 5, lane = t & 31;
+  for (int m = w; m < Mb; m += warps) {
+    const __nv_bfloat16* row = g.A + static_cast<int64_t>(m_base + m) * g.lda;
+    float mx = 0.0f;
+    for (int k = k0 + lane * 8; k < k1; k += 256) {
+      float v[8];
+      load8(row + k, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    }
+    mx = warp_max(mx);
+    if (lane == 0) amax_s[rank * 64 + m] = mx;
+  }
+  named_bar_sync(bar_id, nthr);
+  if (clustered) {
+    cluster_wait();  // every peer's barriers are initialized
+    if (t < Mb) {
+      const uint32_t addr = smem_u32(&amax_s[rank * 64 + t]), bar = smem_u32(amax_bar);
+      const uint32_t v = __float_as_uint(amax_s[rank * 64 + t]);
+      for (int o = 0; o < g.splits; ++o)
+        if (o != rank) st_async_b32(dsmem_map(addr, static_cast<uint32_t>(o)), v, dsmem_map(bar, static_cast<uint32_t>(o)));
+    }
+    mbar_wait_cluster(amax_bar, 0, g.wait_ns);
+  }
+  if (t < 64) {
+    float mx = 0.0f;
+    if (t < Mb) {
+      if (clustered) {
+        for (int o = 0; o < g.splits; ++o) mx = fmaxf(mx, amax_s[o * 64 + t]);
+      } else {
+        mx = amax_s[rank * 64 + t];
+      }
+    }
+    sa_s[t] = t < Mb ? scale_from_amax(mx, qmax) : 0.0f;
+    if (write_scales && t < Mb && g.s_a_out) g.s_a_out[m_base + t] = sa_s[t];
+  }
+  named_bar_sync(bar_id, nthr);
+}
+
+// Fused activation quantization, part 2: 32 consecutive activations of token
+// row `row` starting at column k (zeros past K) as fp32.
+__device__ __forceinline__ void load_act32(const GemmArgs& g, int row, int k, float (&x)[32]) {
+  const __nv_bfloat16* p = g.A + static_cast<int64_t>(row) * g.lda + k;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float v[8];
+    if (k + 8 * c < g.K) {
+      load8(p + 8 * c, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[8 * c + i] = v[i];
+  }
+}
+
 // ------------------------------------------------------------ Swap-AB --
 // One CTA per (128-row weight tile, K range, block of MPAD tokens).
 // D^T[128 x MPAD] in TMEM.
-template <int FMT, int MPAD>
+// FUSED (FP8_Dynamic only): the epilogue warps, idle during the main loop,
+// read bf16 activations (g.A), quantize them per token and write each
+// stage's activation tile themselves (qg_linear_w8a8); tmA is unused.
+template <int FMT, int MPAD, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_f8_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using TS = TileShape<true, MPAD>;
   constexpr bool BLOCK = (FMT == kFmtBlock);
+  static_assert(!(FUSED && BLOCK), "fused quantization is per token");
   constexpr int NBUF = BLOCK ? 4 : 1;
   constexpr uint32_t kTmemCols = pow2_cols(NBUF * MPAD);
   static_assert(kTmemCols <= 256, "two CTAs per SM share the 512 TMEM columns");
@@ -207,22 +290,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->recv_bar, 1);
+    mbar_init(&ctl->amax_bar, 1);
+    if (FUSED)
+      for (int i = 0; i < stages; ++i) mbar_init(&ctl->full_a[i], 4);
     ctl->last_flag = 0;
     ctl->abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmW);
-    prefetch_tmap(&tmA);
+    if (!FUSED) prefetch_tmap(&tmA);
   }
   __syncthreads();
   if (clustered) {
-    // the receive barrier expects the peers' rows; every thread then marks
-    // this CTA's barriers initialized for the cluster (waited on before the
-    // first push, long after)
-    if (threadIdx.x == 0)
+    // the receive barriers expect the peers' rows (and, fused, their row
+    // maxima); every thread then marks this CTA's barriers initialized for
+    // the cluster (waited on before the first push)
+    if (threadIdx.x == 0) {
       mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
                                                                   cluster_mv(Mb) * 4));
+      if (FUSED) mbar_arrive_expect_tx(&ctl->amax_bar, static_cast<uint32_t>((g.splits - 1) * Mb * 4));
+    }
     cluster_arrive_relaxed();
   }
   pdl_launch_dependents();
@@ -240,15 +328,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       const int w_row = n_tile * kBN;
       const int pre = nk < stages ? nk : stages;
+      constexpr uint32_t kTx = FUSED ? TS::kWBytes : TS::kStageBytes;  // fused: threads write the activations
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
-        mbar_arrive_expect_tx(&ctl->full[i], TS::kStageBytes);
+        mbar_arrive_expect_tx(&ctl->full[i], kTx);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) {
-        uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
-        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[i], pol_a);
+      if (!FUSED) {
+        for (int i = 0; i < pre; ++i) {
+          uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
+          tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[i], pol_a);
+        }
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -259,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           break;
         }
         uint8_t* st = smem + static_cast<size_t>(s) * TS::kStageBytes;
-        mbar_arrive_expect_tx(&ctl->full[s], TS::kStageBytes);
+        mbar_arrive_expect_tx(&ctl->full[s], kTx);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
-        tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[s], pol_a);
+        if (!FUSED) tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[s], pol_a);
         issued = i + 1;
       }
       // Every issued copy lands before this CTA may exit or reuse the ring.
@@ -290,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               break;
             }
           }
-          if (!mbar_wait(&ctl->full[s], ph, g.wait_ns)) {
+          if (!mbar_wait(&ctl->full[s], ph, g.wait_ns) || (FUSED && !mbar_wait(&ctl->full_a[s], ph, g.wait_ns))) {
             ok = false;
             break;
           }
@@ -323,8 +414,58 @@ __global__ void __launch_bounds__(kThreads, 2)
       if constexpr (!BLOCK) {
         // scales for the epilogue, fetched while the main loop runs
         const int et0 = threadIdx.x - 64, r = q * 32 + lane, nn = n_tile * kBN + r;
-        if (et0 < MPAD) ctl->sa_s[et0] = et0 < Mb ? __ldg(g.s_a + m_base + et0) : 0.0f;
+        if (!FUSED && et0 < MPAD) ctl->sa_s[et0] = et0 < Mb ? __ldg(g.s_a + m_base + et0) : 0.0f;
         ctl->sw_s[r] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
+      }
+      if constexpr (FUSED) {
+        // per-token scales, then every stage's activation tile as E4M3
+        const int et0 = threadIdx.x - 64;
+        const bool whole_row = !clustered && g.splits > 1;
+        const int k0 = whole_row ? 0 : kb0 * kBK, k1 = whole_row ? g.K : min(g.K, kb1 * kBK);
+        fused_token_scales(g, m_base, Mb, k0, k1, clustered, clustered ? split : 0, 448.0f, ctl->amax_s, ctl->sa_s,
+                           &ctl->amax_bar, et0, 128, 3, n_tile == 0 && split == 0);
+        const bool write_codes = g.a_q_out != nullptr && n_tile == 0;
+        for (int i = 0; i < nk; ++i) {
+          const int s = i % stages;
+          // the weight tile of this use of the slot has landed, so the
+          // previous use (and its activation tile) is finished
+          if (!__all_sync(0xffffffffu, mbar_wait(&ctl->full[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns) &&
+                                           !*abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          const int kt0 = (kb0 + i) * kBK;
+          uint8_t* at = smem + static_cast<size_t>(s) * TS::kStageBytes + TS::kWBytes;
+#pragma unroll
+          for (int piece = et0; piece < MPAD * 4; piece += 128) {
+            const int r = piece >> 2, p = piece & 3;  // token row, 32-element quarter of the 128 K
+            uint32_t w[8];
+            if (r < Mb) {
+              float x[32];
+              load_act32(g, m_base + r, kt0 + 32 * p, x);
+              const Divider dv(ctl->sa_s[r]);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                w[j] = static_cast<uint32_t>(e4m3x2(dv(x[4 * j]), dv(x[4 * j + 1]))) |
+                       (static_cast<uint32_t>(e4m3x2(dv(x[4 * j + 2]), dv(x[4 * j + 3]))) << 16);
+              if (write_codes) {
+                uint8_t* dst = g.a_q_out + static_cast<int64_t>(m_base + r) * g.K + kt0 + 32 * p;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                  if (kt0 + 32 * p + 16 * c < g.K)
+                    *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = 0u;
+            }
+            *reinterpret_cast<uint4*>(at + sw128_chunk(r, 2 * p)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(at + sw128_chunk(r, 2 * p + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->full_a[s]);
+        }
       }
       if constexpr (BLOCK) {
         const int nb = n_tile;  // 128-row tile == weight block row
@@ -409,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 
   if (clustered) {
-    cluster_wait();  // every peer's receive barrier is initialized
     if (warp >= 2) {
+      if (!FUSED) cluster_wait();  // every peer's receive barrier is initialized (fused: waited already)
       // rows go out even after an abort, so that every owner's wait completes
       cluster_push_row(acc, 0, row, split, g.splits, Mb, recv, &ctl->recv_bar);
       named_bar_sync(1, 128);  // this CTA's own rows, stored locally, are visible

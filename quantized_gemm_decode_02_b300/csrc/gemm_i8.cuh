@@ -57,11 +57,13 @@ struct alignas(8) CtrlI8 {
   uint64_t never;
   uint64_t done;
   uint64_t recv_bar;  // split-K: peers' partial rows have landed
+  uint64_t amax_bar;  // fused quantization: peers' partial row maxima have landed
   uint32_t tmem_base;
   int last_flag;
   int abort_flag;
   float sa_s[64];   // per-token scales, staged for the epilogue
   float sw_s[128];  // per-channel scales of the tile's rows
+  float amax_s[kMaxClusterSplits * 64];  // fused quantization: [source rank][token] partial row maxima
 };
 
 template <int MPAD>
@@ -97,12 +99,10 @@ __device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-// Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128_chunk(uint32_t r, uint32_t c) {
-  return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
-}
-
-template <int MPAD>
+// FUSED: the activation warps read bf16 activations (g.A) and quantize them
+// to int8 codes themselves (qg_linear_w8a8): no quantization kernel and no
+// int8 activation tensor in between; tmA is unused.
+template <int MPAD, bool FUSED>
 __global__ void __launch_bounds__(kI8Threads, 2)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = I8Shape<MPAD>;
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->full_a[i], 1);
-      mbar_init(&ctl->empty[i], kI8ConvWarps + kI8AWarps);
+      mbar_init(&ctl->empty[i], kI8ConvWarps + (FUSED ? 0 : kI8AWarps));
     }
     for (int b = 0; b < kI8OpBufs; ++b) {
       mbar_init(&ctl->op_full[b], kI8ConvWarps + kI8AWarps);
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->done, 1);
     mbar_init(&ctl->recv_bar, 1);
+    mbar_init(&ctl->amax_bar, 1);
     ctl->last_flag = 0;
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -152,9 +153,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   }
   __syncthreads();
   if (clustered) {
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
       mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
                                                                   cluster_mv(Mb) * 4));
+      if (FUSED) mbar_arrive_expect_tx(&ctl->amax_bar, static_cast<uint32_t>((g.splits - 1) * Mb * 4));
+    }
     cluster_arrive_relaxed();
   }
   pdl_launch_dependents();
@@ -179,10 +182,12 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) {
-        uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
-        mbar_arrive_expect_tx(&ctl->full_a[i], S::kABytes);
-        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[i], pol_a);
+      if (!FUSED) {
+        for (int i = 0; i < pre; ++i) {
+          uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
+          mbar_arrive_expect_tx(&ctl->full_a[i], S::kABytes);
+          tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[i], pol_a);
+        }
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -195,14 +200,16 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full[s], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
-        mbar_arrive_expect_tx(&ctl->full_a[s], S::kABytes);
-        tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[s], pol_a);
+        if (!FUSED) {
+          mbar_arrive_expect_tx(&ctl->full_a[s], S::kABytes);
+          tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[s], pol_a);
+        }
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit or reuse the ring
       for (int j = issued > stages ? issued - stages : 0; j < issued; ++j) {
         mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
-        mbar_wait(&ctl->full_a[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+        if (!FUSED) mbar_wait(&ctl->full_a[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
       }
     }
   } else {
@@ -249,6 +256,68 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         }
         tc_commit(&ctl->done);  // all issued MMAs complete
       }
+    } else if (FUSED && warp >= kI8AWarp) {
+      // ---------------------------------------- activation quantizers (fused)
+      pdl_wait();  // the activations are written by the kernel this one depends on
+      const int at = threadIdx.x - 32 * kI8AWarp;  // 0..63
+      const bool whole_row = !clustered && g.splits > 1;  // workspace Split-K: scale over the whole row
+      const int k0 = whole_row ? 0 : kb0 * kBK, k1 = whole_row ? g.K : min(g.K, kb1 * kBK);
+      fused_token_scales(g, m_base, Mb, k0, k1, clustered, clustered ? split : 0, 127.0f, ctl->amax_s, ctl->sa_s,
+                         &ctl->amax_bar, at, 32 * kI8AWarps, 3, n_tile == 0 && split == 0);
+      const bool write_codes = g.a_q_out != nullptr && n_tile == 0;
+      bool ok = true;
+      for (int i = 0; i < nk; ++i) {
+        const int buf = i % kI8OpBufs;
+        if (i >= kI8OpBufs &&
+            !__all_sync(0xffffffffu, mbar_wait(&ctl->op_empty[buf], static_cast<uint32_t>(i / kI8OpBufs - 1) & 1u,
+                                               g.wait_ns) && !*abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int kt0 = (kb0 + i) * kBK;
+        uint8_t* ob = opb + buf * S::kOpBBytes;
+#pragma unroll
+        for (int piece = at; piece < MPAD * 4; piece += 32 * kI8AWarps) {
+          const int r = piece >> 2, p = piece & 3;  // token row, 32-element quarter of the 128 K
+          uint32_t o[16];
+          if (r < Mb) {
+            float x[32];
+            load_act32(g, m_base + r, kt0 + 32 * p, x);
+            const Divider dv(ctl->sa_s[r]);
+            uint32_t codes[8];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int q0 = max(-127, min(127, __float2int_rn(dv(x[2 * j]))));
+              const int q1 = max(-127, min(127, __float2int_rn(dv(x[2 * j + 1]))));
+              __half2 hh = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+              o[j] = *reinterpret_cast<uint32_t*>(&hh);
+              const uint32_t pair = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8);
+              if (j & 1) codes[j >> 1] |= pair << 16; else codes[j >> 1] = pair;
+            }
+            if (write_codes) {
+              uint8_t* dst = g.a_q_out + static_cast<int64_t>(m_base + r) * g.K + kt0 + 32 * p;
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                if (kt0 + 32 * p + 16 * c < g.K)
+                  *reinterpret_cast<uint4*>(dst + 16 * c) =
+                      make_uint4(codes[4 * c], codes[4 * c + 1], codes[4 * c + 2], codes[4 * c + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = 0u;
+          }
+          uint8_t* atom = ob + (p >> 1) * (MPAD * 128);
+          const uint32_t c0 = (p & 1) * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(atom + sw128_chunk(r, c0 + j)) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->op_full[buf]);
+      }
+      if (!ok) *abort_flag = 1;
     } else if (warp >= kI8AWarp) {
       // -------------------------------------------- activation converters
       pdl_wait();  // s_a is written by the kernel this one depends on
@@ -391,8 +460,8 @@ __global__ void __launch_bounds__(kI8Threads, 2)
 
   const bool holds_acc = warp >= 2 && warp < kI8AWarp;
   if (clustered) {
-    cluster_wait();  // every peer's receive barrier is initialized
     if (holds_acc) {
+      cluster_wait();  // every peer's receive barrier is initialized
       // rows go out even after an abort, so that every owner's wait completes
       cluster_push_row(iacc, h * kHalf, static_cast<int>(row), split, g.splits, Mb, recv, &ctl->recv_bar);
       named_bar_sync(1, kI8ConvThreads);  // this CTA's own rows, stored locally, are visible

@@ -242,14 +242,14 @@ int launch_gemm(Kernel kernel, const Plan& p, dim3 grid, unsigned threads, size_
   return QG_OK;
 }
 
-template <int FMT, int MPAD>
+template <int FMT, int MPAD, bool FUSED>
 int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                 cudaStream_t stream) {
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kThreads,
-                     qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
+  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles, p.splits, p.m_tiles),
+                     qg::kThreads, qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
 template <int FMT>
@@ -262,19 +262,22 @@ int run_f8_std(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg
 }
 
 template <int MPAD>
-int run_f8_swap_fmt(int fmt, const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g,
-                    int config_id, cudaStream_t stream) {
-  if (fmt == QG_FP8_DYNAMIC) return run_f8_swap<qg::kFmtFP8, MPAD>(p, tmW, tmA, g, config_id, stream);
-  return run_f8_swap<qg::kFmtBlock, MPAD>(p, tmW, tmA, g, config_id, stream);
+int run_f8_swap_fmt(int fmt, bool fused, const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA,
+                    qg::GemmArgs& g, int config_id, cudaStream_t stream) {
+  if (fmt == QG_FP8_DYNAMIC) {
+    if (fused) return run_f8_swap<qg::kFmtFP8, MPAD, true>(p, tmW, tmA, g, config_id, stream);
+    return run_f8_swap<qg::kFmtFP8, MPAD, false>(p, tmW, tmA, g, config_id, stream);
+  }
+  return run_f8_swap<qg::kFmtBlock, MPAD, false>(p, tmW, tmA, g, config_id, stream);
 }
 
-template <int MPAD>
+template <int MPAD, bool FUSED>
 int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
            cudaStream_t stream) {
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_kernel<MPAD>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kI8Threads,
+  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kI8Threads,
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -336,6 +339,101 @@ int load_table_file(const char* path) {
   fclose(f);
   g_table.swap(t);
   return QG_OK;
+}
+
+// Shared body of qg_gemm_w8a8 and qg_linear_w8a8.  With `fused` the kernel
+// reads bf16 activations and quantizes them itself (A_q / s_a optional
+// outputs); otherwise A_q / s_a are the quantized inputs.
+struct FusedIn {
+  const void* A;
+  int64_t lda;
+};
+int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
+               const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
+               int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream,
+               const FusedIn* fused) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (variant < 0 || variant > 3) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
+  if (M < 0 || N <= 0 || K <= 0 || ldy < N)
+    return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld ldy=%lld", (long long)M, (long long)N, (long long)K, (long long)ldy);
+  if (config_id < 0 || config_id > kMaxStages) return fail(QG_ERR_INVALID_ARG, "config_id %d outside [0,%d]", config_id, kMaxStages);
+  if (M == 0) return QG_OK;
+  if ((!fused && (!A_q_dev || !s_a_dev)) || !W_q_dev || !s_w_dev || !Y_dev)
+    return fail(QG_ERR_INVALID_ARG, "null pointer");
+  if (fused && (!fused->A || fused->lda < K || fused->lda % 8 || !aligned(fused->A, 16)))
+    return fail(fused->A ? QG_ERR_ALIGNMENT : QG_ERR_INVALID_ARG,
+                "A must be 16-byte aligned bf16 with lda >= K and lda %% 8 == 0");
+  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
+  if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF || cdiv(N, 128) > 0x7FFFFFFF)
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+  if (!aligned(A_q_dev, 16) || !aligned(W_q_dev, 16) || !aligned(s_a_dev, 4) || !aligned(s_w_dev, 4) ||
+      !aligned(Y_dev, 2) || (debug_acc_dev && !aligned(debug_acc_dev, 4)))
+    return fail(QG_ERR_ALIGNMENT, "A_q/W_q need 16-byte alignment, scales 4, Y 2");
+  if (debug_acc_dev && fmt != QG_W8A8_INT8) return fail(QG_ERR_INVALID_ARG, "debug_acc is W8A8_INT8 only");
+  Plan p;
+  int rc = make_plan(fmt, M, N, K, variant, split_k, &p);
+  if (rc != QG_OK) return rc;
+  const int64_t need = workspace_bytes(p, M, N);
+  if (need > 0) {
+    if (!workspace_dev) return fail(QG_ERR_WORKSPACE_TOO_SMALL, "split_k=%d needs a %lld-byte workspace", split_k, (long long)need);
+    if (static_cast<int64_t>(ws_bytes) < need)
+      return fail(QG_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %lld needed", ws_bytes, (long long)need);
+    if (!aligned(workspace_dev, 256)) return fail(QG_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  }
+  CUtensorMap tmW, tmA;
+  rc = make_map(&tmW, W_q_dev, N, K, K, 128);
+  if (rc != QG_OK) return rc;
+  if (fused) {
+    tmA = tmW;  // unused: the kernel reads the bf16 activations directly
+  } else {
+    rc = make_map(&tmA, A_q_dev, M, K, K, p.swap ? static_cast<uint32_t>(p.mpad) : 128u);
+    if (rc != QG_OK) return rc;
+  }
+
+  qg::GemmArgs g = {};
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.ldy = ldy;
+  g.kt_total = p.kt;
+  g.splits = p.splits;
+  g.s_a = s_a_dev;
+  g.s_w = s_w_dev;
+  g.Y = static_cast<__nv_bfloat16*>(Y_dev);
+  if (p.reduce == qg::kReduceGlobal) {
+    const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
+    g.ws_count = static_cast<int*>(workspace_dev);
+    g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
+  }
+  g.reduce = p.reduce;
+  g.recv_bytes = p.reduce == qg::kReduceCluster
+                     ? qg::cluster_recv_bytes(p.splits, static_cast<int>(std::min<int64_t>(M, p.mpad)))
+                     : 0;
+  g.debug_acc = debug_acc_dev;
+  if (fused) {
+    g.A = static_cast<const __nv_bfloat16*>(fused->A);
+    g.lda = fused->lda;
+    g.a_q_out = static_cast<uint8_t*>(const_cast<void*>(A_q_dev));
+    g.s_a_out = const_cast<float*>(s_a_dev);
+  }
+  g.wait_ns = g_wait_ns;
+  g.force_timeout = g_force_timeout;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const bool fz = fused != nullptr;
+  if (fmt == QG_W8A8_INT8) {
+    if (p.mpad == 16) return fz ? run_i8<16, true>(p, tmW, tmA, g, config_id, s) : run_i8<16, false>(p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return fz ? run_i8<32, true>(p, tmW, tmA, g, config_id, s) : run_i8<32, false>(p, tmW, tmA, g, config_id, s);
+    return fz ? run_i8<64, true>(p, tmW, tmA, g, config_id, s) : run_i8<64, false>(p, tmW, tmA, g, config_id, s);
+  }
+  if (p.swap) {
+    if (p.mpad == 16) return run_f8_swap_fmt<16>(fmt, fz, p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return run_f8_swap_fmt<32>(fmt, fz, p, tmW, tmA, g, config_id, s);
+    return run_f8_swap_fmt<64>(fmt, fz, p, tmW, tmA, g, config_id, s);
+  }
+  if (fmt == QG_FP8_DYNAMIC) return run_f8_std<qg::kFmtFP8>(p, tmW, tmA, g, config_id, s);
+  return run_f8_std<qg::kFmtBlock>(p, tmW, tmA, g, config_id, s);
 }
 
 }  // namespace
@@ -482,73 +580,30 @@ int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream) {
 int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
                  const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
                  int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream) {
+  return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
+                    workspace_dev, ws_bytes, debug_acc_dev, stream, nullptr);
+}
+
+int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, int64_t lda, const void* W_q_dev,
+                   const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k, int config_id,
+                   void* workspace_dev, size_t ws_bytes, void* A_q_dev, float* s_a_dev, int32_t* debug_acc_dev,
+                   void* stream) {
+  const bool swap = variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK;
+  if (fmt == QG_BLOCK_FP8 || !swap) {
+    // quantize into the caller's A_q / s_a, then the GEMM (two launches)
+    if (!A_q_dev || !s_a_dev)
+      return fail(QG_ERR_INVALID_ARG, "qg_linear_w8a8: Block_FP8 and the Standard variants need A_q and s_a buffers");
+    int rc = qg_quant_act(fmt, A_dev, M, K, lda, A_q_dev, s_a_dev, stream);
+    if (rc != QG_OK) return rc;
+    return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
+                      workspace_dev, ws_bytes, debug_acc_dev, stream, nullptr);
+  }
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
-  if (variant < 0 || variant > 3) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
-  if (M < 0 || N <= 0 || K <= 0 || ldy < N)
-    return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld ldy=%lld", (long long)M, (long long)N, (long long)K, (long long)ldy);
-  if (config_id < 0 || config_id > kMaxStages) return fail(QG_ERR_INVALID_ARG, "config_id %d outside [0,%d]", config_id, kMaxStages);
-  if (M == 0) return QG_OK;
-  if (!A_q_dev || !s_a_dev || !W_q_dev || !s_w_dev || !Y_dev) return fail(QG_ERR_INVALID_ARG, "null pointer");
-  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
-  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
-  if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF || cdiv(N, 128) > 0x7FFFFFFF)
-    return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
-  if (!aligned(A_q_dev, 16) || !aligned(W_q_dev, 16) || !aligned(s_a_dev, 4) || !aligned(s_w_dev, 4) ||
-      !aligned(Y_dev, 2) || (debug_acc_dev && !aligned(debug_acc_dev, 4)))
-    return fail(QG_ERR_ALIGNMENT, "A_q/W_q need 16-byte alignment, scales 4, Y 2");
-  if (debug_acc_dev && fmt != QG_W8A8_INT8) return fail(QG_ERR_INVALID_ARG, "debug_acc is W8A8_INT8 only");
-  Plan p;
-  int rc = make_plan(fmt, M, N, K, variant, split_k, &p);
-  if (rc != QG_OK) return rc;
-  const int64_t need = workspace_bytes(p, M, N);
-  if (need > 0) {
-    if (!workspace_dev) return fail(QG_ERR_WORKSPACE_TOO_SMALL, "split_k=%d needs a %lld-byte workspace", split_k, (long long)need);
-    if (static_cast<int64_t>(ws_bytes) < need)
-      return fail(QG_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %lld needed", ws_bytes, (long long)need);
-    if (!aligned(workspace_dev, 256)) return fail(QG_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-  }
-  CUtensorMap tmW, tmA;
-  rc = make_map(&tmW, W_q_dev, N, K, K, 128);
-  if (rc != QG_OK) return rc;
-  rc = make_map(&tmA, A_q_dev, M, K, K, p.swap ? static_cast<uint32_t>(p.mpad) : 128u);
-  if (rc != QG_OK) return rc;
-
-  qg::GemmArgs g = {};
-  g.M = static_cast<int>(M);
-  g.N = static_cast<int>(N);
-  g.K = static_cast<int>(K);
-  g.ldy = ldy;
-  g.kt_total = p.kt;
-  g.splits = p.splits;
-  g.s_a = s_a_dev;
-  g.s_w = s_w_dev;
-  g.Y = static_cast<__nv_bfloat16*>(Y_dev);
-  if (p.reduce == qg::kReduceGlobal) {
-    const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
-    g.ws_count = static_cast<int*>(workspace_dev);
-    g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
-  }
-  g.reduce = p.reduce;
-  g.recv_bytes = p.reduce == qg::kReduceCluster
-                     ? qg::cluster_recv_bytes(p.splits, static_cast<int>(std::min<int64_t>(M, p.mpad)))
-                     : 0;
-  g.debug_acc = debug_acc_dev;
-  g.wait_ns = g_wait_ns;
-  g.force_timeout = g_force_timeout;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  if (fmt == QG_W8A8_INT8) {
-    if (p.mpad == 16) return run_i8<16>(p, tmW, tmA, g, config_id, s);
-    if (p.mpad == 32) return run_i8<32>(p, tmW, tmA, g, config_id, s);
-    return run_i8<64>(p, tmW, tmA, g, config_id, s);
-  }
-  if (p.swap) {
-    if (p.mpad == 16) return run_f8_swap_fmt<16>(fmt, p, tmW, tmA, g, config_id, s);
-    if (p.mpad == 32) return run_f8_swap_fmt<32>(fmt, p, tmW, tmA, g, config_id, s);
-    return run_f8_swap_fmt<64>(fmt, p, tmW, tmA, g, config_id, s);
-  }
-  if (fmt == QG_FP8_DYNAMIC) return run_f8_std<qg::kFmtFP8>(p, tmW, tmA, g, config_id, s);
-  return run_f8_std<qg::kFmtBlock>(p, tmW, tmA, g, config_id, s);
+  if ((A_q_dev && !aligned(A_q_dev, 16)) || (s_a_dev && !aligned(s_a_dev, 4)))
+    return fail(QG_ERR_ALIGNMENT, "A_q needs 16-byte alignment, s_a 4");
+  const FusedIn f{A_dev, lda};
+  return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
+                    workspace_dev, ws_bytes, debug_acc_dev, stream, &f);
 }
 
 int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,

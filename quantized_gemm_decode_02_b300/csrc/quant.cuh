@@ -69,6 +69,31 @@ __device__ __forceinline__ uint2 encode8(const float (&x)[8], float s) {
   return make_uint2(w[0], w[1]);
 }
 
+// Quotient x / s rounded to nearest even, for many x and one s, without a
+// division per element: Markstein's method (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", 1990).  With r
+// the correctly rounded reciprocal of s, q1 = RN(x*r) is within two ulps of
+// x/s; one residual step q2 = q1 + r*(x - s*q1) makes it faithful, and a
+// second one returns the correctly rounded quotient, because each residual
+// x - s*q of a faithful q is exact in one fma.  Valid when s, x/s and the
+// residuals are normal numbers: Divider::exact is false for rows whose scale
+// lies outside [2^-100, 2^100] (those divide with __fdiv_rn), and x/s below
+// 2^-100 only matters up to its sign once encoded (it rounds to zero).
+struct Divider {
+  float s, r;
+  bool exact;
+  __device__ __forceinline__ explicit Divider(float scale) : s(scale) {
+    r = __frcp_rn(scale);
+    exact = scale >= 0x1p-100f && scale <= 0x1p100f;
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    if (!exact) return __fdiv_rn(x, s);
+    const float q1 = __fmul_rn(x, r);
+    const float q2 = __fmaf_rn(__fmaf_rn(-q1, s, x), r, q1);
+    return __fmaf_rn(__fmaf_rn(-q2, s, x), r, q2);
+  }
+};
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -29,7 +29,7 @@ VARIANTS = {"Standard": QG_STANDARD, "Split-K": QG_SPLITK, "Swap-AB": QG_SWAPAB,
 QG_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
-           "qg_gemm_w8a8_noalloc",
+           "qg_linear_w8a8", "qg_gemm_w8a8_noalloc",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
            "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
 
@@ -52,6 +52,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qg_workspace_init.argtypes = [P, SZ, P]
     lib.qg_gemm_w8a8.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
     lib.qg_gemm_w8a8_noalloc.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, P]
+    lib.qg_linear_w8a8.argtypes = [I, I64, I64, I64, P, I64, P, P, P, I64, I, I, I, P, SZ, P, P, P, P]
     lib.qg_select.argtypes = [I, I64, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
     lib.qg_load_table.argtypes = [ctypes.c_char_p]
     lib.qg_set_allow_default.argtypes = [I]
@@ -114,6 +115,15 @@ def qg_gemm_w8a8(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, con
     _check(_lib.qg_gemm_w8a8(_fmt(fmt), M, N, K, _ptr(A_q), _ptr(s_a), _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant,
                              split_k, config_id, _ptr(workspace), ws_bytes, _ptr(debug_acc), _stream(stream)),
            "qg_gemm_w8a8")
+
+
+def qg_linear_w8a8(fmt, M, N, K, A, lda, W_q, s_w, Y, ldy, variant, split_k, config_id=0, workspace=None,
+                   ws_bytes=0, A_q=None, s_a=None, debug_acc=None, stream=None) -> None:
+    """Activation quantization and the GEMM in one call (one kernel for
+    FP8_Dynamic / W8A8_INT8 with Swap-AB)."""
+    _check(_lib.qg_linear_w8a8(_fmt(fmt), M, N, K, _ptr(A), lda, _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant,
+                               split_k, config_id, _ptr(workspace), ws_bytes, _ptr(A_q), _ptr(s_a), _ptr(debug_acc),
+                               _stream(stream)), "qg_linear_w8a8")
 
 
 def qg_gemm_w8a8_noalloc(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, config_id=0, debug_acc=None,

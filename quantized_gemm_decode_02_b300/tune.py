@@ -7,9 +7,10 @@ will run ("Enable CUDA Graph for Autotuner Benchmarking").  This sweep keeps
 that method and replaces the page's LLM-seeded tree search with an exhaustive
 walk over a small grid: for every format, shape and tuned token count it
 times each candidate (variant, split_k, ring depth) as a CUDA graph of R
-launches over rotated weight copies (more than three L2 capacities, so the
-weights stream from HBM), with programmatic dependent launch on, and keeps
-the fastest.
+GEMM launches (qg_gemm_w8a8; with --linear, whole linear layers through
+qg_linear_w8a8 instead) over rotated weight copies (more than three L2
+capacities, so the weights stream from HBM), with programmatic dependent
+launch on, and keeps the fastest.
 
 Rows already present in the output table are skipped, so an interrupted
 sweep resumes where it stopped.
@@ -87,14 +88,15 @@ class Bench:
         # random bytes: valid int8 codes; as E4M3 they include NaN codes,
         # which do not change the kernels' speed
         self.pool = torch.randint(0, 256, (POOL_BYTES,), dtype=torch.uint8, device=device, generator=g)
-        self.Aq = torch.randint(0, 256, (64 * 32768,), dtype=torch.uint8, device=device, generator=g)
-        self.sa = torch.ones(64 * 256, dtype=torch.float32, device=device)
+        self.A = torch.randn(512 * 25600, device=device, generator=g).to(torch.bfloat16)
+        self.Aq = torch.randint(0, 256, (512 * 25600,), dtype=torch.uint8, device=device, generator=g)
+        self.sa = torch.ones(512 * 256, dtype=torch.float32, device=device)
         self.sw = torch.ones(65536 * 4, dtype=torch.float32, device=device)
-        self.Y = torch.empty(64 * 65536, dtype=torch.bfloat16, device=device)
+        self.Y = torch.empty(512 * 51200, dtype=torch.bfloat16, device=device)
         self.ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device=device)
 
-    def time_config(self, fmt, M, N, K, variant, split, cfg, min_bytes=3 * 126e6, reps=5):
+    def time_config(self, fmt, M, N, K, variant, split, cfg, min_bytes=3 * 126e6, reps=5, linear=False):
         """Microseconds per GEMM: median over `reps` replays of a graph of R
         launches, each on its own window of the weight pool."""
         wbytes = N * K
@@ -109,8 +111,16 @@ class Bench:
             with torch.cuda.graph(graph, stream=self.stream):
                 for r in range(R):
                     W = self.pool[r * step:r * step + wbytes]
-                    q.qg_gemm_w8a8(fmt, M, N, K, self.Aq, self.sa, W, self.sw, self.Y, N, variant, split, cfg,
-                                   self.ws if need else None, need, None, stream=self.stream)
+                    if not linear:
+                        q.qg_gemm_w8a8(fmt, M, N, K, self.Aq, self.sa, W, self.sw, self.Y, N, variant, split, cfg,
+                                       self.ws if need else None, need, None, stream=self.stream)
+                        continue
+                    # fused layers write no quantized activations; the others
+                    # quantize into Aq / sa first
+                    fused = fmt != "Block_FP8" and variant in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK)
+                    q.qg_linear_w8a8(fmt, M, N, K, self.A, K, W, self.sw, self.Y, N, variant, split, cfg,
+                                     self.ws if need else None, need, None if fused else self.Aq,
+                                     None if fused else self.sa, None, stream=self.stream)
         finally:
             q.qg_set_launch_flags(0)
         for _ in range(2):
@@ -149,6 +159,7 @@ def main(argv=None):
     ap.add_argument("--models", default="Qwen3-1.7B,Qwen3-8B,Qwen3-32B")
     ap.add_argument("--ms", default=",".join(str(m) for m in TUNED_M))
     ap.add_argument("--log", default=None, help="JSON lines with every candidate's time")
+    ap.add_argument("--linear", action="store_true", help="time qg_linear_w8a8 (quantization + GEMM)")
     args = ap.parse_args(argv)
     device = "cuda:0"
     torch.cuda.set_device(0)
@@ -171,7 +182,7 @@ def main(argv=None):
                         continue
                     best = None
                     for (v, s, c) in candidates(fmt, M, N, K, sms):
-                        us = bench.time_config(fmt, M, N, K, v, s, c)
+                        us = bench.time_config(fmt, M, N, K, v, s, c, linear=args.linear)
                         if log:
                             log.write(json.dumps({"fmt": fmt, "model": model, "layer": layer, "M": M, "N": N, "K": K,
                                                   "variant": v, "split_k": s, "config_id": c, "us": us}) + "\n")

@@ -1,0 +1,134 @@
+"""qg_linear_w8a8: activation quantization fused into the GEMM kernel.
+
+Against the CPU oracle on the same seeded inputs: the quantized activations
+and scales the kernel writes out are bit-exact (the kernel divides with
+Markstein's method, the oracle with one IEEE division: they must agree on
+every code, including ties), INT8 accumulators are bit-exact and Y within one
+bf16 ulp, FP8 within 8e-3 * s_a*s_w*sum|a_q*w_q|.  Against the two-kernel path
+(qg_quant_act + qg_gemm_w8a8) with the same config: identical outputs.
+
+Cases span one CTA per tile, Split-K in clusters (the per-token row maximum
+is agreed across the cluster), Split-K through the workspace (each CTA reads
+the whole row), blocks of 64 tokens, ragged N and K, and rows built so that
+x / s falls exactly on E4M3 / int8 rounding ties."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+SW, SWS, ST = 2, 3, 0
+
+
+@pytest.fixture(scope="module")
+def gc():
+    import gpu_cases
+    return gpu_cases
+
+
+@pytest.fixture(scope="module")
+def q():
+    from quantized_gemm_decode_02_b300 import qgemm
+    return qgemm
+
+
+def tie_rows(fmt: str, M: int, K: int, rng) -> torch.Tensor:
+    """Activations whose quotients x / s land on rounding ties: every row has
+    its maximum at a power of two times QMAX, so s is a power of two and
+    x = s * midpoint is exact in bf16."""
+    A = np.zeros((M, K), np.float32)
+    if fmt == "W8A8_INT8":
+        mids = (np.arange(-126, 127) + 0.5).astype(np.float32)   # k + 1/2
+        qmax = 127.0
+    else:
+        codes = np.array([v for v in range(0x7F) if v not in (0x7F,)], np.uint8)
+        from oracle import oracle as orc
+        vals = np.unique(np.abs(orc.e4m3_decode(codes)))
+        mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)     # E4M3 rounding midpoints
+        mids = np.concatenate([mids, -mids])
+        qmax = 448.0
+    for m in range(M):
+        s = np.float32(2.0 ** int(rng.integers(-12, 4)))
+        row = rng.choice(mids, size=K) * s
+        row[int(rng.integers(0, K))] = qmax * s                   # the row maximum: s = amax / qmax exactly
+        A[m] = row
+    t = torch.from_numpy(A).to(torch.bfloat16)
+    assert torch.equal(t.float(), torch.from_numpy(A)), "tie rows must be exact in bf16"
+    return t
+
+
+def run_linear(orc, gc, q, fmt, M, N, K, variant, split, seed, A=None, check_two_kernel=True):
+    dev = gc.DEV
+    if A is None:
+        A = si.activations(M, K, seed=seed, outliers=True)
+    W = si.weights(N, K, seed=seed)
+    Wq, sw = gc.quant_weight_gpu(fmt, torch.from_numpy(W).to(dev))
+    Ad = A.to(dev)
+    is_int8 = fmt == "W8A8_INT8"
+    need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    Aq = torch.full((M, K), 0x5A, dtype=torch.uint8, device=dev)
+    sa_shape = (M, K // 128) if fmt == "Block_FP8" else (M,)
+    sa = torch.full(sa_shape, -1.0, dtype=torch.float32, device=dev)
+    dbg = torch.full((M, N), -7, dtype=torch.int32, device=dev) if is_int8 else None
+    q.qg_linear_w8a8(fmt, M, N, K, Ad, K, Wq, sw, Y, N, variant, split, 0, ws, need, Aq, sa, dbg)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    oAq, osa, oWq, osw = gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
+    gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y, dbg)
+    if check_two_kernel:
+        Aq2, sa2 = gc.quant_act_gpu(fmt, Ad)
+        Y2, dbg2 = gc.gemm_gpu(fmt, Aq2, sa2, Wq, sw, N, variant, split, debug=is_int8)
+        torch.cuda.synchronize()
+        assert torch.equal(Y, Y2), "fused and two-kernel outputs differ"
+        if is_int8:
+            assert torch.equal(dbg, dbg2)
+    return Y
+
+
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8"])
+@pytest.mark.parametrize("M,split", [(1, 1), (5, 3), (16, 8), (17, 2), (32, 16), (24, 17), (48, 5), (100, 3)])
+def test_fused_linear(orc, gc, q, fmt, M, split):
+    # K = 2320: 19 k-tiles, the last ragged (16 of 128 columns); ragged N
+    run_linear(orc, gc, q, fmt, M, 328, 2320, SWS if split > 1 else SW, split, seed=400 + M + split)
+
+
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8"])
+@pytest.mark.parametrize("split", [1, 4, 20])
+def test_fused_quantization_ties(orc, gc, q, fmt, split):
+    M, N, K = 32, 256, 2560
+    rng = np.random.Generator(np.random.PCG64(77 + split))
+    A = tie_rows(fmt, M, K, rng)
+    run_linear(orc, gc, q, fmt, M, N, K, SWS if split > 1 else SW, split, seed=5, A=A)
+
+
+def test_fused_linear_without_optional_outputs(orc, gc, q):
+    fmt, M, N, K = "W8A8_INT8", 8, 384, 2048
+    A = si.activations(M, K, seed=9)
+    W = si.weights(N, K, seed=9)
+    Wq, sw = gc.quant_weight_gpu(fmt, torch.from_numpy(W).to(gc.DEV))
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=gc.DEV)
+    q.qg_linear_w8a8(fmt, M, N, K, A.to(gc.DEV), K, Wq, sw, Y, N, SWS, 4)
+    torch.cuda.synchronize()
+    oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
+    oWq, osw = orc.quant_weight(fmt, W)
+    gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y)
+
+
+@pytest.mark.parametrize("fmt,variant,split", [("Block_FP8", SWS, 3), ("Block_FP8", SW, 1), ("FP8_Dynamic", ST, 1)])
+def test_two_kernel_linear(orc, gc, q, fmt, variant, split):
+    # Block_FP8 and the Standard variant quantize into the caller's buffers
+    run_linear(orc, gc, q, fmt, 12, 264, 1024, variant, split, seed=11)
+
+
+def test_linear_needs_buffers_when_not_fused(q, gc):
+    d = torch.zeros(1024, dtype=torch.uint8, device=gc.DEV)
+    f = torch.zeros(64, dtype=torch.float32, device=gc.DEV)
+    with pytest.raises(q.QGError) as e:
+        q.qg_linear_w8a8("Block_FP8", 4, 128, 128, d, 128, d, f, d, 128, SW, 1)
+    assert e.value.code == q.QG_ERR_INVALID_ARG
