@@ -112,15 +112,18 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // tile form one cluster (cluster rank == split index).  Row r of the tile is
 // owned by CTA r / R, R = ceil(128 / S).  Every CTA sends its partial of
 // each row to the row's owner with st.async, which lands in the owner's
-// receive buffer recv[s][j][mv] (s = sending rank, j = row - owner*R, mv = M
-// rounded up to 4) and completes bytes on the owner's mbarrier; the owner
-// waits for (S - 1) * rows * mv * 4 bytes, then adds the S partials of each
-// of its elements in the fixed order 0..S-1.  One one-way transfer and one
-// bounded wait; no CTA reads a peer, so none waits for its peers to finish.
+// receive buffer recv[s][j][..] (s = sending rank, j = row - owner*R; a row
+// holds mv = M rounded up to 4 values, padded to an odd number of 16-byte
+// chunks so that reads of consecutive rows hit different banks) and
+// completes bytes on the owner's mbarrier; the owner waits for
+// (S - 1) * rows * mv * 4 bytes, then adds the S partials of each of its
+// elements in the fixed order 0..S-1.  One one-way transfer and one bounded
+// wait; no CTA reads a peer, so none waits for its peers to finish.
 __host__ __device__ constexpr int cluster_rows_per_rank(int S) { return (kBN + S - 1) / S; }
 __host__ __device__ constexpr int cluster_mv(int M) { return (M + 3) & ~3; }
+__host__ __device__ constexpr int cluster_row_stride(int M) { return 4 * ((cluster_mv(M) / 4) | 1); }
 __host__ __device__ constexpr int cluster_recv_bytes(int S, int M) {
-  return S * cluster_rows_per_rank(S) * cluster_mv(M) * 4;
+  return S * cluster_rows_per_rank(S) * cluster_row_stride(M) * 4;
 }
 __device__ __forceinline__ int cluster_rows_of(int rank, int S) {
   const int R = cluster_rows_per_rank(S);
@@ -133,14 +136,14 @@ __device__ __forceinline__ int cluster_rows_of(int rank, int S) {
 template <typename T, int N>
 __device__ __forceinline__ void cluster_push_row(const T (&v)[N], int m0, int row, int rank, int S, int M,
                                                  uint8_t* recv, uint64_t* recv_bar) {
-  const int R = cluster_rows_per_rank(S), mv = cluster_mv(M);
+  const int R = cluster_rows_per_rank(S), mv = cluster_mv(M), rs = cluster_row_stride(M);
   const int o = row / R, j = row - o * R;
   const uint32_t base = smem_u32(recv), bar = smem_u32(recv_bar);
 #pragma unroll
   for (int c = 0; c < N; c += 4) {
     const int m = m0 + c;
     if (m < mv) {
-      const uint32_t off = static_cast<uint32_t>(((rank * R + j) * mv + m) * 4);
+      const uint32_t off = static_cast<uint32_t>(((rank * R + j) * rs + m) * 4);
       const uint32_t w0 = reinterpret_cast<const uint32_t&>(v[c]);
       const uint32_t w1 = reinterpret_cast<const uint32_t&>(v[c + 1]);
       const uint32_t w2 = reinterpret_cast<const uint32_t&>(v[c + 2]);
@@ -154,24 +157,31 @@ __device__ __forceinline__ void cluster_push_row(const T (&v)[N], int m0, int ro
   }
 }
 
-// Owner side, after the receive barrier completed: for each element (m, j)
-// of this CTA's rows, sum the S partials in order and call store(m, row, sum).
+// Owner side, after the receive barrier completed: for each of this CTA's
+// rows j and each group of 4 tokens, sum the S partials in order and call
+// store(m, row, sum) for the tokens m < M.  Consecutive threads take
+// consecutive rows, so each store instruction of a warp writes one
+// contiguous run of a Y row.
 template <typename T, typename Store>
 __device__ __forceinline__ void cluster_sum_rows(const uint8_t* recv, int rank, int S, int M, int tid, int nthreads,
                                                  Store&& store) {
-  const int R = cluster_rows_per_rank(S), mv = cluster_mv(M), rn = cluster_rows_of(rank, S);
-  const T* buf = reinterpret_cast<const T*>(recv);
-  for (int e = tid; e < rn * M; e += nthreads) {
-    const int m = e % M, j = e / M;
-    T v[kMaxClusterSplits];
+  const int R = cluster_rows_per_rank(S), rs = cluster_row_stride(M), rn = cluster_rows_of(rank, S);
+  const int quads = cluster_mv(M) / 4;
+  for (int e = tid; e < rn * quads; e += nthreads) {
+    const int j = e % rn, m0 = 4 * (e / rn);
+    const uint4 v0 = *reinterpret_cast<const uint4*>(recv + static_cast<size_t>((j * rs + m0) * 4));
+    T sum[4] = {reinterpret_cast<const T&>(v0.x), reinterpret_cast<const T&>(v0.y), reinterpret_cast<const T&>(v0.z),
+                reinterpret_cast<const T&>(v0.w)};
+    for (int s = 1; s < S; ++s) {  // the receive buffer is this CTA's own shared memory
+      const uint4 v = *reinterpret_cast<const uint4*>(recv + static_cast<size_t>(((s * R + j) * rs + m0) * 4));
+      sum[0] += reinterpret_cast<const T&>(v.x);
+      sum[1] += reinterpret_cast<const T&>(v.y);
+      sum[2] += reinterpret_cast<const T&>(v.z);
+      sum[3] += reinterpret_cast<const T&>(v.w);
+    }
 #pragma unroll
-    for (int s = 0; s < kMaxClusterSplits; ++s)
-      if (s < S) v[s] = buf[(s * R + j) * mv + m];
-    T sum = v[0];
-#pragma unroll
-    for (int s = 1; s < kMaxClusterSplits; ++s)
-      if (s < S) sum += v[s];
-    store(m, rank * R + j, sum);
+    for (int c = 0; c < 4; ++c)
+      if (m0 + c < M) store(m0 + c, rank * R + j, sum[c]);
   }
 }
 
