@@ -213,17 +213,27 @@ class Workload:
         return g
 
     def capture_timed_kernels(self, stream):
-        """The same step with timing events around every linear layer (its
-        quantization and GEMM; no PDL: the events sit between kernels).
-        Returns (graph, event pairs)."""
+        """The same step with timing events around every GEMM launch (no PDL:
+        the events sit between kernels): around the GEMM kernel alone, with
+        the activation quantization before the first event, or around the
+        one fused kernel.  Returns (graph, event pairs)."""
         g = torch.cuda.CUDAGraph()
         evs = []
+        q = self.q
         with torch.cuda.graph(g, stream=stream):
             for i in range(len(self.recs)):
+                r = self.recs[i]
                 e0 = torch.cuda.Event(enable_timing=True, external=True)
                 e1 = torch.cuda.Event(enable_timing=True, external=True)
-                e0.record(stream)
-                self.enqueue(stream, i)
+                if self.fused_item(i):
+                    e0.record(stream)
+                    self.enqueue(stream, i)
+                else:
+                    q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
+                    e0.record(stream)
+                    q.qg_gemm_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"],
+                                   r["N"], r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes, None,
+                                   stream=stream)
                 e1.record(stream)
                 evs.append((e0, e1))
         return g, evs
@@ -353,6 +363,36 @@ def load_peaks():
         return p.get("hbm_gbs", 6400.0), p.get("bf16_tflops", 1800.0), "measured"
     except (OSError, ValueError):
         return 6400.0, 1800.0, "fallback"
+
+
+TRAFFIC = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+
+
+def kernel_sources_sha() -> str:
+    """SHA-256 over the library's kernel sources (csrc/*, sorted by name)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_gemm_decode_02_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, fused: bool):
+    """DRAM bytes (read + write) per GEMM launch from the committed ncu
+    capture of this workload, or None when there is none or the kernel
+    sources changed since it was taken."""
+    try:
+        with open(TRAFFIC) as fh:
+            rec = json.load(fh).get(workload)
+    except (OSError, ValueError):
+        return None, "no committed capture"
+    if not rec or fused:
+        return None, "no committed capture for this workload and path"
+    if rec.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None, "kernel sources changed since the capture"
+    return rec["dram_bytes_per_launch"], rec["capture"]
 
 
 def tensor_peak(fmt: str, bf16_tflops: float) -> float:
@@ -523,20 +563,21 @@ def main(argv=None):
     n_gemm = len(wl.recs)
     hbm_peak, bf16_peak, peak_kind = load_peaks()
     n_kernels = sum(wl.kernels(i) for i in range(n_gemm))
-    # roofline of the linear layer (its GEMM kernel, with the activation
-    # quantization fused in or in its own kernel before it): algorithmic
-    # bytes (HBM-bound decode) or flops (compute-bound large M) per layer
-    # over the mean time of a layer
+    # roofline of the GEMM kernel: algorithmic bytes (HBM-bound decode) or
+    # flops (compute-bound large M) per launch over the mean launch time
     if hbm:
-        avg_units = wl.bytes_step / n_gemm
+        units = [gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) +
+                 (quant_bytes(r["fmt"], r["M"], r["K"]) if wl.fused_item(i) else 0) for i, r in enumerate(wl.recs)]
+        avg_units = sum(units) / n_gemm
         avg_ms = float(per_ms.sum()) / n_gemm
         achieved = avg_units / (avg_ms * 1e-3) / 1e9
         peak = hbm_peak
+        traffic, traffic_note = measured_traffic(args.workload, wl.fused)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": ("fused quantize+gemm" if wl.fused else "quant_act + gemm") + " (" + "+".join(wl.formats) + ")",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_note": traffic_note,
+                "kernel": ("fused quantize+gemm" if wl.fused else "gemm") + " (" + "+".join(wl.formats) + ")",
                 "peak_kind": peak_kind, "avg_launch_us": round(avg_ms * 1e3, 3),
-                "avg_bytes_per_launch": round(avg_units), "kernels_per_layer": round(n_kernels / n_gemm, 3)}
+                "avg_bytes_per_launch": round(avg_units)}
     else:
         # the E4M3 GEMMs (the dominant kernels) against the kind::f8f6f4 peak;
         # every format's own figure follows
