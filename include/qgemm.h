@@ -56,8 +56,23 @@ typedef enum { QG_FP8_DYNAMIC = 0, QG_W8A8_INT8 = 1, QG_BLOCK_FP8 = 2 } qg_forma
 
 /* Algorithm variants ("Kernel Implementation"): Standard puts tokens on the
  * MMA M side; Swap-AB computes Y^T = W_q . A_q^T so the weight rows take the
- * MMA M side (small M); the *_SPLITK forms also cut K into split_k ranges. */
-typedef enum { QG_STANDARD = 0, QG_SPLITK = 1, QG_SWAPAB = 2, QG_SWAPAB_SPLITK = 3 } qg_variant;
+ * MMA M side (small M); the *_SPLITK forms also cut K into split_k ranges.
+ * QG_SWAPAB_DP4A(_SPLITK) keep the Swap-AB work split but run the int8 dot
+ * products on the CUDA cores (dp4a, int32 accumulation) instead of the
+ * tensor cores: W8A8_INT8 with M <= 8 only (QG_ERR_UNSUPPORTED_SHAPE
+ * otherwise). */
+typedef enum {
+  QG_STANDARD = 0,
+  QG_SPLITK = 1,
+  QG_SWAPAB = 2,
+  QG_SWAPAB_SPLITK = 3,
+  QG_SWAPAB_DP4A = 4,
+  QG_SWAPAB_DP4A_SPLITK = 5
+} qg_variant;
+
+#define QG_CONFIG_RING_MASK 31
+#define QG_CONFIG_PREFETCH_SHIFT 5
+#define QG_CONFIG_MAX_PREFETCH 64
 
 typedef enum {
   QG_OK = 0,
@@ -102,7 +117,14 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *   Y_dev              bf16 [M][ldy] (ldy >= N), fully overwritten;
  *   variant, split_k   a qg_variant and the number of K ranges (1 ..
  *                      ceil(K/128); must be 1 for the non-SPLITK variants);
- *   config_id          shared-memory ring depth (0 = library default);
+ *   config_id          ring | distance << QG_CONFIG_PREFETCH_SHIFT: the
+ *                      shared-memory ring depth in k-tiles (0 = library
+ *                      default: the deepest ring that lets two CTAs share
+ *                      an SM; at most 16) and the L2 prefetch distance: each
+ *                      CTA keeps that many 16 KB weight k-tiles requested
+ *                      into L2 ahead of the ring's loads, the first of them
+ *                      before it waits for the kernel it depends on (0 =
+ *                      off; at most QG_CONFIG_MAX_PREFETCH);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).
@@ -119,15 +141,15 @@ QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_
  * kernel: each CTA quantizes the slice of the activations its K range needs,
  * the CTAs of a Split-K cluster agree on every token's maximum over the
  * whole row through distributed shared memory, and no quantized activation
- * tensor is written unless asked for.  Block_FP8 and the Standard variants
- * run the two kernels in sequence.
+ * tensor is written unless asked for.  Block_FP8, the Standard and the
+ * dp4a variants run the two kernels in sequence.
  *   A_dev      bf16 [M][lda] activations (lda >= K, lda % 8 == 0, 16-byte
  *              aligned), read-only;
  *   W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id, workspace,
  *   ws_bytes, debug_acc_dev   as qg_gemm_w8a8;
  *   A_q_dev, s_a_dev  [M][K] codes and the scales (layouts of qg_quant_act):
  *              optional outputs in the fused case (NULL to skip), required
- *              buffers for Block_FP8 and the Standard variants. */
+ *              buffers for Block_FP8, the Standard and the dp4a variants. */
 QG_API int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, int64_t lda,
                           const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
                           int split_k, int config_id, void* workspace_dev, size_t ws_bytes, void* A_q_dev,

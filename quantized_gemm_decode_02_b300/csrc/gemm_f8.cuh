@@ -41,6 +41,7 @@ struct GemmArgs {
   int kt_total;         // ceil(K / 128)
   int splits;           // >= 1
   int stages;           // shared-memory ring depth
+  int l2_prefetch;      // L2 prefetch distance: weight k-tiles requested ahead of the ring's loads
   int reduce;           // kReduceNone / kReduceCluster / kReduceGlobal
   int recv_bytes;       // kReduceCluster: bytes of the shared-memory receive buffer (cluster_recv_bytes)
   const float* s_a;     // [M] or [M][kt_total]
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive_expect_tx(&ctl->full[i], kTx);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
+      for (int i = pre; i < nk && i < pre + g.l2_prefetch; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * kBK, w_row);
       pdl_wait();
       if (!FUSED) {
         for (int i = 0; i < pre; ++i) {
@@ -362,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint8_t* st = smem + static_cast<size_t>(s) * TS::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full[s], kTx);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
+        if (g.l2_prefetch > 0 && i + g.l2_prefetch < nk) tma_prefetch_l2_2d(&tmW, (kb0 + i + g.l2_prefetch) * kBK, w_row);
         if (!FUSED) tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full[s], pol_a);
         issued = i + 1;
       }
@@ -679,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&ctl->full[i], TS::kStageBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
+      for (int i = pre; i < nk && i < pre + g.l2_prefetch; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * kBK, w_row);
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * TS::kStageBytes;
@@ -695,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + static_cast<size_t>(s) * TS::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full[s], TS::kStageBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
+        if (g.l2_prefetch > 0 && i + g.l2_prefetch < nk) tma_prefetch_l2_2d(&tmW, (kb0 + i + g.l2_prefetch) * kBK, w_row);
         tma_load_2d(st + TS::kWBytes, &tmA, (kb0 + i) * kBK, a_row, &ctl->full[s], pol_a);
         issued = i + 1;
       }

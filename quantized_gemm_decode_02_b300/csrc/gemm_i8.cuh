@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         mbar_arrive_expect_tx(&ctl->full[i], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
+      for (int i = pre; i < nk && i < pre + g.l2_prefetch; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * kBK, w_row);
       pdl_wait();
       if (!FUSED) {
         for (int i = 0; i < pre; ++i) {
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
         uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full[s], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
+        if (g.l2_prefetch > 0 && i + g.l2_prefetch < nk) tma_prefetch_l2_2d(&tmW, (kb0 + i + g.l2_prefetch) * kBK, w_row);
         if (!FUSED) {
           mbar_arrive_expect_tx(&ctl->full_a[s], S::kABytes);
           tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[s], pol_a);

@@ -1,7 +1,7 @@
 // qgemm.cu -- C ABI of the quantized decode GEMM (see include/qgemm.h):
 // argument validation, TMA tensor-map encoding, variant dispatch, the tuned
 // config table and error reporting.  All arithmetic runs in the kernels of
-// quant.cuh, gemm_f8.cuh and gemm_i8.cuh.
+// quant.cuh, gemm_f8.cuh, gemm_i8.cuh and gemm_i8_dp4a.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "gemm_f8.cuh"
 #include "gemm_i8.cuh"
+#include "gemm_i8_dp4a.cuh"
 #include "quant.cuh"
 
 namespace {
@@ -163,6 +164,7 @@ constexpr int kMaxStages = 16;
 
 struct Plan {
   bool swap = false;
+  bool dp4a = false;   // W8A8_INT8 Swap-AB on the CUDA cores (M <= 8)
   int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64
   int n_tiles = 0, m_tiles = 0, kt = 0, splits = 1;
   int reduce = qg::kReduceNone;  // how split partials are summed
@@ -171,7 +173,10 @@ struct Plan {
 int64_t ws_counter_bytes(int64_t tiles) { return cdiv(tiles * 4, 256) * 256; }
 
 int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, Plan* p) {
-  p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK);
+  p->dp4a = (variant == QG_SWAPAB_DP4A || variant == QG_SWAPAB_DP4A_SPLITK);
+  p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->dp4a;
+  if (p->dp4a && (fmt != QG_W8A8_INT8 || M > qg::kDpMaxTokens))
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "the dp4a variants take W8A8_INT8 with M <= %d", qg::kDpMaxTokens);
   p->kt = static_cast<int>(cdiv(K, 128));
   p->n_tiles = static_cast<int>(cdiv(N, 128));
   if (p->swap) {
@@ -183,7 +188,7 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
     p->m_tiles = static_cast<int>(cdiv(M, 128));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   }
-  const bool split_variant = (variant == QG_SPLITK || variant == QG_SWAPAB_SPLITK);
+  const bool split_variant = (variant == QG_SPLITK || variant == QG_SWAPAB_SPLITK || variant == QG_SWAPAB_DP4A_SPLITK);
   if (split_k < 1 || split_k > p->kt)
     return fail(QG_ERR_UNSUPPORTED_SHAPE, "split_k=%d outside [1, ceil(K/128)=%d]", split_k, p->kt);
   if (!split_variant && split_k != 1)
@@ -207,10 +212,12 @@ int64_t workspace_bytes(const Plan& p, int64_t M, int64_t N) {
   return ws_counter_bytes(tiles) + static_cast<int64_t>(p.splits) * M * N * 4;
 }
 
-// Ring depth: config_id > 0 asks for that many stages (capped by the opt-in
-// limit); 0 takes the deepest ring that still lets two CTAs share an SM.
+// config_id = ring | distance << 5 (see qgemm.h).  Ring depth: ring > 0
+// asks for that many stages (capped by the opt-in limit); 0 takes the
+// deepest ring that still lets two CTAs share an SM.
 template <typename SmemFn>
 int pick_stages(int config_id, SmemFn smem_bytes, int* stages) {
+  config_id &= QG_CONFIG_RING_MASK;
   const size_t optin = dev_info().smem_optin, two = two_per_sm_smem();
   int max_stages = kMaxStages;
   while (max_stages > 2 && smem_bytes(max_stages) > optin) --max_stages;
@@ -281,6 +288,16 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
+template <int MT>
+int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+             cudaStream_t stream) {
+  const int rb = g.recv_bytes;
+  int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_dp4a_smem_bytes(st, rb); }, &g.stages);
+  if (rc != QG_OK) return rc;
+  return launch_gemm(qg::gemm_i8_dp4a_kernel<MT>, p, dim3(p.n_tiles, p.splits, 1), qg::kDpThreads,
+                     qg::gemm_dp4a_smem_bytes(g.stages, rb), tmW, tmA, g, stream);
+}
+
 // ------------------------------------------------------------------ table
 struct Key {
   int fmt;
@@ -330,7 +347,7 @@ int load_table_file(const char* path) {
     int fmt, m, variant, split_k, config_id;
     long long n, k;
     if (sscanf(s, "%d %lld %lld %d %d %d %d", &fmt, &n, &k, &m, &variant, &split_k, &config_id) != 7 || fmt < 0 ||
-        fmt > 2 || n <= 0 || k <= 0 || m <= 0 || variant < 0 || variant > 3 || split_k < 1 || config_id < 0) {
+        fmt > 2 || n <= 0 || k <= 0 || m <= 0 || variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK || split_k < 1 || config_id < 0) {
       fclose(f);
       return fail(QG_ERR_TABLE_PARSE, "%s:%d: malformed row", path, lineno);
     }
@@ -353,10 +370,13 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
                int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream,
                const FusedIn* fused) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
-  if (variant < 0 || variant > 3) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
+  if (variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
   if (M < 0 || N <= 0 || K <= 0 || ldy < N)
     return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld ldy=%lld", (long long)M, (long long)N, (long long)K, (long long)ldy);
-  if (config_id < 0 || config_id > kMaxStages) return fail(QG_ERR_INVALID_ARG, "config_id %d outside [0,%d]", config_id, kMaxStages);
+  if (config_id < 0 || (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
+      (config_id >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
+    return fail(QG_ERR_INVALID_ARG, "config_id %d: ring depth above %d or prefetch distance above %d", config_id,
+                kMaxStages, QG_CONFIG_MAX_PREFETCH);
   if (M == 0) return QG_OK;
   if ((!fused && (!A_q_dev || !s_a_dev)) || !W_q_dev || !s_w_dev || !Y_dev)
     return fail(QG_ERR_INVALID_ARG, "null pointer");
@@ -419,9 +439,17 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   }
   g.wait_ns = g_wait_ns;
   g.force_timeout = g_force_timeout;
+  g.l2_prefetch = config_id >> QG_CONFIG_PREFETCH_SHIFT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   const bool fz = fused != nullptr;
+  if (p.dp4a) {
+    if (fz) return fail(QG_ERR_INVALID_ARG, "the dp4a variants take quantized activations");
+    if (M <= 1) return run_dp4a<1>(p, tmW, tmA, g, config_id, s);
+    if (M <= 2) return run_dp4a<2>(p, tmW, tmA, g, config_id, s);
+    if (M <= 4) return run_dp4a<4>(p, tmW, tmA, g, config_id, s);
+    return run_dp4a<8>(p, tmW, tmA, g, config_id, s);
+  }
   if (fmt == QG_W8A8_INT8) {
     if (p.mpad == 16) return fz ? run_i8<16, true>(p, tmW, tmA, g, config_id, s) : run_i8<16, false>(p, tmW, tmA, g, config_id, s);
     if (p.mpad == 32) return fz ? run_i8<32, true>(p, tmW, tmA, g, config_id, s) : run_i8<32, false>(p, tmW, tmA, g, config_id, s);
@@ -565,7 +593,7 @@ int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q
 
 size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k) {
   Plan p;
-  if (fmt < 0 || fmt > 2 || M <= 0 || N <= 0 || K <= 0 || variant < 0 || variant > 3) return 0;
+  if (fmt < 0 || fmt > 2 || M <= 0 || N <= 0 || K <= 0 || variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return 0;
   if (make_plan(fmt, M, N, K, variant, split_k, &p) != QG_OK) return 0;
   return static_cast<size_t>(workspace_bytes(p, M, N));
 }
@@ -592,7 +620,8 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
   if (fmt == QG_BLOCK_FP8 || !swap) {
     // quantize into the caller's A_q / s_a, then the GEMM (two launches)
     if (!A_q_dev || !s_a_dev)
-      return fail(QG_ERR_INVALID_ARG, "qg_linear_w8a8: Block_FP8 and the Standard variants need A_q and s_a buffers");
+      return fail(QG_ERR_INVALID_ARG,
+                  "qg_linear_w8a8: Block_FP8, the Standard and the dp4a variants need A_q and s_a buffers");
     int rc = qg_quant_act(fmt, A_dev, M, K, lda, A_q_dev, s_a_dev, stream);
     if (rc != QG_OK) return rc;
     return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,

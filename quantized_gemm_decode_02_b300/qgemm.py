@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 
 QG_FP8_DYNAMIC, QG_W8A8_INT8, QG_BLOCK_FP8 = 0, 1, 2
-QG_STANDARD, QG_SPLITK, QG_SWAPAB, QG_SWAPAB_SPLITK = 0, 1, 2, 3
+QG_STANDARD, QG_SPLITK, QG_SWAPAB, QG_SWAPAB_SPLITK, QG_SWAPAB_DP4A, QG_SWAPAB_DP4A_SPLITK = 0, 1, 2, 3, 4, 5
 QG_OK = 0
 QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED_SHAPE, QG_ERR_ALIGNMENT = -1, -2, -3
 QG_ERR_WORKSPACE_TOO_SMALL, QG_ERR_NO_CONFIG, QG_ERR_CUDA = -4, -5, -6
@@ -24,9 +24,16 @@ QG_ERR_DEVICE_TIMEOUT, QG_ERR_TABLE_PARSE = -7, -8
 QG_LAUNCH_PDL = 1
 
 FORMATS = {"FP8_Dynamic": QG_FP8_DYNAMIC, "W8A8_INT8": QG_W8A8_INT8, "Block_FP8": QG_BLOCK_FP8}
-VARIANTS = {"Standard": QG_STANDARD, "Split-K": QG_SPLITK, "Swap-AB": QG_SWAPAB, "Swap-AB+Split-K": QG_SWAPAB_SPLITK}
+VARIANTS = {"Standard": QG_STANDARD, "Split-K": QG_SPLITK, "Swap-AB": QG_SWAPAB, "Swap-AB+Split-K": QG_SWAPAB_SPLITK,
+            "Swap-AB dp4a": QG_SWAPAB_DP4A, "Swap-AB dp4a+Split-K": QG_SWAPAB_DP4A_SPLITK}
 
 QG_NOALLOC_SCRATCH_BYTES = 4 << 20
+QG_CONFIG_RING_MASK, QG_CONFIG_PREFETCH_SHIFT, QG_CONFIG_MAX_PREFETCH = 31, 5, 64
+
+
+def config_id(ring: int = 0, prefetch: int = 0) -> int:
+    """config_id of a ring depth (0 = default) and an L2 prefetch distance."""
+    return ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT)
 
 EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
            "qg_linear_w8a8", "qg_gemm_w8a8_noalloc",

@@ -104,8 +104,15 @@ def test_gemm_validation(q):
     assert _gemm(q, variant=1, split=2, ws=OK16, wsb=16) == q.QG_ERR_WORKSPACE_TOO_SMALL
     assert _gemm(q, K=4096, variant=3, split=20) == q.QG_ERR_WORKSPACE_TOO_SMALL
     assert _gemm(q, fmt=1, M=8, variant=0) == q.QG_ERR_UNSUPPORTED_SHAPE  # INT8 runs Swap-AB
+    # the CUDA-core (dp4a) variants: W8A8_INT8 with M <= 8 only
+    assert _gemm(q, fmt=1, M=9, variant=q.QG_SWAPAB_DP4A) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(q, fmt=0, M=1, variant=q.QG_SWAPAB_DP4A) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(q, fmt=1, M=1, variant=q.QG_SWAPAB_DP4A, split=2) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, fmt=1, M=1, variant=6) == q.QG_ERR_INVALID_ARG
     assert _gemm(q, fmt=0, dbg=OK16) == q.QG_ERR_INVALID_ARG              # debug acc is INT8 only
-    assert _gemm(q, cfg=99) == q.QG_ERR_INVALID_ARG
+    assert _gemm(q, cfg=17) == q.QG_ERR_INVALID_ARG                       # ring depth above 16
+    assert _gemm(q, cfg=q.config_id(0, 65)) == q.QG_ERR_INVALID_ARG       # prefetch distance above 64
+    assert _gemm(q, cfg=-1) == q.QG_ERR_INVALID_ARG
     assert _gemm(q, M=0) == q.QG_OK
 
 
@@ -118,6 +125,9 @@ def test_workspace_bytes(q):
     assert q.qg_workspace_bytes(1, 32, 4096, 4096, q.QG_SWAPAB_SPLITK, 17) == 256 + 17 * 32 * 4096 * 4
     assert q.qg_workspace_bytes(0, 300, 256, 1024, q.QG_SPLITK, 2) == 256 + 2 * 300 * 256 * 4
     assert q.qg_workspace_bytes(0, 4, 256, 1024, q.QG_SWAPAB_SPLITK, 99) == 0  # invalid -> 0
+    assert q.qg_workspace_bytes(1, 8, 4096, 4096, q.QG_SWAPAB_DP4A_SPLITK, 16) == 0
+    assert q.qg_workspace_bytes(1, 8, 4096, 4096, q.QG_SWAPAB_DP4A_SPLITK, 17) == 256 + 17 * 8 * 4096 * 4
+    assert q.qg_workspace_bytes(1, 9, 4096, 4096, q.QG_SWAPAB_DP4A_SPLITK, 2) == 0  # M > 8 -> invalid
 
 
 def test_launch_flag_and_limits(q):

@@ -47,6 +47,27 @@ def test_w8a8_int8(orc, gc, M, variant, split):
     gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=200 + M, outliers=True)
 
 
+DP, DPS = 4, 5  # the CUDA-core (dp4a) forms of Swap-AB and Swap-AB+Split-K
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("variant,split", [(DP, 1), (DPS, 2), (DPS, 7), (DPS, 16), (DPS, 18)])
+def test_w8a8_int8_dp4a(orc, gc, M, variant, split):
+    # K = 2304 (18 k-tiles); 16 ranges reduce in a cluster, 18 through the
+    # workspace; ragged N; the int32 accumulators bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=250 + M, outliers=True)
+
+
+@pytest.mark.parametrize("fmt,M,variant,split", [("FP8_Dynamic", 3, SWS, 2), ("FP8_Dynamic", 40, STS, 2),
+                                                  ("Block_FP8", 9, SW, 1), ("W8A8_INT8", 20, SWS, 3),
+                                                  ("W8A8_INT8", 2, DPS, 3)])
+@pytest.mark.parametrize("dist", [1, 4, 64])
+def test_l2_prefetch_distance(orc, q, gc, fmt, M, variant, split, dist):
+    # the prefetch distance only adds L2 requests ahead of the ring (64:
+    # beyond every CTA's K range); results stay those of the oracle
+    gc.run_case(orc, fmt, M, 300, 2304, variant, split, seed=400 + dist, config_id=q.config_id(0, dist))
+
+
 @pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])
 @pytest.mark.parametrize("split", [2, 8, 9, 13, 14, 16, 17])
 def test_split_k_cluster_and_workspace_reductions(orc, gc, fmt, split):
