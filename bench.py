@@ -107,7 +107,8 @@ def workload_dtype(items) -> str:
 class Workload:
     """Device buffers and the captured graphs for one workload."""
 
-    def __init__(self, name: str, device: str, seed: int = 0, pdl: bool = True, fused: bool = False):
+    def __init__(self, name: str, device: str, seed: int = 0, pdl: bool = True, fused: bool = False,
+                 table: str = TABLE):
         from quantized_gemm_decode_02_b300 import qgemm as q
         self.q = q
         self.name = name
@@ -124,8 +125,8 @@ class Workload:
         self.models = sorted({m for _, m, _, _ in spec["items"]})
         self.layers = list(dict.fromkeys(layer for _, _, layer, _ in spec["items"]))
         self.ms = list(dict.fromkeys(M for _, _, _, M in spec["items"]))
-        if os.path.exists(TABLE):
-            q.qg_load_table(TABLE)
+        if os.path.exists(table):
+            q.qg_load_table(table)
         q.qg_set_allow_default(True)
         # one contiguous activation buffer (bf16) and one output buffer (bf16),
         # sliced per item at 256-byte boundaries, so e2e copies are single copies
@@ -485,6 +486,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--table", default=TABLE, help="tuned config table to load (default: the shipped B300 table)")
     ap.add_argument("--fused", action="store_true",
                     help="quantize activations inside the GEMM kernel (qg_linear_w8a8) instead of in their own "
                          "kernel (qg_quant_act + qg_gemm_w8a8); measured slower on B300, so not the default")
@@ -503,7 +505,7 @@ def main(argv=None):
         raise SystemExit("bench.py needs a CUDA device (the compute path is the sm_103a library)")
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    wl = Workload(args.workload, device, seed=rank, pdl=not args.no_pdl, fused=args.fused)
+    wl = Workload(args.workload, device, seed=rank, pdl=not args.no_pdl, fused=args.fused, table=args.table)
     stream = torch.cuda.Stream(device=device)
     graph = wl.capture_step(stream)
     timed_graph, evs = wl.capture_timed_kernels(stream)

@@ -10,9 +10,11 @@ times each candidate (variant, split_k, ring depth) as a CUDA graph of R
 GEMM launches (qg_gemm_w8a8; with --linear, whole linear layers through
 qg_linear_w8a8 instead) over rotated weight copies (more than three L2
 capacities, so the weights stream from HBM), with programmatic dependent
-launch on, and keeps the fastest; a second pass tries the winner with an L2
-prefetch distance of 1, 2 and 4 weight k-tiles (config_id's upper bits) and
-keeps one only when it is more than 1% faster.
+launch on, and keeps the fastest.  With --prefetch-pass a second pass tries
+the winner with an L2 prefetch distance of 1, 2 and 4 weight k-tiles
+(config_id's upper bits) and keeps one only when it is more than 1% faster.
+The shipped table is swept without it: distances that won in these
+same-shape chains lost in the mixed-shape chains of bench.py.
 
 Rows already present in the output table are skipped, so an interrupted
 sweep resumes where it stopped.
@@ -168,6 +170,8 @@ def main(argv=None):
     ap.add_argument("--ms", default=",".join(str(m) for m in TUNED_M))
     ap.add_argument("--log", default=None, help="JSON lines with every candidate's time")
     ap.add_argument("--linear", action="store_true", help="time qg_linear_w8a8 (quantization + GEMM)")
+    ap.add_argument("--prefetch-pass", action="store_true",
+                    help="also try the winner with an L2 prefetch distance (config_id upper bits)")
     args = ap.parse_args(argv)
     device = "cuda:0"
     torch.cuda.set_device(0)
@@ -200,10 +204,10 @@ def main(argv=None):
                         us = timed(v, s, c)
                         if best is None or us < best[0]:
                             best = (us, v, s, c)
-                    # second pass: the winner with an L2 prefetch distance,
-                    # kept only when it is more than 1% faster
+                    # optional second pass: the winner with an L2 prefetch
+                    # distance, kept only when it is more than 1% faster
                     us0, v, s, c0 = best
-                    for dist in PREFETCH_DISTANCES:
+                    for dist in (PREFETCH_DISTANCES if args.prefetch_pass else ()):
                         c = q.config_id(c0, dist)
                         us = timed(v, s, c)
                         if us < 0.99 * us0 and us < best[0]:

@@ -93,6 +93,24 @@ def test_int8_accumulators_identical_across_variants(gc):
         assert torch.equal(Y, outs[0][0])
 
 
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_int8_dp4a_and_tensor_core_variants_identical(gc, M):
+    # the CUDA-core (dp4a) and the tensor-core (exact fp32 segments) forms of
+    # Swap-AB compute the same int32 accumulators and the same Y
+    import seeded_inputs as si
+    N, K = 384, 4096
+    A = si.activations(M, K, seed=15 + M, outliers=True).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=15 + M)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("W8A8_INT8", W)
+    Aq, sa = gc.quant_act_gpu("W8A8_INT8", A)
+    outs = [gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, v, s, debug=True) for v, s in
+            [(SW, 1), (SWS, 4), (DP, 1), (DPS, 3), (DPS, 16), (DPS, 32)]]
+    torch.cuda.synchronize()
+    for Y, d in outs[1:]:
+        assert torch.equal(d, outs[0][1])
+        assert torch.equal(Y, outs[0][0])
+
+
 @pytest.mark.parametrize("fmt", ["FP8_Dynamic", "Block_FP8", "W8A8_INT8"])
 def test_split_k_is_deterministic(gc, fmt):
     import seeded_inputs as si
