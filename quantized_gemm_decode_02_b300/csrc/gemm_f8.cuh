@@ -240,6 +240,25 @@ __device__ __forceinline__ void fused_token_scales(const GemmArgs& g, int m_base
 
 // Fused activation quantization, part 2: 32 consecutive activations of token
 // row `row` starting at column k (zeros past K) as fp32.
+// Raw bf16 activations A[row][k .. k+32) as four 16-byte words (zero past K;
+// K % 16 == 0, so a word is either wholly inside the row or wholly past it).
+__device__ __forceinline__ void load_act_raw(const GemmArgs& g, int row, int k, uint4 (&v)[4]) {
+  const __nv_bfloat16* p = g.A + static_cast<int64_t>(row) * g.lda + k;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    v[c] = k + 8 * c < g.K ? *reinterpret_cast<const uint4*>(p + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void unpack_act32(const uint4 (&v)[4], float (&x)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+      x[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
 __device__ __forceinline__ void load_act32(const GemmArgs& g, int row, int k, float (&x)[32]) {
   const __nv_bfloat16* p = g.A + static_cast<int64_t>(row) * g.lda + k;
 #pragma unroll
@@ -438,11 +457,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         fused_token_scales(g, m_base, Mb, k0, k1, clustered, clustered ? split : 0, 448.0f, ctl->amax_s, ctl->sa_s,
                            &ctl->amax_bar, et0, 128, 3, n_tile == 0 && split == 0);
         const bool write_codes = g.a_q_out != nullptr && n_tile == 0;
+        // Pieces of 32 activations (token row r, quarter p of the k-tile),
+        // kPP per thread.  The next k-tile's pieces are loaded while this
+        // one is quantized, and a stage's activation tile is written as soon
+        // as the MMAs of the stage's previous use are done (empty[s]), ahead
+        // of its weight tile.
+        constexpr int kPP = (MPAD * 4 + 127) / 128;
+        uint4 cur[kPP][4], nxt[kPP][4];
+        auto fetch = [&](int i, uint4(&buf)[kPP][4]) {
+#pragma unroll
+          for (int q = 0; q < kPP; ++q) {
+            const int piece = et0 + 128 * q, r = piece >> 2, p = piece & 3;
+            if (piece < MPAD * 4 && r < Mb)
+              load_act_raw(g, m_base + r, (kb0 + i) * kBK + 32 * p, buf[q]);
+            else
+#pragma unroll
+              for (int c = 0; c < 4; ++c) buf[q][c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        };
+        fetch(0, cur);
         for (int i = 0; i < nk; ++i) {
           const int s = i % stages;
-          // the weight tile of this use of the slot has landed, so the
-          // previous use (and its activation tile) is finished
-          if (!__all_sync(0xffffffffu, mbar_wait(&ctl->full[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns) &&
+          if (i + 1 < nk) fetch(i + 1, nxt);
+          if (i >= stages &&
+              !__all_sync(0xffffffffu, mbar_wait(&ctl->empty[s], static_cast<uint32_t>(i / stages - 1) & 1u, g.wait_ns) &&
                                            !*abort_flag)) {
             *abort_flag = 1;
             break;
@@ -450,12 +488,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int kt0 = (kb0 + i) * kBK;
           uint8_t* at = smem + static_cast<size_t>(s) * TS::kStageBytes + TS::kWBytes;
 #pragma unroll
-          for (int piece = et0; piece < MPAD * 4; piece += 128) {
-            const int r = piece >> 2, p = piece & 3;  // token row, 32-element quarter of the 128 K
+          for (int q = 0; q < kPP; ++q) {
+            const int piece = et0 + 128 * q, r = piece >> 2, p = piece & 3;
+            if (piece >= MPAD * 4) continue;
             uint32_t w[8];
             if (r < Mb) {
               float x[32];
-              load_act32(g, m_base + r, kt0 + 32 * p, x);
+              unpack_act32(cur[q], x);
               const Divider dv(ctl->sa_s[r]);
 #pragma unroll
               for (int j = 0; j < 8; ++j)
@@ -478,6 +517,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->full_a[s]);
+#pragma unroll
+          for (int q = 0; q < kPP; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) cur[q][c] = nxt[q][c];
         }
       }
       if constexpr (BLOCK) {

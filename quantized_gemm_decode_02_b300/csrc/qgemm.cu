@@ -554,6 +554,25 @@ int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_t lda, 
     const int64_t groups = M * (K / 128);
     e = launch(qg::quant_groups_kernel<W>, dim3(static_cast<unsigned>(cdiv(groups, W))), dim3(W * 32), 0, s, A, lda,
                static_cast<int>(M), static_cast<int>(K), Q, s_a_dev);
+  } else if (K <= 512 * 8 * 8) {
+    // rows held in registers: 1, 2, 4 or 8 chunks of 8 values per thread
+    const int ch = K <= 4096 ? 1 : (K <= 8192 ? 2 : (K <= 16384 ? 4 : 8));
+    const bool fp8 = fmt == QG_FP8_DYNAMIC;
+    const float qmax = fp8 ? 448.0f : 127.0f;
+    const dim3 grid(static_cast<unsigned>(M)), block(512);
+    const int k = static_cast<int>(K);
+    if (ch == 1)
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 1>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 1>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+    else if (ch == 2)
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 2>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 2>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+    else if (ch == 4)
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 4>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 4>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+    else
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 8>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 8>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
   } else if (fmt == QG_FP8_DYNAMIC) {
     e = launch(qg::quant_rows_kernel<__nv_bfloat16, qg::kFmtFP8, 512>, dim3(static_cast<unsigned>(M)), dim3(512), 0, s,
                A, lda, static_cast<int>(K), Q, s_a_dev, 448.0f);

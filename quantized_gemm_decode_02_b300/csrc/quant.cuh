@@ -75,7 +75,8 @@ __device__ __forceinline__ uint2 encode8(const float (&x)[8], float s) {
 // the correctly rounded reciprocal of s, q1 = RN(x*r) is within two ulps of
 // x/s; one residual step q2 = q1 + r*(x - s*q1) makes it faithful, and a
 // second one returns the correctly rounded quotient, because each residual
-// x - s*q of a faithful q is exact in one fma.  Valid when s, x/s and the
+// x - s*q of a faithful q is exact in one fma.  A zero x is returned as is,
+// with its sign.  Valid when s, x/s and the
 // residuals are normal numbers: Divider::exact is false for rows whose scale
 // lies outside [2^-100, 2^100] (those divide with __fdiv_rn), and x/s below
 // 2^-100 only matters up to its sign once encoded (it rounds to zero).
@@ -90,7 +91,10 @@ struct Divider {
     if (!exact) return __fdiv_rn(x, s);
     const float q1 = __fmul_rn(x, r);
     const float q2 = __fmaf_rn(__fmaf_rn(-q1, s, x), r, q1);
-    return __fmaf_rn(__fmaf_rn(-q2, s, x), r, q2);
+    const float q3 = __fmaf_rn(__fmaf_rn(-q2, s, x), r, q2);
+    // the residual steps turn -0 into +0; the quotient of +-0 is +-0 (E4M3
+    // keeps the sign of zero)
+    return x == 0.0f ? x : q3;
   }
 };
 
@@ -137,6 +141,67 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const InT* __restri
     float v[8];
     load8(x + k, v);
     *reinterpret_cast<uint2*>(q + k) = encode8<OUT>(v, s);
+  }
+}
+
+// Activation rows (bf16) up to 512 x 8 x CH elements: one CTA per row, each
+// thread keeps its CH chunks of 8 values in registers, so the row is read
+// once with all loads in flight together; a single barrier gives every
+// thread the row maximum; the quotients come from Divider (correctly rounded,
+// the same codes as one IEEE division each).
+template <int OUT, int CH>
+__global__ void __launch_bounds__(512) quant_rows_reg_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int K,
+                                                             uint8_t* __restrict__ Q, float* __restrict__ S,
+                                                             float qmax) {
+  constexpr int kThreads = 512;
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float red[kThreads / 32];
+  const int64_t r = blockIdx.x;
+  const __nv_bfloat16* x = X + r * ldx;
+  float v[CH][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int k = (c * kThreads + static_cast<int>(threadIdx.x)) * 8;
+    if (k < K) {
+      load8(x + k, v[c]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[c][i] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[c][i]));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float s = scale_from_amax(amax, qmax);
+  if (threadIdx.x == 0) S[r] = s;
+  const Divider dv(s);
+  uint8_t* q = Q + r * static_cast<int64_t>(K);
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int k = (c * kThreads + static_cast<int>(threadIdx.x)) * 8;
+    if (k >= K) break;
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if constexpr (OUT == kFmtFP8) {
+        const uint16_t lo = e4m3x2(dv(v[c][4 * h + 0]), dv(v[c][4 * h + 1]));
+        const uint16_t hi = e4m3x2(dv(v[c][4 * h + 2]), dv(v[c][4 * h + 3]));
+        w[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      } else {
+        w[h] = static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 0]))) |
+               (static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 1]))) << 8) |
+               (static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 2]))) << 16) |
+               (static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 3]))) << 24);
+      }
+    }
+    *reinterpret_cast<uint2*>(q + k) = make_uint2(w[0], w[1]);
   }
 }
 

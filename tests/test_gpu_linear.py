@@ -107,6 +107,32 @@ def test_fused_quantization_ties(orc, gc, q, fmt, split):
     run_linear(orc, gc, q, fmt, M, N, K, SWS if split > 1 else SW, split, seed=5, A=A)
 
 
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8"])
+@pytest.mark.parametrize("split", [1, 3])
+def test_fused_signed_zeros(orc, gc, q, fmt, split):
+    # -0.0 quantizes to the E4M3 code 0x80 (its sign kept), +0.0 to 0x00
+    M, N, K = 6, 256, 1024
+    A = si.activations(M, K, seed=31, outliers=True)
+    A[0, ::3] = -0.0
+    A[1, 1::5] = 0.0
+    A[2, :] = -0.0  # an all-zero row: s = 1, every code a signed zero
+    run_linear(orc, gc, q, fmt, M, N, K, SWS if split > 1 else SW, split, seed=31, A=A)
+
+
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8"])
+@pytest.mark.parametrize("K", [2560, 12288, 25600])
+def test_quant_act_ties(orc, gc, fmt, K):
+    # the activation quantization kernel on rows whose quotients land on
+    # rounding ties, bit-exact against the oracle
+    rng = np.random.Generator(np.random.PCG64(K))
+    A = tie_rows(fmt, 8, K, rng)
+    Aq, sa = gc.quant_act_gpu(fmt, A.to(gc.DEV))
+    torch.cuda.synchronize()
+    oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
+    assert np.array_equal(Aq.cpu().numpy().view(gc.oracle_dtype(fmt)), oAq)
+    assert np.array_equal(sa.cpu().numpy(), osa)
+
+
 def test_fused_linear_without_optional_outputs(orc, gc, q):
     fmt, M, N, K = "W8A8_INT8", 8, 384, 2048
     A = si.activations(M, K, seed=9)

@@ -239,3 +239,21 @@ def test_quant_act_row_stride(orc, gc, q):
         oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
         assert np.array_equal(Aq.cpu().numpy().view(gc.oracle_dtype(fmt)), oAq)
         assert np.array_equal(sa.cpu().numpy(), osa)
+
+
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8"])
+@pytest.mark.parametrize("K", [16, 656, 4096, 4112, 8192, 12288, 16400, 25600, 32768, 32784])
+def test_quant_act_row_lengths(orc, gc, fmt, K):
+    # every register-resident row kernel (1, 2, 4, 8 chunks of 8 values per
+    # thread, ragged last chunk) and the looping kernel beyond 32768
+    # elements; outliers put the row maximum anywhere in the row
+    import seeded_inputs as si
+    M = 3
+    A = si.activations(M, K, seed=K, outliers=True)
+    A[1, ::7] = -0.0  # negative zeros keep their sign in E4M3 (code 0x80)
+    A[2, 5::11] = 0.0
+    Aq, sa = gc.quant_act_gpu(fmt, A.to(gc.DEV))
+    torch.cuda.synchronize()
+    oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
+    assert np.array_equal(Aq.cpu().numpy().view(gc.oracle_dtype(fmt)), oAq)
+    assert np.array_equal(sa.cpu().numpy(), osa)
