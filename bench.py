@@ -4,10 +4,10 @@ Workload (default, `int8_qwen3_1.7b`): W8A8_INT8 over the four Qwen3-1.7B
 linear layers (qkv K=2048 N=4096, o K=2048 N=2048, gate_up K=2048 N=12288,
 down K=6144 N=2048) at every tuned decode token count M in
 {1,2,4,8,16,24,32}.  One step is one pass of the whole hot path over that
-batch: for each (M, layer) a dynamic per-token activation quantization
-(qg_quant_act) and the quantized GEMM (qg_gemm_w8a8) with the variant the
-tuned table selects (qg_select), 28 + 28 kernels captured once into a CUDA
-graph with programmatic dependent launch and replayed.  Every (M, layer) pair
+batch: for each (M, layer) one qg_linear_w8a8 call, i.e. a dynamic
+per-token activation quantization kernel and the quantized GEMM kernel with
+the variant the tuned table selects (qg_select); 28 + 28 kernels captured once into a CUDA graph with programmatic
+dependent launch and replayed.  Every (M, layer) pair
 owns distinct weights, so a step streams 352 MB of int8 weights (> 126 MB
 L2): no step finds its weights in L2.
 
@@ -187,19 +187,15 @@ class Workload:
         return 1 if self.fused_item(i) else 2
 
     def enqueue(self, stream, i: int):
-        """One linear layer: activation quantization + GEMM (one kernel when
-        fused, else qg_quant_act then qg_gemm_w8a8)."""
+        """One linear layer through qg_linear_w8a8: activation quantization +
+        GEMM (two kernels; one fused kernel with --fused where the format and
+        variant have one)."""
         r = self.recs[i]
         q = self.q
-        if self.fused:
-            fz = self.fused_item(i)
-            q.qg_linear_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["A"], r["K"], r["Wq"], r["sw"], r["Y"], r["N"],
-                             r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes,
-                             None if fz else r["Aq"], None if fz else r["sa"], None, stream=stream)
-            return
-        q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
-        q.qg_gemm_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"], r["N"],
-                       r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes, None, stream=stream)
+        fz = self.fused and self.fused_item(i)
+        q.qg_linear_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["A"], r["K"], r["Wq"], r["sw"], r["Y"], r["N"],
+                         r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes,
+                         None if fz else r["Aq"], None if fz else r["sa"], None, stream=stream)
 
     def capture_step(self, stream) -> torch.cuda.CUDAGraph:
         """The whole step (quant + GEMM for every item) as one graph."""
@@ -488,8 +484,8 @@ def main(argv=None):
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--table", default=TABLE, help="tuned config table to load (default: the shipped B300 table)")
     ap.add_argument("--fused", action="store_true",
-                    help="quantize activations inside the GEMM kernel (qg_linear_w8a8) instead of in their own "
-                         "kernel (qg_quant_act + qg_gemm_w8a8); measured slower on B300, so not the default")
+                    help="quantize activations inside the GEMM kernel (qg_linear_w8a8's one-kernel form) instead "
+                         "of in their own kernel; measured slower on B300, so not the default")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-graph", action="store_true",
@@ -639,7 +635,7 @@ def main(argv=None):
         cfg.update({
             "gemms_per_step": n_gemm, "kernels_per_step": n_kernels,
             "activation_quantization": "fused into the GEMM kernel (qg_linear_w8a8) where one kernel does both"
-                                       if wl.fused else "own kernel (qg_quant_act)",
+                                       if wl.fused else "own kernel (qg_linear_w8a8, two kernels)",
             "bytes_per_step": wl.bytes_step, "flops_per_step": wl.flops_step,
             "weight_bytes_streamed_per_step": wl.weight_bytes_streamed,
             "l2": (f"inputs larger than L2: {wl.weight_bytes_streamed / 1e6:.0f} MB of weights streamed per step "

@@ -136,20 +136,24 @@ QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_
 /* The whole quantized linear layer in one call: dynamic activation
  * quantization ("Scope": per token, or per 1x128 group for Block_FP8)
  * followed by the quantized GEMM ("Kernel Implementation"), i.e.
- * qg_quant_act then qg_gemm_w8a8 with the same results bit for bit.  For
- * FP8_Dynamic and W8A8_INT8 with the Swap-AB variants both steps run in ONE
- * kernel: each CTA quantizes the slice of the activations its K range needs,
- * the CTAs of a Split-K cluster agree on every token's maximum over the
- * whole row through distributed shared memory, and no quantized activation
- * tensor is written unless asked for.  Block_FP8, the Standard and the
- * dp4a variants run the two kernels in sequence.
+ * qg_quant_act then qg_gemm_w8a8 with the same results bit for bit.
+ * Two forms:
+ *  - two kernels (when A_q_dev and s_a_dev are given; the only form of
+ *    Block_FP8, the Standard and the dp4a variants): the quantization kernel
+ *    writes A_q / s_a, the GEMM follows (with QG_LAUNCH_PDL it streams its
+ *    weights while the quantization runs).  The faster form on B300.
+ *  - one kernel (FP8_Dynamic and W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK,
+ *    when A_q_dev or s_a_dev is NULL, or with QG_LAUNCH_FUSED_QUANT set):
+ *    each CTA quantizes the slice of the activations its K range needs, the
+ *    CTAs of a Split-K cluster agree on every token's maximum over the whole
+ *    row through distributed shared memory, and A_q / s_a are written only
+ *    when given.
  *   A_dev      bf16 [M][lda] activations (lda >= K, lda % 8 == 0, 16-byte
  *              aligned), read-only;
  *   W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id, workspace,
  *   ws_bytes, debug_acc_dev   as qg_gemm_w8a8;
- *   A_q_dev, s_a_dev  [M][K] codes and the scales (layouts of qg_quant_act):
- *              optional outputs in the fused case (NULL to skip), required
- *              buffers for Block_FP8, the Standard and the dp4a variants. */
+ *   A_q_dev, s_a_dev  [M][K] codes and the scales (layouts of qg_quant_act).
+ * Errors are those of qg_quant_act and qg_gemm_w8a8. */
 QG_API int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, int64_t lda,
                           const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
                           int split_k, int config_id, void* workspace_dev, size_t ws_bytes, void* A_q_dev,
@@ -202,6 +206,10 @@ QG_API int qg_set_allow_default(int allow);
  * the stream finishes; W_q / s_w must then not be written by the kernels
  * directly preceding the GEMM in that stream. */
 #define QG_LAUNCH_PDL 1
+/* QG_LAUNCH_FUSED_QUANT makes qg_linear_w8a8 take its one-kernel form
+ * (quantization fused into the GEMM) whenever the format and variant have
+ * one, even when A_q / s_a buffers are given. */
+#define QG_LAUNCH_FUSED_QUANT 2
 QG_API int qg_set_launch_flags(int flags);
 
 /* Bound, in nanoseconds, of every pipeline wait inside the kernels (default

@@ -503,7 +503,8 @@ const char* qg_last_error(void) { return g_err.c_str(); }
 const char* qg_version(void) { return "qgemm-b300 0.1 (sm_103a)"; }
 
 int qg_set_launch_flags(int flags) {
-  if (flags & ~QG_LAUNCH_PDL) return fail(QG_ERR_INVALID_ARG, "unknown launch flag bits 0x%x", flags);
+  if (flags & ~(QG_LAUNCH_PDL | QG_LAUNCH_FUSED_QUANT))
+    return fail(QG_ERR_INVALID_ARG, "unknown launch flag bits 0x%x", flags);
   g_launch_flags = flags;
   return QG_OK;
 }
@@ -635,23 +636,25 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
                    const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k, int config_id,
                    void* workspace_dev, size_t ws_bytes, void* A_q_dev, float* s_a_dev, int32_t* debug_acc_dev,
                    void* stream) {
-  const bool swap = variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK;
-  if (fmt == QG_BLOCK_FP8 || !swap) {
-    // quantize into the caller's A_q / s_a, then the GEMM (two launches)
-    if (!A_q_dev || !s_a_dev)
-      return fail(QG_ERR_INVALID_ARG,
-                  "qg_linear_w8a8: Block_FP8, the Standard and the dp4a variants need A_q and s_a buffers");
-    int rc = qg_quant_act(fmt, A_dev, M, K, lda, A_q_dev, s_a_dev, stream);
-    if (rc != QG_OK) return rc;
-    return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
-                      workspace_dev, ws_bytes, debug_acc_dev, stream, nullptr);
-  }
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
-  if ((A_q_dev && !aligned(A_q_dev, 16)) || (s_a_dev && !aligned(s_a_dev, 4)))
-    return fail(QG_ERR_ALIGNMENT, "A_q needs 16-byte alignment, s_a 4");
-  const FusedIn f{A_dev, lda};
+  const bool fusable = fmt != QG_BLOCK_FP8 && (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK);
+  const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
+  if (fusable && (!buffers || (g_launch_flags & QG_LAUNCH_FUSED_QUANT))) {
+    // one kernel: each CTA quantizes the activations its K range needs
+    if ((A_q_dev && !aligned(A_q_dev, 16)) || (s_a_dev && !aligned(s_a_dev, 4)))
+      return fail(QG_ERR_ALIGNMENT, "A_q needs 16-byte alignment, s_a 4");
+    const FusedIn f{A_dev, lda};
+    return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
+                      workspace_dev, ws_bytes, debug_acc_dev, stream, &f);
+  }
+  // two kernels: quantize into the caller's A_q / s_a, then the GEMM
+  if (!buffers)
+    return fail(QG_ERR_INVALID_ARG,
+                "qg_linear_w8a8: Block_FP8, the Standard and the dp4a variants need A_q and s_a buffers");
+  int rc = qg_quant_act(fmt, A_dev, M, K, lda, A_q_dev, s_a_dev, stream);
+  if (rc != QG_OK) return rc;
   return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
-                    workspace_dev, ws_bytes, debug_acc_dev, stream, &f);
+                    workspace_dev, ws_bytes, debug_acc_dev, stream, nullptr);
 }
 
 int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,

@@ -22,6 +22,7 @@ QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED_SHAPE, QG_ERR_ALIGNMENT = -1, -2, -3
 QG_ERR_WORKSPACE_TOO_SMALL, QG_ERR_NO_CONFIG, QG_ERR_CUDA = -4, -5, -6
 QG_ERR_DEVICE_TIMEOUT, QG_ERR_TABLE_PARSE = -7, -8
 QG_LAUNCH_PDL = 1
+QG_LAUNCH_FUSED_QUANT = 2
 
 FORMATS = {"FP8_Dynamic": QG_FP8_DYNAMIC, "W8A8_INT8": QG_W8A8_INT8, "Block_FP8": QG_BLOCK_FP8}
 VARIANTS = {"Standard": QG_STANDARD, "Split-K": QG_SPLITK, "Swap-AB": QG_SWAPAB, "Swap-AB+Split-K": QG_SWAPAB_SPLITK,
@@ -126,8 +127,9 @@ def qg_gemm_w8a8(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, con
 
 def qg_linear_w8a8(fmt, M, N, K, A, lda, W_q, s_w, Y, ldy, variant, split_k, config_id=0, workspace=None,
                    ws_bytes=0, A_q=None, s_a=None, debug_acc=None, stream=None) -> None:
-    """Activation quantization and the GEMM in one call (one kernel for
-    FP8_Dynamic / W8A8_INT8 with Swap-AB)."""
+    """Activation quantization and the GEMM in one call: two kernels when
+    A_q and s_a are given, else (FP8_Dynamic / W8A8_INT8 with Swap-AB, or
+    with QG_LAUNCH_FUSED_QUANT set) one kernel."""
     _check(_lib.qg_linear_w8a8(_fmt(fmt), M, N, K, _ptr(A), lda, _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant,
                                split_k, config_id, _ptr(workspace), ws_bytes, _ptr(A_q), _ptr(s_a), _ptr(debug_acc),
                                _stream(stream)), "qg_linear_w8a8")

@@ -1,4 +1,6 @@
-"""qg_linear_w8a8: activation quantization fused into the GEMM kernel.
+"""qg_linear_w8a8 in its two forms: activation quantization fused into the
+GEMM kernel (QG_LAUNCH_FUSED_QUANT, or no A_q / s_a buffers), and the
+quantization kernel followed by the GEMM (the default with buffers).
 
 Against the CPU oracle on the same seeded inputs: the quantized activations
 and scales the kernel writes out are bit-exact (the kernel divides with
@@ -61,7 +63,7 @@ def tie_rows(fmt: str, M: int, K: int, rng) -> torch.Tensor:
     return t
 
 
-def run_linear(orc, gc, q, fmt, M, N, K, variant, split, seed, A=None, check_two_kernel=True):
+def run_linear(orc, gc, q, fmt, M, N, K, variant, split, seed, A=None, check_two_kernel=True, fused=True):
     dev = gc.DEV
     if A is None:
         A = si.activations(M, K, seed=seed, outliers=True)
@@ -76,7 +78,11 @@ def run_linear(orc, gc, q, fmt, M, N, K, variant, split, seed, A=None, check_two
     sa_shape = (M, K // 128) if fmt == "Block_FP8" else (M,)
     sa = torch.full(sa_shape, -1.0, dtype=torch.float32, device=dev)
     dbg = torch.full((M, N), -7, dtype=torch.int32, device=dev) if is_int8 else None
-    q.qg_linear_w8a8(fmt, M, N, K, Ad, K, Wq, sw, Y, N, variant, split, 0, ws, need, Aq, sa, dbg)
+    q.qg_set_launch_flags(q.QG_LAUNCH_FUSED_QUANT if fused else 0)
+    try:
+        q.qg_linear_w8a8(fmt, M, N, K, Ad, K, Wq, sw, Y, N, variant, split, 0, ws, need, Aq, sa, dbg)
+    finally:
+        q.qg_set_launch_flags(0)
     torch.cuda.synchronize()
     assert q.qg_device_error() == 0
     oAq, osa, oWq, osw = gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
@@ -146,10 +152,66 @@ def test_fused_linear_without_optional_outputs(orc, gc, q):
     gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y)
 
 
-@pytest.mark.parametrize("fmt,variant,split", [("Block_FP8", SWS, 3), ("Block_FP8", SW, 1), ("FP8_Dynamic", ST, 1)])
-def test_two_kernel_linear(orc, gc, q, fmt, variant, split):
-    # Block_FP8 and the Standard variant quantize into the caller's buffers
-    run_linear(orc, gc, q, fmt, 12, 264, 1024, variant, split, seed=11)
+DP, DPS, STS = 4, 5, 1
+
+
+@pytest.mark.parametrize("fmt,variant,split,M", [
+    ("Block_FP8", SWS, 3, 12), ("Block_FP8", SW, 1, 12), ("FP8_Dynamic", ST, 1, 12), ("FP8_Dynamic", STS, 3, 40),
+    ("FP8_Dynamic", SW, 1, 5), ("FP8_Dynamic", SWS, 4, 24), ("FP8_Dynamic", SWS, 18, 7),
+    ("W8A8_INT8", SW, 1, 9), ("W8A8_INT8", SWS, 3, 32), ("W8A8_INT8", SWS, 18, 3),
+    ("W8A8_INT8", DP, 1, 1), ("W8A8_INT8", DPS, 5, 4), ("W8A8_INT8", DPS, 18, 8)])
+def test_two_kernel_linear(orc, gc, q, fmt, variant, split, M):
+    # the quantization kernel writes the caller's buffers, the GEMM reads
+    # them; every kernel family, every reduction (none, cluster, workspace);
+    # K = 2304 (18 k-tiles)
+    run_linear(orc, gc, q, fmt, M, 264, 2304, variant, split, seed=11 + M, fused=False)
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+def test_two_kernel_linear_graph_replays(orc, gc, q, pdl):
+    # a captured chain of linear layers (quantization + GEMM pairs, with and
+    # without programmatic dependent launch) replayed many times: every
+    # replay gives the results of a direct run
+    dev = gc.DEV
+    cases = [("W8A8_INT8", 1, DPS, 4), ("W8A8_INT8", 16, SWS, 3), ("FP8_Dynamic", 8, SWS, 5), ("Block_FP8", 4, SW, 1),
+             ("FP8_Dynamic", 64, ST, 1), ("W8A8_INT8", 2, DP, 1)]
+    N, K = 384, 2048
+    layers = []
+    for i, (fmt, M, v, s) in enumerate(cases):
+        A = si.activations(M, K, seed=60 + i).to(dev)
+        W = torch.from_numpy(si.weights(N, K, seed=60 + i)).to(dev)
+        Wq, sw = gc.quant_weight_gpu(fmt, W)
+        need = q.qg_workspace_bytes(fmt, M, N, K, v, s)
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        Aq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((M, K // 128) if fmt == "Block_FP8" else (M,), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        layers.append((fmt, M, v, s, A, Wq, sw, ws, need, Aq, sa, Y))
+    stream = torch.cuda.Stream()
+
+    def run_all():
+        for (fmt, M, v, s, A, Wq, sw, ws, need, Aq, sa, Y) in layers:
+            q.qg_linear_w8a8(fmt, M, N, K, A, K, Wq, sw, Y, N, v, s, 0, ws, need, Aq, sa, None, stream=stream)
+
+    with torch.cuda.stream(stream):
+        run_all()
+    torch.cuda.synchronize()
+    ref = [L[-1].clone() for L in layers]
+    q.qg_set_launch_flags(q.QG_LAUNCH_PDL if pdl else 0)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            run_all()
+    finally:
+        q.qg_set_launch_flags(0)
+    for rep in range(40):
+        for L in layers:
+            L[-1].fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert q.qg_device_error() == 0
+        for L, r in zip(layers, ref):
+            assert torch.equal(L[-1], r), f"replay {rep}"
 
 
 def test_linear_needs_buffers_when_not_fused(q, gc):
