@@ -125,12 +125,10 @@ class Bench:
                         q.qg_gemm_w8a8(fmt, M, N, K, self.Aq, self.sa, W, self.sw, self.Y, N, variant, split, cfg,
                                        self.ws if need else None, need, None, stream=self.stream)
                         continue
-                    # fused layers write no quantized activations; the others
-                    # quantize into Aq / sa first
-                    fused = fmt != "Block_FP8" and variant in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK)
+                    # the linear call's two-kernel form (quantization into
+                    # Aq / sa, then the GEMM), as bench.py runs it
                     q.qg_linear_w8a8(fmt, M, N, K, self.A, K, W, self.sw, self.Y, N, variant, split, cfg,
-                                     self.ws if need else None, need, None if fused else self.Aq,
-                                     None if fused else self.sa, None, stream=self.stream)
+                                     self.ws if need else None, need, self.Aq, self.sa, None, stream=self.stream)
         finally:
             q.qg_set_launch_flags(0)
         for _ in range(2):
@@ -169,7 +167,8 @@ def main(argv=None):
     ap.add_argument("--models", default="Qwen3-1.7B,Qwen3-8B,Qwen3-32B")
     ap.add_argument("--ms", default=",".join(str(m) for m in TUNED_M))
     ap.add_argument("--log", default=None, help="JSON lines with every candidate's time")
-    ap.add_argument("--linear", action="store_true", help="time qg_linear_w8a8 (quantization + GEMM)")
+    ap.add_argument("--linear", action="store_true",
+                    help="time qg_linear_w8a8 (quantization kernel + GEMM) instead of the GEMM alone")
     ap.add_argument("--prefetch-pass", action="store_true",
                     help="also try the winner with an L2 prefetch distance (config_id upper bits)")
     args = ap.parse_args(argv)
