@@ -103,6 +103,15 @@ QG_API int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_
 QG_API int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q_dev, float* s_w_dev,
                     void* stream);
 
+/* The same weight quantization on the host, for offline packing of
+ * checkpoints (codes and scales bit for bit those of qg_quant_weight).
+ *   W_host    fp32 [N][K] row-major, read-only (host memory);
+ *   W_q_host  [N][K] E4M3 codes or int8, written (host memory);
+ *   s_w_host  fp32 [N] or [ceil(N/128)][K/128] (Block_FP8), written.
+ * Synchronous; no device work.  Errors: QG_ERR_INVALID_ARG (format, sizes,
+ * null pointers), QG_ERR_UNSUPPORTED_SHAPE (K % 16, Block_FP8 K % 128). */
+QG_API int qg_pack_weight(int fmt, const float* W_host, int64_t N, int64_t K, void* W_q_host, float* s_w_host);
+
 /* Workspace bytes qg_gemm_w8a8 needs for this shape and variant (0 when
  * split_k == 1).  Layout: per-tile arrival counters (must be zero before the
  * first use; the kernels leave them zero again), then the split partials. */

@@ -4,8 +4,10 @@
 // quant.cuh, gemm_f8.cuh, gemm_i8.cuh and gemm_i8_dp4a.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -496,6 +498,25 @@ int noalloc_scratch(void** out) {
 
 }  // namespace
 
+// ------------------------------------------------- host weight packing
+// qg_pack_weight: the weight quantization of qg_quant_weight on the host
+// (fp32 IEEE arithmetic, one division per scale and per code), for callers
+// that quantize checkpoints offline and upload codes and scales.
+namespace {
+
+float pack_scale(float amax, float qmax) { return amax > 0.0f ? amax / qmax : 1.0f; }
+
+uint8_t pack_code(bool int8, float x, float s) {
+  const float q = x / s;
+  if (int8) {
+    const float r = std::min(127.0f, std::max(-127.0f, std::nearbyint(q)));  // ties to even
+    return static_cast<uint8_t>(static_cast<int8_t>(r));
+  }
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3));
+}
+
+}  // namespace
+
 // ====================================================================== ABI
 extern "C" {
 
@@ -582,6 +603,41 @@ int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_t lda, 
                s, A, lda, static_cast<int>(K), Q, s_a_dev, 127.0f);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quant_act launch");
+  return QG_OK;
+}
+
+int qg_pack_weight(int fmt, const float* W_host, int64_t N, int64_t K, void* W_q_host, float* s_w_host) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "bad sizes N=%lld K=%lld", (long long)N, (long long)K);
+  if (!W_host || !W_q_host || !s_w_host) return fail(QG_ERR_INVALID_ARG, "null pointer");
+  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
+  uint8_t* Q = static_cast<uint8_t*>(W_q_host);
+  if (fmt == QG_BLOCK_FP8) {
+    const int64_t kblocks = K / 128;
+    for (int64_t n0 = 0; n0 < N; n0 += 128) {
+      const int64_t n1 = std::min(N, n0 + 128);
+      for (int64_t kb = 0; kb < kblocks; ++kb) {
+        float amax = 0.0f;
+        for (int64_t n = n0; n < n1; ++n)
+          for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) amax = std::max(amax, std::fabs(W_host[n * K + k]));
+        const float sc = pack_scale(amax, 448.0f);
+        s_w_host[(n0 / 128) * kblocks + kb] = sc;
+        for (int64_t n = n0; n < n1; ++n)
+          for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) Q[n * K + k] = pack_code(false, W_host[n * K + k], sc);
+      }
+    }
+    return QG_OK;
+  }
+  const bool int8 = fmt == QG_W8A8_INT8;
+  for (int64_t n = 0; n < N; ++n) {
+    const float* w = W_host + n * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) amax = std::max(amax, std::fabs(w[k]));
+    const float sc = pack_scale(amax, int8 ? 127.0f : 448.0f);
+    s_w_host[n] = sc;
+    for (int64_t k = 0; k < K; ++k) Q[n * K + k] = pack_code(int8, w[k], sc);
+  }
   return QG_OK;
 }
 

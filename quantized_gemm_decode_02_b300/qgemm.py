@@ -36,7 +36,7 @@ def config_id(ring: int = 0, prefetch: int = 0) -> int:
     """config_id of a ring depth (0 = default) and an L2 prefetch distance."""
     return ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT)
 
-EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
+EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
            "qg_linear_w8a8", "qg_gemm_w8a8_noalloc",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
            "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
@@ -55,6 +55,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
     lib.qg_quant_act.argtypes = [I, P, I64, I64, I64, P, P, P]
     lib.qg_quant_weight.argtypes = [I, P, I64, I64, P, P, P]
+    lib.qg_pack_weight.argtypes = [I, P, I64, I64, P, P]
     lib.qg_workspace_bytes.argtypes = [I, I64, I64, I64, I, I]
     lib.qg_workspace_bytes.restype = SZ
     lib.qg_workspace_init.argtypes = [P, SZ, P]
@@ -108,6 +109,14 @@ def qg_quant_act(fmt, A, M, K, lda, A_q, s_a, stream=None) -> None:
 
 def qg_quant_weight(fmt, W, N, K, W_q, s_w, stream=None) -> None:
     _check(_lib.qg_quant_weight(_fmt(fmt), _ptr(W), N, K, _ptr(W_q), _ptr(s_w), _stream(stream)), "qg_quant_weight")
+
+
+def qg_pack_weight(fmt, W, N, K, W_q, s_w) -> None:
+    """Host weight quantization: W, W_q, s_w are CPU tensors (contiguous)."""
+    for t in (W, W_q, s_w):
+        if isinstance(t, torch.Tensor) and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("qg_pack_weight takes contiguous host tensors")
+    _check(_lib.qg_pack_weight(_fmt(fmt), _ptr(W), N, K, _ptr(W_q), _ptr(s_w)), "qg_pack_weight")
 
 
 def qg_workspace_bytes(fmt, M, N, K, variant, split_k) -> int:
