@@ -366,11 +366,12 @@ TRAFFIC = os.path.join(ROOT, "profiles", "gemm_traffic.json")
 
 
 def kernel_sources_sha() -> str:
-    """SHA-256 over the library's kernel sources (csrc/*, sorted by name)."""
+    """SHA-256 over the library's kernel sources (csrc/*.cuh, sorted by name;
+    the host-side ABI file is not part of it)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_gemm_decode_02_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(n for n in os.listdir(csrc) if n.endswith(".cuh")):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode() + b"\0" + fh.read())
     return h.hexdigest()
