@@ -72,7 +72,9 @@ typedef enum {
 
 #define QG_CONFIG_RING_MASK 31
 #define QG_CONFIG_PREFETCH_SHIFT 5
+#define QG_CONFIG_PREFETCH_MASK (127 << 5)
 #define QG_CONFIG_MAX_PREFETCH 64
+#define QG_CONFIG_WIDE (1 << 12)
 
 typedef enum {
   QG_OK = 0,
@@ -133,7 +135,10 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      CTA keeps that many 16 KB weight k-tiles requested
  *                      into L2 ahead of the ring's loads, the first of them
  *                      before it waits for the kernel it depends on (0 =
- *                      off; at most QG_CONFIG_MAX_PREFETCH);
+ *                      off; at most QG_CONFIG_MAX_PREFETCH); plus
+ *                      QG_CONFIG_WIDE for FP8_Dynamic with QG_STANDARD /
+ *                      QG_SPLITK: 256 weight rows per tile (MMA N = 256)
+ *                      instead of 128 (QG_ERR_INVALID_ARG elsewhere);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

@@ -40,6 +40,7 @@ struct GemmArgs {
   int64_t ldy;          // Y row stride (elements)
   int kt_total;         // ceil(K / 128)
   int splits;           // >= 1
+  int m_tiles;          // token blocks (Swap-AB) or 128-token tiles (Standard); blockIdx.x = n_tile * m_tiles + m
   int stages;           // shared-memory ring depth
   int l2_prefetch;      // L2 prefetch distance: weight k-tiles requested ahead of the ring's loads
   int reduce;           // kReduceNone / kReduceCluster / kReduceGlobal
@@ -101,6 +102,18 @@ struct TileShape {
 template <bool SWAP, int MPAD>
 __host__ __device__ constexpr size_t gemm_f8_smem_bytes(int stages, int recv_bytes = 0) {
   return 1024 + static_cast<size_t>(stages) * TileShape<SWAP, MPAD>::kStageBytes + recv_bytes + sizeof(Ctrl);
+}
+// Standard variant stage: BNW weight rows (128, or 256 for the wide tiles
+// of FP8_Dynamic) and 128 token rows of one 128-byte k-tile.
+template <int BNW>
+struct StdShape {
+  static constexpr uint32_t kWBytes = BNW * kBK;
+  static constexpr uint32_t kABytes = 128 * kBK;
+  static constexpr uint32_t kStageBytes = kWBytes + kABytes;  // multiple of 1024
+};
+template <int BNW>
+__host__ __device__ constexpr size_t gemm_f8_std_smem_bytes(int stages) {
+  return 1024 + static_cast<size_t>(stages) * StdShape<BNW>::kStageBytes + sizeof(Ctrl);
 }
 
 __device__ __forceinline__ void store_bf16(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
@@ -299,9 +312,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool clustered = g.reduce == kReduceCluster;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x;
+  // the token blocks of one weight tile are adjacent block indices, so they
+  // run together and all but the first find the tile's weights in L2
+  const int n_tile = static_cast<int>(blockIdx.x / g.m_tiles);
   const int split = blockIdx.y;
-  const int m_blk = blockIdx.z;               // token block: tokens [m_base, m_base + Mb)
+  const int m_blk = static_cast<int>(blockIdx.x % g.m_tiles);  // token block: tokens [m_base, m_base + Mb)
   const int m_base = m_blk * MPAD;
   const int Mb = min(MPAD, g.M - m_base);
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
@@ -636,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __threadfence();
       named_bar_sync(1, 128);
-      const int tile_id = m_blk * gridDim.x + n_tile;
+      const int tile_id = blockIdx.x;
       if (et == 0) {
         const int old = atomicAdd(g.ws_count + tile_id, 1);
         ctl->last_flag = (old == g.splits - 1);
@@ -662,14 +677,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Tokens on the MMA M side: one CTA per (128-token tile, 128-row weight
 // tile, K range); D[128 tokens x 128 weight rows] in TMEM.  Serves M > 32
 // (and M <= 32 when the table picks it); Split-K uses the global workspace.
-template <int FMT>
+// BNW: weight rows per tile and MMA N (128; 256 for FP8_Dynamic's wide
+// tiles, which halve the MMA instructions and the activation-tile loads per
+// output).
+template <int FMT, int BNW>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f8_std_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
-  using TS = TileShape<false, 16>;
+  using TS = StdShape<BNW>;
   constexpr bool BLOCK = (FMT == kFmtBlock);
+  static_assert(BNW == 128 || (BNW == 256 && !BLOCK), "wide tiles are FP8_Dynamic only");
   constexpr int NBUF = BLOCK ? 2 : 1;
-  // D is 128 lanes x 128 cols per buffer, plus (Block) a 128-col running sum.
-  constexpr uint32_t kBufCols = kBN;
+  // D is 128 lanes x BNW cols per buffer, plus (Block) a 128-col running sum.
+  constexpr uint32_t kBufCols = BNW;
   constexpr uint32_t kTmemCols = pow2_cols(NBUF * kBufCols + (BLOCK ? kBN : 0));
   static_assert(kTmemCols <= 512, "TMEM budget");
 
@@ -679,8 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + static_cast<size_t>(stages) * TS::kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x;
-  const int m_tile = blockIdx.z;
+  // the token tiles of one weight tile are adjacent block indices (weights
+  // read from HBM once, then from L2)
+  const int n_tile = static_cast<int>(blockIdx.x / g.m_tiles);
+  const int m_tile = static_cast<int>(blockIdx.x % g.m_tiles);
   const int split = blockIdx.y;
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
@@ -717,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      const int w_row = n_tile * kBN;
+      const int w_row = n_tile * BNW;
       const int a_row = m_tile * 128;
       const int pre = nk < stages ? nk : stages;
       for (int i = 0; i < pre; ++i) {
@@ -752,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(128, kBN, 0, 0);  // E4M3 x E4M3 -> F32
+      constexpr uint32_t idesc = make_idesc(128, BNW, 0, 0);  // E4M3 x E4M3 -> F32
       bool ok = true;
       if (g.force_timeout) ok = mbar_wait(&ctl->never, 0, g.wait_ns);
       for (int i = 0; ok && i < nk; ++i) {
@@ -837,11 +858,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t src_col = BLOCK ? run_col : 0;
     float* part = static_cast<float*>(g.ws_part);
 #pragma unroll 1
-    for (int c = 0; c < kBN && !abort; c += 8) {
+    for (int c = 0; c < BNW && !abort; c += 8) {
       uint32_t t[8];
       tmem_ld_x8(tmem + lane_base + src_col + c, t);
       tmem_ld_wait();
-      const int n0 = n_tile * kBN + c;
+      const int n0 = n_tile * BNW + c;
       if (!m_ok) continue;
       if (g.splits == 1) {
         if (n0 + 8 <= g.N) {
@@ -878,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (g.splits > 1 && !abort) {
       __threadfence();
       named_bar_sync(1, 128);
-      const int tile_id = m_tile * gridDim.x + n_tile;
+      const int tile_id = blockIdx.x;
       if (et == 0) {
         const int old = atomicAdd(g.ws_count + tile_id, 1);
         ctl->last_flag = (old == g.splits - 1);
@@ -887,8 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ctl->last_flag) {
         __threadfence();
         if (m_ok) {
-          for (int c = 0; c < kBN; ++c) {
-            const int n = n_tile * kBN + c;
+          for (int c = 0; c < BNW; ++c) {
+            const int n = n_tile * BNW + c;
             if (n >= g.N) break;
             float sum = 0.0f;
             for (int s = 0; s < g.splits; ++s) sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);

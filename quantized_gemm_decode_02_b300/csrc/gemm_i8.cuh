@@ -116,8 +116,10 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   const bool clustered = g.reduce == kReduceCluster;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x, split = blockIdx.y;
-  const int m_blk = blockIdx.z;               // token block: tokens [m_base, m_base + Mb)
+  // the token blocks of one weight tile are adjacent block indices (weights
+  // read from HBM once, then from L2)
+  const int n_tile = static_cast<int>(blockIdx.x / g.m_tiles), split = blockIdx.y;
+  const int m_blk = static_cast<int>(blockIdx.x % g.m_tiles);  // token block: tokens [m_base, m_base + Mb)
   const int m_base = m_blk * MPAD;
   const int Mb = min(MPAD, g.M - m_base);
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       }
       __threadfence();
       named_bar_sync(1, kI8ConvThreads);
-      const int tile_id = m_blk * gridDim.x + n_tile;
+      const int tile_id = blockIdx.x;
       if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + tile_id, 1) == g.splits - 1);
       named_bar_sync(1, kI8ConvThreads);
       if (ctl->last_flag) {

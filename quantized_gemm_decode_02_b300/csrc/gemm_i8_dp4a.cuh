@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kDpThreads, 2)
   const bool clustered = g.reduce == kReduceCluster;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x, split = blockIdx.y;
+  const int n_tile = blockIdx.x, split = blockIdx.y;  // one token block (m_tiles == 1)
   const int Mb = min(MT, g.M);  // one token block: M <= 8
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);

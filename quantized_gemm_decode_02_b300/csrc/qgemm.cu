@@ -190,6 +190,8 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
     p->m_tiles = static_cast<int>(cdiv(M, 128));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   }
+  if (static_cast<int64_t>(p->n_tiles) * p->m_tiles > 0x7FFFFFFF)
+    return fail(QG_ERR_UNSUPPORTED_SHAPE, "too many output tiles");
   const bool split_variant = (variant == QG_SPLITK || variant == QG_SWAPAB_SPLITK || variant == QG_SWAPAB_DP4A_SPLITK);
   if (split_k < 1 || split_k > p->kt)
     return fail(QG_ERR_UNSUPPORTED_SHAPE, "split_k=%d outside [1, ceil(K/128)=%d]", split_k, p->kt);
@@ -257,17 +259,17 @@ int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, q
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles, p.splits, p.m_tiles),
+  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, 1),
                      qg::kThreads, qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
-template <int FMT>
+template <int FMT, int BNW>
 int run_f8_std(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                cudaStream_t stream) {
-  int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_smem_bytes<false, 16>(st); }, &g.stages);
+  int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_std_smem_bytes<BNW>(st); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_std_kernel<FMT>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kThreads,
-                     qg::gemm_f8_smem_bytes<false, 16>(g.stages), tmW, tmA, g, stream);
+  return launch_gemm(qg::gemm_f8_std_kernel<FMT, BNW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, 1), qg::kThreads,
+                     qg::gemm_f8_std_smem_bytes<BNW>(g.stages), tmW, tmA, g, stream);
 }
 
 template <int MPAD>
@@ -286,7 +288,7 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED>, p, dim3(p.n_tiles, p.splits, p.m_tiles), qg::kI8Threads,
+  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, 1), qg::kI8Threads,
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -375,10 +377,14 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   if (variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
   if (M < 0 || N <= 0 || K <= 0 || ldy < N)
     return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld ldy=%lld", (long long)M, (long long)N, (long long)K, (long long)ldy);
-  if (config_id < 0 || (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
-      (config_id >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
-    return fail(QG_ERR_INVALID_ARG, "config_id %d: ring depth above %d or prefetch distance above %d", config_id,
-                kMaxStages, QG_CONFIG_MAX_PREFETCH);
+  const bool wide = (config_id & QG_CONFIG_WIDE) != 0;
+  if (config_id < 0 || (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+      (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
+      ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
+    return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
+                config_id, kMaxStages, QG_CONFIG_MAX_PREFETCH);
+  if (wide && (fmt != QG_FP8_DYNAMIC || !(variant == QG_STANDARD || variant == QG_SPLITK)))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_WIDE is for the FP8_Dynamic Standard / Split-K variants");
   if (M == 0) return QG_OK;
   if ((!fused && (!A_q_dev || !s_a_dev)) || !W_q_dev || !s_w_dev || !Y_dev)
     return fail(QG_ERR_INVALID_ARG, "null pointer");
@@ -396,6 +402,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   Plan p;
   int rc = make_plan(fmt, M, N, K, variant, split_k, &p);
   if (rc != QG_OK) return rc;
+  if (wide) p.n_tiles = static_cast<int>(cdiv(N, 256));
   const int64_t need = workspace_bytes(p, M, N);
   if (need > 0) {
     if (!workspace_dev) return fail(QG_ERR_WORKSPACE_TOO_SMALL, "split_k=%d needs a %lld-byte workspace", split_k, (long long)need);
@@ -404,7 +411,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (!aligned(workspace_dev, 256)) return fail(QG_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   }
   CUtensorMap tmW, tmA;
-  rc = make_map(&tmW, W_q_dev, N, K, K, 128);
+  rc = make_map(&tmW, W_q_dev, N, K, K, wide ? 256u : 128u);
   if (rc != QG_OK) return rc;
   if (fused) {
     tmA = tmW;  // unused: the kernel reads the bf16 activations directly
@@ -420,11 +427,14 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   g.ldy = ldy;
   g.kt_total = p.kt;
   g.splits = p.splits;
+  g.m_tiles = p.m_tiles;
   g.s_a = s_a_dev;
   g.s_w = s_w_dev;
   g.Y = static_cast<__nv_bfloat16*>(Y_dev);
   if (p.reduce == qg::kReduceGlobal) {
-    const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
+    // the partials start after the counters of 128-row tiles even for wide
+    // tiles, so that no configuration's partials overlap another's counters
+    const int64_t tiles = cdiv(N, 128) * p.m_tiles;
     g.ws_count = static_cast<int*>(workspace_dev);
     g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
   }
@@ -441,7 +451,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   }
   g.wait_ns = g_wait_ns;
   g.force_timeout = g_force_timeout;
-  g.l2_prefetch = config_id >> QG_CONFIG_PREFETCH_SHIFT;
+  g.l2_prefetch = (config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   const bool fz = fused != nullptr;
@@ -462,8 +472,10 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (p.mpad == 32) return run_f8_swap_fmt<32>(fmt, fz, p, tmW, tmA, g, config_id, s);
     return run_f8_swap_fmt<64>(fmt, fz, p, tmW, tmA, g, config_id, s);
   }
-  if (fmt == QG_FP8_DYNAMIC) return run_f8_std<qg::kFmtFP8>(p, tmW, tmA, g, config_id, s);
-  return run_f8_std<qg::kFmtBlock>(p, tmW, tmA, g, config_id, s);
+  if (fmt == QG_FP8_DYNAMIC)
+    return wide ? run_f8_std<qg::kFmtFP8, 256>(p, tmW, tmA, g, config_id, s)
+                : run_f8_std<qg::kFmtFP8, 128>(p, tmW, tmA, g, config_id, s);
+  return run_f8_std<qg::kFmtBlock, 128>(p, tmW, tmA, g, config_id, s);
 }
 
 }  // namespace

@@ -60,7 +60,7 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     and without Split-K (reduced in a cluster, up to 16 ranges) for every M
     (in blocks of 64 tokens above 64); for W8A8_INT8 at M <= 8 also their
     CUDA-core (dp4a) forms; above 32 tokens also the Standard variant of the
-    E4M3 formats.  Ring depth: 0 = two CTAs per SM, 12 = one
+    E4M3 formats (FP8_Dynamic also with 256-row weight tiles).  Ring depth: 0 = two CTAs per SM, 12 = one
     deep ring per SM (6 for Standard, whose stages are twice as large)."""
     n_tiles = (N + 127) // 128
     kt = (K + 127) // 128
@@ -84,6 +84,14 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
             for s in (2, 3, 4, 6, 8):
                 if s <= kt and std_tiles * s <= 4 * sms:
                     out.append((q.QG_SPLITK, s, cfg))
+        if fmt == "FP8_Dynamic":
+            # 256-row weight tiles: ring of 2 (two CTAs per SM) or 4 (one)
+            wide_tiles = -(-N // 256) * -(-M // 128)
+            for cfg in (q.config_id(0, 0, True), q.config_id(4, 0, True)):
+                out.append((q.QG_STANDARD, 1, cfg))
+                for s in (2, 3, 4):
+                    if s <= kt and wide_tiles * s <= 4 * sms:
+                        out.append((q.QG_SPLITK, s, cfg))
     return out
 
 

@@ -112,6 +112,8 @@ def test_gemm_validation(q):
     assert _gemm(q, fmt=0, dbg=OK16) == q.QG_ERR_INVALID_ARG              # debug acc is INT8 only
     assert _gemm(q, cfg=17) == q.QG_ERR_INVALID_ARG                       # ring depth above 16
     assert _gemm(q, cfg=q.config_id(0, 65)) == q.QG_ERR_INVALID_ARG       # prefetch distance above 64
+    assert _gemm(q, cfg=1 << 13) == q.QG_ERR_INVALID_ARG                  # unknown bit
+    assert _gemm(q, cfg=q.config_id(0, 0, True)) == q.QG_ERR_INVALID_ARG  # wide tiles: FP8 Standard only
     assert _gemm(q, cfg=-1) == q.QG_ERR_INVALID_ARG
     assert _gemm(q, M=0) == q.QG_OK
 

@@ -34,6 +34,23 @@ def test_fp8_dynamic(orc, gc, M, variant, split):
     gc.run_case(orc, "FP8_Dynamic", M, 424, 656, variant, split, seed=M)
 
 
+@pytest.mark.parametrize("M", [1, 40, 128, 129, 300])
+@pytest.mark.parametrize("variant,split,ring", [(ST, 1, 0), (STS, 3, 0), (ST, 1, 4), (STS, 2, 3)])
+def test_fp8_dynamic_wide_tiles(orc, q, gc, M, variant, split, ring):
+    # 256-row weight tiles: N = 424 gives one full and one ragged wide tile;
+    # M spans several 128-token tiles (ragged); Split-K through the workspace
+    gc.run_case(orc, "FP8_Dynamic", M, 424, 656, variant, split, seed=50 + M, config_id=q.config_id(ring, 0, True))
+
+
+def test_wide_tiles_rejected_outside_fp8_standard(q, gc):
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device=gc.DEV)
+    f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
+    for fmt, v in (("FP8_Dynamic", SW), ("Block_FP8", ST), ("W8A8_INT8", SW)):
+        with pytest.raises(q.QGError) as e:
+            q.qg_gemm_w8a8(fmt, 8, 256, 256, d, f, d, f, d, 256, v, 1, q.config_id(0, 0, True))
+        assert e.value.code == q.QG_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("M", [1, 7, 16, 24, 32])
 @pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 5), (ST, 1), (STS, 3)])
 def test_block_fp8(orc, gc, M, variant, split):
