@@ -147,6 +147,42 @@ QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_
                  const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
                  int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream);
 
+/* Grouped quantized GEMM for mixture-of-experts layers (the "Model
+ * coverage" item of the page's "Future work"): `groups` GEMMs with the
+ * same N and K in one launch, group g computing
+ *     Y[t][n] = dequant( sum_k A_q[t][k] * W_q[g][n][k] )
+ * for the tokens t in [token_offsets[g], token_offsets[g+1]) (tokens sorted
+ * by group, as a router's permutation leaves them).
+ *   token_offsets_dev  int32 [groups + 1] on the device, nondecreasing
+ *                      within [0, total_tokens] (values outside are
+ *                      clamped); read by the kernel after its dependency
+ *                      wait, so a routing kernel may write them;
+ *   total_tokens       rows of A_q / s_a / Y (0 is a no-op);
+ *   max_tokens         an upper bound of any group's token count: it sizes
+ *                      the token blocks, tokens of a group beyond it are
+ *                      not computed;
+ *   A_q_dev, s_a_dev   [total_tokens][K] codes and their scales (per token,
+ *                      or per token and 128-K group for Block_FP8);
+ *   W_q_dev            [groups][N][K] codes;
+ *   s_w_dev            fp32 [groups][N], or [groups][ceil(N/128)][K/128]
+ *                      (Block_FP8);
+ *   Y_dev              bf16 [total_tokens][ldy];
+ *   variant            QG_SWAPAB, QG_SWAPAB_SPLITK or (W8A8_INT8,
+ *                      max_tokens <= 8) QG_SWAPAB_DP4A(_SPLITK);
+ *   split_k, config_id, workspace (qg_workspace_bytes_grouped bytes),
+ *   debug_acc_dev ([total_tokens][N])   as qg_gemm_w8a8.
+ * CTAs of token blocks past their group's tokens (and of empty groups) exit
+ * at once, so only the groups with tokens stream their weights. */
+QG_API int qg_gemm_w8a8_grouped(int fmt, int groups, const int32_t* token_offsets_dev, int64_t total_tokens,
+                                int64_t max_tokens, int64_t N, int64_t K, const void* A_q_dev,
+                                const float* s_a_dev, const void* W_q_dev, const float* s_w_dev, void* Y_dev,
+                                int64_t ldy, int variant, int split_k, int config_id, void* workspace_dev,
+                                size_t ws_bytes, int32_t* debug_acc_dev, void* stream);
+/* Workspace bytes of qg_gemm_w8a8_grouped (0 when none is needed or the
+ * arguments are invalid). */
+QG_API size_t qg_workspace_bytes_grouped(int fmt, int groups, int64_t total_tokens, int64_t max_tokens, int64_t N,
+                                         int64_t K, int variant, int split_k);
+
 /* The whole quantized linear layer in one call: dynamic activation
  * quantization ("Scope": per token, or per 1x128 group for Block_FP8)
  * followed by the quantized GEMM ("Kernel Implementation"), i.e.

@@ -41,6 +41,12 @@ struct GemmArgs {
   int kt_total;         // ceil(K / 128)
   int splits;           // >= 1
   int m_tiles;          // token blocks (Swap-AB) or 128-token tiles (Standard); blockIdx.x = n_tile * m_tiles + m
+  // grouped launches (qg_gemm_w8a8_grouped): blockIdx.z is the group; its
+  // tokens are rows [group_offsets[z], group_offsets[z+1]) of A_q / s_a / Y
+  // (M counts all groups' tokens), its weights rows [z*N, z*N + N) of W_q,
+  // its weight scales s_w + z*sw_group_stride.  Null: one group, M tokens.
+  const int* group_offsets;
+  int64_t sw_group_stride;
   int stages;           // shared-memory ring depth
   int l2_prefetch;      // L2 prefetch distance: weight k-tiles requested ahead of the ring's loads
   int reduce;           // kReduceNone / kReduceCluster / kReduceGlobal
@@ -117,6 +123,21 @@ __host__ __device__ constexpr size_t gemm_f8_std_smem_bytes(int stages) {
 }
 
 __device__ __forceinline__ void store_bf16(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// This CTA's group (see GemmArgs::group_offsets): first token and token
+// count.  The offsets are inputs, so a grouped launch waits for the kernel it
+// depends on before reading them.
+struct GroupView {
+  int tok0, tokens;
+};
+__device__ __forceinline__ GroupView group_view(const GemmArgs& g) {
+  if (g.group_offsets == nullptr) return GroupView{0, g.M};
+  pdl_wait();
+  // offsets outside [0, M] or decreasing are clamped: no row outside A_q / Y
+  const int t0 = min(max(g.group_offsets[blockIdx.z], 0), g.M);
+  const int t1 = min(max(g.group_offsets[blockIdx.z + 1], t0), g.M);
+  return GroupView{t0, t1 - t0};
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -317,8 +338,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_tile = static_cast<int>(blockIdx.x / g.m_tiles);
   const int split = blockIdx.y;
   const int m_blk = static_cast<int>(blockIdx.x % g.m_tiles);  // token block: tokens [m_base, m_base + Mb)
-  const int m_base = m_blk * MPAD;
-  const int Mb = min(MPAD, g.M - m_base);
+  const GroupView grp = group_view(g);
+  const int m_base = grp.tok0 + m_blk * MPAD;
+  const int Mb = min(MPAD, grp.tok0 + grp.tokens - m_base);
+  if (Mb <= 0) return;  // a token block past its group's tokens (the whole cluster alike)
+  const int w_row0 = static_cast<int>(blockIdx.z) * g.N;  // the group's weight rows
+  const float* s_w = g.s_w + static_cast<int64_t>(blockIdx.z) * g.sw_group_stride;
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
   const int nk = kb1 - kb0;
@@ -371,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // produced the activations.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      const int w_row = n_tile * kBN;
+      const int w_row = w_row0 + n_tile * kBN;
       const int pre = nk < stages ? nk : stages;
       constexpr uint32_t kTx = FUSED ? TS::kWBytes : TS::kStageBytes;  // fused: threads write the activations
       for (int i = 0; i < pre; ++i) {
@@ -462,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // scales for the epilogue, fetched while the main loop runs
         const int et0 = threadIdx.x - 64, r = q * 32 + lane, nn = n_tile * kBN + r;
         if (!FUSED && et0 < MPAD) ctl->sa_s[et0] = et0 < Mb ? __ldg(g.s_a + m_base + et0) : 0.0f;
-        ctl->sw_s[r] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
+        ctl->sw_s[r] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
       }
       if constexpr (FUSED) {
         // per-token scales, then every stage's activation tile as E4M3
@@ -548,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int t = lane + 32 * j;
           sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0) : 0.0f;
         }
-        float sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
+        float sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
         for (int i = 0; i < nk; ++i) {
           const int buf = i % NBUF;
 #pragma unroll
@@ -561,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i + 1)
                                   : 0.0f;
             }
-            sw_next = __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
+            sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
           }
           const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
           if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
@@ -651,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __threadfence();
       named_bar_sync(1, 128);
-      const int tile_id = blockIdx.x;
+      const int tile_id = blockIdx.x + blockIdx.z * gridDim.x;
       if (et == 0) {
         const int old = atomicAdd(g.ws_count + tile_id, 1);
         ctl->last_flag = (old == g.splits - 1);

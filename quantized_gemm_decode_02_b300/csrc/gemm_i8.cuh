@@ -120,8 +120,12 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   // read from HBM once, then from L2)
   const int n_tile = static_cast<int>(blockIdx.x / g.m_tiles), split = blockIdx.y;
   const int m_blk = static_cast<int>(blockIdx.x % g.m_tiles);  // token block: tokens [m_base, m_base + Mb)
-  const int m_base = m_blk * MPAD;
-  const int Mb = min(MPAD, g.M - m_base);
+  const GroupView grp = group_view(g);
+  const int m_base = grp.tok0 + m_blk * MPAD;
+  const int Mb = min(MPAD, grp.tok0 + grp.tokens - m_base);
+  if (Mb <= 0) return;  // a token block past its group's tokens (the whole cluster alike)
+  const int w_row0 = static_cast<int>(blockIdx.z) * g.N;  // the group's weight rows
+  const float* s_w = g.s_w + static_cast<int64_t>(blockIdx.z) * g.sw_group_stride;
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
   const int nk = kb1 - kb0;
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      const int w_row = n_tile * kBN;
+      const int w_row = w_row0 + n_tile * kBN;
       const int pre = nk < stages ? nk : stages;
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       const uint32_t lane_base = ((warp & 3) * 32u) << 16;
       if (h == 0) {
         const int nn = n_tile * kBN + static_cast<int>(row);
-        ctl->sw_s[row] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
+        ctl->sw_s[row] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
       }
       bool ok = true;
 
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       }
       __threadfence();
       named_bar_sync(1, kI8ConvThreads);
-      const int tile_id = blockIdx.x;
+      const int tile_id = blockIdx.x + blockIdx.z * gridDim.x;
       if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + tile_id, 1) == g.splits - 1);
       named_bar_sync(1, kI8ConvThreads);
       if (ctl->last_flag) {

@@ -71,7 +71,12 @@ __global__ void __launch_bounds__(kDpThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, split = blockIdx.y;  // one token block (m_tiles == 1)
-  const int Mb = min(MT, g.M);  // one token block: M <= 8
+  const GroupView grp = group_view(g);
+  const int m_base = grp.tok0;                 // tokens [m_base, m_base + Mb): at most 8
+  const int Mb = min(MT, grp.tokens);
+  if (Mb <= 0) return;  // an empty group (the whole cluster alike)
+  const int w_row0 = static_cast<int>(blockIdx.z) * g.N;  // the group's weight rows
+  const float* s_w = g.s_w + static_cast<int64_t>(blockIdx.z) * g.sw_group_stride;
   const int kb0 = static_cast<int>(static_cast<int64_t>(split) * g.kt_total / g.splits);
   const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * g.kt_total / g.splits);
   const int nk = kb1 - kb0;
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kDpThreads, 2)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      const int w_row = n_tile * kBN;
+      const int w_row = w_row0 + n_tile * kBN;
       const int pre = nk < stages ? nk : stages;
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * DpShape::kStageBytes;
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(kDpThreads, 2)
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + static_cast<size_t>(i) * DpShape::kStageBytes;
         mbar_arrive_expect_tx(&ctl->full_a[i], DpShape::kABytes);
-        tma_load_2d(st + DpShape::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full_a[i], pol_a);
+        tma_load_2d(st + DpShape::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[i], pol_a);
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kDpThreads, 2)
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
         if (g.l2_prefetch > 0 && i + g.l2_prefetch < nk) tma_prefetch_l2_2d(&tmW, (kb0 + i + g.l2_prefetch) * kBK, w_row);
         mbar_arrive_expect_tx(&ctl->full_a[s], DpShape::kABytes);
-        tma_load_2d(st + DpShape::kWBytes, &tmA, (kb0 + i) * kBK, 0, &ctl->full_a[s], pol_a);
+        tma_load_2d(st + DpShape::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[s], pol_a);
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit
@@ -151,10 +156,10 @@ __global__ void __launch_bounds__(kDpThreads, 2)
     // ------------------------------------------------------------- compute
     if (h == 0) {
       const int nn = n_tile * kBN + row;
-      ctl->sw_s[row] = nn < g.N ? __ldg(g.s_w + nn) : 0.0f;
+      ctl->sw_s[row] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
     }
     pdl_wait();  // s_a is written by the kernel this one depends on
-    if (ct < kDpABox) ctl->sa_s[ct] = ct < Mb ? __ldg(g.s_a + ct) : 0.0f;
+    if (ct < kDpABox) ctl->sa_s[ct] = ct < Mb ? __ldg(g.s_a + m_base + ct) : 0.0f;
     for (int i = 0; i < nk; ++i) {
       const int s = i % stages;
       const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
@@ -200,9 +205,9 @@ __global__ void __launch_bounds__(kDpThreads, 2)
   pdl_wait();  // outputs are written only after the kernel this one depends on
   const bool holds_acc = warp >= 1 && h == 0;  // warps 1..4: one full row each
   auto finish = [&](int m, int r, int nn, int32_t sum) {
-    if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m) * g.N + nn] = sum;
+    if (g.debug_acc) g.debug_acc[static_cast<int64_t>(m_base + m) * g.N + nn] = sum;
     const float y = (static_cast<float>(sum) * ctl->sa_s[m]) * ctl->sw_s[r];
-    store_bf16(g.Y + static_cast<int64_t>(m) * g.ldy + nn, y);
+    store_bf16(g.Y + static_cast<int64_t>(m_base + m) * g.ldy + nn, y);
   };
   const int n = n_tile * kBN + row;
   if (clustered) {
@@ -232,22 +237,24 @@ __global__ void __launch_bounds__(kDpThreads, 2)
       if (n_ok) {
 #pragma unroll
         for (int m = 0; m < MT; ++m)
-          if (m < Mb) part[(static_cast<int64_t>(split) * g.M + m) * g.N + n] = acc[m];
+          if (m < Mb) part[(static_cast<int64_t>(split) * g.M + m_base + m) * g.N + n] = acc[m];
       }
       __threadfence();
       named_bar_sync(1, kBN);
-      if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + n_tile, 1) == g.splits - 1);
+      const int tile_id = n_tile + blockIdx.z * gridDim.x;
+      if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + tile_id, 1) == g.splits - 1);
       named_bar_sync(1, kBN);
       if (ctl->last_flag) {
         __threadfence();
         if (n_ok) {
           for (int m = 0; m < Mb; ++m) {
             int32_t sum = 0;
-            for (int s = 0; s < g.splits; ++s) sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m) * g.N + n);
+            for (int s = 0; s < g.splits; ++s)
+              sum += ld_cg_s32(part + (static_cast<int64_t>(s) * g.M + m_base + m) * g.N + n);
             finish(m, row, n, sum);
           }
         }
-        if (ct == 0) g.ws_count[n_tile] = 0;
+        if (ct == 0) g.ws_count[tile_id] = 0;
       }
     }
   }

@@ -165,6 +165,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 constexpr int kMaxStages = 16;
 
 struct Plan {
+  int groups = 1;      // grouped launches: grid z
   bool swap = false;
   bool dp4a = false;   // W8A8_INT8 Swap-AB on the CUDA cores (M <= 8)
   int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64
@@ -210,10 +211,12 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   return QG_OK;
 }
 
-int64_t workspace_bytes(const Plan& p, int64_t M, int64_t N) {
+// rows: the token rows of A_q / Y (all groups' tokens for grouped launches).
+// The counters are those of 128-row tiles (see gemm_entry).
+int64_t workspace_bytes(const Plan& p, int64_t rows, int64_t N) {
   if (p.reduce != qg::kReduceGlobal) return 0;
-  const int64_t tiles = static_cast<int64_t>(p.n_tiles) * p.m_tiles;
-  return ws_counter_bytes(tiles) + static_cast<int64_t>(p.splits) * M * N * 4;
+  const int64_t tiles = p.groups * cdiv(N, 128) * p.m_tiles;
+  return ws_counter_bytes(tiles) + static_cast<int64_t>(p.splits) * rows * N * 4;
 }
 
 // config_id = ring | distance << 5 (see qgemm.h).  Ring depth: ring > 0
@@ -259,7 +262,7 @@ int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, q
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, 1),
+  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
                      qg::kThreads, qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -268,7 +271,7 @@ int run_f8_std(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg
                cudaStream_t stream) {
   int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_std_smem_bytes<BNW>(st); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_std_kernel<FMT, BNW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, 1), qg::kThreads,
+  return launch_gemm(qg::gemm_f8_std_kernel<FMT, BNW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::kThreads,
                      qg::gemm_f8_std_smem_bytes<BNW>(g.stages), tmW, tmA, g, stream);
 }
 
@@ -288,7 +291,7 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, 1), qg::kI8Threads,
+  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::kI8Threads,
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -298,7 +301,7 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_dp4a_smem_bytes(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_dp4a_kernel<MT>, p, dim3(p.n_tiles, p.splits, 1), qg::kDpThreads,
+  return launch_gemm(qg::gemm_i8_dp4a_kernel<MT>, p, dim3(p.n_tiles, p.splits, p.groups), qg::kDpThreads,
                      qg::gemm_dp4a_smem_bytes(g.stages, rb), tmW, tmA, g, stream);
 }
 
@@ -369,10 +372,17 @@ struct FusedIn {
   const void* A;
   int64_t lda;
 };
+// Grouped launch (qg_gemm_w8a8_grouped): M is then the largest group's
+// token count, which sizes the token blocks.
+struct GroupIn {
+  int groups;
+  const int32_t* offsets;
+  int64_t total_tokens;
+};
 int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
                const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant, int split_k,
                int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream,
-               const FusedIn* fused) {
+               const FusedIn* fused, const GroupIn* grouped = nullptr) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
   if (variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
   if (M < 0 || N <= 0 || K <= 0 || ldy < N)
@@ -399,11 +409,25 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
       !aligned(Y_dev, 2) || (debug_acc_dev && !aligned(debug_acc_dev, 4)))
     return fail(QG_ERR_ALIGNMENT, "A_q/W_q need 16-byte alignment, scales 4, Y 2");
   if (debug_acc_dev && fmt != QG_W8A8_INT8) return fail(QG_ERR_INVALID_ARG, "debug_acc is W8A8_INT8 only");
+  // rows of A_q / s_a / Y: M, or all groups' tokens
+  const int64_t rows = grouped ? grouped->total_tokens : M;
+  if (grouped) {
+    if (grouped->groups < 1 || grouped->groups > 65535)
+      return fail(QG_ERR_UNSUPPORTED_SHAPE, "groups=%d outside [1, 65535]", grouped->groups);
+    if (!grouped->offsets || !aligned(grouped->offsets, 4)) return fail(QG_ERR_INVALID_ARG, "token offsets: null or unaligned");
+    if (fused || wide || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK || variant == QG_SWAPAB_DP4A ||
+                           variant == QG_SWAPAB_DP4A_SPLITK))
+      return fail(QG_ERR_INVALID_ARG, "grouped launches run the Swap-AB variants");
+    if (rows < 0 || rows > 0x7FFFFFFF || static_cast<int64_t>(grouped->groups) * N > 0x7FFFFFFF)
+      return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+    if (rows == 0) return QG_OK;
+  }
   Plan p;
   int rc = make_plan(fmt, M, N, K, variant, split_k, &p);
   if (rc != QG_OK) return rc;
+  if (grouped) p.groups = grouped->groups;
   if (wide) p.n_tiles = static_cast<int>(cdiv(N, 256));
-  const int64_t need = workspace_bytes(p, M, N);
+  const int64_t need = workspace_bytes(p, rows, N);
   if (need > 0) {
     if (!workspace_dev) return fail(QG_ERR_WORKSPACE_TOO_SMALL, "split_k=%d needs a %lld-byte workspace", split_k, (long long)need);
     if (static_cast<int64_t>(ws_bytes) < need)
@@ -411,17 +435,21 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (!aligned(workspace_dev, 256)) return fail(QG_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   }
   CUtensorMap tmW, tmA;
-  rc = make_map(&tmW, W_q_dev, N, K, K, wide ? 256u : 128u);
+  rc = make_map(&tmW, W_q_dev, static_cast<int64_t>(p.groups) * N, K, K, wide ? 256u : 128u);
   if (rc != QG_OK) return rc;
   if (fused) {
     tmA = tmW;  // unused: the kernel reads the bf16 activations directly
   } else {
-    rc = make_map(&tmA, A_q_dev, M, K, K, p.swap ? static_cast<uint32_t>(p.mpad) : 128u);
+    rc = make_map(&tmA, A_q_dev, rows, K, K, p.swap ? static_cast<uint32_t>(p.mpad) : 128u);
     if (rc != QG_OK) return rc;
   }
 
   qg::GemmArgs g = {};
-  g.M = static_cast<int>(M);
+  g.M = static_cast<int>(rows);
+  if (grouped) {
+    g.group_offsets = grouped->offsets;
+    g.sw_group_stride = fmt == QG_BLOCK_FP8 ? cdiv(N, 128) * p.kt : N;
+  }
   g.N = static_cast<int>(N);
   g.K = static_cast<int>(K);
   g.ldy = ldy;
@@ -434,7 +462,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   if (p.reduce == qg::kReduceGlobal) {
     // the partials start after the counters of 128-row tiles even for wide
     // tiles, so that no configuration's partials overlap another's counters
-    const int64_t tiles = cdiv(N, 128) * p.m_tiles;
+    const int64_t tiles = p.groups * cdiv(N, 128) * p.m_tiles;
     g.ws_count = static_cast<int*>(workspace_dev);
     g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
   }
@@ -698,6 +726,28 @@ int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, 
                  int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev, void* stream) {
   return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,
                     workspace_dev, ws_bytes, debug_acc_dev, stream, nullptr);
+}
+
+int qg_gemm_w8a8_grouped(int fmt, int groups, const int32_t* token_offsets_dev, int64_t total_tokens,
+                         int64_t max_tokens, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
+                         const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
+                         int split_k, int config_id, void* workspace_dev, size_t ws_bytes, int32_t* debug_acc_dev,
+                         void* stream) {
+  if (max_tokens < 0 || total_tokens < 0) return fail(QG_ERR_INVALID_ARG, "negative token counts");
+  const GroupIn gi{groups, token_offsets_dev, total_tokens};
+  return gemm_entry(fmt, max_tokens, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k,
+                    config_id, workspace_dev, ws_bytes, debug_acc_dev, stream, nullptr, &gi);
+}
+
+size_t qg_workspace_bytes_grouped(int fmt, int groups, int64_t total_tokens, int64_t max_tokens, int64_t N, int64_t K,
+                                  int variant, int split_k) {
+  Plan p;
+  if (fmt < 0 || fmt > 2 || groups < 1 || total_tokens < 0 || max_tokens <= 0 || N <= 0 || K <= 0 || variant < 0 ||
+      variant > QG_SWAPAB_DP4A_SPLITK)
+    return 0;
+  if (make_plan(fmt, max_tokens, N, K, variant, split_k, &p) != QG_OK) return 0;
+  p.groups = groups;
+  return static_cast<size_t>(workspace_bytes(p, total_tokens, N));
 }
 
 int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, int64_t lda, const void* W_q_dev,

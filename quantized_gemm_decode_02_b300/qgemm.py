@@ -39,7 +39,7 @@ def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False) -> int:
     return ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT) | (QG_CONFIG_WIDE if wide else 0)
 
 EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
-           "qg_linear_w8a8", "qg_gemm_w8a8_noalloc",
+           "qg_linear_w8a8", "qg_gemm_w8a8_noalloc", "qg_gemm_w8a8_grouped", "qg_workspace_bytes_grouped",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
            "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
 
@@ -63,6 +63,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qg_workspace_init.argtypes = [P, SZ, P]
     lib.qg_gemm_w8a8.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
     lib.qg_gemm_w8a8_noalloc.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, P]
+    lib.qg_gemm_w8a8_grouped.argtypes = [I, I, P, I64, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
+    lib.qg_workspace_bytes_grouped.argtypes = [I, I, I64, I64, I64, I64, I, I]
+    lib.qg_workspace_bytes_grouped.restype = SZ
     lib.qg_linear_w8a8.argtypes = [I, I64, I64, I64, P, I64, P, P, P, I64, I, I, I, P, SZ, P, P, P, P]
     lib.qg_select.argtypes = [I, I64, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
     lib.qg_load_table.argtypes = [ctypes.c_char_p]
@@ -144,6 +147,21 @@ def qg_linear_w8a8(fmt, M, N, K, A, lda, W_q, s_w, Y, ldy, variant, split_k, con
     _check(_lib.qg_linear_w8a8(_fmt(fmt), M, N, K, _ptr(A), lda, _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant,
                                split_k, config_id, _ptr(workspace), ws_bytes, _ptr(A_q), _ptr(s_a), _ptr(debug_acc),
                                _stream(stream)), "qg_linear_w8a8")
+
+
+def qg_gemm_w8a8_grouped(fmt, groups, token_offsets, total_tokens, max_tokens, N, K, A_q, s_a, W_q, s_w, Y, ldy,
+                         variant, split_k, config_id=0, workspace=None, ws_bytes=0, debug_acc=None,
+                         stream=None) -> None:
+    """Grouped (mixture-of-experts) GEMM: group g's tokens are rows
+    token_offsets[g] .. token_offsets[g+1] of A_q / Y, its weights W_q[g]."""
+    _check(_lib.qg_gemm_w8a8_grouped(_fmt(fmt), groups, _ptr(token_offsets), total_tokens, max_tokens, N, K,
+                                     _ptr(A_q), _ptr(s_a), _ptr(W_q), _ptr(s_w), _ptr(Y), ldy, variant, split_k,
+                                     config_id, _ptr(workspace), ws_bytes, _ptr(debug_acc), _stream(stream)),
+           "qg_gemm_w8a8_grouped")
+
+
+def qg_workspace_bytes_grouped(fmt, groups, total_tokens, max_tokens, N, K, variant, split_k) -> int:
+    return int(_lib.qg_workspace_bytes_grouped(_fmt(fmt), groups, total_tokens, max_tokens, N, K, variant, split_k))
 
 
 def qg_gemm_w8a8_noalloc(fmt, M, N, K, A_q, s_a, W_q, s_w, Y, ldy, variant, split_k, config_id=0, debug_acc=None,

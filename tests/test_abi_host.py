@@ -132,6 +132,17 @@ def test_workspace_bytes(q):
     assert q.qg_workspace_bytes(1, 9, 4096, 4096, q.QG_SWAPAB_DP4A_SPLITK, 2) == 0  # M > 8 -> invalid
 
 
+def test_grouped_workspace_bytes(q):
+    # cluster reductions need none; the workspace holds counters for every
+    # group's tiles and [splits][total_tokens][N] partials
+    assert q.qg_workspace_bytes_grouped(0, 8, 40, 16, 4096, 4096, q.QG_SWAPAB_SPLITK, 4) == 0
+    tiles = 8 * 32 * 1
+    assert q.qg_workspace_bytes_grouped(0, 8, 40, 16, 4096, 4096, q.QG_SWAPAB_SPLITK, 17) == \
+        ((tiles * 4 + 255) // 256) * 256 + 17 * 40 * 4096 * 4
+    assert q.qg_workspace_bytes_grouped(1, 8, 40, 9, 4096, 4096, q.QG_SWAPAB_DP4A_SPLITK, 17) == 0  # invalid
+    assert q.qg_workspace_bytes_grouped(0, 0, 40, 16, 4096, 4096, q.QG_SWAPAB, 1) == 0
+
+
 def test_launch_flag_and_limits(q):
     assert _raw(q).qg_set_launch_flags(6) == q.QG_ERR_INVALID_ARG
     q.qg_set_launch_flags(0)
