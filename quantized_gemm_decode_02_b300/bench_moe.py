@@ -52,6 +52,8 @@ def main(argv=None) -> int:
     ap.add_argument("--fmt", default="FP8_Dynamic", choices=sorted(q.FORMATS))
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step's kernels directly instead of replaying the captured graph (profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -117,13 +119,23 @@ def main(argv=None) -> int:
                                    it["Aq"], it["sa"], Wq, sw, it["Y"], it["N"], it["v"], it["s"], it["c"],
                                    it["ws"], it["need"], None, stream=stream)
 
-    q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
-    graph = torch.cuda.CUDAGraph()
-    try:
-        with torch.cuda.graph(graph, stream=stream):
-            enqueue()
-    finally:
-        q.qg_set_launch_flags(0)
+    if args.no_graph:
+        class _Direct:
+            """Stand-in for the step graph: enqueue the step's kernels."""
+            def replay(self):
+                with torch.cuda.stream(stream):
+                    q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
+                    enqueue()
+                    q.qg_set_launch_flags(0)
+        graph = _Direct()
+    else:
+        q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
+        graph = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(graph, stream=stream):
+                enqueue()
+        finally:
+            q.qg_set_launch_flags(0)
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -153,7 +165,8 @@ def main(argv=None) -> int:
                    "expert_intermediate": INTER, "M": list(TUNED_M), "grouped_gemms_per_step": len(items),
                    "kernels_per_step": 2 * len(items), "bytes_per_step": bytes_step,
                    "weight_bytes_streamed_per_step": weight_bytes,
-                   "graph": "one CUDA graph per step, programmatic dependent launch"},
+                   "graph": ("direct launches" if args.no_graph else "one CUDA graph per step")
+                            + ", programmatic dependent launch"},
         "per_gemm": [{"M": it["M"], "layer": it["layer"], "routed_rows": it["rows"], "experts_with_tokens": it["active"],
                       "max_tokens": it["max_tokens"], "variant": it["v"], "split_k": it["s"]} for it in items],
     }
