@@ -26,6 +26,11 @@
 // k-tile is one scale group, so the MMA writes each k-tile's partial into its
 // own TMEM buffer (NBUF-deep ring) and the epilogue warps promote it,
 // acc += s_a[m,kb] * s_w[n/128,kb] * partial, while later MMAs run.
+//
+// Grid: x = weight tile * token blocks (the token blocks of one weight tile
+// adjacent, so they share its loads in L2), y = K range, z = group of a
+// grouped (mixture-of-experts) launch.  The Standard kernel also takes
+// 256-row weight tiles (FP8_Dynamic, MMA N = 256).
 #pragma once
 #include "common.cuh"
 #include "quant.cuh"
