@@ -25,7 +25,8 @@ TFLOP/s = 2*M*N*K per step / step time for the compute-bound workload.
 Also reported: the roofline of the GEMM kernel (per-launch durations from
 timing events inside a second graph), an end-to-end figure through the C ABI
 with the activations copied from pinned host memory and the outputs copied
-back inside the timed region, SM clocks sampled during the timed region, and
+back inside the timed region (two buffer sets, so one step's copies overlap
+its neighbours' kernels), SM clocks sampled during the timed region, and
 the CPU oracle timed on the host cores on a bounded sample (cpu_baseline).
 `--impl reference` times that oracle alone as the reference arm.
 """
@@ -138,6 +139,7 @@ class Workload:
             y_off.append(y_tot); y_tot += align(M * N * 2)
         self.A_all = torch.empty(a_tot, dtype=torch.uint8, device=device)
         self.Y_all = torch.empty(y_tot, dtype=torch.uint8, device=device)
+        self.a_off, self.y_off = a_off, y_off
         self.recs = []
         ws_need = 0
         weights = {}
@@ -186,25 +188,36 @@ class Workload:
     def kernels(self, i: int) -> int:
         return 1 if self.fused_item(i) else 2
 
-    def enqueue(self, stream, i: int):
+    def rebind(self, A_all, Y_all):
+        """The items with their activations and outputs in other buffers of
+        the same layout (a second buffer set for pipelined e2e steps)."""
+        out = []
+        for i, r in enumerate(self.recs):
+            M, N, K = r["M"], r["N"], r["K"]
+            A = A_all[self.a_off[i]:self.a_off[i] + M * K * 2].view(torch.bfloat16).view(M, K)
+            Y = Y_all[self.y_off[i]:self.y_off[i] + M * N * 2].view(torch.bfloat16).view(M, N)
+            out.append(dict(r, A=A, Y=Y))
+        return out
+
+    def enqueue(self, stream, i: int, recs=None):
         """One linear layer through qg_linear_w8a8: activation quantization +
         GEMM (two kernels; one fused kernel with --fused where the format and
         variant have one)."""
-        r = self.recs[i]
+        r = (recs or self.recs)[i]
         q = self.q
         fz = self.fused and self.fused_item(i)
         q.qg_linear_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["A"], r["K"], r["Wq"], r["sw"], r["Y"], r["N"],
                          r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes,
                          None if fz else r["Aq"], None if fz else r["sa"], None, stream=stream)
 
-    def capture_step(self, stream) -> torch.cuda.CUDAGraph:
+    def capture_step(self, stream, recs=None) -> torch.cuda.CUDAGraph:
         """The whole step (quant + GEMM for every item) as one graph."""
         self.q.qg_set_launch_flags(self.q.QG_LAUNCH_PDL if self.pdl else 0)
         g = torch.cuda.CUDAGraph()
         try:
             with torch.cuda.graph(g, stream=stream):
                 for i in range(len(self.recs)):
-                    self.enqueue(stream, i)
+                    self.enqueue(stream, i, recs)
         finally:
             self.q.qg_set_launch_flags(0)
         return g
@@ -597,25 +610,63 @@ def main(argv=None):
                 "by_format": by_fmt, "avg_launch_us": round(avg_ms * 1e3, 3),
                 "avg_flops_per_launch": round(fl_all / n_gemm)}
 
-    # ---- end to end through the C ABI: pinned host activations in, outputs out
+    # ---- end to end through the C ABI: pinned host activations in, outputs out.
+    # Two buffer sets and two graphs: while step i's kernels run, a copy
+    # stream uploads step i+1's activations and downloads step i-1's outputs
+    # (every step still copies its own inputs in and its outputs out inside
+    # the timed region).
     host_A = torch.empty(wl.A_all.numel(), dtype=torch.uint8, pin_memory=True)
     host_A.copy_(wl.A_all.cpu())
-    host_Y = torch.empty(wl.Y_all.numel(), dtype=torch.uint8, pin_memory=True)
+    host_Y = [torch.empty(wl.Y_all.numel(), dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     e2e_steps = max(10, args.e2e_steps)
-    for _ in range(5):
-        with torch.cuda.stream(stream):
-            wl.A_all.copy_(host_A, non_blocking=True)
-            graph.replay()
-            host_Y.copy_(wl.Y_all, non_blocking=True)
+    A2, Y2 = torch.empty_like(wl.A_all), torch.empty_like(wl.Y_all)
+    if args.no_graph:
+        class _Direct2:
+            def __init__(self, recs):
+                self.recs = recs
+
+            def replay(self):
+                with torch.cuda.stream(stream):
+                    wl.q.qg_set_launch_flags(wl.q.QG_LAUNCH_PDL if wl.pdl else 0)
+                    for i in range(len(self.recs)):
+                        wl.enqueue(stream, i, self.recs)
+                    wl.q.qg_set_launch_flags(0)
+        graph2 = _Direct2(wl.rebind(A2, Y2))
+    else:
+        graph2 = wl.capture_step(stream, wl.rebind(A2, Y2))
+    sets = [(wl.A_all, wl.Y_all, graph), (A2, Y2, graph2)]
+    copy_stream = torch.cuda.Stream(device=device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = torch.cuda.Event()
+
+    def pipelined(n):
+        with torch.cuda.stream(copy_stream):
+            sets[0][0].copy_(host_A, non_blocking=True)
+            ev_in[0].record(copy_stream)
+        for i in range(n):
+            A_i, Y_i, g_i = sets[i % 2]
+            stream.wait_event(ev_in[i % 2])
+            g_i.replay()
+            ev_done[i % 2].record(stream)
+            with torch.cuda.stream(copy_stream):
+                if i + 1 < n:  # after step i-1's download in this stream: its buffers are free
+                    sets[(i + 1) % 2][0].copy_(host_A, non_blocking=True)
+                    ev_in[(i + 1) % 2].record(copy_stream)
+                copy_stream.wait_event(ev_done[i % 2])
+                host_Y[i % 2].copy_(Y_i, non_blocking=True)
+        ev_out.record(copy_stream)
+        stream.wait_event(ev_out)
+
+    with torch.cuda.stream(stream):
+        pipelined(5)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(e2e_steps):
-            wl.A_all.copy_(host_A, non_blocking=True)
-            graph.replay()
-            host_Y.copy_(wl.Y_all, non_blocking=True)
+        copy_stream.wait_event(e0)
+        pipelined(e2e_steps)
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / e2e_steps, device)
@@ -656,7 +707,9 @@ def main(argv=None):
             "config": cfg,
             "roofline": roof,
             "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": int(wl.A_all.numel()),
-                    "d2h_bytes_per_step": int(wl.Y_all.numel()), "ms_per_step": round(e2e_ms, 6)},
+                    "d2h_bytes_per_step": int(wl.Y_all.numel()), "ms_per_step": round(e2e_ms, 6),
+                    "pipelining": "two buffer sets: step i+1's upload and step i-1's download overlap step i's "
+                                  "kernels (copy stream)"},
             "gpu_launches": n_kernels * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
