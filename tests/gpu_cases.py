@@ -1,9 +1,9 @@
 """Helpers for the GPU parity tests: run the CUDA path through the C ABI and
 compare it with the CPU oracle on the same seeded inputs.
 
-Tolerances (BASELINE accuracy contract, restated):
-  * quantizer outputs (A_q, s_a, W_q, s_w): bit-exact, both sides use one IEEE
-    fp32 division and round-to-nearest-even encodes;
+Tolerances (the accuracy contract of the path, restated):
+  * quantizer outputs (A_q, s_a, W_q, s_w): bit-exact, both sides take the
+    correctly rounded fp32 quotient and round-to-nearest-even encodes;
   * W8A8_INT8: the int32 accumulators bit-exact (debug output), Y within one
     bf16 ulp of the oracle (the GPU epilogue rounds three times in fp32, the
     oracle once from the exact value);
