@@ -159,8 +159,9 @@ QG_API int qg_gemm_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_
  *                      wait, so a routing kernel may write them;
  *   total_tokens       rows of A_q / s_a / Y (0 is a no-op);
  *   max_tokens         an upper bound of any group's token count: it sizes
- *                      the token blocks, tokens of a group beyond it are
- *                      not computed;
+ *                      the token blocks; a group's tokens beyond the first
+ *                      max_tokens are not computed (their Y rows are left
+ *                      as they were);
  *   A_q_dev, s_a_dev   [total_tokens][K] codes and their scales (per token,
  *                      or per token and 128-K group for Block_FP8);
  *   W_q_dev            [groups][N][K] codes;

@@ -52,6 +52,7 @@ struct GemmArgs {
   // its weight scales s_w + z*sw_group_stride.  Null: one group, M tokens.
   const int* group_offsets;
   int64_t sw_group_stride;
+  int group_max;        // tokens of a group taken into account (the launch's max_tokens)
   int stages;           // shared-memory ring depth
   int l2_prefetch;      // L2 prefetch distance: weight k-tiles requested ahead of the ring's loads
   int reduce;           // kReduceNone / kReduceCluster / kReduceGlobal
@@ -138,10 +139,12 @@ struct GroupView {
 __device__ __forceinline__ GroupView group_view(const GemmArgs& g) {
   if (g.group_offsets == nullptr) return GroupView{0, g.M};
   pdl_wait();
-  // offsets outside [0, M] or decreasing are clamped: no row outside A_q / Y
+  // offsets outside [0, M] or decreasing are clamped (no row outside A_q /
+  // Y), and a group's tokens beyond group_max are left out (the token blocks
+  // and receive buffers are sized for group_max)
   const int t0 = min(max(g.group_offsets[blockIdx.z], 0), g.M);
   const int t1 = min(max(g.group_offsets[blockIdx.z + 1], t0), g.M);
-  return GroupView{t0, t1 - t0};
+  return GroupView{t0, min(t1 - t0, g.group_max)};
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

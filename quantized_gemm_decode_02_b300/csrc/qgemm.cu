@@ -449,6 +449,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   if (grouped) {
     g.group_offsets = grouped->offsets;
     g.sw_group_stride = fmt == QG_BLOCK_FP8 ? cdiv(N, 128) * p.kt : N;
+    g.group_max = static_cast<int>(M);
   }
   g.N = static_cast<int>(N);
   g.K = static_cast<int>(K);

@@ -100,6 +100,35 @@ def test_grouped_equals_separate_gemms(orc, gc, q):
         assert torch.equal(Yg, Y[t0:t1])
 
 
+@pytest.mark.parametrize("variant,split", [(SWS, 3), (SWS, 18), (DPS, 2)])
+def test_grouped_tokens_beyond_max_are_left_out(orc, gc, q, variant, split):
+    # a group with more tokens than max_tokens: its first max_tokens rows are
+    # computed, the rest of Y stays untouched (no write outside the sized
+    # token blocks and receive buffers)
+    dev = gc.DEV
+    fmt, N, K, counts, max_tokens = "W8A8_INT8", 256, 1024, [3, 11, 2], 4
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    total = int(offs[-1])
+    A = si.activations(total, K, seed=740)
+    W = si.weights(len(counts) * N, K, seed=740)
+    Aq, sa = gc.quant_act_gpu(fmt, A.to(dev))
+    Wq, sw = gc.quant_weight_gpu(fmt, torch.from_numpy(W).to(dev))
+    need = q.qg_workspace_bytes_grouped(fmt, len(counts), total, max_tokens, N, K, variant, split)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    Y = torch.full((total, N), 7.0, dtype=torch.bfloat16, device=dev)
+    q.qg_gemm_w8a8_grouped(fmt, len(counts), torch.from_numpy(offs).to(dev), total, max_tokens, N, K, Aq, sa, Wq,
+                           sw, Y, N, variant, split, 0, ws, need)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
+    oWq, osw = orc.quant_weight(fmt, W)
+    for g in range(len(counts)):
+        t0 = int(offs[g])
+        t1 = min(int(offs[g + 1]), t0 + max_tokens)
+        gc.check_gemm(orc, fmt, oAq[t0:t1], osa[t0:t1], oWq[g * N:(g + 1) * N], osw[g * N:(g + 1) * N], Y[t0:t1])
+        assert torch.all(Y[t1:int(offs[g + 1])] == 7.0)
+
+
 def test_grouped_validation(gc, q):
     d = torch.zeros(1 << 16, dtype=torch.uint8, device=gc.DEV)
     f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
