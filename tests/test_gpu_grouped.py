@@ -106,7 +106,7 @@ def test_grouped_tokens_beyond_max_are_left_out(orc, gc, q, variant, split):
     # computed, the rest of Y stays untouched (no write outside the sized
     # token blocks and receive buffers)
     dev = gc.DEV
-    fmt, N, K, counts, max_tokens = "W8A8_INT8", 256, 1024, [3, 11, 2], 4
+    fmt, N, K, counts, max_tokens = "W8A8_INT8", 256, 2304, [3, 11, 2], 4
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     total = int(offs[-1])
     A = si.activations(total, K, seed=740)
