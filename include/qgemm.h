@@ -14,12 +14,15 @@
  *                   weight scale per 128x128 block;
  * with the Standard, Split-K and Swap-AB algorithm variants of its section
  * "Kernel Implementation", chosen per shape from a tuned table (sections
- * "Per-shape Config Tuning" and "Hybrid Dispatch").
+ * "Per-shape Config Tuning" and "Hybrid Dispatch"); plus a grouped form for
+ * mixture-of-experts layers (its "Future work > Model coverage").
  *
  * Numerics (the page states no formulas; these are this library's readings):
  *   scale s = amax / 448 (E4M3) or amax / 127 (int8) in IEEE fp32, s = 1 for
- *   an all-zero row, group or block; q = round-to-nearest-even(x / s) with
- *   one IEEE fp32 division, saturated to +-448 / [-127, 127];
+ *   an all-zero row, group or block; q = round-to-nearest-even of the
+ *   correctly rounded fp32 quotient x / s (one IEEE division, or Markstein's
+ *   method, which gives the same quotient), saturated to +-448 / [-127, 127],
+ *   the sign of a zero kept;
  *   FP8_Dynamic / INT8:  Y = bf16_rn((float(acc) * s_a[m]) * s_w[n]);
  *   Block_FP8:           Y = bf16_rn(sum_kb s_a[m,kb] * s_w[n/128,kb] * acc_kb).
  *
