@@ -132,6 +132,27 @@ def test_workspace_bytes(q):
     assert q.qg_workspace_bytes(1, 9, 4096, 4096, q.QG_SWAPAB_DP4A_SPLITK, 2) == 0  # M > 8 -> invalid
 
 
+def _grouped(q, fmt=0, groups=4, offs=OK16, total=8, max_tokens=4, N=256, K=256, variant=2, split=1, cfg=0):
+    return _raw(q).qg_gemm_w8a8_grouped(fmt, groups, offs, total, max_tokens, N, K, OK16, OK16, OK16, OK16, OK16, N,
+                                        variant, split, cfg, None, 0, None, None)
+
+
+def test_grouped_validation(q):
+    # every check below returns before any device work
+    assert _grouped(q, groups=0) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _grouped(q, groups=70000) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _grouped(q, offs=None) == q.QG_ERR_INVALID_ARG
+    assert _grouped(q, offs=OK16 + 2) == q.QG_ERR_INVALID_ARG            # unaligned offsets
+    assert _grouped(q, variant=0) == q.QG_ERR_INVALID_ARG                # Standard
+    assert _grouped(q, variant=4, fmt=0) == q.QG_ERR_UNSUPPORTED_SHAPE   # dp4a is INT8 only
+    assert _grouped(q, variant=4, fmt=1, max_tokens=9) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _grouped(q, K=200) == q.QG_ERR_UNSUPPORTED_SHAPE
+    assert _grouped(q, total=-1) == q.QG_ERR_INVALID_ARG
+    assert _grouped(q, split=17, K=4096, variant=3) == q.QG_ERR_WORKSPACE_TOO_SMALL
+    assert _grouped(q, total=0) == q.QG_OK                               # no tokens: nothing to do
+    assert _grouped(q, max_tokens=0) == q.QG_OK
+
+
 def test_grouped_workspace_bytes(q):
     # cluster reductions need none; the workspace holds counters for every
     # group's tiles and [splits][total_tokens][N] partials
