@@ -248,7 +248,11 @@ QG_API int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const 
 QG_API int qg_select(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int* split_k, int* config_id);
 
 /* Load a tuned table (tab-separated "fmt N K M variant split_k config_id"
- * rows, '#' comments), replacing the current one.  NULL reads $QG_TABLE. */
+ * rows, '#' comments), replacing the current one.  NULL reads $QG_TABLE.
+ *
+ * The table and the settings below (default configs, launch flags, wait
+ * limit, forced timeout) are process-wide: any thread may change them, and a
+ * change applies to the calls that start after it. */
 QG_API int qg_load_table(const char* path);
 
 /* Allow (1) or forbid (0, the initial state) qg_select's built-in default

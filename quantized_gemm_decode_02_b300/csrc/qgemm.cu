@@ -7,6 +7,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -43,10 +44,12 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(QG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-std::mutex g_mu;
-int g_launch_flags = 0;
-uint64_t g_wait_ns = 2000000000ull;
-int g_force_timeout = 0;
+// Process-wide settings: any thread may change them, and a change applies to
+// the calls that start after it (a call running meanwhile may see either).
+std::mutex g_mu;  // guards the table and g_allow_default
+std::atomic<int> g_launch_flags{0};
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+std::atomic<int> g_force_timeout{0};
 bool g_allow_default = false;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -93,25 +96,28 @@ struct DevInfo {
   size_t smem_per_sm = 0;    // shared memory of one SM
   size_t smem_reserved = 0;  // shared memory the system reserves per CTA
 };
+// Properties of the current device, queried once per device (thread-safe).
 DevInfo dev_info() {
   static DevInfo cache[64];
+  static std::once_flag once[64];
   int d = 0;
   cudaGetDevice(&d);
   if (d < 0 || d >= 64) d = 0;
-  if (cache[d].sms == 0) {
+  std::call_once(once[d], [d] {
     cudaDeviceProp p;
+    DevInfo& c = cache[d];
     if (cudaGetDeviceProperties(&p, d) == cudaSuccess) {
-      cache[d].sms = p.multiProcessorCount;
-      cache[d].smem_optin = p.sharedMemPerBlockOptin;
-      cache[d].smem_per_sm = p.sharedMemPerMultiprocessor;
-      cache[d].smem_reserved = p.reservedSharedMemPerBlock;
-    } else {
-      cache[d].sms = 148;
-      cache[d].smem_optin = 232448;
-      cache[d].smem_per_sm = 233472;
-      cache[d].smem_reserved = 1024;
+      c.sms = p.multiProcessorCount;
+      c.smem_optin = p.sharedMemPerBlockOptin;
+      c.smem_per_sm = p.sharedMemPerMultiprocessor;
+      c.smem_reserved = p.reservedSharedMemPerBlock;
+    } else {  // no device to ask (host-only callers): B300's figures
+      c.sms = 148;
+      c.smem_optin = 232448;
+      c.smem_per_sm = 233472;
+      c.smem_reserved = 1024;
     }
-  }
+  });
   return cache[d];
 }
 
@@ -133,7 +139,7 @@ cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (g_launch_flags & QG_LAUNCH_PDL) {
+  if (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_PDL) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
@@ -478,8 +484,8 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     g.a_q_out = static_cast<uint8_t*>(const_cast<void*>(A_q_dev));
     g.s_a_out = const_cast<float*>(s_a_dev);
   }
-  g.wait_ns = g_wait_ns;
-  g.force_timeout = g_force_timeout;
+  g.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  g.force_timeout = g_force_timeout.load(std::memory_order_relaxed);
   g.l2_prefetch = (config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -567,15 +573,15 @@ const char* qg_version(void) { return "qgemm-b300 0.1 (sm_103a)"; }
 int qg_set_launch_flags(int flags) {
   if (flags & ~(QG_LAUNCH_PDL | QG_LAUNCH_FUSED_QUANT))
     return fail(QG_ERR_INVALID_ARG, "unknown launch flag bits 0x%x", flags);
-  g_launch_flags = flags;
+  g_launch_flags.store(flags, std::memory_order_relaxed);
   return QG_OK;
 }
 int qg_set_wait_limit_ns(uint64_t ns) {
-  g_wait_ns = ns ? ns : 2000000000ull;
+  g_wait_ns.store(ns ? ns : 2000000000ull, std::memory_order_relaxed);
   return QG_OK;
 }
 int qg_set_force_timeout(int on) {
-  g_force_timeout = on ? 1 : 0;
+  g_force_timeout.store(on ? 1 : 0, std::memory_order_relaxed);
   return QG_OK;
 }
 int qg_set_allow_default(int allow) {
@@ -758,7 +764,7 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
   const bool fusable = fmt != QG_BLOCK_FP8 && (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK);
   const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
-  if (fusable && (!buffers || (g_launch_flags & QG_LAUNCH_FUSED_QUANT))) {
+  if (fusable && (!buffers || (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {
     // one kernel: each CTA quantizes the activations its K range needs
     if ((A_q_dev && !aligned(A_q_dev, 16)) || (s_a_dev && !aligned(s_a_dev, 4)))
       return fail(QG_ERR_ALIGNMENT, "A_q needs 16-byte alignment, s_a 4");

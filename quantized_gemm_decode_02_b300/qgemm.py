@@ -117,10 +117,17 @@ def qg_quant_weight(fmt, W, N, K, W_q, s_w, stream=None) -> None:
 
 
 def qg_pack_weight(fmt, W, N, K, W_q, s_w) -> None:
-    """Host weight quantization: W, W_q, s_w are CPU tensors (contiguous)."""
-    for t in (W, W_q, s_w):
-        if isinstance(t, torch.Tensor) and (t.is_cuda or not t.is_contiguous()):
+    """Host weight quantization: W (fp32 [N, K]), W_q (1-byte [N, K]) and s_w
+    (fp32 [N] or [ceil(N/128), K/128]) are contiguous CPU tensors."""
+    f = _fmt(fmt)
+    n_scales = -(-N // 128) * (K // 128) if f == QG_BLOCK_FP8 else N
+    for t, dt, n, name in ((W, torch.float32, N * K, "W"), (W_q, None, N * K, "W_q"), (s_w, torch.float32, n_scales, "s_w")):
+        if not isinstance(t, torch.Tensor):
+            continue
+        if t.is_cuda or not t.is_contiguous():
             raise ValueError("qg_pack_weight takes contiguous host tensors")
+        if (dt is not None and t.dtype != dt) or (dt is None and t.element_size() != 1) or t.numel() < n:
+            raise ValueError(f"qg_pack_weight: {name} must hold {n} {'fp32' if dt else '1-byte'} values")
     _check(_lib.qg_pack_weight(_fmt(fmt), _ptr(W), N, K, _ptr(W_q), _ptr(s_w)), "qg_pack_weight")
 
 

@@ -74,6 +74,31 @@ def test_pack_weight_errors(q):
     assert e.value.code == q.QG_ERR_INVALID_ARG
 
 
+def test_pack_weight_binding_rejects_short_or_mistyped_host_tensors(q):
+    """The host quantizer writes N*K codes and the scales through raw
+    pointers: the binding refuses tensors that cannot hold them."""
+    N, K = 4, 128
+    W = torch.zeros((N, K), dtype=torch.float32)
+    Wq = torch.zeros((N, K), dtype=torch.uint8)
+    sw = torch.zeros(N, dtype=torch.float32)
+    bad = [
+        (W[:, :64].contiguous(), Wq, sw),            # W too short
+        (W.double(), Wq, sw),                        # W not fp32
+        (W, Wq[:2].contiguous(), sw),                # W_q too short
+        (W, Wq.to(torch.int16), sw),                 # W_q not 1-byte
+        (W, Wq, sw[:3].contiguous()),                # s_w too short
+        (W, Wq, torch.zeros((N, 2), dtype=torch.float32)[:, 0]),  # not contiguous
+    ]
+    for w, wq, s in bad:
+        with pytest.raises(ValueError):
+            q.qg_pack_weight("FP8_Dynamic", w, N, K, wq, s)
+    with pytest.raises(ValueError):                  # Block_FP8: one scale per 128x128 block
+        q.qg_pack_weight("Block_FP8", torch.zeros((200, K)), 200, K, torch.zeros((200, K), dtype=torch.uint8),
+                         torch.zeros(1, dtype=torch.float32))
+    q.qg_pack_weight("Block_FP8", torch.zeros((200, K)), 200, K, torch.zeros((200, K), dtype=torch.uint8),
+                     torch.zeros(2, dtype=torch.float32))
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])
 def test_pack_weight_equals_device_quantizer(q, fmt):
