@@ -122,6 +122,14 @@ QG_API int qg_pack_weight(int fmt, const float* W_host, int64_t N, int64_t K, vo
  * first use; the kernels leave them zero again), then the split partials. */
 QG_API size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k);
 
+/* Validate a configuration without launching anything: the checks of
+ * qg_gemm_w8a8 that need no pointer (format, variant, sizes, config_id,
+ * K % 16 / K % 128, split_k range, the W8A8_INT8 and dp4a restrictions).
+ * Returns the status qg_gemm_w8a8 would return for them; QG_OK does not
+ * check pointers, alignment or the workspace size.  qg_load_table applies
+ * the same checks to every row at its token count. */
+QG_API int qg_check_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, int config_id);
+
 /* Zero a workspace's counters (cudaMemsetAsync on `stream`). */
 QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
 
@@ -249,6 +257,9 @@ QG_API int qg_select(int fmt, int64_t M, int64_t N, int64_t K, int* variant, int
 
 /* Load a tuned table (tab-separated "fmt N K M variant split_k config_id"
  * rows, '#' comments), replacing the current one.  NULL reads $QG_TABLE.
+ * A row that does not parse, or whose configuration qg_check_config rejects
+ * at the row's M, fails the load with QG_ERR_TABLE_PARSE (the current table
+ * is kept).
  *
  * The table and the settings below (default configs, launch flags, wait
  * limit, forced timeout) are process-wide: any thread may change them, and a

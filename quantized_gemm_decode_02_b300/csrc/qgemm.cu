@@ -311,6 +311,37 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
                      qg::gemm_dp4a_smem_bytes(g.stages, rb), tmW, tmA, g, stream);
 }
 
+// The config_id checks of qg_gemm_w8a8: known bits, ring depth, prefetch
+// distance, and wide tiles only for the FP8_Dynamic Standard / Split-K forms.
+int check_config_bits(int fmt, int variant, int config_id) {
+  if (config_id < 0 || (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+      (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
+      ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
+    return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
+                config_id, kMaxStages, QG_CONFIG_MAX_PREFETCH);
+  if ((config_id & QG_CONFIG_WIDE) && (fmt != QG_FP8_DYNAMIC || !(variant == QG_STANDARD || variant == QG_SPLITK)))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_WIDE is for the FP8_Dynamic Standard / Split-K variants");
+  if ((config_id & QG_CONFIG_RING_MASK) == 1) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
+  return QG_OK;
+}
+
+// Every check of qg_gemm_w8a8 that needs no pointer: format, variant, sizes,
+// config_id, K alignment, and the variant's plan (split_k range, token and
+// tile limits, the INT8 and dp4a restrictions).
+int check_shape_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, int config_id) {
+  if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
+  if (variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return fail(QG_ERR_INVALID_ARG, "unknown variant %d", variant);
+  if (M < 1 || N <= 0 || K <= 0)
+    return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld", (long long)M, (long long)N, (long long)K);
+  int rc = check_config_bits(fmt, variant, config_id);
+  if (rc != QG_OK) return rc;
+  if (K % 16) return fail(QG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
+  if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+  Plan p;
+  return make_plan(fmt, M, N, K, variant, split_k, &p);
+}
+
 // ------------------------------------------------------------------ table
 struct Key {
   int fmt;
@@ -364,6 +395,13 @@ int load_table_file(const char* path) {
       fclose(f);
       return fail(QG_ERR_TABLE_PARSE, "%s:%d: malformed row", path, lineno);
     }
+    // a row must be a configuration the GEMM accepts at its token count (and
+    // so at every smaller one qg_select sends to it)
+    if (check_shape_config(fmt, m, n, k, variant, split_k, config_id) != QG_OK) {
+      const std::string why = g_err;
+      fclose(f);
+      return fail(QG_ERR_TABLE_PARSE, "%s:%d: invalid configuration: %s", path, lineno, why.c_str());
+    }
     t[Key{fmt, n, k, m}] = Row{variant, split_k, config_id};
   }
   fclose(f);
@@ -394,13 +432,8 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   if (M < 0 || N <= 0 || K <= 0 || ldy < N)
     return fail(QG_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld ldy=%lld", (long long)M, (long long)N, (long long)K, (long long)ldy);
   const bool wide = (config_id & QG_CONFIG_WIDE) != 0;
-  if (config_id < 0 || (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
-      (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
-      ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
-    return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
-                config_id, kMaxStages, QG_CONFIG_MAX_PREFETCH);
-  if (wide && (fmt != QG_FP8_DYNAMIC || !(variant == QG_STANDARD || variant == QG_SPLITK)))
-    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_WIDE is for the FP8_Dynamic Standard / Split-K variants");
+  const int crc = check_config_bits(fmt, variant, config_id);
+  if (crc != QG_OK) return crc;
   if (M == 0) return QG_OK;
   if ((!fused && (!A_q_dev || !s_a_dev)) || !W_q_dev || !s_w_dev || !Y_dev)
     return fail(QG_ERR_INVALID_ARG, "null pointer");
@@ -719,6 +752,10 @@ size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant,
   if (fmt < 0 || fmt > 2 || M <= 0 || N <= 0 || K <= 0 || variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return 0;
   if (make_plan(fmt, M, N, K, variant, split_k, &p) != QG_OK) return 0;
   return static_cast<size_t>(workspace_bytes(p, M, N));
+}
+
+int qg_check_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, int config_id) {
+  return check_shape_config(fmt, M, N, K, variant, split_k, config_id);
 }
 
 int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream) {

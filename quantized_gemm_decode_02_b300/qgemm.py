@@ -38,7 +38,7 @@ def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False) -> int:
     (FP8_Dynamic Standard / Split-K) 256-row weight tiles."""
     return ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT) | (QG_CONFIG_WIDE if wide else 0)
 
-EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_workspace_init", "qg_gemm_w8a8",
+EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_check_config", "qg_workspace_init", "qg_gemm_w8a8",
            "qg_linear_w8a8", "qg_gemm_w8a8_noalloc", "qg_gemm_w8a8_grouped", "qg_workspace_bytes_grouped",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
            "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
@@ -60,6 +60,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qg_pack_weight.argtypes = [I, P, I64, I64, P, P]
     lib.qg_workspace_bytes.argtypes = [I, I64, I64, I64, I, I]
     lib.qg_workspace_bytes.restype = SZ
+    lib.qg_check_config.argtypes = [I, I64, I64, I64, I, I, I]
     lib.qg_workspace_init.argtypes = [P, SZ, P]
     lib.qg_gemm_w8a8.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
     lib.qg_gemm_w8a8_noalloc.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, P]
@@ -133,6 +134,12 @@ def qg_pack_weight(fmt, W, N, K, W_q, s_w) -> None:
 
 def qg_workspace_bytes(fmt, M, N, K, variant, split_k) -> int:
     return int(_lib.qg_workspace_bytes(_fmt(fmt), M, N, K, variant, split_k))
+
+
+def qg_check_config(fmt, M, N, K, variant, split_k, config_id=0) -> int:
+    """Status qg_gemm_w8a8 would return for this configuration's pointer-free
+    checks (QG_OK = accepted); no exception, no launch."""
+    return int(_lib.qg_check_config(_fmt(fmt), M, N, K, variant, split_k, config_id))
 
 
 def qg_workspace_init(workspace, ws_bytes, stream=None) -> None:

@@ -216,3 +216,78 @@ def test_default_config_fills_the_gpu(q):
         assert v in (q.QG_STANDARD, q.QG_SPLITK)
     finally:
         q.qg_set_allow_default(False)
+
+
+def test_check_config_returns_the_gemm_status(q):
+    """qg_check_config gives, without pointers, the status qg_gemm_w8a8
+    returns for the same configuration's pointer-free checks."""
+    cases = [dict(fmt=5), dict(variant=9), dict(K=200), dict(fmt=2, K=272), dict(split=2), dict(variant=3, split=3),
+             dict(variant=3, split=0), dict(fmt=1, M=8, variant=0), dict(fmt=1, M=9, variant=q.QG_SWAPAB_DP4A),
+             dict(fmt=0, M=1, variant=q.QG_SWAPAB_DP4A), dict(cfg=17), dict(cfg=q.config_id(0, 65)),
+             dict(cfg=1 << 13), dict(cfg=q.config_id(0, 0, True)), dict(cfg=-1), dict(cfg=1)]
+    for c in cases:
+        fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
+        v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)
+        want = _gemm(q, fmt=fmt, M=M, K=K, variant=v, split=s, cfg=cfg)
+        assert want != q.QG_OK
+        assert q.qg_check_config(fmt, M, 256, K, v, s, cfg) == want, c
+    # accepted configurations (never launched here)
+    assert q.qg_check_config(1, 8, 4096, 2048, q.QG_SWAPAB_DP4A_SPLITK, 16, 0) == q.QG_OK
+    assert q.qg_check_config(0, 300, 4096, 4096, q.QG_SPLITK, 3, q.config_id(4, 0, True)) == q.QG_OK
+    assert q.qg_check_config(2, 32, 4096, 12288, q.QG_SWAPAB_SPLITK, 96, q.config_id(12, 64)) == q.QG_OK
+    assert q.qg_check_config(0, 0, 256, 256, 2, 1, 0) == q.QG_ERR_INVALID_ARG   # a configuration has M >= 1
+
+
+def test_table_rows_are_checked_at_load(q, tmp_path):
+    good = tmp_path / "good.tsv"
+    good.write_text("1\t2048\t2048\t8\t5\t2\t0\n")
+    q.qg_load_table(str(good))
+    for row, why in [("1\t2048\t2048\t16\t5\t2\t0\n", "dp4a above 8 tokens"),
+                     ("1\t2048\t2048\t8\t0\t1\t0\n", "INT8 Standard"),
+                     ("0\t2048\t2048\t8\t3\t17\t0\n", "split_k above ceil(K/128)"),
+                     ("0\t2048\t2048\t8\t2\t1\t4096\n", "wide tiles on Swap-AB"),
+                     ("2\t2048\t2000\t8\t2\t1\t0\n", "Block_FP8 K % 128")]:
+        bad = tmp_path / "bad.tsv"
+        bad.write_text("# ok row first\n1\t4096\t2048\t1\t4\t1\t0\n" + row)
+        with pytest.raises(q.QGError) as e:
+            q.qg_load_table(str(bad))
+        assert e.value.code == q.QG_ERR_TABLE_PARSE, why
+        assert "bad.tsv:3" in q.qg_last_error(), why
+    # a rejected file leaves the loaded table in place
+    q.qg_set_allow_default(False)
+    assert q.qg_select("W8A8_INT8", 5, 2048, 2048) == (q.QG_SWAPAB_DP4A_SPLITK, 2, 0)
+    with pytest.raises(q.QGError):
+        q.qg_select("W8A8_INT8", 1, 4096, 2048)
+
+
+def test_shipped_table_covers_every_bench_workload(q):
+    """Every (format, shape, token count) bench.py and its workloads launch
+    has a tuned row, and the row is a configuration the GEMM accepts."""
+    import bench
+    import seeded_inputs as si
+    q.qg_load_table(bench.TABLE)
+    q.qg_set_allow_default(False)
+    seen = set()
+    for name, wl in bench.WORKLOADS.items():
+        for fmt, model, layer, M in wl["items"]:
+            K, N = si.QWEN3_LINEARS[model][layer]
+            if (fmt, M, N, K) in seen:
+                continue
+            seen.add((fmt, M, N, K))
+            v, s, c = q.qg_select(fmt, M, N, K)
+            assert q.qg_check_config(fmt, M, N, K, v, s, c) == q.QG_OK, (name, fmt, model, layer, M)
+    assert len(seen) > 300
+
+
+def test_tuner_candidates_are_accepted(q):
+    """The offline sweep only times configurations the GEMM accepts."""
+    from quantized_gemm_decode_02_b300 import tune
+    n = 0
+    for fmt in tune.FMT_ID:
+        for shapes in tune.SHAPES.values():
+            for K, N in shapes.values():
+                for M in tune.TUNED_M + (64, 128, 256, 384, 512):
+                    for v, s, c in tune.candidates(fmt, M, N, K, 148):
+                        assert q.qg_check_config(fmt, M, N, K, v, s, c) == q.QG_OK, (fmt, M, N, K, v, s, c)
+                        n += 1
+    assert n > 1000
