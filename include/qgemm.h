@@ -291,7 +291,11 @@ QG_API int qg_set_wait_limit_ns(uint64_t ns);
 QG_API int qg_set_force_timeout(int on);
 
 /* Synchronize the current device, then read and clear its status word:
- * *code = 0 or the first qg_status a kernel reported. */
+ * *code = 0 or the first qg_status a kernel reported.  After a reported
+ * QG_ERR_DEVICE_TIMEOUT the Y of the launches since the last check is
+ * unspecified, and a Split-K workspace they used may hold stale arrival
+ * counters: run qg_workspace_init on it before its next use
+ * (qg_gemm_w8a8_noalloc clears its own counters on every call). */
 QG_API int qg_device_error(int* code);
 
 /* Thread-local description of the last failure (never NULL). */

@@ -7,8 +7,8 @@ library never loads it and shares no code with it.
 The arithmetic lives in ``qg_oracle.c`` (plain C, element by element, exact
 int64 / fp64 accumulation); this module compiles it with gcc, marshals numpy
 arrays through ctypes and splits large GEMMs over host threads (each thread
-computes a disjoint set of output columns; the C code drops the GIL-free
-ctypes call).  See the header of ``qg_oracle.c`` for the method's source,
+computes a disjoint set of output columns; ctypes releases the GIL for
+the duration of each C call).  See the header of ``qg_oracle.c`` for the method's source,
 "Building a High-Performance and Portable vLLM Linear Backend with Helion",
 and for the readings taken where that page is silent.
 
