@@ -310,17 +310,24 @@ def _oracle_items(name):
     return out
 
 
-def _oracle_pass(orc, name, cols, cache, cores):
-    """quant_act + GEMM in the oracle for every item, all token rows, the
-    first `cols` output columns.  Returns (seconds, bytes, flops)."""
+def _oracle_pass(orc, name, cols, cache, cores, items=None):
+    """quant_act + GEMM in the oracle for the workload's items (or the listed
+    item indices), all token rows, the first `cols` output columns.  The
+    quantized weights and the activations are prepared once and cached
+    (set-up, not timed).  Returns (seconds, bytes, flops)."""
     t_total, processed, flops = 0.0, 0, 0
-    for idx, (fmt, M, N, K) in enumerate(_oracle_items(name)):
+    all_items = _oracle_items(name)
+    for idx in (range(len(all_items)) if items is None else items):
+        fmt, M, N, K = all_items[idx]
         nc = min(cols, N)
-        key = (fmt, N, K, nc)
-        if key not in cache:
-            cache[key] = orc.quant_weight(fmt, si.weights(nc, K, seed=idx))  # setup, not timed
-        Wq, sw = cache[key]
-        A = si.bf16_to_f32_numpy(si.activations(M, K, seed=idx))
+        wkey = (fmt, N, K, nc)
+        if wkey not in cache:
+            cache[wkey] = orc.quant_weight(fmt, si.weights(nc, K, seed=idx))
+        Wq, sw = cache[wkey]
+        akey = ("A", idx)
+        if akey not in cache:
+            cache[akey] = si.bf16_to_f32_numpy(si.activations(M, K, seed=idx))
+        A = cache[akey]
         t0 = time.perf_counter()
         Aq, sa = orc.quant_act(fmt, A)
         orc.gemm(fmt, Aq, sa, Wq, sw, threads=cores)
@@ -449,6 +456,24 @@ def _config(name, wl_items):
             "M": list(dict.fromkeys(M for _, _, _, M in wl_items))}
 
 
+REFERENCE_BUDGET_S = 120.0  # wall time of a whole --impl reference run, warm-up included
+
+
+def reference_plan(n_items: int, t_item: float, t_pass16: float, runs: int, budget_s: float = REFERENCE_BUDGET_S):
+    """Per-step sample of the reference arm so that `runs` steps (warm-up
+    included) take about `budget_s` seconds: (columns, items per step).  The
+    whole workload per step at the widest column count whose pass fits the
+    per-step share; when even 16 columns over every item do not fit, a
+    rotating subset of the items, at least one per step."""
+    per_step = budget_s / max(1, runs)
+    if t_pass16 <= per_step:
+        cols = 16
+        while cols < 8192 and t_pass16 * (cols * 2) / 16 <= per_step:
+            cols *= 2
+        return cols, n_items
+    return 16, max(1, min(n_items, int(per_step / max(t_item, 1e-9))))
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle as it stands, each step a bounded
     sample of the workload sized so the whole run stays within ~2 minutes."""
@@ -460,22 +485,33 @@ def run_reference(args, world, rank):
     spec = WORKLOADS[name]
     cores = os.cpu_count() or 1
     cache = {}
-    t16, _, _ = _oracle_pass(orc, name, 16, cache, cores)          # calibration
-    per_step = 120.0 / max(1, args.steps + args.warmup)
-    cols = 16
-    while cols < 8192 and t16 * (cols * 2) / 16 <= per_step:
-        cols *= 2
+    n_items = len(_oracle_items(name))
+    _oracle_pass(orc, name, 16, cache, cores)                      # inputs prepared, not timed
+    w0 = time.perf_counter()
+    _oracle_pass(orc, name, 16, cache, cores)                      # calibration (wall time)
+    t_pass16 = time.perf_counter() - w0
+    cols, per_step = reference_plan(n_items, t_pass16 / n_items, t_pass16, args.steps + args.warmup)
+    nxt = 0
+
+    def step():
+        nonlocal nxt
+        idx = [(nxt + i) % n_items for i in range(per_step)]
+        nxt = (nxt + per_step) % n_items
+        return _oracle_pass(orc, name, cols, cache, cores, items=idx)
+
     for _ in range(args.warmup):
-        _oracle_pass(orc, name, cols, cache, cores)
+        step()
     t_sum, b_sum, f_sum = 0.0, 0, 0
     for _ in range(args.steps):
-        t, b, f = _oracle_pass(orc, name, cols, cache, cores)
+        t, b, f = step()
         t_sum += t
         b_sum += b
         f_sum += f
     value, unit = _rate(spec["bound"], b_sum, f_sum, t_sum)
-    sample = (f"{name}: all {len(_oracle_items(name))} (format, M, layer) items, all token rows, the first {cols} "
-              f"output columns per layer, per step; quant_act + GEMM in the C oracle on {cores} threads")
+    which = (f"all {n_items} (format, M, layer) items" if per_step == n_items else
+             f"{per_step} of the {n_items} (format, M, layer) items in turn")
+    sample = (f"{name}: {which}, all token rows, the first {cols} output columns per layer, per step; "
+              f"quant_act + GEMM in the C oracle on {cores} threads")
     line = {"metric": METRIC_HBM if spec["bound"] == "hbm" else METRIC_TENSOR,
             "value": value, "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_sum / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
