@@ -46,3 +46,9 @@ def test_reference_arm_prints_the_contract_line(bench):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == bench.DEFAULT_WORKLOAD
+
+
+def test_cpu_baseline_leg_reports_a_bounded_sample(bench):
+    r = bench.cpu_oracle_leg(bench.DEFAULT_WORKLOAD, budget_s=0.5)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] >= 1
+    assert "all 28 (format, M, layer) items" in r["sample"]
