@@ -449,9 +449,12 @@ def max_over_ranks(world, v: float, device) -> float:
 
 
 def _config(name, wl_items):
+    """The workload's description: formats, linear shapes (K, N) and token counts."""
     fmts = sorted({f for f, _, _, _ in wl_items})
-    models = sorted({m for _, m, _, _ in wl_items})
-    return {"workload": name, "formats": fmts, "models": models,
+    shapes = {}
+    for _, model, layer, _ in wl_items:
+        shapes.setdefault(f"{model} {layer}", list(si.QWEN3_LINEARS[model][layer]))
+    return {"workload": name, "formats": fmts, "shapes_k_n": shapes,
             "layers": list(dict.fromkeys(layer for _, _, layer, _ in wl_items)),
             "M": list(dict.fromkeys(M for _, _, _, M in wl_items))}
 

@@ -46,6 +46,8 @@ def test_reference_arm_prints_the_contract_line(bench):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == bench.DEFAULT_WORKLOAD
+    assert not {"model", "models", "global_batch", "seq_len"} & set(line["config"])  # a workload, not a model
+    assert line["config"]["shapes_k_n"]["Qwen3-1.7B down"] == [6144, 2048]
 
 
 def test_cpu_baseline_leg_reports_a_bounded_sample(bench):
