@@ -1,34 +1,40 @@
 """Benchmark of the quantized decode GEMM hot path on B300.
 
-Workload (default, `int8_qwen3_1.7b`): W8A8_INT8 over the four Qwen3-1.7B
-linear layers (qkv K=2048 N=4096, o K=2048 N=2048, gate_up K=2048 N=12288,
-down K=6144 N=2048) at every tuned decode token count M in
-{1,2,4,8,16,24,32}.  One step is one pass of the whole hot path over that
-batch: for each (M, layer) one qg_linear_w8a8 call, i.e. a dynamic
-per-token activation quantization kernel and the quantized GEMM kernel with
-the variant the tuned table selects (qg_select); 28 + 28 kernels captured once into a CUDA graph with programmatic
-dependent launch and replayed.  Every (M, layer) pair
-owns distinct weights, so a step streams 352 MB of int8 weights (> 126 MB
-L2): no step finds its weights in L2.
+Workload (default, `layer_qwen3_8b`): all three formats (FP8_Dynamic,
+W8A8_INT8, Block_FP8) on one Qwen3-8B layer's four linears (qkv K=4096
+N=6144, o K=4096 N=4096, gate_up K=4096 N=24576, down K=12288 N=4096) at
+every decode token count M = 1..32, activations A ~ N(0,1) with 1% outliers
+x20.  One step is one pass of the whole hot path over that batch: for each
+(format, M, layer) one qg_linear_w8a8 call, i.e. a dynamic activation
+quantization kernel (per token, or per 1x128 group for Block_FP8) and the
+quantized GEMM kernel with the variant the tuned table selects (qg_select);
+384 + 384 kernels captured once into one CUDA graph with programmatic
+dependent launch and replayed.  Weights: one copy per (format, layer) and
+token-count parity, so two uses of a copy are separated by the other
+linears' 193 MB of weights (> 126 MB L2): no GEMM finds its weights in L2.
 
-Other workloads (--workload): Block_FP8 over the Qwen3-8B linears at M=1..32;
+Other workloads (--workload): W8A8_INT8 over the Qwen3-1.7B linears at
+M in {1,2,4,8,16,24,32}; Block_FP8 over the Qwen3-8B linears at M=1..32;
 FP8_Dynamic over the Qwen3-32B linears; FP8_Dynamic at M=1 on the Qwen3-1.7B
-o_proj shape; `layer_qwen3_8b`, all three formats on one Qwen3-8B layer's
-four linears chained in one graph at every M in 1..32; `large_m_qwen3_8b`,
-the same linears at M = 64..512 (compute-bound: TFLOP/s against the tensor
-peak of each format's MMA kind).
+o_proj shape; FP8_Dynamic / W8A8_INT8 over the Qwen3-8B linears;
+`large_m_qwen3_8b`, the layer at M = 64..512 (compute-bound: TFLOP/s
+against the tensor peak of each format's MMA kind).
 
 Metric: HBM GB/s = algorithmic bytes per step / step time (the kernels must
 move the weights, activations, scales and outputs once), plus us per GEMM;
 TFLOP/s = 2*M*N*K per step / step time for the compute-bound workload.
 
-Also reported: the roofline of the GEMM kernel (per-launch durations from
-timing events inside a second graph), an end-to-end figure through the C ABI
-with the activations copied from pinned host memory and the outputs copied
-back inside the timed region (two buffer sets, so one step's copies overlap
-its neighbours' kernels), SM clocks sampled during the timed region, and
-the CPU oracle timed on the host cores on a bounded sample (cpu_baseline).
-`--impl reference` times that oracle alone as the reference arm.
+Also reported: the roofline of the GEMM kernels from an in-chain timeline
+(the same graph, programmatic dependent launch kept, every kernel stamping
+its first CTA start and last CTA end with %globaltimer through the library's
+timing log: a kernel's time is from its predecessor's end to its own end, so
+the kernels' times add up to the step), an end-to-end figure through the C
+ABI with the activations copied from pinned host memory and the outputs
+copied back inside the timed region (two buffer sets, so one step's copies
+overlap its neighbours' kernels), SM clocks sampled during the timed region,
+and the CPU oracle timed on the host cores on a bounded sample
+(cpu_baseline).  `--impl reference` times that oracle alone as the
+reference arm.
 """
 from __future__ import annotations
 
@@ -62,7 +68,8 @@ def _items(fmts, model, layers, ms):
 
 
 # name: items, whether items share weights (one copy per (format, layer) and
-# token-count parity), roofline bound
+# token-count parity), roofline bound; activations with 1% outliers x20 for
+# every format (`outliers`), else for Block_FP8 only
 WORKLOADS = {
     "int8_qwen3_1.7b": dict(items=_items(["W8A8_INT8"], "Qwen3-1.7B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
     "fp8_qwen3_1.7b_o_m1": dict(items=_items(["FP8_Dynamic"], "Qwen3-1.7B", ("o",), (1,)), shared=False, bound="hbm"),
@@ -73,12 +80,13 @@ WORKLOADS = {
     "int8_qwen3_8b": dict(items=_items(["W8A8_INT8"], "Qwen3-8B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
     # all three formats on one Qwen3-8B layer's four linears, chained in one
     # graph, at every token count 1..32
-    "layer_qwen3_8b": dict(items=_items(FORMATS, "Qwen3-8B", LAYERS, range(1, 33)), shared=True, bound="hbm"),
+    "layer_qwen3_8b": dict(items=_items(FORMATS, "Qwen3-8B", LAYERS, range(1, 33)), shared=True, bound="hbm",
+                           outliers=True),
     # the compute-bound regime beyond the decode range
     "large_m_qwen3_8b": dict(items=_items(FORMATS, "Qwen3-8B", LAYERS, (64, 128, 256, 384, 512)), shared=True,
-                             bound="tensor"),
+                             bound="tensor", outliers=True),
 }
-DEFAULT_WORKLOAD = "int8_qwen3_1.7b"
+DEFAULT_WORKLOAD = "layer_qwen3_8b"
 METRIC_HBM = "HBM GB/s (% of B300 peak) and us/GEMM at M=1..32 on Qwen3 linear shapes"
 METRIC_TENSOR = "TFLOP/s (% of B300 tensor peak) at M=64..512 on Qwen3 linear shapes"
 
@@ -109,23 +117,26 @@ class Workload:
     """Device buffers and the captured graphs for one workload."""
 
     def __init__(self, name: str, device: str, seed: int = 0, pdl: bool = True, fused: bool = False,
-                 table: str = TABLE):
+                 table: str = TABLE, items=None):
+        """`items`: (format, model, layer, M) list replacing the workload's
+        own (a slice of it, for tests), with the workload's other settings."""
         from quantized_gemm_decode_02_b300 import qgemm as q
         self.q = q
         self.name = name
         self.fused = fused
         spec = WORKLOADS[name]
+        spec_items = spec["items"] if items is None else list(items)
         self.bound = spec["bound"]
         self.device = device
         self.pdl = pdl
         self.items = []  # (fmt, M, layer, N, K)
-        for fmt, model, layer, M in spec["items"]:
+        for fmt, model, layer, M in spec_items:
             K, N = si.QWEN3_LINEARS[model][layer]
             self.items.append((fmt, M, layer, N, K))
         self.formats = sorted({it[0] for it in self.items})
-        self.models = sorted({m for _, m, _, _ in spec["items"]})
-        self.layers = list(dict.fromkeys(layer for _, _, layer, _ in spec["items"]))
-        self.ms = list(dict.fromkeys(M for _, _, _, M in spec["items"]))
+        self.models = sorted({m for _, m, _, _ in spec_items})
+        self.layers = list(dict.fromkeys(layer for _, _, layer, _ in spec_items))
+        self.ms = list(dict.fromkeys(M for _, _, _, M in spec_items))
         if os.path.exists(table):
             q.qg_load_table(table)
         q.qg_set_allow_default(True)
@@ -143,18 +154,21 @@ class Workload:
         self.recs = []
         ws_need = 0
         weights = {}
+        wseeds = {}  # weight copy -> seed of its fp32 weights (si.weights_device)
         for i, (fmt, M, layer, N, K) in enumerate(self.items):
             variant, split, cfg = q.qg_select(fmt, M, N, K)
             need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
             ws_need = max(ws_need, need)
             A = self.A_all[a_off[i]:a_off[i] + M * K * 2].view(torch.bfloat16).view(M, K)
-            A.copy_(si.activations_device(M, K, seed=seed * 1000 + i, device=device, outliers=(fmt == "Block_FP8")))
+            A.copy_(si.activations_device(M, K, seed=seed * 1000 + i, device=device,
+                                          outliers=spec.get("outliers", False) or fmt == "Block_FP8"))
             # distinct weights per item, or (shared workloads) one copy per
             # (format, layer) and token-count parity: consecutive uses of a
             # copy are separated by the other linears' weights (> L2)
             wkey = (fmt, layer, self.ms.index(M) % 2) if spec["shared"] else i
             if wkey not in weights:
-                W = si.weights_device(N, K, seed=seed * 1000 + len(weights), device=device)
+                wseeds[wkey] = seed * 1000 + len(weights)
+                W = si.weights_device(N, K, seed=wseeds[wkey], device=device)
                 Wq = torch.empty((N, K), dtype=torch.uint8, device=device)
                 if fmt == "Block_FP8":
                     sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device)
@@ -168,7 +182,7 @@ class Workload:
             Aq = torch.empty((M, K), dtype=torch.uint8, device=device)
             Y = self.Y_all[y_off[i]:y_off[i] + M * N * 2].view(torch.bfloat16).view(M, N)
             self.recs.append(dict(fmt=fmt, M=M, layer=layer, N=N, K=K, A=A, Aq=Aq, sa=sa, Wq=Wq, sw=sw, Y=Y,
-                                  variant=variant, split=split, cfg=cfg, ws_need=need))
+                                  variant=variant, split=split, cfg=cfg, ws_need=need, wseed=wseeds[wkey]))
         self.ws = torch.zeros(max(ws_need, 256), dtype=torch.uint8, device=device)
         self.ws_bytes = ws_need
         torch.cuda.synchronize()
@@ -210,43 +224,81 @@ class Workload:
                          r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes,
                          None if fz else r["Aq"], None if fz else r["sa"], None, stream=stream)
 
-    def capture_step(self, stream, recs=None) -> torch.cuda.CUDAGraph:
-        """The whole step (quant + GEMM for every item) as one graph."""
-        self.q.qg_set_launch_flags(self.q.QG_LAUNCH_PDL if self.pdl else 0)
+    def capture_step(self, stream, recs=None, timing_log=None) -> torch.cuda.CUDAGraph:
+        """The whole step (quant + GEMM for every item) as one graph; with a
+        timing log every kernel of the step stamps its slot pair (launch
+        order: each item's quantization kernel, then its GEMM)."""
+        q = self.q
+        q.qg_set_launch_flags(q.QG_LAUNCH_PDL if self.pdl else 0)
+        if timing_log is not None:
+            q.qg_set_timing_log(timing_log, timing_log.numel() // 2)
         g = torch.cuda.CUDAGraph()
         try:
             with torch.cuda.graph(g, stream=stream):
                 for i in range(len(self.recs)):
                     self.enqueue(stream, i, recs)
+            if timing_log is not None and q.qg_timing_log_count() != timing_log.numel() // 2:
+                raise RuntimeError(f"timing log: {q.qg_timing_log_count()} launches, expected "
+                                   f"{timing_log.numel() // 2}")
         finally:
-            self.q.qg_set_launch_flags(0)
+            q.qg_set_launch_flags(0)
+            if timing_log is not None:
+                q.qg_set_timing_log(None, 0)
         return g
 
-    def capture_timed_kernels(self, stream):
-        """The same step with timing events around every GEMM launch (no PDL:
-        the events sit between kernels): around the GEMM kernel alone, with
-        the activation quantization before the first event, or around the
-        one fused kernel.  Returns (graph, event pairs)."""
-        g = torch.cuda.CUDAGraph()
-        evs = []
-        q = self.q
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(len(self.recs)):
-                r = self.recs[i]
-                e0 = torch.cuda.Event(enable_timing=True, external=True)
-                e1 = torch.cuda.Event(enable_timing=True, external=True)
-                if self.fused_item(i):
-                    e0.record(stream)
-                    self.enqueue(stream, i)
-                else:
-                    q.qg_quant_act(r["fmt"], r["A"], r["M"], r["K"], r["K"], r["Aq"], r["sa"], stream=stream)
-                    e0.record(stream)
-                    q.qg_gemm_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["Aq"], r["sa"], r["Wq"], r["sw"], r["Y"],
-                                   r["N"], r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes, None,
-                                   stream=stream)
-                e1.record(stream)
-                evs.append((e0, e1))
-        return g, evs
+    def kernel_roles(self):
+        """(item index, 'quant' | 'gemm' | 'fused') of every kernel of a step, in launch order."""
+        out = []
+        for i in range(len(self.recs)):
+            if self.fused_item(i):
+                out.append((i, "fused"))
+            else:
+                out += [(i, "quant"), (i, "gemm")]
+        return out
+
+
+def timeline(wl, stream, reps: int, direct: bool = False):
+    """Per-kernel times inside the step graph, programmatic dependent launch
+    kept.  Every kernel stamps its earliest CTA start and latest CTA end
+    (%globaltimer) into its slot pair; a kernel's time is from the latest
+    end of the kernels before it to its own end (the first kernel: from its
+    own start), so the times of a step's kernels add up to the step's span.
+    Returns (mean time per kernel in us, mean step span in us)."""
+    roles = wl.kernel_roles()
+    n = len(roles)
+    log = torch.zeros(2 * n, dtype=torch.int64, device=wl.device)
+    q = wl.q
+
+    class _Direct:
+        """The step's kernels launched directly, each with its slot pair."""
+        def replay(self):
+            q.qg_set_launch_flags(q.QG_LAUNCH_PDL if wl.pdl else 0)
+            q.qg_set_timing_log(log, n)
+            try:
+                for i in range(len(wl.recs)):
+                    wl.enqueue(stream, i)
+            finally:
+                q.qg_set_launch_flags(0)
+                q.qg_set_timing_log(None, 0)
+
+    g = _Direct() if direct else wl.capture_step(stream, timing_log=log)
+    start_fill = torch.full((n,), -1, dtype=torch.int64, device=wl.device)  # UINT64_MAX for atomicMin
+    acc = np.zeros(n)
+    span = 0.0
+    for r in range(reps + 3):
+        with torch.cuda.stream(stream):
+            log.view(n, 2)[:, 0].copy_(start_fill)
+            log.view(n, 2)[:, 1].zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        if r < 3:
+            continue
+        t = log.view(n, 2).cpu().numpy().view(np.uint64).astype(np.float64)
+        starts, ends = t[:, 0], t[:, 1]
+        prev = np.maximum.accumulate(np.concatenate([[starts[0]], ends[:-1]]))
+        acc += np.maximum(ends - prev, 0.0)
+        span += ends.max() - starts[0]
+    return acc / reps / 1e3, span / reps / 1e3
 
 
 # ------------------------------------------------------------------- clocks
@@ -493,7 +545,8 @@ def run_reference(args, world, rank):
     w0 = time.perf_counter()
     _oracle_pass(orc, name, 16, cache, cores)                      # calibration (wall time)
     t_pass16 = time.perf_counter() - w0
-    cols, per_step = reference_plan(n_items, t_pass16 / n_items, t_pass16, args.steps + args.warmup)
+    cols, per_step = reference_plan(n_items, t_pass16 / n_items, t_pass16, args.steps + args.warmup,
+                                    budget_s=args.reference_budget_s)
     nxt = 0
 
     def step():
@@ -530,9 +583,11 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--reference-budget-s", type=float, default=REFERENCE_BUDGET_S,
+                    help="wall time of a whole --impl reference run, warm-up included")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--table", default=TABLE, help="tuned config table to load (default: the shipped B300 table)")
@@ -541,6 +596,9 @@ def main(argv=None):
                          "of in their own kernel; measured slower on B300, so not the default")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--launches-only", action="store_true",
+                    help="run the warm-up and timed steps only and print a short line (for a kernel profiler's "
+                         "launch list); no timeline, e2e or CPU legs")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step's kernels directly instead of replaying the captured graph "
                          "(for profilers that cannot follow graph nodes; not used for reported numbers)")
@@ -557,7 +615,6 @@ def main(argv=None):
     wl = Workload(args.workload, device, seed=rank, pdl=not args.no_pdl, fused=args.fused, table=args.table)
     stream = torch.cuda.Stream(device=device)
     graph = wl.capture_step(stream)
-    timed_graph, evs = wl.capture_timed_kernels(stream)
     torch.cuda.synchronize()
 
     if args.no_graph:
@@ -599,36 +656,59 @@ def main(argv=None):
 
     value = world * rate(wl.bytes_step, wl.flops_step, ms_step)
     assert wl.q.qg_device_error() == 0
-
-    # ---- per-launch GEMM durations (timing events inside a second graph)
-    reps = max(20, min(200, args.steps // 10))
-    per = np.zeros(len(wl.recs))
-    for _ in range(3):
-        timed_graph.replay()
-    torch.cuda.synchronize()
-    for _ in range(reps):
-        timed_graph.replay()
-        torch.cuda.synchronize()
-        per += np.array([e0.elapsed_time(e1) for (e0, e1) in evs])
-    per_ms = per / reps
     n_gemm = len(wl.recs)
-    hbm_peak, bf16_peak, peak_kind = load_peaks()
     n_kernels = sum(wl.kernels(i) for i in range(n_gemm))
-    # roofline of the GEMM kernel: algorithmic bytes (HBM-bound decode) or
-    # flops (compute-bound large M) per launch over the mean launch time
+    if args.launches_only:
+        # for a kernel profiler's launch list: the timed steps only
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": round(ms_step, 6), "kernels_per_step": n_kernels,
+                              "launches_only": True}), flush=True)
+        return 0
+
+    # ---- in-chain timeline: each kernel's time inside the step (stamps)
+    reps = max(10, min(100, args.steps))
+    per_kernel_us, span_us = timeline(wl, stream, reps, direct=args.no_graph)
+    assert wl.q.qg_device_error() == 0
+    roles = wl.kernel_roles()
+    gemm_us = np.zeros(n_gemm)   # the GEMM kernel's time (fused: quantize + GEMM)
+    quant_us = np.zeros(n_gemm)  # the activation quantization kernel's time
+    for (i, role), t in zip(roles, per_kernel_us):
+        if role == "quant":
+            quant_us[i] += t
+        else:
+            gemm_us[i] += t
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
+    timing_note = ("in-chain timeline of the step graph (programmatic dependent launch kept): every kernel stamps "
+                   "its first CTA start and last CTA end with %globaltimer; a kernel's time runs from the latest "
+                   "end of the kernels before it to its own end, so the kernels' times add up to the step span")
+    chain = {"step_span_us": round(span_us, 3), "ms_per_step_us": round(ms_step * 1e3, 3),
+             "gemm_us_per_step": round(float(gemm_us.sum()), 3),
+             "quant_us_per_step": round(float(quant_us.sum()), 3)}
+    # roofline of the GEMM kernels: algorithmic bytes (HBM-bound decode) or
+    # flops (compute-bound large M) over their in-chain time
     if hbm:
         units = [gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) +
                  (quant_bytes(r["fmt"], r["M"], r["K"]) if wl.fused_item(i) else 0) for i, r in enumerate(wl.recs)]
         avg_units = sum(units) / n_gemm
-        avg_ms = float(per_ms.sum()) / n_gemm
-        achieved = avg_units / (avg_ms * 1e-3) / 1e9
+        avg_us = float(gemm_us.sum()) / n_gemm
+        achieved = sum(units) / (float(gemm_us.sum()) * 1e-6) / 1e9
         peak = hbm_peak
+        by_fmt = {}
+        for fmt in wl.formats:
+            idx = [i for i, r in enumerate(wl.recs) if r["fmt"] == fmt]
+            b = sum(units[i] for i in idx)
+            ach = b / (float(gemm_us[idx].sum()) * 1e-6) / 1e9
+            by_fmt[fmt] = {"achieved": round(ach, 1), "frac": round(ach / peak, 4),
+                           "gemm_us": round(float(gemm_us[idx].sum()), 3)}
         traffic, traffic_note = measured_traffic(args.workload, wl.fused)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_note": traffic_note,
                 "kernel": ("fused quantize+gemm" if wl.fused else "gemm") + " (" + "+".join(wl.formats) + ")",
-                "peak_kind": peak_kind, "avg_launch_us": round(avg_ms * 1e3, 3),
-                "avg_bytes_per_launch": round(avg_units)}
+                "peak_kind": peak_kind, "avg_launch_us": round(avg_us, 3),
+                "avg_bytes_per_launch": round(avg_units), "by_format": by_fmt, "timing": timing_note,
+                "chain": chain,
+                "step_frac": round(value / world / peak, 4)}
     else:
         # the E4M3 GEMMs (the dominant kernels) against the kind::f8f6f4 peak;
         # every format's own figure follows
@@ -636,18 +716,18 @@ def main(argv=None):
         for fmt in wl.formats:
             idx = [i for i, r in enumerate(wl.recs) if r["fmt"] == fmt]
             fl = sum(2 * wl.recs[i]["M"] * wl.recs[i]["N"] * wl.recs[i]["K"] for i in idx)
-            t = float(per_ms[idx].sum())
-            ach = fl / (t * 1e-3) / 1e12
+            t = float(gemm_us[idx].sum())
+            ach = fl / (t * 1e-6) / 1e12
             pk = tensor_peak(fmt, bf16_peak)
-            by_fmt[fmt] = {"achieved": round(ach, 1), "peak": round(pk, 1), "frac": round(ach / pk, 4)}
+            by_fmt[fmt] = {"achieved": round(ach, 1), "peak": round(pk, 1), "frac": round(ach / pk, 4),
+                           "gemm_us": round(t, 3)}
         main_fmt = "FP8_Dynamic" if "FP8_Dynamic" in by_fmt else wl.formats[0]
-        fl_all = wl.flops_step
-        avg_ms = float(per_ms.sum()) / n_gemm
+        avg_us = float(gemm_us.sum()) / n_gemm
         roof = {"bound": "tensor", "achieved": by_fmt[main_fmt]["achieved"], "peak": by_fmt[main_fmt]["peak"],
                 "unit": "TFLOP/s", "frac": by_fmt[main_fmt]["frac"], "traffic": None,
                 "kernel": f"gemm ({main_fmt})", "peak_kind": peak_kind + " bf16 x nominal kind ratio",
-                "by_format": by_fmt, "avg_launch_us": round(avg_ms * 1e3, 3),
-                "avg_flops_per_launch": round(fl_all / n_gemm)}
+                "by_format": by_fmt, "avg_launch_us": round(avg_us, 3),
+                "avg_flops_per_launch": round(wl.flops_step / n_gemm), "timing": timing_note, "chain": chain}
 
     # ---- end to end through the C ABI: pinned host activations in, outputs out.
     # Two buffer sets and two graphs: while step i's kernels run, a copy
@@ -716,9 +796,10 @@ def main(argv=None):
         cpu = cpu_oracle_leg(args.workload)
 
     per_gemm = [{"fmt": r["fmt"], "M": r["M"], "layer": r["layer"], "N": r["N"], "K": r["K"],
-                 "variant": r["variant"], "split_k": r["split"], "us": round(float(per_ms[i]) * 1e3, 3),
-                 "GBps": round(gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) / (per_ms[i] * 1e-3) / 1e9, 1),
-                 "TFLOPs": round(2 * r["M"] * r["N"] * r["K"] / (per_ms[i] * 1e-3) / 1e12, 2)}
+                 "variant": r["variant"], "split_k": r["split"], "us": round(float(gemm_us[i]), 3),
+                 "quant_us": round(float(quant_us[i]), 3),
+                 "GBps": round(gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) / (max(gemm_us[i], 1e-3) * 1e-6) / 1e9, 1),
+                 "TFLOPs": round(2 * r["M"] * r["N"] * r["K"] / (max(gemm_us[i], 1e-3) * 1e-6) / 1e12, 2)}
                 for i, r in enumerate(wl.recs)]
     if rank == 0:
         unit = "GB/s" if hbm else "TFLOP/s"

@@ -235,9 +235,12 @@ QG_API int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* 
  *   Limit: a shape whose scratch (qg_workspace_bytes) exceeds
  *   QG_NOALLOC_SCRATCH_BYTES is rejected with QG_ERR_WORKSPACE_TOO_SMALL;
  *   use fewer splits, or qg_gemm_w8a8 with a caller workspace.
- *   Set-up: the first call on a device looks up the array's device address
- *   with that device current (cudaGetSymbolAddress); make that first call
- *   before any stream capture.  It never calls cudaMalloc / cudaFree.
+ *   Set-up: the first call in each CUDA context (normally once per device,
+ *   in its primary context) looks up the array's device address with the
+ *   caller's device current (cudaGetSymbolAddress) and keeps it for that
+ *   context; make that first call before any stream capture, and again
+ *   after a cudaDeviceReset (the new context has the array at another
+ *   address).  It never calls cudaMalloc / cudaFree.
  *   Sharing: every call uses the same array, which keeps the last call's
  *   contents; each call clears the tile counters (cudaMemsetAsync on
  *   `stream`) before its kernel.  Calls whose kernels overlap on the GPU
@@ -297,6 +300,28 @@ QG_API int qg_set_force_timeout(int on);
  * counters: run qg_workspace_init on it before its next use
  * (qg_gemm_w8a8_noalloc clears its own counters on every call). */
 QG_API int qg_device_error(int* code);
+
+/* Launch timing inside a stream or a captured graph, where timing events
+ * would sit between kernels and break programmatic dependent launch.  While
+ * a log is set, every kernel launch of qg_quant_act, qg_gemm_w8a8 and the
+ * entry points built on them takes the next slot pair of the log, in launch
+ * order: log_dev[2*i] receives the earliest CTA start and log_dev[2*i + 1]
+ * the latest CTA end of launch i, in %globaltimer nanoseconds (atomicMin /
+ * atomicMax: the caller fills the start slots with UINT64_MAX and the end
+ * slots with 0 before the launches run, e.g. before every graph replay).
+ * Launches beyond `slots` pairs, and every launch while no log is set, are
+ * not timed and cost nothing extra.  A graph captured while the log is set
+ * keeps writing its slots on every replay.
+ *   log_dev  device array of 2 * slots uint64, owned by the caller, or NULL
+ *            to turn the log off;  slots >= 0.
+ * Setting a log (or NULL) restarts the slot count at 0.  The log is
+ * process-wide, like the settings above.  Errors: QG_ERR_INVALID_ARG for
+ * slots < 0 or an unaligned log. */
+QG_API int qg_set_timing_log(uint64_t* log_dev, int slots);
+
+/* Slot pairs handed out since the last qg_set_timing_log (may exceed the
+ * log's capacity: the launches past it were not timed). */
+QG_API int qg_timing_log_count(void);
 
 /* Thread-local description of the last failure (never NULL). */
 QG_API const char* qg_last_error(void);

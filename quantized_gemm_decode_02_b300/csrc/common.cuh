@@ -26,6 +26,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Optional launch timing (a null `ts` turns it off): ts[0] collects the
+// earliest CTA start and ts[1] the latest CTA end of one launch, both in
+// %globaltimer nanoseconds, one 64-bit atomic per CTA for each.  The start
+// stamp is taken by thread 0 on entry; the end stamp after a barrier of the
+// whole CTA, so every thread of a CTA that calls it must reach it.
+__device__ __forceinline__ void stamp_start(unsigned long long* ts) {
+  if (ts != nullptr && threadIdx.x == 0) atomicMin(ts, static_cast<unsigned long long>(global_timer_ns()));
+}
+__device__ __forceinline__ void stamp_end(unsigned long long* ts) {
+  if (ts == nullptr) return;
+  __syncthreads();
+  if (threadIdx.x == 0) atomicMax(ts + 1, static_cast<unsigned long long>(global_timer_ns()));
+}
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(

@@ -71,6 +71,7 @@ struct GemmArgs {
   float* s_a_out;          // per-token scales, or null
   uint64_t wait_ns;     // bound of every pipeline wait
   int force_timeout;    // test hook: the MMA thread first waits on a barrier nothing arrives on
+  unsigned long long* tstamp;  // launch timing slot pair (stamp_start / stamp_end), or null
 };
 
 constexpr int kBN = 128;         // weight rows per tile (and Block_FP8 block size)
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr uint32_t kTmemCols = pow2_cols(NBUF * MPAD);
   static_assert(kTmemCols <= 256, "two CTAs per SM share the 512 TMEM columns");
 
+  stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
@@ -666,6 +668,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (nn < g.N) out(m, r, nn, sum);
         });
       }
+    } else {
+      // the producer and MMA warps pair their early arrive with a wait too
+      // (every peer arrived right after its set-up, so this returns at once)
+      cluster_wait();
     }
   } else if (warp >= 2 && !abort) {
     const bool n_ok = n < g.N;
@@ -704,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
+  stamp_end(g.tstamp);
 }
 
 // ----------------------------------------------------------- Standard --
@@ -725,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTmemCols = pow2_cols(NBUF * kBufCols + (BLOCK ? kBN : 0));
   static_assert(kTmemCols <= 512, "TMEM budget");
 
+  stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
@@ -961,6 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  stamp_end(g.tstamp);
 }
 
 }  // namespace qg

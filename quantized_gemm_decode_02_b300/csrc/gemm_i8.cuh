@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = I8Shape<MPAD>;
   constexpr int kHalf = S::kHalf;
+  stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
@@ -480,6 +481,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
           if (nn < g.N) finish(m, r, nn, sum);
         });
       }
+    } else if (!(FUSED && warp >= kI8AWarp)) {
+      // the other warps pair their early arrive with a wait too (every peer
+      // arrived right after its set-up, so this returns at once); the fused
+      // quantizer warps waited before their row-maximum exchange
+      cluster_wait();
     }
   } else if (holds_acc && !abort) {
     const bool n_ok = n < g.N;
@@ -519,6 +525,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       }
     }
   }
+  stamp_end(g.tstamp);
 }
 
 }  // namespace qg

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kDpThreads, 2)
     gemm_i8_dp4a_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   static_assert(MT == 1 || MT == 2 || MT == 4 || MT == 8, "MT");
   constexpr int MV = MT < 4 ? 4 : MT;  // accumulators padded to the 4-token groups of the cluster exchange
+  stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
@@ -223,6 +224,10 @@ __global__ void __launch_bounds__(kDpThreads, 2)
           if (nn < g.N) finish(m, r, nn, sum);
         });
       }
+    } else {
+      // the other warps pair their early arrive with a wait too (every peer
+      // arrived right after its set-up, so this returns at once)
+      cluster_wait();
     }
   } else if (holds_acc && !abort) {
     const bool n_ok = n < g.N;
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(kDpThreads, 2)
       }
     }
   }
+  stamp_end(g.tstamp);
 }
 
 }  // namespace qg

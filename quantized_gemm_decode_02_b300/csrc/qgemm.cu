@@ -51,6 +51,17 @@ std::atomic<int> g_launch_flags{0};
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 std::atomic<int> g_force_timeout{0};
 bool g_allow_default = false;
+// launch timing log (qg_set_timing_log): slot pairs handed out in launch order
+std::atomic<unsigned long long*> g_ts_log{nullptr};
+std::atomic<int> g_ts_cap{0};
+std::atomic<int> g_ts_next{0};
+
+unsigned long long* next_ts_slot() {
+  unsigned long long* log = g_ts_log.load(std::memory_order_relaxed);
+  if (!log) return nullptr;
+  const int i = g_ts_next.fetch_add(1, std::memory_order_relaxed);
+  return i < g_ts_cap.load(std::memory_order_relaxed) ? log + 2 * static_cast<int64_t>(i) : nullptr;
+}
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -521,6 +532,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   g.force_timeout = g_force_timeout.load(std::memory_order_relaxed);
   g.l2_prefetch = (config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  g.tstamp = next_ts_slot();
 
   const bool fz = fused != nullptr;
   if (p.dp4a) {
@@ -556,23 +568,70 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[QG_NOALLOC_SCRA
 namespace {
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
+// The scratch array's device address belongs to one CUDA context (a reset
+// device or a caller's own context loads the library's module again, at
+// another address), so the looked-up address is cached per context, keyed on
+// the context's process-unique ID (cuCtxGetId), never on the device ordinal.
+struct NoallocEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+std::vector<NoallocEntry> g_noalloc_cache;
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
+}
+
+// ID of the calling thread's current context (0 when none is current yet).
+int current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  });
+  if (!get_current || !get_id) return fail(QG_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId entry points unavailable");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return fail(QG_ERR_CUDA, "cuCtxGetCurrent failed");
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return fail(QG_ERR_CUDA, "cuCtxGetId failed");
+  return QG_OK;
+}
+
+// Device address of g_noalloc_scratch in the current context, looked up
+// (cudaGetSymbolAddress) the first time a context calls, with the caller's
+// device current.
 int noalloc_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(QG_ERR_INVALID_ARG, "device index %d unsupported", dev);
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
-    g_noalloc_addr[dev] = p;
-  }
-  *out = g_noalloc_addr[dev];
+  unsigned long long id = 0;
+  int rc = current_ctx_id(&id);
+  if (rc != QG_OK) return rc;
+  if (id != 0)
+    for (const NoallocEntry& e : g_noalloc_cache)
+      if (e.ctx_id == id) {
+        *out = e.addr;
+        return QG_OK;
+      }
+  // first call in this context (or no context yet: the lookup makes the
+  // device's primary context current)
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+  rc = current_ctx_id(&id);
+  if (rc != QG_OK) return rc;
+  if (id == 0) return fail(QG_ERR_CUDA, "no current CUDA context after the symbol lookup");
+  g_noalloc_cache.push_back(NoallocEntry{id, p});
+  *out = p;
   return QG_OK;
 }
 
@@ -613,6 +672,16 @@ int qg_set_wait_limit_ns(uint64_t ns) {
   g_wait_ns.store(ns ? ns : 2000000000ull, std::memory_order_relaxed);
   return QG_OK;
 }
+int qg_set_timing_log(uint64_t* log_dev, int slots) {
+  if (slots < 0) return fail(QG_ERR_INVALID_ARG, "slots=%d < 0", slots);
+  if (log_dev && !aligned(log_dev, 8)) return fail(QG_ERR_INVALID_ARG, "timing log must be 8-byte aligned");
+  g_ts_log.store(nullptr, std::memory_order_relaxed);
+  g_ts_cap.store(log_dev ? slots : 0, std::memory_order_relaxed);
+  g_ts_next.store(0, std::memory_order_relaxed);
+  g_ts_log.store(reinterpret_cast<unsigned long long*>(log_dev), std::memory_order_relaxed);
+  return QG_OK;
+}
+int qg_timing_log_count(void) { return g_ts_next.load(std::memory_order_relaxed); }
 int qg_set_force_timeout(int on) {
   g_force_timeout.store(on ? 1 : 0, std::memory_order_relaxed);
   return QG_OK;
@@ -650,12 +719,13 @@ int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_t lda, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(A_dev);
   uint8_t* Q = static_cast<uint8_t*>(A_q_dev);
+  unsigned long long* ts = next_ts_slot();
   cudaError_t e;
   if (fmt == QG_BLOCK_FP8) {
     constexpr int W = 8;
     const int64_t groups = M * (K / 128);
     e = launch(qg::quant_groups_kernel<W>, dim3(static_cast<unsigned>(cdiv(groups, W))), dim3(W * 32), 0, s, A, lda,
-               static_cast<int>(M), static_cast<int>(K), Q, s_a_dev);
+               static_cast<int>(M), static_cast<int>(K), Q, s_a_dev, ts);
   } else if (K <= 512 * 8 * 8) {
     // rows held in registers: 1, 2, 4 or 8 chunks of 8 values per thread
     const int ch = K <= 4096 ? 1 : (K <= 8192 ? 2 : (K <= 16384 ? 4 : 8));
@@ -664,23 +734,23 @@ int qg_quant_act(int fmt, const void* A_dev, int64_t M, int64_t K, int64_t lda, 
     const dim3 grid(static_cast<unsigned>(M)), block(512);
     const int k = static_cast<int>(K);
     if (ch == 1)
-      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 1>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
-              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 1>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 1>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 1>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts);
     else if (ch == 2)
-      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 2>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
-              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 2>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 2>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 2>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts);
     else if (ch == 4)
-      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 4>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
-              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 4>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 4>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 4>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts);
     else
-      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 8>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax)
-              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 8>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax);
+      e = fp8 ? launch(qg::quant_rows_reg_kernel<qg::kFmtFP8, 8>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts)
+              : launch(qg::quant_rows_reg_kernel<qg::kFmtINT8, 8>, grid, block, 0, s, A, lda, k, Q, s_a_dev, qmax, ts);
   } else if (fmt == QG_FP8_DYNAMIC) {
     e = launch(qg::quant_rows_kernel<__nv_bfloat16, qg::kFmtFP8, 512>, dim3(static_cast<unsigned>(M)), dim3(512), 0, s,
-               A, lda, static_cast<int>(K), Q, s_a_dev, 448.0f);
+               A, lda, static_cast<int>(K), Q, s_a_dev, 448.0f, ts);
   } else {
     e = launch(qg::quant_rows_kernel<__nv_bfloat16, qg::kFmtINT8, 512>, dim3(static_cast<unsigned>(M)), dim3(512), 0,
-               s, A, lda, static_cast<int>(K), Q, s_a_dev, 127.0f);
+               s, A, lda, static_cast<int>(K), Q, s_a_dev, 127.0f, ts);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quant_act launch");
   return QG_OK;
@@ -738,10 +808,10 @@ int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q
                dim3(256), 0, s, W_dev, static_cast<int>(N), static_cast<int>(K), Q, s_w_dev);
   } else if (fmt == QG_FP8_DYNAMIC) {
     e = launch(qg::quant_rows_kernel<float, qg::kFmtFP8, 256>, dim3(static_cast<unsigned>(N)), dim3(256), 0, s, W_dev,
-               K, static_cast<int>(K), Q, s_w_dev, 448.0f);
+               K, static_cast<int>(K), Q, s_w_dev, 448.0f, nullptr);
   } else {
     e = launch(qg::quant_rows_kernel<float, qg::kFmtINT8, 256>, dim3(static_cast<unsigned>(N)), dim3(256), 0, s, W_dev,
-               K, static_cast<int>(K), Q, s_w_dev, 127.0f);
+               K, static_cast<int>(K), Q, s_w_dev, 127.0f, nullptr);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quant_weight launch");
   return QG_OK;

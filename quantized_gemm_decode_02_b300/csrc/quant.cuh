@@ -110,7 +110,8 @@ __device__ __forceinline__ float warp_max(float v) {
 template <typename InT, int OUT, int THREADS>
 __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const InT* __restrict__ X, int64_t ldx, int K,
                                                             uint8_t* __restrict__ Q, float* __restrict__ S,
-                                                            float qmax) {
+                                                            float qmax, unsigned long long* ts) {
+  stamp_start(ts);
   // Let the next kernel (a GEMM that first streams its static weights) be
   // scheduled now; this kernel's own inputs are read only after the wait.
   pdl_launch_dependents();
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const InT* __restri
     load8(x + k, v);
     *reinterpret_cast<uint2*>(q + k) = encode8<OUT>(v, s);
   }
+  stamp_end(ts);
 }
 
 // Activation rows (bf16) up to 512 x 8 x CH elements: one CTA per row, each
@@ -152,8 +154,9 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const InT* __restri
 template <int OUT, int CH>
 __global__ void __launch_bounds__(512) quant_rows_reg_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int K,
                                                              uint8_t* __restrict__ Q, float* __restrict__ S,
-                                                             float qmax) {
+                                                             float qmax, unsigned long long* ts) {
   constexpr int kThreads = 512;
+  stamp_start(ts);
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float red[kThreads / 32];
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(512) quant_rows_reg_kernel(const __nv_bfloat16
     }
     *reinterpret_cast<uint2*>(q + k) = make_uint2(w[0], w[1]);
   }
+  stamp_end(ts);
 }
 
 // Block_FP8 activations: one warp per 1x128 group (32 lanes x 4 values).
@@ -210,29 +214,32 @@ __global__ void __launch_bounds__(512) quant_rows_reg_kernel(const __nv_bfloat16
 template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) quant_groups_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
                                                                  int rows, int K, uint8_t* __restrict__ Q,
-                                                                 float* __restrict__ S) {
+                                                                 float* __restrict__ S, unsigned long long* ts) {
+  stamp_start(ts);
   // Let the next kernel (a GEMM that first streams its static weights) be
   // scheduled now; this kernel's own inputs are read only after the wait.
   pdl_launch_dependents();
   pdl_wait();
   const int groups = K / 128;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
-  if (gid >= static_cast<int64_t>(rows) * groups) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t r = gid / groups;
-  const int g = static_cast<int>(gid % groups);
-  const __nv_bfloat16* x = X + r * ldx + g * 128 + lane * 4;
-  uint2 u = *reinterpret_cast<const uint2*>(x);
-  float v[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                __uint_as_float(u.y & 0xFFFF0000u)};
-  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-  amax = warp_max(amax);
-  const float s = scale_from_amax(amax, 448.0f);
-  if (lane == 0) S[r * groups + g] = s;
-  uint16_t lo = e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
-  uint16_t hi = e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
-  *reinterpret_cast<uint32_t*>(Q + r * static_cast<int64_t>(K) + g * 128 + lane * 4) =
-      static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  if (gid < static_cast<int64_t>(rows) * groups) {  // (no early return: the end stamp is a CTA barrier)
+    const int lane = threadIdx.x & 31;
+    const int64_t r = gid / groups;
+    const int g = static_cast<int>(gid % groups);
+    const __nv_bfloat16* x = X + r * ldx + g * 128 + lane * 4;
+    uint2 u = *reinterpret_cast<const uint2*>(x);
+    float v[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                  __uint_as_float(u.y & 0xFFFF0000u)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = warp_max(amax);
+    const float s = scale_from_amax(amax, 448.0f);
+    if (lane == 0) S[r * groups + g] = s;
+    uint16_t lo = e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
+    uint16_t hi = e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
+    *reinterpret_cast<uint32_t*>(Q + r * static_cast<int64_t>(K) + g * 128 + lane * 4) =
+        static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  stamp_end(ts);
 }
 
 // Block_FP8 weights: one CTA of 256 threads per 128x128 block of W[N, K]

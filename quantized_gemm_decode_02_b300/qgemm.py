@@ -41,7 +41,8 @@ def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False) -> int:
 EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_check_config", "qg_workspace_init", "qg_gemm_w8a8",
            "qg_linear_w8a8", "qg_gemm_w8a8_noalloc", "qg_gemm_w8a8_grouped", "qg_workspace_bytes_grouped",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
-           "qg_set_force_timeout", "qg_device_error", "qg_last_error", "qg_version")
+           "qg_set_force_timeout", "qg_set_timing_log", "qg_timing_log_count", "qg_device_error", "qg_last_error",
+           "qg_version")
 
 
 class QGError(RuntimeError):
@@ -74,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qg_set_launch_flags.argtypes = [I]
     lib.qg_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.qg_set_force_timeout.argtypes = [I]
+    lib.qg_set_timing_log.argtypes = [P, I]
+    lib.qg_timing_log_count.argtypes = []
     lib.qg_device_error.argtypes = [ctypes.POINTER(I)]
     lib.qg_last_error.restype = ctypes.c_char_p
     lib.qg_version.restype = ctypes.c_char_p
@@ -211,6 +214,17 @@ def qg_set_wait_limit_ns(ns: int) -> None:
 
 def qg_set_force_timeout(on: bool) -> None:
     _check(_lib.qg_set_force_timeout(1 if on else 0), "qg_set_force_timeout")
+
+
+def qg_set_timing_log(log, slots: int) -> None:
+    """Give every following launch a slot pair of `log` (uint64 device
+    tensor of 2 * slots: earliest CTA start, latest CTA end); None turns
+    the log off."""
+    _check(_lib.qg_set_timing_log(_ptr(log), slots), "qg_set_timing_log")
+
+
+def qg_timing_log_count() -> int:
+    return int(_lib.qg_timing_log_count())
 
 
 def qg_device_error() -> int:

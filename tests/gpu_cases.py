@@ -8,7 +8,17 @@ Tolerances (the accuracy contract of the path, restated):
     bf16 ulp of the oracle (the GPU epilogue rounds three times in fp32, the
     oracle once from the exact value);
   * FP8_Dynamic / Block_FP8: |Y_gpu - y_exact| <= 8e-3 * magnitude, where the
-    magnitude is s_a*s_w*sum_k|a_q*w_q| (per 128-K group for Block_FP8).
+    magnitude is s_a*s_w*sum_k|a_q*w_q| (per 128-K group for Block_FP8);
+    and the tight bound that the arithmetic gives:
+        |Y_gpu - y_exact| <= 2^-8 * |y_exact| + (K/16 + 8 + S) * 2^-23 * magnitude
+    (one bf16 rounding of the fp32 result; E4M3 products are exact in fp32,
+    and each fp32 addition that forms the sum -- one per MMA instruction of
+    K = 32 into the accumulator, one per Block_FP8 promotion of a 128-K
+    group with its fp32 scale product, one per Split-K partial, a few for
+    the adder tree inside an instruction and the scale multiplications --
+    is counted as one rounding of at most 2^-23 of the magnitude), plus the
+    whole-output check that the relative RMS error stays within 2^-8, the
+    size of a bf16 rounding: a scale that is 1% off fails both.
 """
 from __future__ import annotations
 
@@ -19,6 +29,7 @@ import seeded_inputs as si
 from quantized_gemm_decode_02_b300 import qgemm as q
 
 FP8_BOUND = 8e-3
+MAX_SPLITS = 32  # Split-K partials added in any test configuration (the tight bound's S)
 
 DEV = "cuda:0"
 
@@ -116,6 +127,21 @@ def check_gemm(orc, fmt, oAq, osa, oWq, osw, Y, dbg=None, ns=None):
     bad = err > bound
     assert not np.isnan(got).any(), "NaN in output (unwritten element?)"
     assert not bad.any(), f"{bad.sum()} elements outside bound; worst ratio {np.max(err / np.maximum(bound, 1e-300)):.3g}"
+    check_fp8_tight(exact, got, mag, oAq.shape[1])
+
+
+def check_fp8_tight(exact, got, mag, K, splits=MAX_SPLITS):
+    """The tight FP8 bound of the module docstring, element by element, and
+    the relative RMS error of the whole output."""
+    err = np.abs(got - exact)
+    tight = 2.0 ** -8 * np.abs(exact) + (K / 16 + 8 + splits) * 2.0 ** -23 * mag
+    bad = err > tight
+    assert not bad.any(), (f"{bad.sum()} elements outside the tight bound; worst ratio "
+                           f"{np.max(err / np.maximum(tight, 1e-300)):.3g}")
+    ss = float((exact ** 2).sum())
+    if ss > 0:
+        rms = float(np.sqrt((err ** 2).sum() / ss))
+        assert rms <= 2.0 ** -8, f"relative RMS error {rms:.3g} above 2^-8"
 
 
 def run_case(orc, fmt, M, N, K, variant, split_k, seed=0, outliers=False, config_id=0, debug=True):

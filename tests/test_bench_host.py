@@ -35,7 +35,7 @@ def test_reference_plan_fits_the_budget(bench, runs, t_pass16):
 def test_reference_arm_prints_the_contract_line(bench):
     out = io.StringIO()
     with redirect_stdout(out):
-        rc = bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"])
+        rc = bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3", "--reference-budget-s", "10"])
     assert rc == 0
     line = json.loads(out.getvalue().strip().splitlines()[-1])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
@@ -47,10 +47,11 @@ def test_reference_arm_prints_the_contract_line(bench):
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == bench.DEFAULT_WORKLOAD
     assert not {"model", "models", "global_batch", "seq_len"} & set(line["config"])  # a workload, not a model
-    assert line["config"]["shapes_k_n"]["Qwen3-1.7B down"] == [6144, 2048]
+    assert line["config"]["shapes_k_n"]["Qwen3-8B down"] == [12288, 4096]
+    assert line["config"]["formats"] == ["Block_FP8", "FP8_Dynamic", "W8A8_INT8"]
 
 
 def test_cpu_baseline_leg_reports_a_bounded_sample(bench):
     r = bench.cpu_oracle_leg(bench.DEFAULT_WORKLOAD, budget_s=0.5)
     assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] >= 1
-    assert "all 28 (format, M, layer) items" in r["sample"]
+    assert "all 384 (format, M, layer) items" in r["sample"]

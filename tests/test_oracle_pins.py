@@ -504,3 +504,61 @@ def test_abs_magnitude_bounds_the_accumulator(orc):
         if fmt == "FP8_Dynamic":
             ref = (np.abs(tv[Aq]) @ np.abs(tv[Wq]).T) * sa[:, None].astype(np.float64) * sw[None, :].astype(np.float64)
             assert np.allclose(mag, ref, rtol=1e-13)
+
+
+def _blocky_inputs(M, N, K, seed):
+    """Activations and weights whose 1x128 groups and 128x128 blocks have
+    clearly different magnitudes (factor 1 + group / block index), so that a
+    scale taken from the wrong group or block changes the result by several
+    percent."""
+    A = si.bf16_to_f32_numpy(si.activations(M, K, seed=seed))
+    A = A * np.repeat(1.0 + np.arange((K + 127) // 128), 128)[None, :K].astype(np.float32)
+    A = si.bf16_to_f32_numpy(torch.from_numpy(A.astype(np.float32)).to(torch.bfloat16))
+    W = si.weights(N, K, seed=seed + 1)
+    fac = (1.0 + 2.0 * np.arange((N + 127) // 128))[:, None] * (1.0 + 0.5 * np.arange((K + 127) // 128))[None, :]
+    W = (W * np.repeat(np.repeat(fac, 128, 0), 128, 1)[:N, :K]).astype(np.float32)
+    return A, W
+
+
+def test_block_abs_magnitude_equals_exact_rationals(orc):
+    # Fraction brute force of the magnitude the Block_FP8 bound multiplies,
+    # sum_kb s_a[m,kb] * s_w[n/128,kb] * sum_{k in kb} |a_q * w_q|, term by
+    # term from independent decode tables (ragged N: the third block row
+    # has 44 rows)
+    M, N, K = 2, 300, 384
+    A, W = _blocky_inputs(M, N, K, seed=93)
+    Aq, sa = orc.quant_act("Block_FP8", A)
+    Wq, sw = orc.quant_weight("Block_FP8", W)
+    ns = np.array([0, 127, 128, 200, 255, 256, 299])
+    mag = orc.abs_magnitude("Block_FP8", Aq, sa, Wq, sw, ns=ns)
+    for m in range(M):
+        for j, n in enumerate(ns):
+            exact = Fraction(0)
+            for kb in range(K // 128):
+                part = sum(abs(_frac_e4m3(int(Aq[m, k])) * _frac_e4m3(int(Wq[n, k])))
+                           for k in range(kb * 128, kb * 128 + 128))
+                exact += Fraction(float(sa[m, kb])) * Fraction(float(sw[n // 128, kb])) * part
+            assert abs(Fraction(float(mag[m, j])) - exact) <= exact * Fraction(1, 2 ** 45)
+
+
+def test_block_abs_magnitude_per_block_numpy(orc):
+    # the same magnitude from numpy, one 128-K group at a time with that
+    # group's activation scale and the weight scale of the row's block
+    M, N, K = 3, 300, 512
+    A, W = _blocky_inputs(M, N, K, seed=95)
+    Aq, sa = orc.quant_act("Block_FP8", A)
+    Wq, sw = orc.quant_weight("Block_FP8", W)
+    assert len(np.unique(sw)) == sw.size               # every block has its own scale
+    tv = np.abs(torch_e4m3_values())
+    ref = np.zeros((M, N))
+    for kb in range(K // 128):
+        ks = slice(kb * 128, kb * 128 + 128)
+        part = tv[Aq[:, ks]] @ tv[Wq[:, ks]].T                           # [M, N]
+        coef = sa[:, kb].astype(np.float64)[:, None] * sw[np.arange(N) // 128, kb].astype(np.float64)[None, :]
+        ref += coef * part
+    mag = orc.abs_magnitude("Block_FP8", Aq, sa, Wq, sw)
+    assert np.allclose(mag, ref, rtol=1e-13, atol=0)
+    # a plausible slip, a per-channel magnitude (one scale per row and column),
+    # is far from it
+    wrong = (tv[Aq] @ tv[Wq].T) * sa[:, :1].astype(np.float64) * sw[np.arange(N) // 128, :1].T.astype(np.float64)
+    assert np.max(np.abs(wrong - ref) / ref) > 0.05

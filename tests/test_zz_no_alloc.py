@@ -78,6 +78,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(orc, gc, q, fmt):
 
 def test_noalloc_without_split_k(orc, gc, q):
     fmt, M, N, K = "W8A8_INT8", 5, 260, 1024
+    # no Split-K, and Split-K reduced inside a thread-block cluster, need no scratch
+    assert q.qg_workspace_bytes(fmt, M, N, K, q.QG_SWAPAB, 1) == 0
+    assert q.qg_workspace_bytes(fmt, M, N, K, q.QG_SWAPAB_SPLITK, 4) == 0
     Aq, sa, Wq, sw = _inputs(gc, fmt, M, N, K, seed=32)
     Y_ref, dbg_ref = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, q.QG_SWAPAB, 1, debug=True)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=gc.DEV)
