@@ -78,6 +78,7 @@ typedef enum {
 #define QG_CONFIG_PREFETCH_MASK (127 << 5)
 #define QG_CONFIG_MAX_PREFETCH 64
 #define QG_CONFIG_WIDE (1 << 12)
+#define QG_CONFIG_MMA_SYNC (1 << 13)
 
 typedef enum {
   QG_OK = 0,
@@ -149,7 +150,15 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      off; at most QG_CONFIG_MAX_PREFETCH); plus
  *                      QG_CONFIG_WIDE for FP8_Dynamic with QG_STANDARD /
  *                      QG_SPLITK: 256 weight rows per tile (MMA N = 256)
- *                      instead of 128 (QG_ERR_INVALID_ARG elsewhere);
+ *                      instead of 128 (QG_ERR_INVALID_ARG elsewhere); plus
+ *                      QG_CONFIG_MMA_SYNC for W8A8_INT8 with QG_SWAPAB /
+ *                      QG_SWAPAB_SPLITK: the int8 products run on the
+ *                      warp-level tensor-core instructions (mma.sync, the
+ *                      operands widened to f16 in registers, token blocks
+ *                      of up to 32) instead of tcgen05 with the widened
+ *                      weights in tensor memory; same exact int32 result
+ *                      (QG_ERR_INVALID_ARG elsewhere, and in the one-kernel
+ *                      form of qg_linear_w8a8, which then runs two kernels);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

@@ -108,6 +108,15 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int c0
                "r"(c0), "r"(c1)
                : "memory");
 }
+// Bulk L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned
+// global address: a hint that returns no data.  Issued before a dependency
+// wait it is safe even if the producer still writes the range: L2 is the
+// point of coherence, so later writes update the prefetched lines and the
+// reads after the wait see them.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -24,6 +24,7 @@
 #include "gemm_f8.cuh"
 #include "gemm_i8.cuh"
 #include "gemm_i8_dp4a.cuh"
+#include "gemm_i8_mma.cuh"
 #include "quant.cuh"
 
 namespace {
@@ -185,21 +186,37 @@ struct Plan {
   int groups = 1;      // grouped launches: grid z
   bool swap = false;
   bool dp4a = false;   // W8A8_INT8 Swap-AB on the CUDA cores (M <= 8)
-  int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64
+  bool mma = false;    // W8A8_INT8 Swap-AB on mma.sync (QG_CONFIG_MMA_SYNC)
+  int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64 (mma.sync: 8 / 16 / 24 / 32)
+  int ctr_tiles = 0;   // Split-K arrival counters of one group: enough for every kernel's token blocks
   int n_tiles = 0, m_tiles = 0, kt = 0, splits = 1;
   int reduce = qg::kReduceNone;  // how split partials are summed
 };
 
 int64_t ws_counter_bytes(int64_t tiles) { return cdiv(tiles * 4, 256) * 256; }
 
-int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, Plan* p) {
+int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, int config_id, Plan* p) {
   p->dp4a = (variant == QG_SWAPAB_DP4A || variant == QG_SWAPAB_DP4A_SPLITK);
   p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->dp4a;
+  p->mma = (config_id & QG_CONFIG_MMA_SYNC) != 0;
   if (p->dp4a && (fmt != QG_W8A8_INT8 || M > qg::kDpMaxTokens))
     return fail(QG_ERR_UNSUPPORTED_SHAPE, "the dp4a variants take W8A8_INT8 with M <= %d", qg::kDpMaxTokens);
+  if (p->mma && (fmt != QG_W8A8_INT8 || !p->swap || p->dp4a))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
   p->kt = static_cast<int>(cdiv(K, 128));
   p->n_tiles = static_cast<int>(cdiv(N, 128));
-  if (p->swap) {
+  // counters for blocks of 16 tokens cover every kernel's token blocking
+  // (16 / 32 / 64, mma.sync 8..32, Standard 128), so qg_workspace_bytes needs
+  // no config_id
+  const int64_t ctr = cdiv(N, 128) * cdiv(M, 16);
+  if (ctr > 0x7FFFFFFF) return fail(QG_ERR_UNSUPPORTED_SHAPE, "too many output tiles");
+  p->ctr_tiles = static_cast<int>(ctr);
+  if (p->mma) {
+    // token groups of 8 on the MMA N side; more than 32 tokens run as blocks of 32
+    p->mpad = M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 24 ? 24 : 32));
+    p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
+    if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
+  } else if (p->swap) {
     // tokens padded to the MMA N side; more than 64 tokens run as blocks of 64
     p->mpad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
@@ -232,8 +249,7 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
 // The counters are those of 128-row tiles (see gemm_entry).
 int64_t workspace_bytes(const Plan& p, int64_t rows, int64_t N) {
   if (p.reduce != qg::kReduceGlobal) return 0;
-  const int64_t tiles = p.groups * cdiv(N, 128) * p.m_tiles;
-  return ws_counter_bytes(tiles) + static_cast<int64_t>(p.splits) * rows * N * 4;
+  return ws_counter_bytes(static_cast<int64_t>(p.groups) * p.ctr_tiles) + static_cast<int64_t>(p.splits) * rows * N * 4;
 }
 
 // config_id = ring | distance << 5 (see qgemm.h).  Ring depth: ring > 0
@@ -312,6 +328,16 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
+template <int NG>
+int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+               cudaStream_t stream) {
+  const int rb = g.recv_bytes;
+  int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_mma_smem_bytes<NG>(st, rb); }, &g.stages);
+  if (rc != QG_OK) return rc;
+  return launch_gemm(qg::gemm_i8_mma_kernel<NG>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::kMsThreads,
+                     qg::gemm_i8_mma_smem_bytes<NG>(g.stages, rb), tmW, tmA, g, stream);
+}
+
 template <int MT>
 int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
              cudaStream_t stream) {
@@ -325,13 +351,15 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
 // The config_id checks of qg_gemm_w8a8: known bits, ring depth, prefetch
 // distance, and wide tiles only for the FP8_Dynamic Standard / Split-K forms.
 int check_config_bits(int fmt, int variant, int config_id) {
-  if (config_id < 0 || (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+  if (config_id < 0 || (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
                 config_id, kMaxStages, QG_CONFIG_MAX_PREFETCH);
   if ((config_id & QG_CONFIG_WIDE) && (fmt != QG_FP8_DYNAMIC || !(variant == QG_STANDARD || variant == QG_SPLITK)))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_WIDE is for the FP8_Dynamic Standard / Split-K variants");
+  if ((config_id & QG_CONFIG_MMA_SYNC) && (fmt != QG_W8A8_INT8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK)))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
   if ((config_id & QG_CONFIG_RING_MASK) == 1) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
   return QG_OK;
 }
@@ -350,7 +378,7 @@ int check_shape_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, in
   if (fmt == QG_BLOCK_FP8 && K % 128) return fail(QG_ERR_UNSUPPORTED_SHAPE, "Block_FP8 needs K %% 128 == 0");
   if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
   Plan p;
-  return make_plan(fmt, M, N, K, variant, split_k, &p);
+  return make_plan(fmt, M, N, K, variant, split_k, config_id, &p);
 }
 
 // ------------------------------------------------------------------ table
@@ -473,7 +501,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (rows == 0) return QG_OK;
   }
   Plan p;
-  int rc = make_plan(fmt, M, N, K, variant, split_k, &p);
+  int rc = make_plan(fmt, M, N, K, variant, split_k, config_id, &p);
   if (rc != QG_OK) return rc;
   if (grouped) p.groups = grouped->groups;
   if (wide) p.n_tiles = static_cast<int>(cdiv(N, 256));
@@ -513,9 +541,8 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   if (p.reduce == qg::kReduceGlobal) {
     // the partials start after the counters of 128-row tiles even for wide
     // tiles, so that no configuration's partials overlap another's counters
-    const int64_t tiles = p.groups * cdiv(N, 128) * p.m_tiles;
     g.ws_count = static_cast<int*>(workspace_dev);
-    g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(tiles);
+    g.ws_part = static_cast<uint8_t*>(workspace_dev) + ws_counter_bytes(static_cast<int64_t>(p.groups) * p.ctr_tiles);
   }
   g.reduce = p.reduce;
   g.recv_bytes = p.reduce == qg::kReduceCluster
@@ -541,6 +568,13 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (M <= 2) return run_dp4a<2>(p, tmW, tmA, g, config_id, s);
     if (M <= 4) return run_dp4a<4>(p, tmW, tmA, g, config_id, s);
     return run_dp4a<8>(p, tmW, tmA, g, config_id, s);
+  }
+  if (p.mma) {
+    if (fz) return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC takes quantized activations");
+    if (p.mpad == 8) return run_i8_mma<1>(p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 16) return run_i8_mma<2>(p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 24) return run_i8_mma<3>(p, tmW, tmA, g, config_id, s);
+    return run_i8_mma<4>(p, tmW, tmA, g, config_id, s);
   }
   if (fmt == QG_W8A8_INT8) {
     if (p.mpad == 16) return fz ? run_i8<16, true>(p, tmW, tmA, g, config_id, s) : run_i8<16, false>(p, tmW, tmA, g, config_id, s);
@@ -820,7 +854,7 @@ int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q
 size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k) {
   Plan p;
   if (fmt < 0 || fmt > 2 || M <= 0 || N <= 0 || K <= 0 || variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return 0;
-  if (make_plan(fmt, M, N, K, variant, split_k, &p) != QG_OK) return 0;
+  if (make_plan(fmt, M, N, K, variant, split_k, 0, &p) != QG_OK) return 0;
   return static_cast<size_t>(workspace_bytes(p, M, N));
 }
 
@@ -859,7 +893,7 @@ size_t qg_workspace_bytes_grouped(int fmt, int groups, int64_t total_tokens, int
   if (fmt < 0 || fmt > 2 || groups < 1 || total_tokens < 0 || max_tokens <= 0 || N <= 0 || K <= 0 || variant < 0 ||
       variant > QG_SWAPAB_DP4A_SPLITK)
     return 0;
-  if (make_plan(fmt, max_tokens, N, K, variant, split_k, &p) != QG_OK) return 0;
+  if (make_plan(fmt, max_tokens, N, K, variant, split_k, 0, &p) != QG_OK) return 0;
   p.groups = groups;
   return static_cast<size_t>(workspace_bytes(p, total_tokens, N));
 }
@@ -869,7 +903,8 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
                    void* workspace_dev, size_t ws_bytes, void* A_q_dev, float* s_a_dev, int32_t* debug_acc_dev,
                    void* stream) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
-  const bool fusable = fmt != QG_BLOCK_FP8 && (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK);
+  const bool fusable = fmt != QG_BLOCK_FP8 && (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) &&
+                       !(config_id & QG_CONFIG_MMA_SYNC);
   const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
   if (fusable && (!buffers || (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {
     // one kernel: each CTA quantizes the activations its K range needs
@@ -903,9 +938,9 @@ int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A
     int rc = noalloc_scratch(&ws);
     if (rc != QG_OK) return rc;
     Plan p;
-    rc = make_plan(fmt, M, N, K, variant, split_k, &p);
+    rc = make_plan(fmt, M, N, K, variant, split_k, config_id, &p);
     if (rc != QG_OK) return rc;
-    const int64_t counters = ws_counter_bytes(static_cast<int64_t>(p.n_tiles) * p.m_tiles);
+    const int64_t counters = ws_counter_bytes(p.ctr_tiles);
     cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(counters), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clear noalloc counters");
   }

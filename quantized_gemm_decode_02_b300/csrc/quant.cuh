@@ -112,13 +112,15 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const InT* __restri
                                                             uint8_t* __restrict__ Q, float* __restrict__ S,
                                                             float qmax, unsigned long long* ts) {
   stamp_start(ts);
+  const int64_t r = blockIdx.x;
+  const InT* x = X + r * ldx;
+  // the row requested into L2 before the wait (see prefetch_l2_bulk)
+  if (threadIdx.x == 0) prefetch_l2_bulk(x, static_cast<uint32_t>(K) * static_cast<uint32_t>(sizeof(InT)));
   // Let the next kernel (a GEMM that first streams its static weights) be
   // scheduled now; this kernel's own inputs are read only after the wait.
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float red[THREADS / 32];
-  const int64_t r = blockIdx.x;
-  const InT* x = X + r * ldx;
   float amax = 0.0f;
   for (int k = threadIdx.x * 8; k < K; k += THREADS * 8) {
     float v[8];
@@ -157,11 +159,13 @@ __global__ void __launch_bounds__(512) quant_rows_reg_kernel(const __nv_bfloat16
                                                              float qmax, unsigned long long* ts) {
   constexpr int kThreads = 512;
   stamp_start(ts);
+  const int64_t r = blockIdx.x;
+  const __nv_bfloat16* x = X + r * ldx;
+  // the row's bytes requested into L2 while the kernel ahead finishes (K % 16 == 0: 32-byte multiple)
+  if (threadIdx.x == 0) prefetch_l2_bulk(x, static_cast<uint32_t>(K) * 2u);
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float red[kThreads / 32];
-  const int64_t r = blockIdx.x;
-  const __nv_bfloat16* x = X + r * ldx;
   float v[CH][8];
   float amax = 0.0f;
 #pragma unroll
@@ -216,12 +220,15 @@ __global__ void __launch_bounds__(WARPS * 32) quant_groups_kernel(const __nv_bfl
                                                                  int rows, int K, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S, unsigned long long* ts) {
   stamp_start(ts);
+  const int groups = K / 128;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+  // each warp's 256-byte group requested into L2 before the wait (see prefetch_l2_bulk)
+  if ((threadIdx.x & 31) == 0 && gid < static_cast<int64_t>(rows) * groups)
+    prefetch_l2_bulk(X + (gid / groups) * ldx + (gid % groups) * 128, 256u);
   // Let the next kernel (a GEMM that first streams its static weights) be
   // scheduled now; this kernel's own inputs are read only after the wait.
   pdl_launch_dependents();
   pdl_wait();
-  const int groups = K / 128;
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
   if (gid < static_cast<int64_t>(rows) * groups) {  // (no early return: the end stamp is a CTA barrier)
     const int lane = threadIdx.x & 31;
     const int64_t r = gid / groups;

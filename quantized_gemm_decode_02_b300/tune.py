@@ -59,9 +59,11 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     """(variant, split_k, config_id) candidates for one shape: Swap-AB with
     and without Split-K (reduced in a cluster, up to 16 ranges) for every M
     (in blocks of 64 tokens above 64); for W8A8_INT8 at M <= 8 also their
-    CUDA-core (dp4a) forms; above 32 tokens also the Standard variant of the
-    E4M3 formats (FP8_Dynamic also with 256-row weight tiles).  Ring depth: 0 = two CTAs per SM, 12 = one
-    deep ring per SM (6 for Standard, whose stages are twice as large)."""
+    CUDA-core (dp4a) forms, and for W8A8_INT8 at every M the mma.sync forms
+    (QG_CONFIG_MMA_SYNC); above 32 tokens also the Standard variant of the
+    E4M3 formats (FP8_Dynamic also with 256-row weight tiles).  Ring depth:
+    0 = two CTAs per SM, 12 = one deep ring per SM (6 for Standard, whose
+    stages are twice as large)."""
     n_tiles = (N + 127) // 128
     kt = (K + 127) // 128
     mpad = 16 if M <= 16 else (32 if M <= 32 else 64)
@@ -77,6 +79,16 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
                 if tiles * s > 12 * sms or kt // s < 1:
                     continue
                 out.append((split, s, cfg))
+    if fmt == "W8A8_INT8":
+        # the mma.sync form of Swap-AB (token groups of 8, blocks of 32)
+        mma_tiles = n_tiles * -(-M // (8 * min(4, -(-M // 8))))
+        for ring in (0, 12):
+            cfg = q.config_id(ring, 0, mma_sync=True)
+            out.append((q.QG_SWAPAB, 1, cfg))
+            for s in range(2, min(16, kt) + 1):
+                if mma_tiles * s > 12 * sms or kt // s < 1:
+                    continue
+                out.append((q.QG_SWAPAB_SPLITK, s, cfg))
     if M > 32 and fmt != "W8A8_INT8":
         std_tiles = n_tiles * -(-M // 128)
         for cfg in (0, 6):

@@ -216,8 +216,9 @@ def test_graph_capture_and_pdl_replay(orc, gc, q):
     assert q.qg_device_error() == 0
 
 
-@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])
-def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt):
+@pytest.mark.parametrize("fmt,mma_sync", [("FP8_Dynamic", False), ("W8A8_INT8", False), ("W8A8_INT8", True),
+                                          ("Block_FP8", False)])
+def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt, mma_sync):
     import seeded_inputs as si
     M, N, K = 4, 256, 1024
     A = si.activations(M, K, seed=1)
@@ -229,14 +230,15 @@ def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt):
     assert q.qg_device_error() == 0
     q.qg_set_wait_limit_ns(2_000_000)  # 2 ms
     q.qg_set_force_timeout(True)
+    cfg = q.config_id(0, 0, mma_sync=mma_sync)
     try:
-        gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1)
+        gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1, config_id=cfg)
         assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
     finally:
         q.qg_set_force_timeout(False)
         q.qg_set_wait_limit_ns(0)
     assert q.qg_device_error() == 0
-    Y, dbg = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1, debug=fmt == "W8A8_INT8")
+    Y, dbg = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1, config_id=cfg, debug=fmt == "W8A8_INT8")
     torch.cuda.synchronize()
     oAq, osa, oWq, osw = gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
     gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y, dbg)
@@ -274,3 +276,48 @@ def test_quant_act_row_lengths(orc, gc, fmt, K):
     oAq, osa = orc.quant_act(fmt, si.bf16_to_f32_numpy(A))
     assert np.array_equal(Aq.cpu().numpy().view(gc.oracle_dtype(fmt)), oAq)
     assert np.array_equal(sa.cpu().numpy(), osa)
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 17, 24, 25, 32, 33, 70])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 7), (SWS, 16), (SWS, 18)])
+def test_w8a8_int8_mma_sync(orc, q, gc, M, variant, split):
+    # the mma.sync form of Swap-AB: token groups of 8 (M = 1..32 in one
+    # block of 8/16/24/32, M = 33 and 70 in blocks of 32 with a ragged last
+    # block); K = 2304: 18 k-tiles, three exact 1024-K segments at split 1;
+    # 16 ranges reduce in a cluster, 18 through the workspace; ragged N; the
+    # int32 accumulators bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=600 + M, outliers=True,
+                config_id=q.config_id(0, 0, mma_sync=True))
+
+
+@pytest.mark.parametrize("M", [3, 12, 32])
+@pytest.mark.parametrize("ring", [2, 3, 6])
+def test_w8a8_int8_mma_sync_ring_depths(orc, q, gc, M, ring):
+    # shallow and deep rings (the ring wraps many times over 32 k-tiles)
+    gc.run_case(orc, "W8A8_INT8", M, 256, 4096, SWS, 1 if ring != 3 else 2, seed=650 + ring,
+                config_id=q.config_id(ring, 0, mma_sync=True))
+
+
+def test_int8_mma_sync_identical_to_tensor_memory_kernel(gc, q):
+    # the mma.sync kernel and the tcgen05 kernel compute the same int32
+    # accumulators and the same Y
+    import seeded_inputs as si
+    M, N, K = 29, 384, 4096
+    A = si.activations(M, K, seed=31, outliers=True).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=31)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("W8A8_INT8", W)
+    Aq, sa = gc.quant_act_gpu("W8A8_INT8", A)
+    Y0, d0 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, debug=True)
+    Y1, d1 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=q.config_id(0, 0, mma_sync=True),
+                         debug=True)
+    torch.cuda.synchronize()
+    assert torch.equal(d0, d1) and torch.equal(Y0, Y1)
+
+
+def test_mma_sync_config_rejected_outside_int8_swap_ab(q, gc):
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device=gc.DEV)
+    f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
+    for fmt, v in (("FP8_Dynamic", SW), ("Block_FP8", SW), ("W8A8_INT8", 4), ("W8A8_INT8", ST)):
+        with pytest.raises(q.QGError) as e:
+            q.qg_gemm_w8a8(fmt, 8, 256, 256, d, f, d, f, d, 256, v, 1, q.config_id(0, 0, mma_sync=True))
+        assert e.value.code == q.QG_ERR_INVALID_ARG
