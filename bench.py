@@ -195,9 +195,11 @@ class Workload:
 
     def fused_item(self, i: int) -> bool:
         """Whether item i runs as one kernel (activation quantization inside
-        the GEMM): FP8_Dynamic / W8A8_INT8 with the Swap-AB variants."""
+        the GEMM): FP8_Dynamic / W8A8_INT8 with the Swap-AB variants on the
+        tcgen05 kernels."""
         r = self.recs[i]
-        return self.fused and r["fmt"] != "Block_FP8" and r["variant"] in (self.q.QG_SWAPAB, self.q.QG_SWAPAB_SPLITK)
+        return (self.fused and r["fmt"] != "Block_FP8" and r["variant"] in (self.q.QG_SWAPAB, self.q.QG_SWAPAB_SPLITK)
+                and not r["cfg"] & self.q.QG_CONFIG_MMA_SYNC)
 
     def kernels(self, i: int) -> int:
         return 1 if self.fused_item(i) else 2

@@ -79,6 +79,7 @@ typedef enum {
 #define QG_CONFIG_MAX_PREFETCH 64
 #define QG_CONFIG_WIDE (1 << 12)
 #define QG_CONFIG_MMA_SYNC (1 << 13)
+#define QG_CONFIG_MMA_NARROW (1 << 14)
 
 typedef enum {
   QG_OK = 0,
@@ -159,6 +160,9 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      weights in tensor memory; same exact int32 result
  *                      (QG_ERR_INVALID_ARG elsewhere, and in the one-kernel
  *                      form of qg_linear_w8a8, which then runs two kernels);
+ *                      with QG_CONFIG_MMA_SYNC also QG_CONFIG_MMA_NARROW:
+ *                      eight MMA warps of 16 weight rows instead of four
+ *                      of 32 (more warps to hide the widening's latency);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

@@ -25,18 +25,21 @@
 // k-tile (two 16-byte shared-memory loads), and one 32-bit word of four int8
 // values becomes the two f16x2 fragment registers of one step.
 //
-// CTA = 6 warps, one 128-row weight tile x one K range x one block of up to
-// 32 tokens (NG groups of 8, the MMA N side):
+// CTA = 2 + 8/TPW warps, one 128-row weight tile x one K range x one block
+// of up to 32 tokens (NG groups of 8, the MMA N side):
 //   warp 0      TMA: int8 W tile (128 x 128 B, 128-byte swizzle) and the
 //               int8 activation tile (8*NG token rows, zero-filled past M)
 //               into a `stages`-deep ring, weights and activations on
 //               separate barriers (weights fetched before the dependency
 //               wait);
-//   warps 1..4  32 weight rows each (two m16 tiles): per k-tile 8 shared
-//               loads of 16 bytes, 8 steps of widening and 2*NG MMAs;
-//   warp 5      widens the activation tile once per k-tile into f16
+//   MMA warps   8/TPW warps of 16*TPW weight rows each (TPW m16 tiles; TPW
+//               = 2: four warps, TPW = 1: eight warps, twice the warps
+//               to hide the widening's latency): per k-tile 4*TPW shared
+//               loads of 16 bytes, 8 steps of widening and TPW*NG MMAs
+//               per step;
+//   last warp   widens the activation tile once per k-tile into f16
 //               fragments in shared memory ([step][group][lane], 8 bytes),
-//               read by the four MMA warps.
+//               read by every MMA warp.
 // The epilogue, the Split-K reduction (cluster push or workspace) and the
 // scales are those of the other Swap-AB kernels, one thread per weight row.
 #pragma once
@@ -46,9 +49,11 @@
 
 namespace qg {
 
-constexpr int kMsWarps = 4;                          // MMA warps (1..4), 32 weight rows each
-constexpr int kMsAWarp = 1 + kMsWarps;               // activation widening warp (5)
-constexpr int kMsThreads = 32 * (kMsAWarp + 1);      // 192
+// MMA warps (1 .. 8/TPW) of 16*TPW weight rows each, then the activation
+// widening warp; the first four MMA warps' 128 threads run the per-row
+// epilogue
+__host__ __device__ constexpr int ms_mma_warps(int tpw) { return 8 / tpw; }
+__host__ __device__ constexpr int ms_threads(int tpw) { return 32 * (ms_mma_warps(tpw) + 2); }
 constexpr int kMsABufs = 3;                          // f16 activation fragment buffers in flight
 constexpr int kMsMaxGroups = 4;                      // token groups of 8 per block (32 tokens)
 
@@ -95,11 +100,14 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
   return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-template <int NG>
-__global__ void __launch_bounds__(kMsThreads, 2)
+template <int NG, int TPW>
+__global__ void __launch_bounds__(ms_threads(TPW), 2)
     gemm_i8_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = MsShape<NG>;
   constexpr int MPAD = S::kMpad;
+  constexpr int kMsWarps = ms_mma_warps(TPW);  // MMA warps 1..kMsWarps
+  constexpr int kMsAWarp = 1 + kMsWarps;       // activation widening warp
+  constexpr int kEpi = 128;                     // per-row epilogue threads (warps 1..4)
   stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -157,9 +165,9 @@ __global__ void __launch_bounds__(kMsThreads, 2)
 
   // MMA warps: int32 sums of weight rows r0 = 32*cw + 16*t + gid and r0 + 8
   // for tokens 8*grp + 2*tig + {0,1} (the D fragment layout)
-  int32_t iacc[2][NG][4];
+  int32_t iacc[TPW][NG][4];
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
+  for (int t = 0; t < TPW; ++t)
 #pragma unroll
     for (int q = 0; q < NG; ++q)
 #pragma unroll
@@ -242,9 +250,9 @@ __global__ void __launch_bounds__(kMsThreads, 2)
     const int cw = warp - 1;
     // test hook (qg_set_force_timeout): wait on a barrier nothing arrives on
     bool ok = !g.force_timeout || __all_sync(0xffffffffu, mbar_wait(&ctl->never, 0, g.wait_ns));
-    float facc[2][NG][4];
+    float facc[TPW][NG][4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
+    for (int t = 0; t < TPW; ++t)
 #pragma unroll
       for (int q = 0; q < NG; ++q)
 #pragma unroll
@@ -258,12 +266,12 @@ __global__ void __launch_bounds__(kMsThreads, 2)
       }
       // this lane's 32 bytes of k of the four rows it holds: [tile][row r0 / r0 + 8][16-byte half]
       const uint8_t* wt = smem + static_cast<size_t>(s) * S::kStageBytes;
-      uint4 wv[2][2][2];
+      uint4 wv[TPW][2][2];
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+      for (int t = 0; t < TPW; ++t)
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-          const uint32_t row = static_cast<uint32_t>(32 * cw + 16 * t + 8 * rr + gid);
+          const uint32_t row = static_cast<uint32_t>(16 * TPW * cw + 16 * t + 8 * rr + gid);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
             wv[t][rr][hh] = *reinterpret_cast<const uint4*>(wt + sw128_chunk(row, 2 * tig + hh));
@@ -276,9 +284,9 @@ __global__ void __launch_bounds__(kMsThreads, 2)
       const uint8_t* fb = frag + b * S::kFragBytes;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint32_t a[2][4];
+        uint32_t a[TPW][4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < TPW; ++t) {
           uint32_t lo0, hi0, lo1, hi1;
           int8x4_to_f16x4(word_of(wv[t][0][c >> 2], c & 3), lo0, hi0);
           int8x4_to_f16x4(word_of(wv[t][1][c >> 2], c & 3), lo1, hi1);
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(kMsThreads, 2)
         for (int q = 0; q < NG; ++q) {
           const uint2 bv = *reinterpret_cast<const uint2*>(fb + ((c * NG + q) * 32 + lane) * 8);
 #pragma unroll
-          for (int t = 0; t < 2; ++t) mma_16816_f16(facc[t][q], a[t][0], a[t][1], a[t][2], a[t][3], bv.x, bv.y);
+          for (int t = 0; t < TPW; ++t) mma_16816_f16(facc[t][q], a[t][0], a[t][1], a[t][2], a[t][3], bv.x, bv.y);
         }
       }
       mbar_arrive(&ctl->empty[s]);   // the weight bytes are consumed (in registers)
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(kMsThreads, 2)
       // close an exact 1024-K segment (or the range) into int32
       if ((i % kI8SegTiles) == kI8SegTiles - 1 || i == nk - 1) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < TPW; ++t)
 #pragma unroll
           for (int q = 0; q < NG; ++q)
 #pragma unroll
@@ -310,9 +318,9 @@ __global__ void __launch_bounds__(kMsThreads, 2)
       }
     }
     if (!ok) *abort_flag = 1;
-    const int r = threadIdx.x - 32;  // 0..127: weight row of the tile for the per-row epilogue
+    const int r = threadIdx.x - 32;  // weight row of the tile for the per-row epilogue
     const int nn = n_tile * kBN + r;
-    ctl->sw_s[r] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
+    if (r < kBN) ctl->sw_s[r] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
   }
   // ------------------------------------------------- per-row accumulators
   __syncthreads();  // the ring is idle: every issued copy was consumed by the MMA warps
@@ -321,18 +329,18 @@ __global__ void __launch_bounds__(kMsThreads, 2)
   if (warp >= 1 && warp <= kMsWarps) {
     const int cw = warp - 1;
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
+    for (int t = 0; t < TPW; ++t)
 #pragma unroll
       for (int q = 0; q < NG; ++q) {
-        const int row = 32 * cw + 16 * t + gid, m = 8 * q + 2 * tig;
+        const int row = 16 * TPW * cw + 16 * t + gid, m = 8 * q + 2 * tig;
         *reinterpret_cast<int2*>(acc_s + row * S::kAccStride + m) = make_int2(iacc[t][q][0], iacc[t][q][1]);
         *reinterpret_cast<int2*>(acc_s + (row + 8) * S::kAccStride + m) = make_int2(iacc[t][q][2], iacc[t][q][3]);
       }
   }
   __syncthreads();
   pdl_wait();  // outputs are written only after the kernel this one depends on
-  const bool holds_row = warp >= 1 && warp <= kMsWarps;
-  const int ct = threadIdx.x - 32;  // row of the tile (MMA warps)
+  const bool holds_row = warp >= 1 && warp <= kEpi / 32;
+  const int ct = threadIdx.x - 32;  // row of the tile (the first four MMA warps)
   int32_t acc[MPAD];
   if (holds_row) {
 #pragma unroll
@@ -353,10 +361,10 @@ __global__ void __launch_bounds__(kMsThreads, 2)
       cluster_wait();  // every peer's receive barrier is initialized
       // rows go out even after an abort, so that every owner's wait completes
       cluster_push_row(acc, 0, ct, split, g.splits, Mb, recv, &ctl->recv_bar);
-      named_bar_sync(1, 32 * kMsWarps);  // this CTA's own rows, stored locally, are visible
+      named_bar_sync(1, kEpi);  // this CTA's own rows, stored locally, are visible
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
       if (got && !abort) {
-        cluster_sum_rows<int32_t>(recv, split, g.splits, Mb, ct, 32 * kMsWarps, [&](int m, int r, int32_t sum) {
+        cluster_sum_rows<int32_t>(recv, split, g.splits, Mb, ct, kEpi, [&](int m, int r, int32_t sum) {
           const int nn = n_tile * kBN + r;
           if (nn < g.N) finish(m, r, nn, sum);
         });
@@ -382,10 +390,10 @@ __global__ void __launch_bounds__(kMsThreads, 2)
           if (m < Mb) part[(static_cast<int64_t>(split) * g.M + m_base + m) * g.N + n] = acc[m];
       }
       __threadfence();
-      named_bar_sync(1, 32 * kMsWarps);
+      named_bar_sync(1, kEpi);
       const int tile_id = blockIdx.x + blockIdx.z * gridDim.x;
       if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + tile_id, 1) == g.splits - 1);
-      named_bar_sync(1, 32 * kMsWarps);
+      named_bar_sync(1, kEpi);
       if (ctl->last_flag) {
         __threadfence();
         if (n_ok) {

@@ -328,14 +328,21 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
-template <int NG>
-int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
-               cudaStream_t stream) {
+template <int NG, int TPW>
+int run_i8_mma_t(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                 cudaStream_t stream) {
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_mma_smem_bytes<NG>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_mma_kernel<NG>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::kMsThreads,
-                     qg::gemm_i8_mma_smem_bytes<NG>(g.stages, rb), tmW, tmA, g, stream);
+  return launch_gemm(qg::gemm_i8_mma_kernel<NG, TPW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
+                     qg::ms_threads(TPW), qg::gemm_i8_mma_smem_bytes<NG>(g.stages, rb), tmW, tmA, g, stream);
+}
+// QG_CONFIG_MMA_NARROW: eight MMA warps of 16 weight rows instead of four of 32
+template <int NG>
+int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+               cudaStream_t stream) {
+  if (config_id & QG_CONFIG_MMA_NARROW) return run_i8_mma_t<NG, 1>(p, tmW, tmA, g, config_id, stream);
+  return run_i8_mma_t<NG, 2>(p, tmW, tmA, g, config_id, stream);
 }
 
 template <int MT>
@@ -351,7 +358,9 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
 // The config_id checks of qg_gemm_w8a8: known bits, ring depth, prefetch
 // distance, and wide tiles only for the FP8_Dynamic Standard / Split-K forms.
 int check_config_bits(int fmt, int variant, int config_id) {
-  if (config_id < 0 || (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+  if (config_id < 0 ||
+      (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_RING_MASK |
+                     QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -360,6 +369,8 @@ int check_config_bits(int fmt, int variant, int config_id) {
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_WIDE is for the FP8_Dynamic Standard / Split-K variants");
   if ((config_id & QG_CONFIG_MMA_SYNC) && (fmt != QG_W8A8_INT8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK)))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
+  if ((config_id & QG_CONFIG_MMA_NARROW) && !(config_id & QG_CONFIG_MMA_SYNC))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_NARROW needs QG_CONFIG_MMA_SYNC");
   if ((config_id & QG_CONFIG_RING_MASK) == 1) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
   return QG_OK;
 }

@@ -19,6 +19,16 @@ same-shape chains lost in the mixed-shape chains of bench.py.
 Rows already present in the output table are skipped, so an interrupted
 sweep resumes where it stopped.
 
+With --layer-context TABLE_IN the rows are re-tuned where they run: for
+each token count the candidates of one linear are timed inside the chain
+of the whole decoder layer (activation quantization and GEMM of qkv, o,
+gate_up and down in order, one CUDA graph with programmatic dependent
+launch), the other linears keeping their current rows, one linear after
+the other.  A linear's best configuration depends on its neighbours there
+(which SMs the previous GEMM still holds when its thread-block clusters
+are placed, how much of its weights it streams before its dependency
+wait), which a chain of one shape does not show.
+
 Usage:  python -m quantized_gemm_decode_02_b300.tune --out TABLE
             [--formats FP8_Dynamic,W8A8_INT8,Block_FP8]
             [--models Qwen3-1.7B,Qwen3-8B,Qwen3-32B] [--ms 1,2,4,8,16,24,32]
@@ -82,8 +92,8 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     if fmt == "W8A8_INT8":
         # the mma.sync form of Swap-AB (token groups of 8, blocks of 32)
         mma_tiles = n_tiles * -(-M // (8 * min(4, -(-M // 8))))
-        for ring in (0, 12):
-            cfg = q.config_id(ring, 0, mma_sync=True)
+        for ring, narrow in ((0, False), (12, False), (0, True), (12, True)):
+            cfg = q.config_id(ring, 0, mma_sync=True, narrow=narrow)
             out.append((q.QG_SWAPAB, 1, cfg))
             for s in range(2, min(16, kt) + 1):
                 if mma_tiles * s > 12 * sms or kt // s < 1:
@@ -168,6 +178,98 @@ class Bench:
         return statistics.median(times)
 
 
+def time_layer_chain(bench, fmt, M, layers, cfgs, passes=3, reps=5):
+    """Microseconds per pass of one decoder layer's linears, in order, each
+    a qg_linear_w8a8 call (quantization kernel + GEMM) with its config from
+    `cfgs`, captured as one CUDA graph with programmatic dependent launch:
+    `passes` x `windows` passes, each window with its own weights (two
+    windows when they fit the pool: a layer's weights are then re-read only
+    after the other window's; one window when the layer alone exceeds
+    L2 several times)."""
+    sizes = [N * K for (K, N) in layers]
+    windows = 2 if 2 * sum((sz + 255) // 256 * 256 for sz in sizes) <= POOL_BYTES else 1
+    offs, o = [], 0
+    for w in range(windows):
+        row = []
+        for sz in sizes:
+            row.append(o)
+            o += (sz + 255) // 256 * 256
+        offs.append(row)
+    if o > POOL_BYTES:
+        raise ValueError("layer weights exceed the pool")
+    q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=bench.stream):
+            for _ in range(passes):
+                for w in range(windows):
+                    for (K, N), off, (v, sp, c) in zip(layers, offs[w], cfgs):
+                        need = q.qg_workspace_bytes(fmt, M, N, K, v, sp)
+                        W = bench.pool[off:off + N * K]
+                        q.qg_linear_w8a8(fmt, M, N, K, bench.A, K, W, bench.sw, bench.Y, N, v, sp, c,
+                                         bench.ws if need else None, need, bench.Aq, bench.sa, None,
+                                         stream=bench.stream)
+    finally:
+        q.qg_set_launch_flags(0)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(reps):
+        with torch.cuda.stream(bench.stream):
+            e0.record(bench.stream)
+            graph.replay()
+            e1.record(bench.stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3 / (passes * windows))
+    del graph
+    return statistics.median(times)
+
+
+def layer_context_pass(bench, table_in, out_path, fmts, models, ms, sms, log=None):
+    """Coordinate descent over one layer's linears in their decoder order:
+    for every token count, each linear's candidates are timed inside the
+    whole layer chain (the other linears keep their current rows), and the
+    best chain time keeps its row.  Writes a complete table."""
+    rows = read_table(table_in)
+    for fmt in fmts:
+        fid = FMT_ID[fmt]
+        for model in models:
+            layers = list(SHAPES[model].items())
+            shapes = [ks for _, ks in layers]
+            for M in ms:
+                cfgs = []
+                for (K, N) in shapes:
+                    key = (fid, N, K, M)
+                    cfgs.append(rows[key] if key in rows else q.qg_select(fmt, M, N, K))
+                base = time_layer_chain(bench, fmt, M, shapes, cfgs)
+                best_total = base
+                for li, (layer, (K, N)) in enumerate(layers):
+                    for cand in candidates(fmt, M, N, K, sms):
+                        if cand == cfgs[li]:
+                            continue
+                        trial = list(cfgs)
+                        trial[li] = cand
+                        us = time_layer_chain(bench, fmt, M, shapes, trial)
+                        if log:
+                            log.write(json.dumps({"pass": "layer", "fmt": fmt, "model": model, "layer": layer, "M": M,
+                                                  "variant": cand[0], "split_k": cand[1], "config_id": cand[2],
+                                                  "chain_us": us}) + "\n")
+                        if us < 0.995 * best_total:
+                            best_total, cfgs = us, trial
+                for (K, N), cfg in zip(shapes, cfgs):
+                    rows[(fid, N, K, M)] = tuple(cfg)
+                print(f"{fmt:12s} {model:10s} M={M:2d}: layer chain {base:7.2f} -> {best_total:7.2f} us  "
+                      f"{[tuple(c) for c in cfgs]}", flush=True)
+    with open(out_path, "w") as fh:
+        fh.write("# fmt\tN\tK\tM\tvariant\tsplit_k\tconfig_id   (written by quantized_gemm_decode_02_b300/tune.py)\n")
+        for (f, n, k, m) in sorted(rows):
+            v, sp, c = rows[(f, n, k, m)]
+            fh.write(f"{f}\t{n}\t{k}\t{m}\t{v}\t{sp}\t{c}\n")
+
+
 def read_table(path):
     rows = {}
     if os.path.exists(path):
@@ -191,11 +293,23 @@ def main(argv=None):
                     help="time qg_linear_w8a8 (quantization kernel + GEMM) instead of the GEMM alone")
     ap.add_argument("--prefetch-pass", action="store_true",
                     help="also try the winner with an L2 prefetch distance (config_id upper bits)")
+    ap.add_argument("--layer-context", metavar="TABLE_IN",
+                    help="re-tune the rows of TABLE_IN inside whole-layer chains (quantization + GEMM of qkv, o, "
+                         "gate_up, down in order) and write the complete table to --out")
     args = ap.parse_args(argv)
     device = "cuda:0"
     torch.cuda.set_device(0)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     bench = Bench(device)
+    if args.layer_context:
+        q.qg_load_table(args.layer_context)
+        q.qg_set_allow_default(True)
+        log = open(args.log, "a") if args.log else None
+        layer_context_pass(bench, args.layer_context, args.out, args.formats.split(","), args.models.split(","),
+                           [int(m) for m in args.ms.split(",")], sms, log)
+        if log:
+            log.close()
+        return 0
     done = read_table(args.out)
     os.makedirs(os.path.dirname(os.path.abspath(args.out)), exist_ok=True)
     new_file = not os.path.exists(args.out)

@@ -290,6 +290,14 @@ def test_w8a8_int8_mma_sync(orc, q, gc, M, variant, split):
                 config_id=q.config_id(0, 0, mma_sync=True))
 
 
+@pytest.mark.parametrize("M", [1, 9, 24, 32, 70])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 3), (SWS, 16), (SWS, 18)])
+def test_w8a8_int8_mma_sync_narrow_warps(orc, q, gc, M, variant, split):
+    # eight MMA warps of 16 weight rows (QG_CONFIG_MMA_NARROW): same checks
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=700 + M, outliers=True,
+                config_id=q.config_id(0, 0, narrow=True))
+
+
 @pytest.mark.parametrize("M", [3, 12, 32])
 @pytest.mark.parametrize("ring", [2, 3, 6])
 def test_w8a8_int8_mma_sync_ring_depths(orc, q, gc, M, ring):
@@ -310,8 +318,11 @@ def test_int8_mma_sync_identical_to_tensor_memory_kernel(gc, q):
     Y0, d0 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, debug=True)
     Y1, d1 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=q.config_id(0, 0, mma_sync=True),
                          debug=True)
+    Y2, d2 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=q.config_id(0, 0, narrow=True),
+                         debug=True)
     torch.cuda.synchronize()
     assert torch.equal(d0, d1) and torch.equal(Y0, Y1)
+    assert torch.equal(d0, d2) and torch.equal(Y0, Y2)
 
 
 def test_mma_sync_config_rejected_outside_int8_swap_ab(q, gc):
@@ -321,3 +332,6 @@ def test_mma_sync_config_rejected_outside_int8_swap_ab(q, gc):
         with pytest.raises(q.QGError) as e:
             q.qg_gemm_w8a8(fmt, 8, 256, 256, d, f, d, f, d, 256, v, 1, q.config_id(0, 0, mma_sync=True))
         assert e.value.code == q.QG_ERR_INVALID_ARG
+    with pytest.raises(q.QGError) as e:  # the narrow form is a form of the mma.sync kernel only
+        q.qg_gemm_w8a8("W8A8_INT8", 8, 256, 256, d, f, d, f, d, 256, SW, 1, q.QG_CONFIG_MMA_NARROW)
+    assert e.value.code == q.QG_ERR_INVALID_ARG
