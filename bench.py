@@ -195,11 +195,11 @@ class Workload:
 
     def fused_item(self, i: int) -> bool:
         """Whether item i runs as one kernel (activation quantization inside
-        the GEMM): FP8_Dynamic / W8A8_INT8 with the Swap-AB variants on the
-        tcgen05 kernels."""
+        the GEMM): the Swap-AB variants on the tcgen05 kernels when the
+        table row asks for it (QG_CONFIG_FUSED_QUANT) or with --fused."""
         r = self.recs[i]
-        return (self.fused and r["fmt"] != "Block_FP8" and r["variant"] in (self.q.QG_SWAPAB, self.q.QG_SWAPAB_SPLITK)
-                and not r["cfg"] & self.q.QG_CONFIG_MMA_SYNC)
+        fusable = r["variant"] in (self.q.QG_SWAPAB, self.q.QG_SWAPAB_SPLITK) and not r["cfg"] & self.q.QG_CONFIG_MMA_SYNC
+        return fusable and (self.fused or bool(r["cfg"] & self.q.QG_CONFIG_FUSED_QUANT))
 
     def kernels(self, i: int) -> int:
         return 1 if self.fused_item(i) else 2
@@ -808,8 +808,11 @@ def main(argv=None):
         cfg = _config(args.workload, WORKLOADS[args.workload]["items"])
         cfg.update({
             "gemms_per_step": n_gemm, "kernels_per_step": n_kernels,
-            "activation_quantization": "fused into the GEMM kernel (qg_linear_w8a8) where one kernel does both"
-                                       if wl.fused else "own kernel (qg_linear_w8a8, two kernels)",
+            "activation_quantization": ("fused into the GEMM kernel wherever one kernel does both (--fused)"
+                                        if wl.fused else
+                                        f"qg_linear_w8a8: {sum(wl.fused_item(i) for i in range(n_gemm))} of {n_gemm} "
+                                        "linears in one kernel (table rows with QG_CONFIG_FUSED_QUANT), the others "
+                                        "a quantization kernel and the GEMM"),
             "bytes_per_step": wl.bytes_step, "flops_per_step": wl.flops_step,
             "weight_bytes_streamed_per_step": wl.weight_bytes_streamed,
             "l2": (f"inputs larger than L2: {wl.weight_bytes_streamed / 1e6:.0f} MB of weights streamed per step "

@@ -80,6 +80,7 @@ typedef enum {
 #define QG_CONFIG_WIDE (1 << 12)
 #define QG_CONFIG_MMA_SYNC (1 << 13)
 #define QG_CONFIG_MMA_NARROW (1 << 14)
+#define QG_CONFIG_FUSED_QUANT (1 << 15)
 
 typedef enum {
   QG_OK = 0,
@@ -163,6 +164,10 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      with QG_CONFIG_MMA_SYNC also QG_CONFIG_MMA_NARROW:
  *                      eight MMA warps of 16 weight rows instead of four
  *                      of 32 (more warps to hide the widening's latency);
+ *                      plus QG_CONFIG_FUSED_QUANT (Swap-AB variants on the
+ *                      tcgen05 kernels): a hint for qg_linear_w8a8 to take
+ *                      its one-kernel form even when A_q / s_a buffers are
+ *                      given (qg_gemm_w8a8 accepts and ignores it);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).
@@ -213,16 +218,21 @@ QG_API size_t qg_workspace_bytes_grouped(int fmt, int groups, int64_t total_toke
  * followed by the quantized GEMM ("Kernel Implementation"), i.e.
  * qg_quant_act then qg_gemm_w8a8 with the same results bit for bit.
  * Two forms:
- *  - two kernels (when A_q_dev and s_a_dev are given; the only form of
- *    Block_FP8, the Standard and the dp4a variants): the quantization kernel
- *    writes A_q / s_a, the GEMM follows (with QG_LAUNCH_PDL it streams its
- *    weights while the quantization runs).  The faster form on B300.
- *  - one kernel (FP8_Dynamic and W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK,
- *    when A_q_dev or s_a_dev is NULL, or with QG_LAUNCH_FUSED_QUANT set):
- *    each CTA quantizes the slice of the activations its K range needs, the
- *    CTAs of a Split-K cluster agree on every token's maximum over the whole
- *    row through distributed shared memory, and A_q / s_a are written only
- *    when given.
+ *  - two kernels (when A_q_dev and s_a_dev are given and config_id does not
+ *    carry QG_CONFIG_FUSED_QUANT; the only form of the Standard, dp4a and
+ *    mma.sync kernels): the quantization kernel writes A_q / s_a, the GEMM
+ *    follows (with QG_LAUNCH_PDL it streams its weights while the
+ *    quantization runs).  The faster form on B300 for the per-token formats.
+ *  - one kernel (QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernels, when
+ *    A_q_dev or s_a_dev is NULL, config_id carries QG_CONFIG_FUSED_QUANT,
+ *    or QG_LAUNCH_FUSED_QUANT is set): each CTA quantizes the slice of the
+ *    activations its K range needs.  FP8_Dynamic / W8A8_INT8: the CTAs of
+ *    a Split-K cluster agree on every token's maximum over the whole row
+ *    through distributed shared memory.  Block_FP8: a group's scale needs
+ *    only its own 128 values, so four more warps of each CTA quantize every
+ *    k-tile on their own, with no wait for another CTA: one kernel and one
+ *    dependency wait per linear layer instead of two.  A_q / s_a are
+ *    written only when given (by the CTAs of the first weight tile).
  *   A_dev      bf16 [M][lda] activations (lda >= K, lda % 8 == 0, 16-byte
  *              aligned), read-only;
  *   W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id, workspace,

@@ -77,6 +77,15 @@ struct GemmArgs {
 constexpr int kBN = 128;         // weight rows per tile (and Block_FP8 block size)
 constexpr int kBK = 128;         // bytes of K per k-tile (one 128-byte swizzle row)
 constexpr int kThreads = 192;
+// Block_FP8 with fused quantization adds four quantizer warps (6..9)
+constexpr int kThreadsBlockFused = 320;
+// Block_FP8 fused: ring of per-k-tile activation scales passed from the
+// quantizer warps to the promotion warps (slots >= stages + 4 TMEM buffers)
+constexpr int kSaRing = 16;
+constexpr int kMaxStagesBlockFused = kSaRing - 4;
+__host__ __device__ constexpr int swap_threads(int fmt, bool fused) {
+  return (fmt == 2 && fused) ? kThreadsBlockFused : kThreads;
+}
 constexpr uint64_t kDrainNs = 200000000ull;  // bound for draining in-flight copies on exit
 
 __host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
@@ -94,12 +103,14 @@ struct alignas(8) Ctrl {
   uint64_t recv_bar;  // split-K: peers' partial rows have landed
   uint64_t amax_bar;  // fused quantization: peers' partial row maxima have landed
   uint64_t full_a[16];  // fused quantization: the stage's activation tile is written
+  uint64_t sfull[kSaRing];  // Block_FP8 fused: the k-tile's activation scales are in amax_s (ring slot)
   uint32_t tmem_base;
   int last_flag;
   int abort_flag;
   float sa_s[64];   // per-token scales, staged for the epilogue
   float sw_s[128];  // per-channel scales of the tile's rows
   float amax_s[kMaxClusterSplits * 64];  // fused quantization: [source rank][token] partial row maxima
+                                         // (Block_FP8 fused: [ring slot][token] activation scales)
 };
 
 template <bool SWAP, int MPAD>
@@ -318,18 +329,111 @@ __device__ __forceinline__ void load_act32(const GemmArgs& g, int row, int k, fl
   }
 }
 
+// Block_FP8 fused quantization, run by warps 6..9 (qt = 0..127).  For each
+// k-tile of the CTA's K range: the bf16 activations of the block's tokens,
+// in pieces of 32 values (token row r, quarter p of the 128-wide group),
+// are loaded one k-tile ahead; the four threads of a row agree on the
+// group's maximum (two shuffles) and take s = amax / 448 ("Scope": one
+// scale per 1x128 activation group); the codes (the correctly rounded
+// quotient, round-to-nearest-even, saturated) go into the stage's
+// activation tile once the MMAs of the stage's previous use are done, and
+// the scales into the k-tile's ring slot for the promotion warps.  The CTAs
+// of the first weight tile also write A_q / s_a when the caller gave them.
+template <int MPAD>
+__device__ __forceinline__ void block_fused_quantize(const GemmArgs& g, Ctrl* ctl, uint8_t* smem, uint32_t stage_bytes,
+                                                     uint32_t w_bytes, int stages, int nk, int kb0, int m_base, int Mb,
+                                                     int n_tile, volatile int* abort_flag) {
+  pdl_wait();  // the activations are written by the kernel this one depends on
+  const int qt = static_cast<int>(threadIdx.x) - 192, lane = threadIdx.x & 31;
+  constexpr int kPP = (MPAD * 4 + 127) / 128;  // pieces per thread
+  const bool write_out = g.a_q_out != nullptr && n_tile == 0;
+  uint4 cur[kPP][4], nxt[kPP][4];
+  auto fetch = [&](int i, uint4(&buf)[kPP][4]) {
+#pragma unroll
+    for (int q = 0; q < kPP; ++q) {
+      const int piece = qt + 128 * q, r = piece >> 2, p = piece & 3;
+      if (piece < MPAD * 4 && r < Mb)
+        load_act_raw(g, m_base + r, (kb0 + i) * kBK + 32 * p, buf[q]);
+      else
+#pragma unroll
+        for (int c = 0; c < 4; ++c) buf[q][c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  fetch(0, cur);
+  bool ok = true;
+  for (int i = 0; i < nk; ++i) {
+    const int s = i % stages, slot = i % kSaRing;
+    if (i + 1 < nk) fetch(i + 1, nxt);
+    if (i >= stages &&
+        !__all_sync(0xffffffffu, mbar_wait(&ctl->empty[s], static_cast<uint32_t>(i / stages - 1) & 1u, g.wait_ns) &&
+                                     !*abort_flag)) {
+      ok = false;
+      break;
+    }
+    const int kb = kb0 + i, kt0 = kb * kBK;
+    uint8_t* at = smem + static_cast<size_t>(s) * stage_bytes + w_bytes;
+#pragma unroll
+    for (int q = 0; q < kPP; ++q) {
+      const int piece = qt + 128 * q, r = piece >> 2, p = piece & 3;
+      float x[32];
+      unpack_act32(cur[q], x);
+      float mx = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(x[j]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));  // the row's four quarters
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float sc = scale_from_amax(mx, 448.0f);
+      if (piece < MPAD * 4) {
+        const Divider dv(sc);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          w[j] = static_cast<uint32_t>(e4m3x2(dv(x[4 * j]), dv(x[4 * j + 1]))) |
+                 (static_cast<uint32_t>(e4m3x2(dv(x[4 * j + 2]), dv(x[4 * j + 3]))) << 16);
+        *reinterpret_cast<uint4*>(at + sw128_chunk(r, 2 * p)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(at + sw128_chunk(r, 2 * p + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        if (p == 0) ctl->amax_s[slot * 64 + r] = r < Mb ? sc : 0.0f;
+        if (write_out && r < Mb) {
+          uint8_t* dst = g.a_q_out + static_cast<int64_t>(m_base + r) * g.K + kt0 + 32 * p;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+          if (p == 0 && g.s_a_out) g.s_a_out[static_cast<int64_t>(m_base + r) * g.kt_total + kb] = sc;
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile is read by the MMA (async proxy)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->full_a[s]);
+    mbar_arrive(&ctl->sfull[slot]);  // every lane: its scales are written (release)
+#pragma unroll
+    for (int q = 0; q < kPP; ++q)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) cur[q][c] = nxt[q][c];
+  }
+  if (!ok) *abort_flag = 1;
+}
+
 // ------------------------------------------------------------ Swap-AB --
 // One CTA per (128-row weight tile, K range, block of MPAD tokens).
 // D^T[128 x MPAD] in TMEM.
-// FUSED (FP8_Dynamic only): the epilogue warps, idle during the main loop,
-// read bf16 activations (g.A), quantize them per token and write each
-// stage's activation tile themselves (qg_linear_w8a8); tmA is unused.
+// FUSED (qg_linear_w8a8's one-kernel form): the kernel reads bf16
+// activations (g.A) and quantizes them itself; tmA is unused.
+//   FP8_Dynamic: the epilogue warps, idle during the main loop, take the
+//     per-token row maximum (agreed across a Split-K cluster) and write
+//     each stage's activation tile.
+//   Block_FP8: four more warps (6..9) quantize each k-tile's 1x128 groups
+//     on their own -- a group's scale needs only its 128 values, so no CTA
+//     waits for another -- write the stage's activation tile, and pass the
+//     k-tile's scales to the promotion warps through a ring in shared
+//     memory (amax_s, barriers sfull).
 template <int FMT, int MPAD, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(swap_threads(FMT, FUSED),
+                                  (FMT == kFmtBlock && FUSED && MPAD > 32) ? 1 : 2)  // (64-token blocks: registers)
     gemm_f8_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using TS = TileShape<true, MPAD>;
   constexpr bool BLOCK = (FMT == kFmtBlock);
-  static_assert(!(FUSED && BLOCK), "fused quantization is per token");
+  constexpr bool QWARPS = BLOCK && FUSED;                // quantizer warps 6..9
+  constexpr int kT = swap_threads(FMT, FUSED);
   constexpr int NBUF = BLOCK ? 4 : 1;
   constexpr uint32_t kTmemCols = pow2_cols(NBUF * MPAD);
   static_assert(kTmemCols <= 256, "two CTAs per SM share the 512 TMEM columns");
@@ -373,6 +477,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&ctl->amax_bar, 1);
     if (FUSED)
       for (int i = 0; i < stages; ++i) mbar_init(&ctl->full_a[i], 4);
+    if (QWARPS)
+      for (int j = 0; j < kSaRing; ++j) mbar_init(&ctl->sfull[j], 128);
     ctl->last_flag = 0;
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -389,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
       mbar_arrive_expect_tx(&ctl->recv_bar, static_cast<uint32_t>((g.splits - 1) * cluster_rows_of(split, g.splits) *
                                                                   cluster_mv(Mb) * 4));
-      if (FUSED) mbar_arrive_expect_tx(&ctl->amax_bar, static_cast<uint32_t>((g.splits - 1) * Mb * 4));
+      if (FUSED && !BLOCK) mbar_arrive_expect_tx(&ctl->amax_bar, static_cast<uint32_t>((g.splits - 1) * Mb * 4));
     }
     cluster_arrive_relaxed();
   }
@@ -444,10 +550,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
     tc_fence_before();
-    named_bar_sync(2, kThreads - 32);
+    named_bar_sync(2, kT - 32);
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    if (warp == 1) {
+    if (QWARPS && warp >= 6) {
+      // --------------------------------- Block_FP8 activation quantizers
+      block_fused_quantize<MPAD>(g, ctl, smem, TS::kStageBytes, TS::kWBytes, stages, nk, kb0, m_base, Mb, n_tile,
+                                 abort_flag);
+    } else if (warp == 1) {
       // -------------------------------------------------------- MMA issuer
       if (lane == 0) {
         constexpr uint32_t idesc = make_idesc(128, MPAD, 0, 0);  // E4M3 x E4M3 -> F32
@@ -499,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!FUSED && et0 < MPAD) ctl->sa_s[et0] = et0 < Mb ? __ldg(g.s_a + m_base + et0) : 0.0f;
         ctl->sw_s[r] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
       }
-      if constexpr (FUSED) {
+      if constexpr (FUSED && !BLOCK) {
         // per-token scales, then every stage's activation tile as E4M3
         const int et0 = threadIdx.x - 64;
         const bool whole_row = !clustered && g.splits > 1;
@@ -578,23 +688,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         // lane l holds s_a of tokens l, l + 32, ... for the current k-tile
         constexpr int kSaw = (MPAD + 31) / 32;
         float sa_next[kSaw], sa_cur[kSaw];
+        if constexpr (!FUSED) {
 #pragma unroll
-        for (int j = 0; j < kSaw; ++j) {
-          const int t = lane + 32 * j;
-          sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0) : 0.0f;
+          for (int j = 0; j < kSaw; ++j) {
+            const int t = lane + 32 * j;
+            sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0) : 0.0f;
+          }
         }
         float sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
         for (int i = 0; i < nk; ++i) {
           const int buf = i % NBUF;
-#pragma unroll
-          for (int j = 0; j < kSaw; ++j) sa_cur[j] = sa_next[j];
-          const float sw_cur = sw_next;
-          if (i + 1 < nk) {
+          if constexpr (FUSED) {
+            // this k-tile's scales, from the quantizer warps through the ring
+            const int slot = i % kSaRing;
+            if (!__all_sync(0xffffffffu, mbar_wait(&ctl->sfull[slot], static_cast<uint32_t>(i / kSaRing) & 1u,
+                                                   g.wait_ns) && !*abort_flag)) {
+              *abort_flag = 1;
+              break;
+            }
 #pragma unroll
             for (int j = 0; j < kSaw; ++j) {
               const int t = lane + 32 * j;
-              sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i + 1)
-                                  : 0.0f;
+              sa_cur[j] = t < MPAD ? ctl->amax_s[slot * 64 + t] : 0.0f;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kSaw; ++j) sa_cur[j] = sa_next[j];
+          }
+          const float sw_cur = sw_next;
+          if (i + 1 < nk) {
+            if constexpr (!FUSED) {
+#pragma unroll
+              for (int j = 0; j < kSaw; ++j) {
+                const int t = lane + 32 * j;
+                sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i + 1)
+                                    : 0.0f;
+              }
             }
             sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
           }
@@ -655,9 +784,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     store_bf16(g.Y + static_cast<int64_t>(m_base + m) * g.ldy + nn, y);
   };
 
+  const bool epi = warp >= 2 && warp < 6;   // the epilogue warps hold the accumulators
   if (clustered) {
-    if (warp >= 2) {
-      if (!FUSED) cluster_wait();  // every peer's receive barrier is initialized (fused: waited already)
+    if (epi) {
+      if (!FUSED || BLOCK) cluster_wait();  // every peer's receive barrier is initialized (fused FP8: waited already)
       // rows go out even after an abort, so that every owner's wait completes
       cluster_push_row(acc, 0, row, split, g.splits, Mb, recv, &ctl->recv_bar);
       named_bar_sync(1, 128);  // this CTA's own rows, stored locally, are visible
@@ -669,11 +799,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         });
       }
     } else {
-      // the producer and MMA warps pair their early arrive with a wait too
-      // (every peer arrived right after its set-up, so this returns at once)
+      // the producer, MMA (and quantizer) warps pair their early arrive with
+      // a wait too (every peer arrived right after its set-up, so this
+      // returns at once)
       cluster_wait();
     }
-  } else if (warp >= 2 && !abort) {
+  } else if (epi && !abort) {
     const bool n_ok = n < g.N;
     if (g.reduce == kReduceNone) {
       if (n_ok) {

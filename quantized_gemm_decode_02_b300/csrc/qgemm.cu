@@ -295,8 +295,11 @@ int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, q
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_f8_smem_bytes<true, MPAD>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
+  // Block_FP8 fused: the scale ring holds stages + 4 k-tiles
+  if (FMT == qg::kFmtBlock && FUSED && g.stages > qg::kMaxStagesBlockFused) g.stages = qg::kMaxStagesBlockFused;
   return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
-                     qg::kThreads, qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
+                     qg::swap_threads(FMT, FUSED), qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g,
+                     stream);
 }
 
 template <int FMT, int BNW>
@@ -315,6 +318,7 @@ int run_f8_swap_fmt(int fmt, bool fused, const Plan& p, const CUtensorMap& tmW, 
     if (fused) return run_f8_swap<qg::kFmtFP8, MPAD, true>(p, tmW, tmA, g, config_id, stream);
     return run_f8_swap<qg::kFmtFP8, MPAD, false>(p, tmW, tmA, g, config_id, stream);
   }
+  if (fused) return run_f8_swap<qg::kFmtBlock, MPAD, true>(p, tmW, tmA, g, config_id, stream);
   return run_f8_swap<qg::kFmtBlock, MPAD, false>(p, tmW, tmA, g, config_id, stream);
 }
 
@@ -359,8 +363,8 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
 // distance, and wide tiles only for the FP8_Dynamic Standard / Split-K forms.
 int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
-      (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_RING_MASK |
-                     QG_CONFIG_PREFETCH_MASK)) ||
+      (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
+                     QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -371,6 +375,9 @@ int check_config_bits(int fmt, int variant, int config_id) {
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
   if ((config_id & QG_CONFIG_MMA_NARROW) && !(config_id & QG_CONFIG_MMA_SYNC))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_NARROW needs QG_CONFIG_MMA_SYNC");
+  if ((config_id & QG_CONFIG_FUSED_QUANT) &&
+      (!(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || (config_id & QG_CONFIG_MMA_SYNC)))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_FUSED_QUANT is for the Swap-AB variants on the tcgen05 kernels");
   if ((config_id & QG_CONFIG_RING_MASK) == 1) return fail(QG_ERR_INVALID_ARG, "config_id (stages) must be >= 2");
   return QG_OK;
 }
@@ -914,10 +921,10 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
                    void* workspace_dev, size_t ws_bytes, void* A_q_dev, float* s_a_dev, int32_t* debug_acc_dev,
                    void* stream) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
-  const bool fusable = fmt != QG_BLOCK_FP8 && (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) &&
-                       !(config_id & QG_CONFIG_MMA_SYNC);
+  const bool fusable = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) && !(config_id & QG_CONFIG_MMA_SYNC);
   const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
-  if (fusable && (!buffers || (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {
+  if (fusable && (!buffers || (config_id & QG_CONFIG_FUSED_QUANT) ||
+                  (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {
     // one kernel: each CTA quantizes the activations its K range needs
     if ((A_q_dev && !aligned(A_q_dev, 16)) || (s_a_dev && !aligned(s_a_dev, 4)))
       return fail(QG_ERR_ALIGNMENT, "A_q needs 16-byte alignment, s_a 4");
@@ -928,7 +935,7 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
   // two kernels: quantize into the caller's A_q / s_a, then the GEMM
   if (!buffers)
     return fail(QG_ERR_INVALID_ARG,
-                "qg_linear_w8a8: Block_FP8, the Standard and the dp4a variants need A_q and s_a buffers");
+                "qg_linear_w8a8: the Standard, dp4a and mma.sync forms need A_q and s_a buffers");
   int rc = qg_quant_act(fmt, A_dev, M, K, lda, A_q_dev, s_a_dev, stream);
   if (rc != QG_OK) return rc;
   return gemm_entry(fmt, M, N, K, A_q_dev, s_a_dev, W_q_dev, s_w_dev, Y_dev, ldy, variant, split_k, config_id,

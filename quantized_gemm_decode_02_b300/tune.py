@@ -19,7 +19,8 @@ same-shape chains lost in the mixed-shape chains of bench.py.
 Rows already present in the output table are skipped, so an interrupted
 sweep resumes where it stopped.
 
-With --layer-context TABLE_IN the rows are re-tuned where they run: for
+With --layer-context TABLE_IN the rows are re-tuned where they run (for
+Block_FP8 also the one-kernel form of the linear, QG_CONFIG_FUSED_QUANT): for
 each token count the candidates of one linear are timed inside the chain
 of the whole decoder layer (activation quantization and GEMM of qkv, o,
 gate_up and down in order, one CUDA graph with programmatic dependent
@@ -247,7 +248,12 @@ def layer_context_pass(bench, table_in, out_path, fmts, models, ms, sms, log=Non
                 base = time_layer_chain(bench, fmt, M, shapes, cfgs)
                 best_total = base
                 for li, (layer, (K, N)) in enumerate(layers):
-                    for cand in candidates(fmt, M, N, K, sms):
+                    cands = candidates(fmt, M, N, K, sms)
+                    if fmt == "Block_FP8":
+                        # the one-kernel form of the linear (quantization inside the GEMM)
+                        cands += [(v, sp, c | q.QG_CONFIG_FUSED_QUANT) for (v, sp, c) in cands
+                                  if v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK)]
+                    for cand in cands:
                         if cand == cfgs[li]:
                             continue
                         trial = list(cfgs)

@@ -39,9 +39,9 @@ def q():
 
 
 def tie_rows(fmt: str, M: int, K: int, rng) -> torch.Tensor:
-    """Activations whose quotients x / s land on rounding ties: every row has
-    its maximum at a power of two times QMAX, so s is a power of two and
-    x = s * midpoint is exact in bf16."""
+    """Activations whose quotients x / s land on rounding ties: every row (for
+    Block_FP8 every 1x128 group) has its maximum at a power of two times
+    QMAX, so s is a power of two and x = s * midpoint is exact in bf16."""
     A = np.zeros((M, K), np.float32)
     if fmt == "W8A8_INT8":
         mids = (np.arange(-126, 127) + 0.5).astype(np.float32)   # k + 1/2
@@ -53,11 +53,13 @@ def tie_rows(fmt: str, M: int, K: int, rng) -> torch.Tensor:
         mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)     # E4M3 rounding midpoints
         mids = np.concatenate([mids, -mids])
         qmax = 448.0
+    span = 128 if fmt == "Block_FP8" else K                       # the scale's span: a 1x128 group or the row
     for m in range(M):
-        s = np.float32(2.0 ** int(rng.integers(-12, 4)))
-        row = rng.choice(mids, size=K) * s
-        row[int(rng.integers(0, K))] = qmax * s                   # the row maximum: s = amax / qmax exactly
-        A[m] = row
+        for k0 in range(0, K, span):
+            s = np.float32(2.0 ** int(rng.integers(-12, 4)))
+            seg = rng.choice(mids, size=span) * s
+            seg[int(rng.integers(0, span))] = qmax * s              # the maximum: s = amax / qmax exactly
+            A[m, k0:k0 + span] = seg
     t = torch.from_numpy(A).to(torch.bfloat16)
     assert torch.equal(t.float(), torch.from_numpy(A)), "tie rows must be exact in bf16"
     return t
@@ -217,6 +219,68 @@ def test_two_kernel_linear_graph_replays(orc, gc, q, pdl):
 def test_linear_needs_buffers_when_not_fused(q, gc):
     d = torch.zeros(1024, dtype=torch.uint8, device=gc.DEV)
     f = torch.zeros(64, dtype=torch.float32, device=gc.DEV)
-    with pytest.raises(q.QGError) as e:
-        q.qg_linear_w8a8("Block_FP8", 4, 128, 128, d, 128, d, f, d, 128, SW, 1)
-    assert e.value.code == q.QG_ERR_INVALID_ARG
+    for fmt, v, cfg in (("Block_FP8", ST, 0), ("W8A8_INT8", DP, 0), ("W8A8_INT8", SW, q.config_id(mma_sync=True))):
+        with pytest.raises(q.QGError) as e:
+            q.qg_linear_w8a8(fmt, 4, 128, 128, d, 128, d, f, d, 128, v, 1, cfg)
+        assert e.value.code == q.QG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M,split", [(1, 1), (5, 3), (16, 8), (17, 2), (32, 16), (24, 17), (48, 5), (100, 3)])
+def test_fused_linear_block_fp8(orc, gc, q, M, split):
+    # Block_FP8 in one kernel: quantizer warps scale every 1x128 group
+    # themselves; K = 2304 (18 k-tiles), ragged N; cluster and workspace
+    # Split-K; 17 ranges through the workspace; blocks of 64 tokens above 64
+    run_linear(orc, gc, q, "Block_FP8", M, 328, 2304, SWS if split > 1 else SW, split, seed=450 + M + split)
+
+
+@pytest.mark.parametrize("split", [1, 4, 20])
+def test_fused_block_fp8_ties_and_zeros(orc, gc, q, split):
+    # groups whose quotients land on E4M3 rounding ties (per-group scales are
+    # powers of two), signed zeros and an all-zero group
+    M, N, K = 32, 256, 2560
+    rng = np.random.Generator(np.random.PCG64(91 + split))
+    A = tie_rows("Block_FP8", M, K, rng)
+    A[0, :128] = -0.0
+    A[1, 256:384] = 0.0
+    A[2, ::7] = -0.0
+    run_linear(orc, gc, q, "Block_FP8", M, N, K, SWS if split > 1 else SW, split, seed=6, A=A)
+
+
+@pytest.mark.parametrize("ring", [2, 6, 12, 16])
+def test_fused_block_fp8_ring_depths(orc, gc, q, ring):
+    # the scale ring between the quantizer and promotion warps holds
+    # stages + 4 k-tiles; a requested ring deeper than 12 is capped
+    M, N, K = 20, 256, 4096
+    A = si.activations(M, K, seed=70 + ring, outliers=True)
+    W = si.weights(N, K, seed=70 + ring)
+    Wq, sw = gc.quant_weight_gpu("Block_FP8", torch.from_numpy(W).to(gc.DEV))
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=gc.DEV)
+    Aq = torch.empty((M, K), dtype=torch.uint8, device=gc.DEV)
+    sa = torch.empty((M, K // 128), dtype=torch.float32, device=gc.DEV)
+    q.qg_linear_w8a8("Block_FP8", M, N, K, A.to(gc.DEV), K, Wq, sw, Y, N, SW, 1, q.config_id(ring, fused=True),
+                     None, 0, Aq, sa)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    oAq, osa, oWq, osw = gc.check_quant(orc, "Block_FP8", A, W, Aq, sa, Wq, sw)
+    gc.check_gemm(orc, "Block_FP8", oAq, osa, oWq, osw, Y)
+
+
+def test_fused_quant_config_bit_selects_one_kernel(orc, gc, q):
+    # with A_q / s_a buffers given, the table bit asks for the one-kernel
+    # form: the GEMM writes the buffers itself (same codes as the
+    # quantization kernel) and the outputs match the two-kernel form
+    fmt, M, N, K = "Block_FP8", 9, 384, 2048
+    A = si.activations(M, K, seed=71, outliers=True).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=71)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu(fmt, W)
+    outs = []
+    for cfg in (0, q.config_id(fused=True)):
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=gc.DEV)
+        Aq = torch.full((M, K), 0x5A, dtype=torch.uint8, device=gc.DEV)
+        sa = torch.full((M, K // 128), -1.0, dtype=torch.float32, device=gc.DEV)
+        q.qg_linear_w8a8(fmt, M, N, K, A, K, Wq, sw, Y, N, SWS, 4, cfg, None, 0, Aq, sa)
+        torch.cuda.synchronize()
+        outs.append((Y, Aq, sa))
+    assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert q.qg_device_error() == 0
