@@ -81,6 +81,7 @@ typedef enum {
 #define QG_CONFIG_MMA_SYNC (1 << 13)
 #define QG_CONFIG_MMA_NARROW (1 << 14)
 #define QG_CONFIG_FUSED_QUANT (1 << 15)
+#define QG_CONFIG_PERSIST (1 << 16)
 
 typedef enum {
   QG_OK = 0,
@@ -168,6 +169,15 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      tcgen05 kernels): a hint for qg_linear_w8a8 to take
  *                      its one-kernel form even when A_q / s_a buffers are
  *                      given (qg_gemm_w8a8 accepts and ignores it);
+ *                      plus QG_CONFIG_PERSIST for FP8_Dynamic with
+ *                      QG_STANDARD (the compute-bound regime, M of 64 and
+ *                      more): a persistent kernel (at most one CTA per SM)
+ *                      whose thread-block cluster pairs take two 128-token
+ *                      tiles of one 256-row weight tile, each loading half
+ *                      of the weight tile by TMA multicast into both CTAs,
+ *                      with two TMEM accumulators so that a tile's epilogue
+ *                      overlaps the next tile's MMAs; only the ring depth
+ *                      may be combined with it (QG_ERR_INVALID_ARG else);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

@@ -25,6 +25,7 @@
 #include "gemm_i8.cuh"
 #include "gemm_i8_dp4a.cuh"
 #include "gemm_i8_mma.cuh"
+#include "gemm_f8_persist.cuh"
 #include "quant.cuh"
 
 namespace {
@@ -140,10 +141,11 @@ size_t two_per_sm_smem() {
 }
 
 // Launch with the library's launch flags; cluster_y > 1 groups that many
-// consecutive blockIdx.y into one thread-block cluster.
+// consecutive blockIdx.y into one thread-block cluster (cluster_x likewise
+// along x).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                           unsigned cluster_y, Args&&... args) {
+cudaError_t launch_cluster_xy(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              unsigned cluster_x, unsigned cluster_y, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -156,9 +158,9 @@ cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
-  if (cluster_y > 1) {
+  if (cluster_x > 1 || cluster_y > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.x = cluster_x;
     attr[n].val.clusterDim.y = cluster_y;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -166,6 +168,11 @@ cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           unsigned cluster_y, Args&&... args) {
+  return launch_cluster_xy(kernel, grid, block, smem, stream, 1u, cluster_y, std::forward<Args>(args)...);
 }
 
 template <typename... KArgs, typename... Args>
@@ -187,6 +194,7 @@ struct Plan {
   bool swap = false;
   bool dp4a = false;   // W8A8_INT8 Swap-AB on the CUDA cores (M <= 8)
   bool mma = false;    // W8A8_INT8 Swap-AB on mma.sync (QG_CONFIG_MMA_SYNC)
+  bool persist = false;  // FP8_Dynamic Standard as the persistent pair kernel (QG_CONFIG_PERSIST)
   int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64 (mma.sync: 8 / 16 / 24 / 32)
   int ctr_tiles = 0;   // Split-K arrival counters of one group: enough for every kernel's token blocks
   int n_tiles = 0, m_tiles = 0, kt = 0, splits = 1;
@@ -199,6 +207,9 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   p->dp4a = (variant == QG_SWAPAB_DP4A || variant == QG_SWAPAB_DP4A_SPLITK);
   p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->dp4a;
   p->mma = (config_id & QG_CONFIG_MMA_SYNC) != 0;
+  p->persist = (config_id & QG_CONFIG_PERSIST) != 0;
+  if (p->persist && (fmt != QG_FP8_DYNAMIC || variant != QG_STANDARD))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PERSIST is for FP8_Dynamic with QG_STANDARD");
   if (p->dp4a && (fmt != QG_W8A8_INT8 || M > qg::kDpMaxTokens))
     return fail(QG_ERR_UNSUPPORTED_SHAPE, "the dp4a variants take W8A8_INT8 with M <= %d", qg::kDpMaxTokens);
   if (p->mma && (fmt != QG_W8A8_INT8 || !p->swap || p->dp4a))
@@ -221,6 +232,11 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
     p->mpad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
+  } else if (p->persist) {
+    // pair tiles of 256 tokens x 256 weight rows
+    p->m_tiles = static_cast<int>(cdiv(M, 256));
+    p->n_tiles = static_cast<int>(cdiv(N, 256));
+    if (static_cast<int64_t>(p->m_tiles) * p->n_tiles > 0x7FFFFFFF) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else {
     p->m_tiles = static_cast<int>(cdiv(M, 128));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
@@ -349,6 +365,51 @@ int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg
   return run_i8_mma_t<NG, 2>(p, tmW, tmA, g, config_id, stream);
 }
 
+// Persistent pair kernel: one CTA per SM at most (two per cluster); the
+// ring takes the deepest depth that fits one CTA's shared memory unless
+// config_id asks for fewer stages.
+int run_f8_persist(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                   cudaStream_t stream) {
+  const DevInfo d = dev_info();
+  int st = 8;
+  while (st > 2 && qg::gemm_f8_persist_smem_bytes(st) > d.smem_optin) --st;
+  const int want = config_id & QG_CONFIG_RING_MASK;
+  if (want >= 2 && want < st) st = want;
+  g.stages = st;
+  const size_t smem = qg::gemm_f8_persist_smem_bytes(st);
+  cudaError_t e = set_smem(qg::gemm_f8_persist_kernel, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  // the tile schedule is static, so only clusters that can all be resident
+  // at once are launched (a cluster placed later would finish its share late)
+  int resident = 0;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(qg::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&resident, qg::gemm_f8_persist_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // clear the query's error; fall back to one pair per two SMs
+      resident = 0;
+    }
+  }
+  const int sms = d.sms > 0 ? d.sms : 148;
+  if (resident <= 0 || resident > sms / 2) resident = sms / 2;
+  const int clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, resident)));
+  g.reduce = qg::kReduceNone;
+  e = launch_cluster_xy(qg::gemm_f8_persist_kernel, dim3(2 * clusters), dim3(qg::kThreads), smem, stream, 2u, 1u, tmW,
+                        tmA, g);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+  return QG_OK;
+}
+
 template <int MT>
 int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
              cudaStream_t stream) {
@@ -364,7 +425,7 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
 int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
-                     QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_PERSIST | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -375,6 +436,10 @@ int check_config_bits(int fmt, int variant, int config_id) {
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
   if ((config_id & QG_CONFIG_MMA_NARROW) && !(config_id & QG_CONFIG_MMA_SYNC))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_NARROW needs QG_CONFIG_MMA_SYNC");
+  if ((config_id & QG_CONFIG_PERSIST) &&
+      (fmt != QG_FP8_DYNAMIC || variant != QG_STANDARD ||
+       (config_id & (QG_CONFIG_WIDE | QG_CONFIG_PREFETCH_MASK | QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT))))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PERSIST is for FP8_Dynamic with QG_STANDARD (ring depth only)");
   if ((config_id & QG_CONFIG_FUSED_QUANT) &&
       (!(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || (config_id & QG_CONFIG_MMA_SYNC)))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_FUSED_QUANT is for the Swap-AB variants on the tcgen05 kernels");
@@ -586,6 +651,10 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (M <= 2) return run_dp4a<2>(p, tmW, tmA, g, config_id, s);
     if (M <= 4) return run_dp4a<4>(p, tmW, tmA, g, config_id, s);
     return run_dp4a<8>(p, tmW, tmA, g, config_id, s);
+  }
+  if (p.persist) {
+    if (fz) return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PERSIST takes quantized activations");
+    return run_f8_persist(p, tmW, tmA, g, config_id, s);
   }
   if (p.mma) {
     if (fz) return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_SYNC takes quantized activations");

@@ -108,6 +108,10 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
                 if s <= kt and std_tiles * s <= 4 * sms:
                     out.append((q.QG_SPLITK, s, cfg))
         if fmt == "FP8_Dynamic":
+            # the persistent pair kernel (one CTA per SM, weight tile shared
+            # by TMA multicast, two TMEM accumulators): deepest ring, or 3
+            for ring in (0, 3):
+                out.append((q.QG_STANDARD, 1, q.config_id(ring, persist=True)))
             # 256-row weight tiles: ring of 2 (two CTAs per SM) or 4 (one)
             wide_tiles = -(-N // 256) * -(-M // 128)
             for cfg in (q.config_id(0, 0, True), q.config_id(4, 0, True)):

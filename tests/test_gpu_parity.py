@@ -335,3 +335,73 @@ def test_mma_sync_config_rejected_outside_int8_swap_ab(q, gc):
     with pytest.raises(q.QGError) as e:  # the narrow form is a form of the mma.sync kernel only
         q.qg_gemm_w8a8("W8A8_INT8", 8, 256, 256, d, f, d, f, d, 256, SW, 1, q.QG_CONFIG_MMA_NARROW)
     assert e.value.code == q.QG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M", [64, 100, 256, 300, 513])
+@pytest.mark.parametrize("N,K", [(424, 656), (1024, 2048)])
+def test_fp8_persistent_pairs(orc, q, gc, M, N, K):
+    # the persistent pair kernel (QG_CONFIG_PERSIST): 256-token pair tiles
+    # (the second CTA of the last pair partly or wholly past M), 256-row
+    # weight tiles (N = 424: one full, one ragged), ragged K (656: the last
+    # k-tile 16 wide)
+    gc.run_case(orc, "FP8_Dynamic", M, N, K, ST, 1, seed=800 + M + N, outliers=True,
+                config_id=q.config_id(persist=True))
+
+
+@pytest.mark.parametrize("ring", [2, 3])
+def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring):
+    # 3 x 80 = 240 pair tiles: every cluster takes several tiles, so both
+    # TMEM accumulators and the weight-scale slots are reused; shallow rings
+    # wrap many times.  Sampled columns against the oracle.
+    import seeded_inputs as si
+    M, N, K = 600, 20480, 512
+    A = si.activations(M, K, seed=820 + ring, outliers=True)
+    W = si.weights(N, K, seed=820 + ring)
+    Wq, sw = gc.quant_weight_gpu("FP8_Dynamic", torch.from_numpy(W).to(gc.DEV))
+    Aq, sa = gc.quant_act_gpu("FP8_Dynamic", A.to(gc.DEV))
+    Y, _ = gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, ST, 1, config_id=q.config_id(ring, persist=True))
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    ns = np.concatenate([np.arange(0, 300), np.arange(10000, 10300), np.arange(N - 300, N)])
+    oAq, osa = orc.quant_act("FP8_Dynamic", si.bf16_to_f32_numpy(A))
+    oWq, osw = orc.quant_weight("FP8_Dynamic", W)
+    assert np.array_equal(Aq.cpu().numpy(), oAq)
+    gc.check_gemm(orc, "FP8_Dynamic", oAq, osa, oWq, osw, Y, ns=ns)
+    assert not torch.isnan(Y.float()).any()
+
+
+def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc):
+    import seeded_inputs as si
+    M, N, K = 300, 1024, 1024
+    A = si.activations(M, K, seed=830)
+    W = si.weights(N, K, seed=830)
+    Wq, sw = gc.quant_weight_gpu("FP8_Dynamic", torch.from_numpy(W).to(gc.DEV))
+    Aq, sa = gc.quant_act_gpu("FP8_Dynamic", A.to(gc.DEV))
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    cfg = q.config_id(persist=True)
+    q.qg_set_wait_limit_ns(2_000_000)
+    q.qg_set_force_timeout(True)
+    try:
+        gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, ST, 1, config_id=cfg)
+        assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
+    finally:
+        q.qg_set_force_timeout(False)
+        q.qg_set_wait_limit_ns(0)
+    Y, _ = gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, ST, 1, config_id=cfg)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    oAq, osa, oWq, osw = gc.check_quant(orc, "FP8_Dynamic", A, W, Aq, sa, Wq, sw)
+    gc.check_gemm(orc, "FP8_Dynamic", oAq, osa, oWq, osw, Y)
+
+
+def test_persist_config_rejected_elsewhere(q, gc):
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device=gc.DEV)
+    f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
+    for fmt, v, s, cfg in (("Block_FP8", ST, 1, q.config_id(persist=True)),
+                           ("FP8_Dynamic", SW, 1, q.config_id(persist=True)),
+                           ("FP8_Dynamic", STS, 2, q.config_id(persist=True)),
+                           ("FP8_Dynamic", ST, 1, q.config_id(persist=True, wide=True))):
+        with pytest.raises(q.QGError) as e:
+            q.qg_gemm_w8a8(fmt, 64, 256, 256, d, f, d, f, d, 256, v, s, cfg)
+        assert e.value.code == q.QG_ERR_INVALID_ARG
