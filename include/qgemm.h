@@ -82,6 +82,8 @@ typedef enum {
 #define QG_CONFIG_MMA_NARROW (1 << 14)
 #define QG_CONFIG_FUSED_QUANT (1 << 15)
 #define QG_CONFIG_PERSIST (1 << 16)
+#define QG_CONFIG_MMA_DP4A_SHIFT 17
+#define QG_CONFIG_MMA_DP4A_MASK (7 << 17)
 
 typedef enum {
   QG_OK = 0,
@@ -164,7 +166,12 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      form of qg_linear_w8a8, which then runs two kernels);
  *                      with QG_CONFIG_MMA_SYNC also QG_CONFIG_MMA_NARROW:
  *                      eight MMA warps of 16 weight rows instead of four
- *                      of 32 (more warps to hide the widening's latency);
+ *                      of 32 (more warps to hide the widening's latency),
+ *                      and with that d << QG_CONFIG_MMA_DP4A_SHIFT (d = 1..4,
+ *                      M <= 16): the first 16*d rows of each weight tile go
+ *                      to d warps of dp4a threads instead, on the integer
+ *                      pipe the widening leaves idle (same exact result;
+ *                      QG_ERR_UNSUPPORTED_SHAPE for M > 16);
  *                      plus QG_CONFIG_FUSED_QUANT (Swap-AB variants on the
  *                      tcgen05 kernels): a hint for qg_linear_w8a8 to take
  *                      its one-kernel form even when A_q / s_a buffers are
@@ -177,7 +184,9 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      of the weight tile by TMA multicast into both CTAs,
  *                      with two TMEM accumulators so that a tile's epilogue
  *                      overlaps the next tile's MMAs; only the ring depth
- *                      may be combined with it (QG_ERR_INVALID_ARG else);
+ *                      and the L2 prefetch distance (weight k-tiles of the
+ *                      CTA's half requested ahead, across tiles) may be
+ *                      combined with it (QG_ERR_INVALID_ARG else);
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

@@ -685,17 +685,32 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
       }
       if constexpr (BLOCK) {
         const int nb = n_tile;  // 128-row tile == weight block row
+        // Two-kernel form: the products s_a[m,kb] * s_w[nb,kb] of the CTA's
+        // whole K range are loaded with every request in flight right after
+        // the dependency wait, into amax_s (unused by this form) when they
+        // fit, so no k-tile's promotion waits on a load; otherwise each
+        // k-tile's scales are fetched one k-tile ahead.
+        const bool staged = !FUSED && nk * MPAD <= kMaxClusterSplits * 64;
+        if (staged) {
+          for (int e = threadIdx.x - 64; e < nk * MPAD; e += 128) {
+            const int i = e / MPAD, t = e - i * MPAD;
+            ctl->amax_s[e] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) *
+                                          __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
+                                    : 0.0f;
+          }
+          named_bar_sync(1, 128);
+        }
         // lane l holds s_a of tokens l, l + 32, ... for the current k-tile
         constexpr int kSaw = (MPAD + 31) / 32;
         float sa_next[kSaw], sa_cur[kSaw];
-        if constexpr (!FUSED) {
+        if (!FUSED && !staged) {
 #pragma unroll
           for (int j = 0; j < kSaw; ++j) {
             const int t = lane + 32 * j;
             sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0) : 0.0f;
           }
         }
-        float sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
+        float sw_next = staged ? 0.0f : __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
         for (int i = 0; i < nk; ++i) {
           const int buf = i % NBUF;
           if constexpr (FUSED) {
@@ -711,12 +726,12 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
               const int t = lane + 32 * j;
               sa_cur[j] = t < MPAD ? ctl->amax_s[slot * 64 + t] : 0.0f;
             }
-          } else {
+          } else if (!staged) {
 #pragma unroll
             for (int j = 0; j < kSaw; ++j) sa_cur[j] = sa_next[j];
           }
           const float sw_cur = sw_next;
-          if (i + 1 < nk) {
+          if (i + 1 < nk && !staged) {
             if constexpr (!FUSED) {
 #pragma unroll
               for (int j = 0; j < kSaw; ++j) {
@@ -744,10 +759,16 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&ctl->tempty[buf]);
+          if (staged) {
+            const float* coefs = ctl->amax_s + i * MPAD;
 #pragma unroll
-          for (int m = 0; m < MPAD; ++m) {
-            const float coef = __shfl_sync(0xffffffffu, sa_cur[m / 32], m & 31) * sw_cur;
-            acc[m] = fmaf(coef, __uint_as_float(v[m]), acc[m]);
+            for (int m = 0; m < MPAD; ++m) acc[m] = fmaf(coefs[m], __uint_as_float(v[m]), acc[m]);
+          } else {
+#pragma unroll
+            for (int m = 0; m < MPAD; ++m) {
+              const float coef = __shfl_sync(0xffffffffu, sa_cur[m / 32], m & 31) * sw_cur;
+              acc[m] = fmaf(coef, __uint_as_float(v[m]), acc[m]);
+            }
           }
         }
         // the MMA thread's final commit: all MMAs done before teardown

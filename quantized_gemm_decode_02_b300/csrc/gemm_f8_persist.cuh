@@ -141,6 +141,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pol_w);
         }
       }
+      // this CTA's weight half of the k-tile `ahead` k-tiles past (tile t,
+      // k-tile kk) is requested into L2 (no shared memory): the ring then
+      // only has to cover the L2 latency, not the HBM one
+      const int ahead = g.l2_prefetch;
+      auto prefetch_ahead = [&](int t, int kk) {
+        int t2 = t, k2 = kk + ahead;
+        while (k2 >= nk && t2 < tiles) {
+          k2 -= nk;
+          t2 += clusters;
+        }
+        if (t2 < tiles) tma_prefetch_l2_2d(&tmW, k2 * kBK, (t2 / tp_count) * kPsRows + static_cast<int>(rank) * kPsTok);
+      };
+      if (ahead > 0 && first >= 0)
+        for (int kk = pre; kk < pre + ahead; ++kk) prefetch_ahead(first, kk - ahead);
       pdl_wait();
       int i = 0;  // k-tile counter over all of this CTA's tiles (the ring position)
       bool ok = true;
@@ -151,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < nk; ++kk, ++i) {
           const int s = i % stages;
           uint8_t* st = smem + static_cast<size_t>(s) * kPsStageBytes;
+          if (ahead > 0 && i >= pre) prefetch_ahead(t, kk);
           if (i >= pre) {
             if (i >= stages && (!mbar_wait(&ctl->empty[s], (static_cast<uint32_t>(i / stages) & 1u) ^ 1u, g.wait_ns) ||
                                 *abort_flag)) {

@@ -40,6 +40,11 @@
 //   last warp   widens the activation tile once per k-tile into f16
 //               fragments in shared memory ([step][group][lane], 8 bytes),
 //               read by every MMA warp.
+// With DPW > 0 (eight-warp layout, up to 16 tokens) the first 16*DPW weight
+// rows go to DPW warps of dp4a threads instead (two per row, a K half each,
+// exact int32 sums as in gemm_i8_dp4a.cuh): dp4a runs on its own integer
+// pipe, which the widening and the MMAs leave idle, so the two halves of the
+// tile proceed side by side.
 // The epilogue, the Split-K reduction (cluster push or workspace) and the
 // scales are those of the other Swap-AB kernels, one thread per weight row.
 #pragma once
@@ -100,14 +105,16 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
   return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-template <int NG, int TPW>
+template <int NG, int TPW, int DPW>
 __global__ void __launch_bounds__(ms_threads(TPW), 2)
     gemm_i8_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = MsShape<NG>;
   constexpr int MPAD = S::kMpad;
-  constexpr int kMsWarps = ms_mma_warps(TPW);  // MMA warps 1..kMsWarps
-  constexpr int kMsAWarp = 1 + kMsWarps;       // activation widening warp
-  constexpr int kEpi = 128;                     // per-row epilogue threads (warps 1..4)
+  static_assert(DPW == 0 || (TPW == 1 && NG <= 2 && DPW <= 4), "dp4a rows: eight-warp layout, up to 16 tokens");
+  constexpr int kRD = 16 * DPW;                      // weight rows on dp4a (rows 0 .. kRD-1)
+  constexpr int kMsWarps = ms_mma_warps(TPW) - DPW;  // MMA warps 1..kMsWarps (rows kRD ..)
+  constexpr int kMsAWarp = 1 + kMsWarps + DPW;       // activation widening warp (dp4a warps before it)
+  constexpr int kEpi = 128;                          // per-row epilogue threads (warps 1..4)
   stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->full_a[i], 1);
-      mbar_init(&ctl->empty[i], 32 * (kMsWarps + 1));
+      mbar_init(&ctl->empty[i], 32 * (kMsWarps + DPW + 1));
     }
     for (int b = 0; b < kMsABufs; ++b) {
       mbar_init(&ctl->afull[b], 32);
@@ -165,6 +172,10 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
 
   // MMA warps: int32 sums of weight rows r0 = 32*cw + 16*t + gid and r0 + 8
   // for tokens 8*grp + 2*tig + {0,1} (the D fragment layout)
+  // dp4a threads: int32 sums of their row's K half for every token
+  int32_t dacc[DPW > 0 ? MPAD : 1];
+#pragma unroll
+  for (int m = 0; m < (DPW > 0 ? MPAD : 1); ++m) dacc[m] = 0;
   int32_t iacc[TPW][NG][4];
 #pragma unroll
   for (int t = 0; t < TPW; ++t)
@@ -245,6 +256,39 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
       mbar_arrive(&ctl->afull[b]);  // this lane's fragments are written (release)
     }
     if (!ok) *abort_flag = 1;
+  } else if (DPW > 0 && warp > kMsWarps) {
+    // ---------------------------------------------------------- dp4a warps
+    const int d = static_cast<int>(threadIdx.x) - 32 * (1 + kMsWarps);  // 0 .. 32*DPW-1
+    const int row = d % (kRD > 0 ? kRD : 1), h = d / (kRD > 0 ? kRD : 1);  // weight row, K half
+    bool ok = true;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % stages;
+      const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
+      const bool w = mbar_wait(&ctl->full[s], ph, g.wait_ns) && mbar_wait(&ctl->full_a[s], ph, g.wait_ns);
+      if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* wt = smem + static_cast<size_t>(s) * S::kStageBytes;
+      const uint8_t* at = wt + S::kWBytes;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * h + cc;
+        const uint4 wv = *reinterpret_cast<const uint4*>(wt + sw128_chunk(static_cast<uint32_t>(row), c));
+#pragma unroll
+        for (int m = 0; m < (DPW > 0 ? MPAD : 1); ++m) {
+          const uint4 av = *reinterpret_cast<const uint4*>(at + sw128_chunk(static_cast<uint32_t>(m), c));
+          int32_t a = dacc[m];
+          a = __dp4a(static_cast<int>(wv.x), static_cast<int>(av.x), a);
+          a = __dp4a(static_cast<int>(wv.y), static_cast<int>(av.y), a);
+          a = __dp4a(static_cast<int>(wv.z), static_cast<int>(av.z), a);
+          a = __dp4a(static_cast<int>(wv.w), static_cast<int>(av.w), a);
+          dacc[m] = a;
+        }
+      }
+      mbar_arrive(&ctl->empty[s]);  // this lane's reads of the stage are done
+    }
+    if (!ok) *abort_flag = 1;
   } else {
     // ---------------------------------------------------------- MMA warps
     const int cw = warp - 1;
@@ -271,7 +315,7 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
       for (int t = 0; t < TPW; ++t)
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-          const uint32_t row = static_cast<uint32_t>(16 * TPW * cw + 16 * t + 8 * rr + gid);
+          const uint32_t row = static_cast<uint32_t>(kRD + 16 * TPW * cw + 16 * t + 8 * rr + gid);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
             wv[t][rr][hh] = *reinterpret_cast<const uint4*>(wt + sw128_chunk(row, 2 * tig + hh));
@@ -318,29 +362,39 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
       }
     }
     if (!ok) *abort_flag = 1;
-    const int r = threadIdx.x - 32;  // weight row of the tile for the per-row epilogue
-    const int nn = n_tile * kBN + r;
-    if (r < kBN) ctl->sw_s[r] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
   }
   // ------------------------------------------------- per-row accumulators
   __syncthreads();  // the ring is idle: every issued copy was consumed by the MMA warps
   const bool abort = ctl->abort_flag != 0;  // stable after the barrier: uniform
-  int32_t* acc_s = reinterpret_cast<int32_t*>(smem);  // [128 rows][kAccStride] over stage 0
+  // [128 rows][kAccStride] over the idle ring, then (dp4a rows) the second
+  // K half's sums [kRD rows][kAccStride]
+  int32_t* acc_s = reinterpret_cast<int32_t*>(smem);
+  int32_t* acc2_s = acc_s + kBN * S::kAccStride;
   if (warp >= 1 && warp <= kMsWarps) {
     const int cw = warp - 1;
 #pragma unroll
     for (int t = 0; t < TPW; ++t)
 #pragma unroll
       for (int q = 0; q < NG; ++q) {
-        const int row = 16 * TPW * cw + 16 * t + gid, m = 8 * q + 2 * tig;
+        const int row = kRD + 16 * TPW * cw + 16 * t + gid, m = 8 * q + 2 * tig;
         *reinterpret_cast<int2*>(acc_s + row * S::kAccStride + m) = make_int2(iacc[t][q][0], iacc[t][q][1]);
         *reinterpret_cast<int2*>(acc_s + (row + 8) * S::kAccStride + m) = make_int2(iacc[t][q][2], iacc[t][q][3]);
       }
+  } else if (DPW > 0 && warp > kMsWarps && warp < kMsAWarp) {
+    const int d = static_cast<int>(threadIdx.x) - 32 * (1 + kMsWarps);
+    const int row = d % (kRD > 0 ? kRD : 1), h = d / (kRD > 0 ? kRD : 1);
+    int32_t* dst = (h == 0 ? acc_s : acc2_s) + row * S::kAccStride;
+#pragma unroll
+    for (int m = 0; m < (DPW > 0 ? MPAD : 1); ++m) dst[m] = dacc[m];
+  }
+  const bool holds_row = warp >= 1 && warp <= kEpi / 32;
+  const int ct = threadIdx.x - 32;  // row of the tile (warps 1..4)
+  if (holds_row) {
+    const int nn = n_tile * kBN + ct;
+    ctl->sw_s[ct] = nn < g.N ? __ldg(s_w + nn) : 0.0f;
   }
   __syncthreads();
   pdl_wait();  // outputs are written only after the kernel this one depends on
-  const bool holds_row = warp >= 1 && warp <= kEpi / 32;
-  const int ct = threadIdx.x - 32;  // row of the tile (the first four MMA warps)
   int32_t acc[MPAD];
   if (holds_row) {
 #pragma unroll
@@ -348,6 +402,10 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
       const int2 v = *reinterpret_cast<const int2*>(acc_s + ct * S::kAccStride + m);
       acc[m] = v.x;
       acc[m + 1] = v.y;
+    }
+    if (DPW > 0 && ct < kRD) {
+#pragma unroll
+      for (int m = 0; m < MPAD; ++m) acc[m] += acc2_s[ct * S::kAccStride + m];
     }
   }
   auto finish = [&](int m, int r, int nn, int32_t sum) {

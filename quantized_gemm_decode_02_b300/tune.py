@@ -93,8 +93,12 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     if fmt == "W8A8_INT8":
         # the mma.sync form of Swap-AB (token groups of 8, blocks of 32)
         mma_tiles = n_tiles * -(-M // (8 * min(4, -(-M // 8))))
-        for ring, narrow in ((0, False), (12, False), (0, True), (12, True)):
-            cfg = q.config_id(ring, 0, mma_sync=True, narrow=narrow)
+        forms = [q.config_id(ring, 0, mma_sync=True, narrow=narrow)
+                 for ring, narrow in ((0, False), (12, False), (0, True), (12, True))]
+        if M <= 16:
+            # dp4a warps on the first 16*d rows of each tile, mma.sync on the rest
+            forms += [q.config_id(0, 0, dp4a_rows16=d) for d in (1, 2, 3, 4)]
+        for cfg in forms:
             out.append((q.QG_SWAPAB, 1, cfg))
             for s in range(2, min(16, kt) + 1):
                 if mma_tiles * s > 12 * sms or kt // s < 1:
@@ -111,7 +115,8 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
             # the persistent pair kernel (one CTA per SM, weight tile shared
             # by TMA multicast, two TMEM accumulators): deepest ring, or 3
             for ring in (0, 3):
-                out.append((q.QG_STANDARD, 1, q.config_id(ring, persist=True)))
+                for dist in (0, 4, 8, 16):
+                    out.append((q.QG_STANDARD, 1, q.config_id(ring, dist, persist=True)))
             # 256-row weight tiles: ring of 2 (two CTAs per SM) or 4 (one)
             wide_tiles = -(-N // 256) * -(-M // 128)
             for cfg in (q.config_id(0, 0, True), q.config_id(4, 0, True)):

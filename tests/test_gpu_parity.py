@@ -405,3 +405,48 @@ def test_persist_config_rejected_elsewhere(q, gc):
         with pytest.raises(q.QGError) as e:
             q.qg_gemm_w8a8(fmt, 64, 256, 256, d, f, d, f, d, 256, v, s, cfg)
         assert e.value.code == q.QG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dpw", [1, 2, 4])
+@pytest.mark.parametrize("M", [1, 8, 13, 16])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 3), (SWS, 18)])
+def test_w8a8_int8_mma_sync_with_dp4a_rows(orc, q, gc, dpw, M, variant, split):
+    # the first 16*dpw rows of each weight tile on dp4a warps, the rest on
+    # mma.sync: ragged N (the last tile's dp4a rows partly past N), three
+    # exact segments, cluster and workspace reductions; int32 bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=900 + 10 * dpw + M, outliers=True,
+                config_id=q.config_id(0, 0, dp4a_rows16=dpw))
+
+
+def test_int8_dp4a_rows_identical_to_other_kernels(gc, q):
+    import seeded_inputs as si
+    M, N, K = 11, 384, 4096
+    A = si.activations(M, K, seed=41, outliers=True).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=41)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("W8A8_INT8", W)
+    Aq, sa = gc.quant_act_gpu("W8A8_INT8", A)
+    outs = [gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=c, debug=True)
+            for c in (0, q.config_id(mma_sync=True), q.config_id(dp4a_rows16=3))]
+    torch.cuda.synchronize()
+    for Y, d in outs[1:]:
+        assert torch.equal(d, outs[0][1]) and torch.equal(Y, outs[0][0])
+
+
+def test_dp4a_rows_rejected_beyond_16_tokens_and_without_narrow(q, gc):
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device=gc.DEV)
+    f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
+    with pytest.raises(q.QGError) as e:
+        q.qg_gemm_w8a8("W8A8_INT8", 17, 256, 256, d, f, d, f, d, 256, SW, 1, q.config_id(dp4a_rows16=2))
+    assert e.value.code == q.QG_ERR_UNSUPPORTED_SHAPE
+    with pytest.raises(q.QGError) as e:
+        q.qg_gemm_w8a8("W8A8_INT8", 8, 256, 256, d, f, d, f, d, 256, SW, 1,
+                       q.QG_CONFIG_MMA_SYNC | (2 << q.QG_CONFIG_MMA_DP4A_SHIFT))
+    assert e.value.code == q.QG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dist", [4, 16, 64])
+def test_fp8_persistent_l2_prefetch(orc, q, gc, dist):
+    # L2 prefetch of the weight halves ahead of the ring, across tiles (64:
+    # beyond every CTA's remaining k-tiles); results unchanged
+    gc.run_case(orc, "FP8_Dynamic", 300, 1024, 2048, ST, 1, seed=840 + dist, outliers=True,
+                config_id=q.config_id(0, dist, persist=True))
