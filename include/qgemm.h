@@ -84,6 +84,7 @@ typedef enum {
 #define QG_CONFIG_PERSIST (1 << 16)
 #define QG_CONFIG_MMA_DP4A_SHIFT 17
 #define QG_CONFIG_MMA_DP4A_MASK (7 << 17)
+#define QG_CONFIG_MMA_S8 (1 << 20)
 
 typedef enum {
   QG_OK = 0,
@@ -171,7 +172,13 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      M <= 16): the first 16*d rows of each weight tile go
  *                      to d warps of dp4a threads instead, on the integer
  *                      pipe the widening leaves idle (same exact result;
- *                      QG_ERR_UNSUPPORTED_SHAPE for M > 16);
+ *                      QG_ERR_UNSUPPORTED_SHAPE for M > 16); and with
+ *                      QG_CONFIG_MMA_SYNC (any of the forms above) also
+ *                      QG_CONFIG_MMA_S8: the MMA warps run the int8 form
+ *                      of the instruction (m16n8k32, s8 operands, s32
+ *                      accumulate) on the unwidened bytes -- same exact
+ *                      result, no widening, at B300's much lower int8 MMA
+ *                      rate;
  *                      plus QG_CONFIG_FUSED_QUANT (Swap-AB variants on the
  *                      tcgen05 kernels): a hint for qg_linear_w8a8 to take
  *                      its one-kernel form even when A_q / s_a buffers are

@@ -40,11 +40,22 @@
 //   last warp   widens the activation tile once per k-tile into f16
 //               fragments in shared memory ([step][group][lane], 8 bytes),
 //               read by every MMA warp.
+// With S8 the products run on the int8 form of the instruction instead
+// (mma.sync m16n8k32, s8 operands, s32 accumulate): no widening at all, and
+// the exact int32 sum needs no segments.  The K permutation becomes: for the
+// 32-wide step c (0..3) the lane takes physical k = 32t + 8c + {0..3} as the
+// fragment's logical 4t + {0..3} and 32t + 8c + {4..7} as 16 + 4t + {0..3},
+// so it still reads the same 32 contiguous bytes of each of its rows per
+// k-tile, and each MMA warp takes its activation fragments straight from the
+// stage's activation tile (the last warp only loads the activation scales).
+// B300 runs this instruction far below its FP8 rate (about 143 TOPS measured
+// on the part), which bounds the form to small token counts.
 // With DPW > 0 (eight-warp layout, up to 16 tokens) the first 16*DPW weight
 // rows go to DPW warps of dp4a threads instead (two per row, a K half each,
-// exact int32 sums as in gemm_i8_dp4a.cuh): dp4a runs on its own integer
-// pipe, which the widening and the MMAs leave idle, so the two halves of the
-// tile proceed side by side.
+// exact int32 sums as in gemm_i8_dp4a.cuh): dp4a runs on the integer pipe,
+// which the MMAs leave idle, so the two parts of the tile proceed side by
+// side (with the widening form the widening competes for that pipe; with
+// S8 nothing does).
 // The epilogue, the Split-K reduction (cluster push or workspace) and the
 // scales are those of the other Swap-AB kernels, one thread per weight row.
 #pragma once
@@ -101,11 +112,19 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A . B for one m16n8k32 step: A 16x32 s8 (row), B 32x8 s8 (col), D s32.
+__device__ __forceinline__ void mma_16832_s8(int32_t (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
   return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-template <int NG, int TPW, int DPW>
+template <int NG, int TPW, int DPW, bool S8>
 __global__ void __launch_bounds__(ms_threads(TPW), 2)
     gemm_i8_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = MsShape<NG>;
@@ -144,7 +163,7 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->full_a[i], 1);
-      mbar_init(&ctl->empty[i], 32 * (kMsWarps + DPW + 1));
+      mbar_init(&ctl->empty[i], 32 * (kMsWarps + DPW + (S8 ? 0 : 1)));
     }
     for (int b = 0; b < kMsABufs; ++b) {
       mbar_init(&ctl->afull[b], 32);
@@ -229,7 +248,7 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
     pdl_wait();  // s_a is written by the kernel this one depends on
     if (lane < MPAD) ctl->sa_s[lane] = lane < Mb ? __ldg(g.s_a + m_base + lane) : 0.0f;
     bool ok = true;
-    for (int i = 0; i < nk; ++i) {
+    for (int i = 0; !S8 && i < nk; ++i) {
       const int s = i % stages, b = i % kMsABufs;
       bool w = mbar_wait(&ctl->full_a[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns);
       if (i >= kMsABufs)
@@ -294,6 +313,49 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
     const int cw = warp - 1;
     // test hook (qg_set_force_timeout): wait on a barrier nothing arrives on
     bool ok = !g.force_timeout || __all_sync(0xffffffffu, mbar_wait(&ctl->never, 0, g.wait_ns));
+    if constexpr (S8) {
+      for (int i = 0; ok && i < nk; ++i) {
+        const int s = i % stages;
+        const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->full[s], ph, g.wait_ns) &&
+                                         mbar_wait(&ctl->full_a[s], ph, g.wait_ns) && !*abort_flag)) {
+          ok = false;
+          break;
+        }
+        // this lane's 32 bytes of k of its weight rows and of its token rows
+        const uint8_t* wt = smem + static_cast<size_t>(s) * S::kStageBytes;
+        const uint8_t* at = wt + S::kWBytes;
+        uint4 wv[TPW][2][2], av[NG][2];
+#pragma unroll
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t row = static_cast<uint32_t>(kRD + 16 * TPW * cw + 16 * t + 8 * rr + gid);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              wv[t][rr][hh] = *reinterpret_cast<const uint4*>(wt + sw128_chunk(row, 2 * tig + hh));
+          }
+#pragma unroll
+        for (int q = 0; q < NG; ++q)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            av[q][hh] = *reinterpret_cast<const uint4*>(at + sw128_chunk(static_cast<uint32_t>(8 * q + gid), 2 * tig + hh));
+        mbar_arrive(&ctl->empty[s]);  // both tiles are in registers
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int hh = c >> 1, j = 2 * (c & 1);
+#pragma unroll
+          for (int q = 0; q < NG; ++q) {
+            const uint32_t b0 = word_of(av[q][hh], j), b1 = word_of(av[q][hh], j + 1);
+#pragma unroll
+            for (int t = 0; t < TPW; ++t)
+              mma_16832_s8(iacc[t][q], word_of(wv[t][0][hh], j), word_of(wv[t][1][hh], j), word_of(wv[t][0][hh], j + 1),
+                           word_of(wv[t][1][hh], j + 1), b0, b1);
+          }
+        }
+      }
+      if (!ok) *abort_flag = 1;
+    } else {
     float facc[TPW][NG][4];
 #pragma unroll
     for (int t = 0; t < TPW; ++t)
@@ -362,6 +424,7 @@ __global__ void __launch_bounds__(ms_threads(TPW), 2)
       }
     }
     if (!ok) *abort_flag = 1;
+    }
   }
   // ------------------------------------------------- per-row accumulators
   __syncthreads();  // the ring is idle: every issued copy was consumed by the MMA warps

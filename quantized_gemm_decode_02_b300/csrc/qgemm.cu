@@ -350,31 +350,38 @@ int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::Ge
                      qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
-template <int NG, int TPW, int DPW>
+template <int NG, int TPW, int DPW, bool S8 = false>
 int run_i8_mma_t(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                  cudaStream_t stream) {
   const int rb = g.recv_bytes;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_mma_smem_bytes<NG>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_mma_kernel<NG, TPW, DPW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
+  return launch_gemm(qg::gemm_i8_mma_kernel<NG, TPW, DPW, S8>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
                      qg::ms_threads(TPW), qg::gemm_i8_mma_smem_bytes<NG>(g.stages, rb), tmW, tmA, g, stream);
 }
 // QG_CONFIG_MMA_NARROW: eight MMA warps of 16 weight rows instead of four of
-// 32; with it, QG_CONFIG_MMA_DP4A rows of 16 go to dp4a warps (up to 16 tokens)
-template <int NG>
-int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
-               cudaStream_t stream) {
-  if (!(config_id & QG_CONFIG_MMA_NARROW)) return run_i8_mma_t<NG, 2, 0>(p, tmW, tmA, g, config_id, stream);
+// 32; with it, QG_CONFIG_MMA_DP4A rows of 16 go to dp4a warps (up to 16
+// tokens); QG_CONFIG_MMA_S8: the int8 form of the instruction (no widening)
+template <int NG, bool S8>
+int run_i8_mma_form(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                    cudaStream_t stream) {
+  if (!(config_id & QG_CONFIG_MMA_NARROW)) return run_i8_mma_t<NG, 2, 0, S8>(p, tmW, tmA, g, config_id, stream);
   if constexpr (NG <= 2) {
     switch ((config_id & QG_CONFIG_MMA_DP4A_MASK) >> QG_CONFIG_MMA_DP4A_SHIFT) {
-      case 1: return run_i8_mma_t<NG, 1, 1>(p, tmW, tmA, g, config_id, stream);
-      case 2: return run_i8_mma_t<NG, 1, 2>(p, tmW, tmA, g, config_id, stream);
-      case 3: return run_i8_mma_t<NG, 1, 3>(p, tmW, tmA, g, config_id, stream);
-      case 4: return run_i8_mma_t<NG, 1, 4>(p, tmW, tmA, g, config_id, stream);
+      case 1: return run_i8_mma_t<NG, 1, 1, S8>(p, tmW, tmA, g, config_id, stream);
+      case 2: return run_i8_mma_t<NG, 1, 2, S8>(p, tmW, tmA, g, config_id, stream);
+      case 3: return run_i8_mma_t<NG, 1, 3, S8>(p, tmW, tmA, g, config_id, stream);
+      case 4: return run_i8_mma_t<NG, 1, 4, S8>(p, tmW, tmA, g, config_id, stream);
       default: break;
     }
   }
-  return run_i8_mma_t<NG, 1, 0>(p, tmW, tmA, g, config_id, stream);
+  return run_i8_mma_t<NG, 1, 0, S8>(p, tmW, tmA, g, config_id, stream);
+}
+template <int NG>
+int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+               cudaStream_t stream) {
+  if (config_id & QG_CONFIG_MMA_S8) return run_i8_mma_form<NG, true>(p, tmW, tmA, g, config_id, stream);
+  return run_i8_mma_form<NG, false>(p, tmW, tmA, g, config_id, stream);
 }
 
 // Persistent pair kernel: one CTA per SM at most (two per cluster); the
@@ -437,7 +444,8 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
 int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
-                     QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_RING_MASK |
+                     QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -451,9 +459,12 @@ int check_config_bits(int fmt, int variant, int config_id) {
   if ((config_id & QG_CONFIG_MMA_DP4A_MASK) &&
       (!(config_id & QG_CONFIG_MMA_NARROW) || ((config_id & QG_CONFIG_MMA_DP4A_MASK) >> QG_CONFIG_MMA_DP4A_SHIFT) > 4))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_DP4A needs QG_CONFIG_MMA_NARROW and at most 4 groups of 16 rows");
+  if ((config_id & QG_CONFIG_MMA_S8) && !(config_id & QG_CONFIG_MMA_SYNC))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_S8 needs QG_CONFIG_MMA_SYNC");
   if ((config_id & QG_CONFIG_PERSIST) &&
       (fmt != QG_FP8_DYNAMIC || variant != QG_STANDARD ||
-       (config_id & (QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_MMA_DP4A_MASK))))
+       (config_id & (QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_MMA_DP4A_MASK |
+                     QG_CONFIG_MMA_S8))))
     return fail(QG_ERR_INVALID_ARG,
                 "QG_CONFIG_PERSIST is for FP8_Dynamic with QG_STANDARD (ring depth and prefetch distance only)");
   if ((config_id & QG_CONFIG_FUSED_QUANT) &&

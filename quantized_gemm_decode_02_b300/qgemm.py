@@ -36,19 +36,24 @@ QG_CONFIG_MMA_NARROW = 1 << 14
 QG_CONFIG_FUSED_QUANT = 1 << 15
 QG_CONFIG_PERSIST = 1 << 16
 QG_CONFIG_MMA_DP4A_SHIFT = 17
+QG_CONFIG_MMA_S8 = 1 << 20
 
 
 def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False, mma_sync: bool = False,
-              narrow: bool = False, fused: bool = False, persist: bool = False, dp4a_rows16: int = 0) -> int:
+              narrow: bool = False, fused: bool = False, persist: bool = False, dp4a_rows16: int = 0,
+              s8: bool = False) -> int:
     """config_id of a ring depth (0 = default), an L2 prefetch distance,
     (FP8_Dynamic Standard / Split-K) 256-row weight tiles, (W8A8_INT8
     Swap-AB) the mma.sync kernel with eight narrow MMA warps if `narrow`,
     (Swap-AB on the tcgen05 kernels) qg_linear_w8a8's one-kernel form, and
     (FP8_Dynamic Standard) the persistent pair kernel; dp4a_rows16 groups
-    of 16 weight rows on dp4a warps (implies the narrow mma.sync kernel)."""
+    of 16 weight rows on dp4a warps (implies the narrow mma.sync kernel);
+    `s8`: the mma.sync kernel on the int8 form of the instruction (implies
+    mma_sync)."""
     narrow = narrow or dp4a_rows16 > 0
     return (ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT) | (QG_CONFIG_WIDE if wide else 0)
-            | (QG_CONFIG_MMA_SYNC if mma_sync or narrow else 0) | (QG_CONFIG_MMA_NARROW if narrow else 0)
+            | (QG_CONFIG_MMA_SYNC if mma_sync or narrow or s8 else 0) | (QG_CONFIG_MMA_NARROW if narrow else 0)
+            | (QG_CONFIG_MMA_S8 if s8 else 0)
             | (QG_CONFIG_FUSED_QUANT if fused else 0) | (QG_CONFIG_PERSIST if persist else 0)
             | (dp4a_rows16 << QG_CONFIG_MMA_DP4A_SHIFT))
 

@@ -71,7 +71,7 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     and without Split-K (reduced in a cluster, up to 16 ranges) for every M
     (in blocks of 64 tokens above 64); for W8A8_INT8 at M <= 8 also their
     CUDA-core (dp4a) forms, and for W8A8_INT8 at every M the mma.sync forms
-    (QG_CONFIG_MMA_SYNC); above 32 tokens also the Standard variant of the
+    (QG_CONFIG_MMA_SYNC, widened or QG_CONFIG_MMA_S8); above 32 tokens also the Standard variant of the
     E4M3 formats (FP8_Dynamic also with 256-row weight tiles).  Ring depth:
     0 = two CTAs per SM, 12 = one deep ring per SM (6 for Standard, whose
     stages are twice as large)."""
@@ -93,11 +93,15 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     if fmt == "W8A8_INT8":
         # the mma.sync form of Swap-AB (token groups of 8, blocks of 32)
         mma_tiles = n_tiles * -(-M // (8 * min(4, -(-M // 8))))
-        forms = [q.config_id(ring, 0, mma_sync=True, narrow=narrow)
-                 for ring, narrow in ((0, False), (12, False), (0, True), (12, True))]
+        # on f16-widened operands, and on the int8 form of the instruction
+        # (no widening, B300's low int8 MMA rate: worth it at small M)
+        forms = [q.config_id(ring, 0, mma_sync=True, narrow=narrow, s8=s8)
+                 for s8 in (False, True) for ring, narrow in ((0, False), (12, False), (0, True), (12, True))]
         if M <= 16:
-            # dp4a warps on the first 16*d rows of each tile, mma.sync on the rest
-            forms += [q.config_id(0, 0, dp4a_rows16=d) for d in (1, 2, 3, 4)]
+            # dp4a warps on the first 16*d rows of each tile, s8 mma.sync on
+            # the rest: two pipes side by side (with the widening form the
+            # dp4a rows were never faster on B300 and are not swept)
+            forms += [q.config_id(0, 0, dp4a_rows16=d, s8=True) for d in (1, 2, 3, 4)]
         for cfg in forms:
             out.append((q.QG_SWAPAB, 1, cfg))
             for s in range(2, min(16, kt) + 1):

@@ -224,7 +224,9 @@ def test_check_config_returns_the_gemm_status(q):
     cases = [dict(fmt=5), dict(variant=9), dict(K=200), dict(fmt=2, K=272), dict(split=2), dict(variant=3, split=3),
              dict(variant=3, split=0), dict(fmt=1, M=8, variant=0), dict(fmt=1, M=9, variant=q.QG_SWAPAB_DP4A),
              dict(fmt=0, M=1, variant=q.QG_SWAPAB_DP4A), dict(cfg=17), dict(cfg=q.config_id(0, 65)),
-             dict(cfg=1 << 13), dict(cfg=q.config_id(0, 0, True)), dict(cfg=-1), dict(cfg=1)]
+             dict(cfg=1 << 13), dict(cfg=q.config_id(0, 0, True)), dict(cfg=-1), dict(cfg=1),
+             dict(fmt=1, M=8, cfg=q.QG_CONFIG_MMA_S8),                               # s8 without mma.sync
+             dict(fmt=0, M=8, cfg=q.config_id(s8=True))]
     for c in cases:
         fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
         v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)
@@ -233,6 +235,11 @@ def test_check_config_returns_the_gemm_status(q):
         assert q.qg_check_config(fmt, M, 256, K, v, s, cfg) == want, c
     # accepted configurations (never launched here)
     assert q.qg_check_config(1, 8, 4096, 2048, q.QG_SWAPAB_DP4A_SPLITK, 16, 0) == q.QG_OK
+    assert q.qg_check_config(1, 24, 4096, 4096, q.QG_SWAPAB_SPLITK, 4, q.config_id(s8=True)) == q.QG_OK
+    assert q.qg_check_config(1, 8, 4096, 4096, q.QG_SWAPAB, 1, q.config_id(narrow=True, s8=True)) == q.QG_OK
+    assert q.qg_check_config(1, 16, 4096, 4096, q.QG_SWAPAB, 1, q.config_id(dp4a_rows16=4, s8=True)) == q.QG_OK
+    assert q.qg_check_config(1, 17, 4096, 4096, q.QG_SWAPAB, 1,
+                             q.config_id(dp4a_rows16=1, s8=True)) == q.QG_ERR_UNSUPPORTED_SHAPE
     assert q.qg_check_config(0, 300, 4096, 4096, q.QG_SPLITK, 3, q.config_id(4, 0, True)) == q.QG_OK
     assert q.qg_check_config(2, 32, 4096, 12288, q.QG_SWAPAB_SPLITK, 96, q.config_id(12, 64)) == q.QG_OK
     assert q.qg_check_config(0, 0, 256, 256, 2, 1, 0) == q.QG_ERR_INVALID_ARG   # a configuration has M >= 1

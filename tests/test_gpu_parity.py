@@ -217,7 +217,7 @@ def test_graph_capture_and_pdl_replay(orc, gc, q):
 
 
 @pytest.mark.parametrize("fmt,mma_sync", [("FP8_Dynamic", False), ("W8A8_INT8", False), ("W8A8_INT8", True),
-                                          ("Block_FP8", False)])
+                                          ("W8A8_INT8", "s8"), ("Block_FP8", False)])
 def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt, mma_sync):
     import seeded_inputs as si
     M, N, K = 4, 256, 1024
@@ -230,7 +230,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt, mma_
     assert q.qg_device_error() == 0
     q.qg_set_wait_limit_ns(2_000_000)  # 2 ms
     q.qg_set_force_timeout(True)
-    cfg = q.config_id(0, 0, mma_sync=mma_sync)
+    cfg = q.config_id(0, 0, mma_sync=mma_sync is True, s8=mma_sync == "s8")
     try:
         gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1, config_id=cfg)
         assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
@@ -298,6 +298,34 @@ def test_w8a8_int8_mma_sync_narrow_warps(orc, q, gc, M, variant, split):
                 config_id=q.config_id(0, 0, narrow=True))
 
 
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 17, 24, 25, 32, 33, 70])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 7), (SWS, 16), (SWS, 18)])
+def test_w8a8_int8_mma_sync_s8(orc, q, gc, M, variant, split):
+    # the int8 form of mma.sync (m16n8k32, s8 operands, s32 accumulate, no
+    # widening): token groups of 8, blocks of up to 32 with a ragged last
+    # block, cluster and workspace reductions, ragged N; the int32
+    # accumulators bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=1600 + M, outliers=True,
+                config_id=q.config_id(0, 0, s8=True))
+
+
+@pytest.mark.parametrize("M", [1, 9, 24, 32, 70])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 3), (SWS, 16), (SWS, 18)])
+def test_w8a8_int8_mma_sync_s8_narrow_warps(orc, q, gc, M, variant, split):
+    # the s8 form with eight MMA warps of 16 weight rows
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=1700 + M, outliers=True,
+                config_id=q.config_id(0, 0, narrow=True, s8=True))
+
+
+@pytest.mark.parametrize("M,K", [(4, 2320), (13, 4096 + 48), (32, 144)])
+@pytest.mark.parametrize("ring", [2, 5])
+def test_w8a8_int8_mma_sync_s8_ragged_k(orc, q, gc, M, K, ring):
+    # K not a multiple of 128: the last k-tile's zero fill adds nothing;
+    # shallow and deeper rings
+    gc.run_case(orc, "W8A8_INT8", M, 256, K, SWS, 2, seed=1800 + M + ring, outliers=True,
+                config_id=q.config_id(ring, 0, s8=True))
+
+
 @pytest.mark.parametrize("M", [3, 12, 32])
 @pytest.mark.parametrize("ring", [2, 3, 6])
 def test_w8a8_int8_mma_sync_ring_depths(orc, q, gc, M, ring):
@@ -320,9 +348,15 @@ def test_int8_mma_sync_identical_to_tensor_memory_kernel(gc, q):
                          debug=True)
     Y2, d2 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=q.config_id(0, 0, narrow=True),
                          debug=True)
+    Y3, d3 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=q.config_id(0, 0, s8=True),
+                         debug=True)
+    Y4, d4 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=q.config_id(0, 0, narrow=True, s8=True),
+                         debug=True)
     torch.cuda.synchronize()
     assert torch.equal(d0, d1) and torch.equal(Y0, Y1)
     assert torch.equal(d0, d2) and torch.equal(Y0, Y2)
+    assert torch.equal(d0, d3) and torch.equal(Y0, Y3)
+    assert torch.equal(d0, d4) and torch.equal(Y0, Y4)
 
 
 def test_mma_sync_config_rejected_outside_int8_swap_ab(q, gc):
@@ -407,15 +441,17 @@ def test_persist_config_rejected_elsewhere(q, gc):
         assert e.value.code == q.QG_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("s8", [False, True])
 @pytest.mark.parametrize("dpw", [1, 2, 4])
 @pytest.mark.parametrize("M", [1, 8, 13, 16])
 @pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 3), (SWS, 18)])
-def test_w8a8_int8_mma_sync_with_dp4a_rows(orc, q, gc, dpw, M, variant, split):
+def test_w8a8_int8_mma_sync_with_dp4a_rows(orc, q, gc, dpw, M, variant, split, s8):
     # the first 16*dpw rows of each weight tile on dp4a warps, the rest on
-    # mma.sync: ragged N (the last tile's dp4a rows partly past N), three
-    # exact segments, cluster and workspace reductions; int32 bit-exact
-    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=900 + 10 * dpw + M, outliers=True,
-                config_id=q.config_id(0, 0, dp4a_rows16=dpw))
+    # mma.sync (widened or s8): ragged N (the last tile's dp4a rows partly
+    # past N), three exact segments, cluster and workspace reductions; int32
+    # bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=900 + 10 * dpw + M + 100 * s8, outliers=True,
+                config_id=q.config_id(0, 0, dp4a_rows16=dpw, s8=s8))
 
 
 def test_int8_dp4a_rows_identical_to_other_kernels(gc, q):
@@ -426,7 +462,8 @@ def test_int8_dp4a_rows_identical_to_other_kernels(gc, q):
     Wq, sw = gc.quant_weight_gpu("W8A8_INT8", W)
     Aq, sa = gc.quant_act_gpu("W8A8_INT8", A)
     outs = [gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 4, config_id=c, debug=True)
-            for c in (0, q.config_id(mma_sync=True), q.config_id(dp4a_rows16=3))]
+            for c in (0, q.config_id(mma_sync=True), q.config_id(dp4a_rows16=3),
+                      q.config_id(dp4a_rows16=2, s8=True))]
     torch.cuda.synchronize()
     for Y, d in outs[1:]:
         assert torch.equal(d, outs[0][1]) and torch.equal(Y, outs[0][0])
