@@ -85,6 +85,7 @@ typedef enum {
 #define QG_CONFIG_MMA_DP4A_SHIFT 17
 #define QG_CONFIG_MMA_DP4A_MASK (7 << 17)
 #define QG_CONFIG_MMA_S8 (1 << 20)
+#define QG_CONFIG_PAIR_MMA (1 << 21)
 
 typedef enum {
   QG_OK = 0,
@@ -193,7 +194,11 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      overlaps the next tile's MMAs; only the ring depth
  *                      and the L2 prefetch distance (weight k-tiles of the
  *                      CTA's half requested ahead, across tiles) may be
- *                      combined with it (QG_ERR_INVALID_ARG else);
+ *                      combined with it (QG_ERR_INVALID_ARG else); with it
+ *                      also QG_CONFIG_PAIR_MMA: the pair runs each MMA as one
+ *                      tcgen05.mma.cta_group::2 (M = 256 tokens, each CTA
+ *                      holding only its own half of the weight tile, no
+ *                      multicast), issued by the pair's even CTA;
  *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

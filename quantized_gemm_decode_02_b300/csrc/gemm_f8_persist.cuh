@@ -26,6 +26,19 @@
 // warps 2..5 epilogue (thread = token row = TMEM lane).  Every wait is
 // bounded; both CTAs of a pair end with a cluster barrier, so neither exits
 // while its peer may still write into its shared memory.
+//
+// PAIR (QG_CONFIG_PAIR_MMA): the pair runs one tcgen05.mma.cta_group::2 per
+// K step instead of one cta_group::1 MMA in each CTA: M = 256 tokens (128
+// from each CTA's shared memory, each CTA's TMEM receiving its own 128
+// rows), N = 256 weight rows of which each CTA holds only its own half (the
+// tensor cores of the pair exchange the halves), so a stage is 16 KB of
+// activations + 16 KB of weights per CTA (32 KB instead of 48: deeper ring)
+// and no multicast is needed.  The even CTA (the leader) issues every MMA;
+// both CTAs' TMA loads complete on the leader's full barrier (cta_group::2
+// copies), its commits arrive on the barriers of both CTAs (multicast), the
+// epilogue warps of both CTAs release an accumulator buffer by arriving on
+// the leader's tempty barrier, and the TMEM is allocated and freed
+// collectively by one warp of each CTA.
 #pragma once
 #include "common.cuh"
 #include "gemm_f8.cuh"
@@ -38,6 +51,12 @@ constexpr uint32_t kPsABytes = kPsTok * kBK;      // 16 KB
 constexpr uint32_t kPsWBytes = kPsRows * kBK;     // 32 KB (two multicast halves)
 constexpr uint32_t kPsStageBytes = kPsABytes + kPsWBytes;
 constexpr uint32_t kPsTmemCols = 2 * kPsRows;     // two accumulator buffers
+constexpr uint32_t kPs2WBytes = kPsTok * kBK;     // PAIR: this CTA's 128-row weight half, 16 KB
+
+template <bool PAIR>
+__host__ __device__ constexpr uint32_t ps_stage_bytes() {
+  return PAIR ? kPsABytes + kPs2WBytes : kPsStageBytes;
+}
 
 struct alignas(8) CtrlPs {
   uint64_t full[8];     // the stage's activation tile and both weight halves landed
@@ -45,14 +64,16 @@ struct alignas(8) CtrlPs {
   uint64_t tfull[2];    // accumulator buffer written (MMA commit)
   uint64_t tempty[2];   // accumulator buffer drained (epilogue)
   uint64_t never;       // the forced-timeout test hook waits on it
+  uint64_t done;        // PAIR: every MMA of the pair has completed (leader's final commit)
   uint32_t tmem_base;
   int abort_flag;
   int epi_bad[4];          // per epilogue warp: its wait failed or the kernel aborted (this tile)
   float sw_s[2][kPsRows];  // per-channel scales of the buffer's weight tile
 };
 
+template <bool PAIR = false>
 __host__ __device__ constexpr size_t gemm_f8_persist_smem_bytes(int stages) {
-  return 1024 + static_cast<size_t>(stages) * kPsStageBytes + sizeof(CtrlPs);
+  return 1024 + static_cast<size_t>(stages) * ps_stage_bytes<PAIR>() + sizeof(CtrlPs);
 }
 
 // 2-D TMA load multicast to the CTAs of ctaMask: the box lands at the same
@@ -75,6 +96,53 @@ __device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t mask
                : "memory");
 }
 
+// ---- cta_group::2 forms (every tcgen05 instruction of a kernel takes the
+// same cta_group) ----
+// TMEM allocation for the CTA pair: one warp of each CTA executes it; the
+// same columns are reserved in both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// One MMA of the pair (issued by one thread of the leader): A rows from each
+// CTA's shared memory at a_desc, B halves from each CTA's at b_desc, D rows
+// of each CTA into its own TMEM at d_tmem.
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier at the same offset in each CTA of ctaMask once every
+// pair MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+// 2-D TMA load into this CTA's shared memory whose bytes complete on the
+// mbarrier at cluster address `cbar` (the leader's, for either CTA).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm, int c0, int c1, uint32_t cbar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(cbar), "l"(policy)
+      : "memory");
+}
+// Arrive (release, cluster scope) on the mbarrier at cluster address `cbar`.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -83,15 +151,18 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 
 // One CTA of a pair.  g.m_tiles = pair tiles along the tokens (ceil(M/256)),
 // g.kt_total = k-tiles; tiles = g.m_tiles * ceil(N/256).
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f8_persist_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
+  constexpr uint32_t kStage = ps_stage_bytes<PAIR>();
   stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
-  CtrlPs* ctl = reinterpret_cast<CtrlPs*>(smem + static_cast<size_t>(stages) * kPsStageBytes);
+  CtrlPs* ctl = reinterpret_cast<CtrlPs*>(smem + static_cast<size_t>(stages) * kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();           // 0 or 1: token half of the pair tile
+  const bool leader = rank == 0;
   const int cluster = static_cast<int>(blockIdx.x >> 1), clusters = static_cast<int>(gridDim.x >> 1);
   const int tp_count = g.m_tiles, wn_count = (g.N + kPsRows - 1) / kPsRows;
   const int tiles = tp_count * wn_count;
@@ -100,13 +171,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
-      mbar_init(&ctl->empty[i], 2);  // one commit from each CTA of the pair
+      mbar_init(&ctl->empty[i], PAIR ? 1 : 2);  // PAIR: the leader's one commit; else one from each CTA
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], 128);
+      mbar_init(&ctl->tempty[b], PAIR ? 8 : 128);  // PAIR: one arrive per epilogue warp of both CTAs
     }
     mbar_init(&ctl->never, 1);
+    mbar_init(&ctl->done, 1);
     ctl->abort_flag = 0;
     fence_barrier_init();
   }
@@ -114,32 +186,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmA);
   }
-  if (warp == 1) tmem_alloc(&ctl->tmem_base, kPsTmemCols);
+  // the peer's barriers are initialized before any copy or commit reaches
+  // them (and, PAIR, before the collective TMEM allocation)
+  cluster_sync();
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(&ctl->tmem_base, kPsTmemCols);
+    else tmem_alloc(&ctl->tmem_base, kPsTmemCols);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers are initialized before any multicast reaches them
   const uint32_t tmem = ctl->tmem_base;
   pdl_launch_dependents();
   volatile int* abort_flag = &ctl->abort_flag;
+  // PAIR: cluster addresses of the leader's barriers
+  const uint32_t full0 = dsmem_map(smem_u32(&ctl->full[0]), 0);
+  const uint32_t tempty0 = dsmem_map(smem_u32(&ctl->tempty[0]), 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       const uint16_t both = 0x3;
+      // this CTA's weight half of tile t's k-tile kk into stage s (PAIR: its
+      // own shared memory only; else multicast into both CTAs), and the
+      // stage's activation tile
+      auto load_w = [&](int s, int wn, int kk) {
+        uint8_t* st = smem + static_cast<size_t>(s) * kStage;
+        const int w_row = wn * kPsRows + static_cast<int>(rank) * kPsTok;
+        if constexpr (PAIR)
+          tma_load_2d_pair(st + kPsABytes, &tmW, kk * kBK, w_row, full0 + 8u * static_cast<uint32_t>(s), pol_w);
+        else
+          tma_load_2d_multicast(st + kPsABytes + rank * (kPsWBytes / 2), &tmW, kk * kBK, w_row, &ctl->full[s], both,
+                                pol_w);
+      };
+      auto load_a = [&](int s, int a_row, int kk) {
+        uint8_t* st = smem + static_cast<size_t>(s) * kStage;
+        if constexpr (PAIR)
+          tma_load_2d_pair(st, &tmA, kk * kBK, a_row, full0 + 8u * static_cast<uint32_t>(s), pol_a);
+        else
+          tma_load_2d(st, &tmA, kk * kBK, a_row, &ctl->full[s], pol_a);
+      };
+      // PAIR: the leader expects both CTAs' bytes of a stage on its barrier
+      auto expect = [&](int s) {
+        if (!PAIR) mbar_arrive_expect_tx(&ctl->full[s], kStage);
+        else if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * kStage);
+      };
       // the weights of the first tile's first stages are requested before
       // the wait for the kernel this one depends on, its activations after
       const int first = cluster < tiles ? cluster : -1;
       const int pre = first >= 0 ? (nk < stages ? nk : stages) : 0;
-      if (pre > 0) {
-        const int w_row = (first / tp_count) * kPsRows + static_cast<int>(rank) * kPsTok;
-        for (int kk = 0; kk < pre; ++kk) {
-          uint8_t* st = smem + static_cast<size_t>(kk) * kPsStageBytes;
-          mbar_arrive_expect_tx(&ctl->full[kk], kPsStageBytes);
-          tma_load_2d_multicast(st + kPsABytes + rank * (kPsWBytes / 2), &tmW, kk * kBK, w_row, &ctl->full[kk], both,
-                                pol_w);
-        }
+      for (int kk = 0; kk < pre; ++kk) {
+        expect(kk);
+        load_w(kk, first / tp_count, kk);
       }
       // this CTA's weight half of the k-tile `ahead` k-tiles past (tile t,
       // k-tile kk) is requested into L2 (no shared memory): the ring then
@@ -161,10 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cluster; ok && t < tiles; t += clusters) {
         const int tp = t % tp_count, wn = t / tp_count;
         const int a_row = tp * 2 * kPsTok + static_cast<int>(rank) * kPsTok;
-        const int w_row = wn * kPsRows + static_cast<int>(rank) * kPsTok;
         for (int kk = 0; kk < nk; ++kk, ++i) {
           const int s = i % stages;
-          uint8_t* st = smem + static_cast<size_t>(s) * kPsStageBytes;
           if (ahead > 0 && i >= pre) prefetch_ahead(t, kk);
           if (i >= pre) {
             if (i >= stages && (!mbar_wait(&ctl->empty[s], (static_cast<uint32_t>(i / stages) & 1u) ^ 1u, g.wait_ns) ||
@@ -172,30 +269,39 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&ctl->full[s], kPsStageBytes);
-            tma_load_2d_multicast(st + kPsABytes + rank * (kPsWBytes / 2), &tmW, kk * kBK, w_row, &ctl->full[s], both,
-                                  pol_w);
+            expect(s);
+            load_w(s, wn, kk);
           }
-          tma_load_2d(st, &tmA, kk * kBK, a_row, &ctl->full[s], pol_a);
+          load_a(s, a_row, kk);
         }
       }
       if (!ok) *abort_flag = 1;
-      // every stage this CTA expects lands (its own copies and the peer's
-      // half) before the CTA may leave
-      for (int j = i > stages ? i - stages : 0; j < i; ++j)
-        mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+      // every stage this CTA expects lands before the CTA may leave: its own
+      // copies and the peer's half (the full barrier), or, for the PAIR
+      // peer, whose copies complete on the leader's barrier, the MMAs that
+      // consumed them (its empty barrier)
+      for (int j = i > stages ? i - stages : 0; j < i; ++j) {
+        if (PAIR && !leader)
+          mbar_wait(&ctl->empty[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+        else
+          mbar_wait(&ctl->full[j % stages], static_cast<uint32_t>(j / stages) & 1u, kDrainNs);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kPsTok, kPsRows, 0, 0);  // E4M3 x E4M3 -> F32, 128 x 256
+    if (lane == 0 && (!PAIR || leader)) {
+      // E4M3 x E4M3 -> F32: 128 x 256 per CTA, or 256 x 256 for the pair
+      constexpr uint32_t idesc = make_idesc(PAIR ? 2 * kPsTok : kPsTok, kPsRows, 0, 0);
       bool ok = !g.force_timeout || mbar_wait(&ctl->never, 0, g.wait_ns);
       int i = 0, lt = 0;
       for (int t = cluster; ok && t < tiles; t += clusters, ++lt) {
         const int b = lt & 1;
-        if (lt >= 2 && !mbar_wait(&ctl->tempty[b], (static_cast<uint32_t>(lt / 2) & 1u) ^ 1u, g.wait_ns)) {
-          ok = false;
-          break;
+        if (lt >= 2) {
+          const uint32_t par = (static_cast<uint32_t>(lt / 2) & 1u) ^ 1u;
+          if (!(PAIR ? mbar_wait_cluster(&ctl->tempty[b], par, g.wait_ns) : mbar_wait(&ctl->tempty[b], par, g.wait_ns))) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(b * kPsRows);
@@ -206,22 +312,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * kPsStageBytes);
+          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * kStage);
           const uint32_t w_addr = a_addr + kPsABytes;
 #pragma unroll
-          for (int k4 = 0; k4 < kBK / 32; ++k4)
-            mma_f8f6f4(d, sw128_kmajor_desc(a_addr + k4 * 32), sw128_kmajor_desc(w_addr + k4 * 32), idesc,
-                       (kk > 0 || k4 > 0) ? 1u : 0u);
-          tc_commit_multicast(&ctl->empty[s], 0x3);  // the stage is free in both CTAs once both committed
+          for (int k4 = 0; k4 < kBK / 32; ++k4) {
+            const uint32_t acc = (kk > 0 || k4 > 0) ? 1u : 0u;
+            if constexpr (PAIR)
+              mma_f8f6f4_pair(d, sw128_kmajor_desc(a_addr + k4 * 32), sw128_kmajor_desc(w_addr + k4 * 32), idesc, acc);
+            else
+              mma_f8f6f4(d, sw128_kmajor_desc(a_addr + k4 * 32), sw128_kmajor_desc(w_addr + k4 * 32), idesc, acc);
+          }
+          // the stage is free in both CTAs once both (PAIR: the pair's) MMAs committed
+          if constexpr (PAIR) tc_commit_pair_multicast(&ctl->empty[s], 0x3);
+          else tc_commit_multicast(&ctl->empty[s], 0x3);
         }
         if (!ok) break;
-        tc_commit(&ctl->tfull[b]);
+        if constexpr (PAIR) tc_commit_pair_multicast(&ctl->tfull[b], 0x3);
+        else tc_commit(&ctl->tfull[b]);
       }
       if (!ok) {
         *abort_flag = 1;
         mbar_arrive(&ctl->tfull[0]);
         mbar_arrive(&ctl->tfull[1]);
       }
+      // PAIR: both CTAs learn when every MMA (which writes both TMEMs and
+      // reads both CTAs' shared memory) has completed
+      if constexpr (PAIR) tc_commit_pair_multicast(&ctl->done, 0x3);
+    }
+    if (PAIR) {
+      __syncwarp();
+      mbar_wait(&ctl->done, 0, g.wait_ns);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -274,16 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&ctl->tempty[b]);
+      if constexpr (PAIR) {
+        __syncwarp();  // the warp's TMEM reads of the buffer are done
+        if (lane == 0) mbar_arrive_remote(tempty0 + 8u * static_cast<uint32_t>(b));
+      } else {
+        mbar_arrive(&ctl->tempty[b]);
+      }
       named_bar_sync(1, 128);  // every thread is done with sw_s[b] and epi_bad before the next tile
     }
   }
   // ------------------------------------------- teardown: TMEM, then the pair
   tc_fence_before();
   __syncthreads();
+  // PAIR: the leader's MMAs write both CTAs' TMEM, and the deallocation is
+  // collective: both CTAs are past their last TMEM use (and the MMAs done)
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kPsTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, kPsTmemCols);
+    else tmem_dealloc(tmem, kPsTmemCols);
   }
   // every copy this CTA issued into its peer, and the peer's into this CTA,
   // has been consumed (or the CTA gave up after a bounded wait) before

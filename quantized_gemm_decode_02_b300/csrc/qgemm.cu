@@ -386,17 +386,19 @@ int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg
 
 // Persistent pair kernel: one CTA per SM at most (two per cluster); the
 // ring takes the deepest depth that fits one CTA's shared memory unless
-// config_id asks for fewer stages.
-int run_f8_persist(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
-                   cudaStream_t stream) {
+// config_id asks for fewer stages.  PAIR: the cta_group::2 form
+// (QG_CONFIG_PAIR_MMA).
+template <bool PAIR>
+int run_f8_persist_t(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                     cudaStream_t stream) {
   const DevInfo d = dev_info();
   int st = 8;
-  while (st > 2 && qg::gemm_f8_persist_smem_bytes(st) > d.smem_optin) --st;
+  while (st > 2 && qg::gemm_f8_persist_smem_bytes<PAIR>(st) > d.smem_optin) --st;
   const int want = config_id & QG_CONFIG_RING_MASK;
   if (want >= 2 && want < st) st = want;
   g.stages = st;
-  const size_t smem = qg::gemm_f8_persist_smem_bytes(st);
-  cudaError_t e = set_smem(qg::gemm_f8_persist_kernel, smem);
+  const size_t smem = qg::gemm_f8_persist_smem_bytes<PAIR>(st);
+  cudaError_t e = set_smem(qg::gemm_f8_persist_kernel<PAIR>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   // the tile schedule is static, so only clusters that can all be resident
@@ -414,7 +416,7 @@ int run_f8_persist(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&resident, qg::gemm_f8_persist_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&resident, qg::gemm_f8_persist_kernel<PAIR>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // clear the query's error; fall back to one pair per two SMs
       resident = 0;
     }
@@ -423,10 +425,15 @@ int run_f8_persist(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA
   if (resident <= 0 || resident > sms / 2) resident = sms / 2;
   const int clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, resident)));
   g.reduce = qg::kReduceNone;
-  e = launch_cluster_xy(qg::gemm_f8_persist_kernel, dim3(2 * clusters), dim3(qg::kThreads), smem, stream, 2u, 1u, tmW,
-                        tmA, g);
+  e = launch_cluster_xy(qg::gemm_f8_persist_kernel<PAIR>, dim3(2 * clusters), dim3(qg::kThreads), smem, stream, 2u, 1u,
+                        tmW, tmA, g);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return QG_OK;
+}
+int run_f8_persist(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                   cudaStream_t stream) {
+  return (config_id & QG_CONFIG_PAIR_MMA) ? run_f8_persist_t<true>(p, tmW, tmA, g, config_id, stream)
+                                          : run_f8_persist_t<false>(p, tmW, tmA, g, config_id, stream);
 }
 
 template <int MT>
@@ -444,8 +451,8 @@ int run_dp4a(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::
 int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
-                     QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_RING_MASK |
-                     QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_PAIR_MMA |
+                     QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -461,6 +468,8 @@ int check_config_bits(int fmt, int variant, int config_id) {
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_DP4A needs QG_CONFIG_MMA_NARROW and at most 4 groups of 16 rows");
   if ((config_id & QG_CONFIG_MMA_S8) && !(config_id & QG_CONFIG_MMA_SYNC))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_S8 needs QG_CONFIG_MMA_SYNC");
+  if ((config_id & QG_CONFIG_PAIR_MMA) && !(config_id & QG_CONFIG_PERSIST))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PAIR_MMA is a form of the QG_CONFIG_PERSIST kernel");
   if ((config_id & QG_CONFIG_PERSIST) &&
       (fmt != QG_FP8_DYNAMIC || variant != QG_STANDARD ||
        (config_id & (QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_MMA_DP4A_MASK |

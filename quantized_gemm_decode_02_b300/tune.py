@@ -116,11 +116,13 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
                 if s <= kt and std_tiles * s <= 4 * sms:
                     out.append((q.QG_SPLITK, s, cfg))
         if fmt == "FP8_Dynamic":
-            # the persistent pair kernel (one CTA per SM, weight tile shared
-            # by TMA multicast, two TMEM accumulators): deepest ring, or 3
-            for ring in (0, 3):
-                for dist in (0, 4, 8, 16):
-                    out.append((q.QG_STANDARD, 1, q.config_id(ring, dist, persist=True)))
+            # the persistent pair kernel (one CTA per SM, two TMEM
+            # accumulators; the weight tile shared by TMA multicast, or each
+            # CTA holding its half under cta_group::2 MMAs): deepest ring or
+            # shallower ones (L2 prefetch distances were never faster)
+            for pair in (False, True):
+                for ring in (0, 3, 4):
+                    out.append((q.QG_STANDARD, 1, q.config_id(ring, 0, persist=True, pair_mma=pair)))
             # 256-row weight tiles: ring of 2 (two CTAs per SM) or 4 (one)
             wide_tiles = -(-N // 256) * -(-M // 128)
             for cfg in (q.config_id(0, 0, True), q.config_id(4, 0, True)):

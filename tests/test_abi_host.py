@@ -226,7 +226,9 @@ def test_check_config_returns_the_gemm_status(q):
              dict(fmt=0, M=1, variant=q.QG_SWAPAB_DP4A), dict(cfg=17), dict(cfg=q.config_id(0, 65)),
              dict(cfg=1 << 13), dict(cfg=q.config_id(0, 0, True)), dict(cfg=-1), dict(cfg=1),
              dict(fmt=1, M=8, cfg=q.QG_CONFIG_MMA_S8),                               # s8 without mma.sync
-             dict(fmt=0, M=8, cfg=q.config_id(s8=True))]
+             dict(fmt=0, M=8, cfg=q.config_id(s8=True)),
+             dict(fmt=0, M=300, variant=0, cfg=q.QG_CONFIG_PAIR_MMA),                # pair MMA without persist
+             dict(fmt=2, M=300, variant=0, cfg=q.config_id(pair_mma=True))]
     for c in cases:
         fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
         v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)
@@ -241,6 +243,7 @@ def test_check_config_returns_the_gemm_status(q):
     assert q.qg_check_config(1, 17, 4096, 4096, q.QG_SWAPAB, 1,
                              q.config_id(dp4a_rows16=1, s8=True)) == q.QG_ERR_UNSUPPORTED_SHAPE
     assert q.qg_check_config(0, 300, 4096, 4096, q.QG_SPLITK, 3, q.config_id(4, 0, True)) == q.QG_OK
+    assert q.qg_check_config(0, 512, 24576, 4096, q.QG_STANDARD, 1, q.config_id(3, 8, pair_mma=True)) == q.QG_OK
     assert q.qg_check_config(2, 32, 4096, 12288, q.QG_SWAPAB_SPLITK, 96, q.config_id(12, 64)) == q.QG_OK
     assert q.qg_check_config(0, 0, 256, 256, 2, 1, 0) == q.QG_ERR_INVALID_ARG   # a configuration has M >= 1
 

@@ -371,19 +371,22 @@ def test_mma_sync_config_rejected_outside_int8_swap_ab(q, gc):
     assert e.value.code == q.QG_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("pair_mma", [False, True])
 @pytest.mark.parametrize("M", [64, 100, 256, 300, 513])
 @pytest.mark.parametrize("N,K", [(424, 656), (1024, 2048)])
-def test_fp8_persistent_pairs(orc, q, gc, M, N, K):
+def test_fp8_persistent_pairs(orc, q, gc, M, N, K, pair_mma):
     # the persistent pair kernel (QG_CONFIG_PERSIST): 256-token pair tiles
     # (the second CTA of the last pair partly or wholly past M), 256-row
     # weight tiles (N = 424: one full, one ragged), ragged K (656: the last
-    # k-tile 16 wide)
+    # k-tile 16 wide); with pair_mma each MMA is one cta_group::2 instruction
+    # of the pair (M = 256) on the two CTAs' weight halves
     gc.run_case(orc, "FP8_Dynamic", M, N, K, ST, 1, seed=800 + M + N, outliers=True,
-                config_id=q.config_id(persist=True))
+                config_id=q.config_id(persist=True, pair_mma=pair_mma))
 
 
+@pytest.mark.parametrize("pair_mma", [False, True])
 @pytest.mark.parametrize("ring", [2, 3])
-def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring):
+def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring, pair_mma):
     # 3 x 80 = 240 pair tiles: every cluster takes several tiles, so both
     # TMEM accumulators and the weight-scale slots are reused; shallow rings
     # wrap many times.  Sampled columns against the oracle.
@@ -393,7 +396,8 @@ def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring):
     W = si.weights(N, K, seed=820 + ring)
     Wq, sw = gc.quant_weight_gpu("FP8_Dynamic", torch.from_numpy(W).to(gc.DEV))
     Aq, sa = gc.quant_act_gpu("FP8_Dynamic", A.to(gc.DEV))
-    Y, _ = gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, ST, 1, config_id=q.config_id(ring, persist=True))
+    Y, _ = gc.gemm_gpu("FP8_Dynamic", Aq, sa, Wq, sw, N, ST, 1,
+                       config_id=q.config_id(ring, persist=True, pair_mma=pair_mma))
     torch.cuda.synchronize()
     assert q.qg_device_error() == 0
     ns = np.concatenate([np.arange(0, 300), np.arange(10000, 10300), np.arange(N - 300, N)])
@@ -404,7 +408,8 @@ def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring):
     assert not torch.isnan(Y.float()).any()
 
 
-def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc):
+@pytest.mark.parametrize("pair_mma", [False, True])
+def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc, pair_mma):
     import seeded_inputs as si
     M, N, K = 300, 1024, 1024
     A = si.activations(M, K, seed=830)
@@ -413,7 +418,7 @@ def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc):
     Aq, sa = gc.quant_act_gpu("FP8_Dynamic", A.to(gc.DEV))
     torch.cuda.synchronize()
     assert q.qg_device_error() == 0
-    cfg = q.config_id(persist=True)
+    cfg = q.config_id(persist=True, pair_mma=pair_mma)
     q.qg_set_wait_limit_ns(2_000_000)
     q.qg_set_force_timeout(True)
     try:
@@ -435,7 +440,8 @@ def test_persist_config_rejected_elsewhere(q, gc):
     for fmt, v, s, cfg in (("Block_FP8", ST, 1, q.config_id(persist=True)),
                            ("FP8_Dynamic", SW, 1, q.config_id(persist=True)),
                            ("FP8_Dynamic", STS, 2, q.config_id(persist=True)),
-                           ("FP8_Dynamic", ST, 1, q.config_id(persist=True, wide=True))):
+                           ("FP8_Dynamic", ST, 1, q.config_id(persist=True, wide=True)),
+                           ("FP8_Dynamic", ST, 1, q.QG_CONFIG_PAIR_MMA)):
         with pytest.raises(q.QGError) as e:
             q.qg_gemm_w8a8(fmt, 64, 256, 256, d, f, d, f, d, 256, v, s, cfg)
         assert e.value.code == q.QG_ERR_INVALID_ARG
@@ -481,9 +487,10 @@ def test_dp4a_rows_rejected_beyond_16_tokens_and_without_narrow(q, gc):
     assert e.value.code == q.QG_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("pair_mma", [False, True])
 @pytest.mark.parametrize("dist", [4, 16, 64])
-def test_fp8_persistent_l2_prefetch(orc, q, gc, dist):
+def test_fp8_persistent_l2_prefetch(orc, q, gc, dist, pair_mma):
     # L2 prefetch of the weight halves ahead of the ring, across tiles (64:
     # beyond every CTA's remaining k-tiles); results unchanged
     gc.run_case(orc, "FP8_Dynamic", 300, 1024, 2048, ST, 1, seed=840 + dist, outliers=True,
-                config_id=q.config_id(0, dist, persist=True))
+                config_id=q.config_id(0, dist, persist=True, pair_mma=pair_mma))
