@@ -153,12 +153,17 @@ class Workload:
         self.a_off, self.y_off = a_off, y_off
         self.recs = []
         ws_need = 0
+        ws_prew = 0  # QG_CONFIG_I8_PREWIDEN items: a workspace of their own (their fp16 copy must not land on
+                     # the Split-K arrival counters of other items)
         weights = {}
         wseeds = {}  # weight copy -> seed of its fp32 weights (si.weights_device)
         for i, (fmt, M, layer, N, K) in enumerate(self.items):
             variant, split, cfg = q.qg_select(fmt, M, N, K)
-            need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
-            ws_need = max(ws_need, need)
+            need = q.qg_workspace_bytes_config(fmt, M, N, K, variant, split, cfg)
+            if cfg & q.QG_CONFIG_I8_PREWIDEN:
+                ws_prew = max(ws_prew, need)
+            else:
+                ws_need = max(ws_need, need)
             A = self.A_all[a_off[i]:a_off[i] + M * K * 2].view(torch.bfloat16).view(M, K)
             A.copy_(si.activations_device(M, K, seed=seed * 1000 + i, device=device,
                                           outliers=spec.get("outliers", False) or fmt == "Block_FP8"))
@@ -185,6 +190,8 @@ class Workload:
                                   variant=variant, split=split, cfg=cfg, ws_need=need, wseed=wseeds[wkey]))
         self.ws = torch.zeros(max(ws_need, 256), dtype=torch.uint8, device=device)
         self.ws_bytes = ws_need
+        self.ws_prew = torch.zeros(max(ws_prew, 256), dtype=torch.uint8, device=device)
+        self.ws_prew_bytes = ws_prew
         torch.cuda.synchronize()
         self.bytes_gemm = sum(gemm_bytes(r["fmt"], r["M"], r["N"], r["K"]) for r in self.recs)
         self.bytes_quant = sum(quant_bytes(r["fmt"], r["M"], r["K"]) for r in self.recs)
@@ -202,7 +209,10 @@ class Workload:
         return fusable and (self.fused or bool(r["cfg"] & self.q.QG_CONFIG_FUSED_QUANT))
 
     def kernels(self, i: int) -> int:
-        return 1 if self.fused_item(i) else 2
+        if self.fused_item(i):
+            return 1
+        # QG_CONFIG_I8_PREWIDEN: quantization, activation widening, GEMM
+        return 3 if self.recs[i]["cfg"] & self.q.QG_CONFIG_I8_PREWIDEN else 2
 
     def rebind(self, A_all, Y_all):
         """The items with their activations and outputs in other buffers of
@@ -222,8 +232,10 @@ class Workload:
         r = (recs or self.recs)[i]
         q = self.q
         fz = self.fused and self.fused_item(i)
+        prew = bool(r["cfg"] & q.QG_CONFIG_I8_PREWIDEN)
         q.qg_linear_w8a8(r["fmt"], r["M"], r["N"], r["K"], r["A"], r["K"], r["Wq"], r["sw"], r["Y"], r["N"],
-                         r["variant"], r["split"], r["cfg"], self.ws, self.ws_bytes,
+                         r["variant"], r["split"], r["cfg"], self.ws_prew if prew else self.ws,
+                         self.ws_prew_bytes if prew else self.ws_bytes,
                          None if fz else r["Aq"], None if fz else r["sa"], None, stream=stream)
 
     def capture_step(self, stream, recs=None, timing_log=None) -> torch.cuda.CUDAGraph:

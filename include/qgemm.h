@@ -86,6 +86,7 @@ typedef enum {
 #define QG_CONFIG_MMA_DP4A_MASK (7 << 17)
 #define QG_CONFIG_MMA_S8 (1 << 20)
 #define QG_CONFIG_PAIR_MMA (1 << 21)
+#define QG_CONFIG_I8_PREWIDEN (1 << 22)
 
 typedef enum {
   QG_OK = 0,
@@ -125,10 +126,19 @@ QG_API int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, vo
  * null pointers), QG_ERR_UNSUPPORTED_SHAPE (K % 16, Block_FP8 K % 128). */
 QG_API int qg_pack_weight(int fmt, const float* W_host, int64_t N, int64_t K, void* W_q_host, float* s_w_host);
 
-/* Workspace bytes qg_gemm_w8a8 needs for this shape and variant (0 when
- * split_k == 1).  Layout: per-tile arrival counters (must be zero before the
- * first use; the kernels leave them zero again), then the split partials. */
+/* Workspace bytes qg_gemm_w8a8 needs for this shape and variant with every
+ * config_id except QG_CONFIG_I8_PREWIDEN (0 when the splits reduce without a
+ * workspace, in particular when split_k == 1).  Layout: per-tile arrival
+ * counters (must be zero before the first use; the kernels leave them zero
+ * again), then the split partials.  Returns 0 for an invalid configuration. */
 QG_API size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k);
+
+/* The same for a given config_id (exact for every config_id):
+ * QG_CONFIG_I8_PREWIDEN adds, 256-byte aligned after the Split-K part, the
+ * fp16 copy of the activations (M x K x 2 bytes), which qg_gemm_w8a8 writes
+ * before its GEMM kernel reads it (no initial contents needed). */
+QG_API size_t qg_workspace_bytes_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k,
+                                        int config_id);
 
 /* Validate a configuration without launching anything: the checks of
  * qg_gemm_w8a8 that need no pointer (format, variant, sizes, config_id,
@@ -199,7 +209,22 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      tcgen05.mma.cta_group::2 (M = 256 tokens, each CTA
  *                      holding only its own half of the weight tile, no
  *                      multicast), issued by the pair's even CTA;
- *   workspace_dev      qg_workspace_bytes() bytes (may be NULL when 0);
+ *                      plus QG_CONFIG_I8_PREWIDEN for W8A8_INT8 with
+ *                      QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernel
+ *                      (the compute-bound regime): the call first widens the
+ *                      activations once into an exact fp16 copy in the
+ *                      workspace (a second kernel), and the GEMM loads that
+ *                      copy by TMA instead of widening it in every CTA, in
+ *                      token blocks of 64 (M <= 64) or 128 -- each weight
+ *                      tile widened once per 128 tokens; only the ring
+ *                      depth and the L2 prefetch distance may be combined
+ *                      with it, and it is not for grouped launches or the
+ *                      one-kernel form of qg_linear_w8a8 (QG_ERR_INVALID_ARG);
+ *                      its workspace (qg_workspace_bytes_config) then holds
+ *                      that copy, which may cover where another call keeps
+ *                      its Split-K arrival counters: give such calls a
+ *                      workspace of their own;
+ *   workspace_dev      qg_workspace_bytes_config() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).
  * Concurrent calls on different streams must use different workspaces. */
@@ -286,7 +311,7 @@ QG_API int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* 
  * QG_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that loads
  * the library holds that array until the process exits.
  *   Arguments: as qg_gemm_w8a8 without workspace_dev / ws_bytes.
- *   Limit: a shape whose scratch (qg_workspace_bytes) exceeds
+ *   Limit: a shape whose scratch (qg_workspace_bytes_config) exceeds
  *   QG_NOALLOC_SCRATCH_BYTES is rejected with QG_ERR_WORKSPACE_TOO_SMALL;
  *   use fewer splits, or qg_gemm_w8a8 with a caller workspace.
  *   Set-up: the first call in each CUDA context (normally once per device,

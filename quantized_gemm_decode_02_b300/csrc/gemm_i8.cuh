@@ -32,6 +32,16 @@
 // Split-K reduces through distributed shared memory across the cluster of
 // a tile's CTAs (up to 16 ranges) or through the caller workspace, exactly
 // as the FP8 kernel does, in int32.
+//
+// PREW (QG_CONFIG_I8_PREWIDEN, the compute-bound regime beyond the decode
+// range): the activations are widened once per launch by widen_i8_kernel
+// into an fp16 copy in the workspace, and the producer loads that copy by
+// TMA straight into the stage in the MMA's operand layout (two 128-byte
+// swizzle atoms of 64 K).  No activation converter warps, no operand copy:
+// the MMA reads the B operand from the stage and releases it with a commit.
+// Each weight tile is widened once per block of up to 128 tokens (instead of
+// once per 64, with the activations widened again in every CTA), so a
+// widened weight byte feeds twice the MMA work.
 #pragma once
 #include "common.cuh"
 #include "gemm_f8.cuh"
@@ -61,7 +71,7 @@ struct alignas(8) CtrlI8 {
   uint32_t tmem_base;
   int last_flag;
   int abort_flag;
-  float sa_s[64];   // per-token scales, staged for the epilogue
+  float sa_s[128];  // per-token scales, staged for the epilogue
   float sw_s[128];  // per-channel scales of the tile's rows
   float amax_s[kMaxClusterSplits * 64];  // fused quantization: [source rank][token] partial row maxima
 };
@@ -72,17 +82,21 @@ struct I8Shape {
   static constexpr uint32_t kABytes = MPAD * kBK;          // int8 activations
   static constexpr uint32_t kStageBytes = kWBytes + kABytes;
   static constexpr uint32_t kOpBBytes = MPAD * 256;        // fp16 activations: 2 swizzle atoms of 64 K
+  static constexpr uint32_t kPrewStageBytes = kWBytes + kOpBBytes;  // PREW: int8 weights + fp16 activations
   static constexpr uint32_t kACols = 64;                   // 128 fp16 per row = 64 TMEM columns
   static constexpr uint32_t kDCols = MPAD;
   static constexpr int kHalf = MPAD / 2;                   // tokens drained per converter warp
   static constexpr uint32_t kTmemCols = pow2_cols(kI8OpBufs * kACols + 2 * kDCols);
 };
 
-template <int MPAD>
+template <int MPAD, bool PREW = false>
 __host__ __device__ constexpr size_t gemm_i8_smem_bytes(int stages, int recv_bytes = 0) {
-  return 1024 + static_cast<size_t>(stages) * I8Shape<MPAD>::kStageBytes +
-         static_cast<size_t>(kI8OpBufs) * I8Shape<MPAD>::kOpBBytes + recv_bytes + sizeof(CtrlI8);
+  return PREW ? 1024 + static_cast<size_t>(stages) * I8Shape<MPAD>::kPrewStageBytes + recv_bytes + sizeof(CtrlI8)
+              : 1024 + static_cast<size_t>(stages) * I8Shape<MPAD>::kStageBytes +
+                    static_cast<size_t>(kI8OpBufs) * I8Shape<MPAD>::kOpBBytes + recv_bytes + sizeof(CtrlI8);
 }
+// threads of the kernel: the PREW form has no activation converter warps
+__host__ __device__ constexpr int i8_threads(bool prew) { return prew ? 32 * kI8AWarp : kI8Threads; }
 
 // 4 int8 (one 32-bit word, element 0 in the low byte) -> two fp16x2 words:
 // bias each byte by 128 into an unsigned byte u, form the fp16 1024 + u by
@@ -99,20 +113,42 @@ __device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+// int8 activation codes -> their exact fp16 values (the B operand of the
+// PREW form), 16 codes a thread per step; n16 = codes / 16.
+__global__ void __launch_bounds__(256) widen_i8_kernel(const uint8_t* __restrict__ src, uint4* __restrict__ dst,
+                                                       int64_t n16) {
+  pdl_launch_dependents();  // the GEMM may start streaming its weights
+  pdl_wait();               // the codes come from the kernel this one depends on
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    uint32_t o[8];
+    int8x4_to_f16x4(v.x, o[0], o[1]);
+    int8x4_to_f16x4(v.y, o[2], o[3]);
+    int8x4_to_f16x4(v.z, o[4], o[5]);
+    int8x4_to_f16x4(v.w, o[6], o[7]);
+    dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // FUSED: the activation warps read bf16 activations (g.A) and quantize them
 // to int8 codes themselves (qg_linear_w8a8): no quantization kernel and no
 // int8 activation tensor in between; tmA is unused.
-template <int MPAD, bool FUSED>
-__global__ void __launch_bounds__(kI8Threads, 2)
+template <int MPAD, bool FUSED, bool PREW = false>
+__global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = I8Shape<MPAD>;
   constexpr int kHalf = S::kHalf;
+  static_assert(!(PREW && FUSED), "the pre-widened form takes quantized activations");
+  static_assert(MPAD <= 128, "token blocks of at most 128");
+  constexpr uint32_t kStage = PREW ? S::kPrewStageBytes : S::kStageBytes;
   stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int stages = g.stages;
-  uint8_t* opb = smem + static_cast<size_t>(stages) * S::kStageBytes;  // fp16 activation buffers
-  uint8_t* recv = opb + kI8OpBufs * S::kOpBBytes;                        // split-K receive buffer
+  uint8_t* opb = smem + static_cast<size_t>(stages) * kStage;                // fp16 activation buffers (not PREW)
+  uint8_t* recv = opb + (PREW ? 0 : kI8OpBufs * S::kOpBBytes);               // split-K receive buffer
   CtrlI8* ctl = reinterpret_cast<CtrlI8*>(recv + g.recv_bytes);
   const bool clustered = g.reduce == kReduceCluster;
 
@@ -136,10 +172,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
     for (int i = 0; i < stages; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->full_a[i], 1);
-      mbar_init(&ctl->empty[i], kI8ConvWarps + (FUSED ? 0 : kI8AWarps));
+      // PREW: the MMAs read the stage's activations, so their commit releases it too
+      mbar_init(&ctl->empty[i], kI8ConvWarps + (PREW ? 1 : (FUSED ? 0 : kI8AWarps)));
     }
     for (int b = 0; b < kI8OpBufs; ++b) {
-      mbar_init(&ctl->op_full[b], kI8ConvWarps + kI8AWarps);
+      mbar_init(&ctl->op_full[b], kI8ConvWarps + (PREW ? 0 : kI8AWarps));
       mbar_init(&ctl->op_empty[b], 1);
     }
     for (int d = 0; d < 2; ++d) {
@@ -183,19 +220,27 @@ __global__ void __launch_bounds__(kI8Threads, 2)
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       const int w_row = w_row0 + n_tile * kBN;
       const int pre = nk < stages ? nk : stages;
+      // the stage's activation tile: int8 codes, or (PREW) their fp16 copy
+      // as two 64-K swizzle atoms in the MMA's operand layout
+      auto load_act = [&](uint8_t* st, int i, uint64_t* bar) {
+        if constexpr (PREW) {
+          mbar_arrive_expect_tx(bar, S::kOpBBytes);
+          for (int atom = 0; atom < 2; ++atom)
+            tma_load_2d(st + S::kWBytes + atom * (MPAD * 128), &tmA, (kb0 + i) * kBK + 64 * atom, m_base, bar, pol_a);
+        } else {
+          mbar_arrive_expect_tx(bar, S::kABytes);
+          tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, bar, pol_a);
+        }
+      };
       for (int i = 0; i < pre; ++i) {
-        uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
+        uint8_t* st = smem + static_cast<size_t>(i) * kStage;
         mbar_arrive_expect_tx(&ctl->full[i], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[i], pol_w);
       }
       for (int i = pre; i < nk && i < pre + g.l2_prefetch; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * kBK, w_row);
       pdl_wait();
       if (!FUSED) {
-        for (int i = 0; i < pre; ++i) {
-          uint8_t* st = smem + static_cast<size_t>(i) * S::kStageBytes;
-          mbar_arrive_expect_tx(&ctl->full_a[i], S::kABytes);
-          tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[i], pol_a);
-        }
+        for (int i = 0; i < pre; ++i) load_act(smem + static_cast<size_t>(i) * kStage, i, &ctl->full_a[i]);
       }
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -205,14 +250,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
           *abort_flag = 1;
           break;
         }
-        uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
+        uint8_t* st = smem + static_cast<size_t>(s) * kStage;
         mbar_arrive_expect_tx(&ctl->full[s], S::kWBytes);
         tma_load_2d(st, &tmW, (kb0 + i) * kBK, w_row, &ctl->full[s], pol_w);
         if (g.l2_prefetch > 0 && i + g.l2_prefetch < nk) tma_prefetch_l2_2d(&tmW, (kb0 + i + g.l2_prefetch) * kBK, w_row);
-        if (!FUSED) {
-          mbar_arrive_expect_tx(&ctl->full_a[s], S::kABytes);
-          tma_load_2d(st + S::kWBytes, &tmA, (kb0 + i) * kBK, m_base, &ctl->full_a[s], pol_a);
-        }
+        if (!FUSED) load_act(st, i, &ctl->full_a[s]);
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit or reuse the ring
@@ -224,7 +266,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   } else {
     if (warp == 1) tmem_alloc(&ctl->tmem_base, S::kTmemCols);
     tc_fence_before();
-    named_bar_sync(2, kI8Threads - 32);
+    named_bar_sync(2, i8_threads(PREW) - 32);
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t tmem_a = tmem;                                   // kI8OpBufs x 64 columns
@@ -247,8 +289,15 @@ __global__ void __launch_bounds__(kI8Threads, 2)
             ok = false;
             break;
           }
+          // PREW: the fp16 activations come straight from the stage
+          const int s = i % stages;
+          if (PREW && !mbar_wait(&ctl->full_a[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t b_base = smem_u32(opb + buf * S::kOpBBytes);
+          const uint32_t b_base =
+              PREW ? smem_u32(smem + static_cast<size_t>(s) * kStage + S::kWBytes) : smem_u32(opb + buf * S::kOpBBytes);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t b_addr = b_base + (kk >> 2) * (MPAD * 128) + (kk & 3) * 32;
@@ -256,6 +305,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
                        (!seg_start || kk > 0) ? 1u : 0u);
           }
           tc_commit(&ctl->op_empty[buf]);
+          if (PREW) tc_commit(&ctl->empty[s]);  // the stage's activations are consumed
           if ((i % kI8SegTiles) == kI8SegTiles - 1 || i == nk - 1) tc_commit(&ctl->d_full[d]);
         }
         if (!ok) {
@@ -343,7 +393,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
           break;
         }
         // activation tile -> fp16, swizzled K-major B operand (2 atoms of 64 K)
-        const uint8_t* src = smem + static_cast<size_t>(s) * S::kStageBytes + S::kWBytes;
+        const uint8_t* src = smem + static_cast<size_t>(s) * kStage + S::kWBytes;
         uint8_t* ob = opb + buf * S::kOpBBytes;
 #pragma unroll
         for (int piece = at; piece < MPAD * 4; piece += 32 * kI8AWarps) {
@@ -417,7 +467,7 @@ __global__ void __launch_bounds__(kI8Threads, 2)
           ok = false;
           break;
         }
-        const uint8_t* st = smem + static_cast<size_t>(s) * S::kStageBytes;
+        const uint8_t* st = smem + static_cast<size_t>(s) * kStage;
         // this thread's 64 weight bytes -> fp16 -> TMEM operand buffer
 #pragma unroll
         for (int c = 4 * h; c < 4 * h + 4; ++c) {
@@ -468,6 +518,11 @@ __global__ void __launch_bounds__(kI8Threads, 2)
   };
 
   const bool holds_acc = warp >= 2 && warp < kI8AWarp;
+  if (PREW && holds_acc) {
+    // no activation warps staged the token scales: the accumulator threads do
+    if (ct < MPAD) ctl->sa_s[ct] = ct < Mb ? __ldg(g.s_a + m_base + ct) : 0.0f;
+    named_bar_sync(1, kI8ConvThreads);
+  }
   if (clustered) {
     if (holds_acc) {
       cluster_wait();  // every peer's receive barrier is initialized

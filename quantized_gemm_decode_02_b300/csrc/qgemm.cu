@@ -102,6 +102,23 @@ int make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int64_t
   return QG_OK;
 }
 
+// 2-D fp16 tensor map over rows x K elements (dense rows), box of 64
+// elements (128 bytes) x box_rows rows, 128-byte swizzle: one MMA operand
+// swizzle atom of 64 K; rows past the end read zero.
+int make_map_f16(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled (fp16) failed (%d)", static_cast<int>(r));
+  return QG_OK;
+}
+
 // -------------------------------------------------------------- launching
 struct DevInfo {
   int sms = 0;
@@ -195,6 +212,8 @@ struct Plan {
   bool dp4a = false;   // W8A8_INT8 Swap-AB on the CUDA cores (M <= 8)
   bool mma = false;    // W8A8_INT8 Swap-AB on mma.sync (QG_CONFIG_MMA_SYNC)
   bool persist = false;  // FP8_Dynamic Standard as the persistent pair kernel (QG_CONFIG_PERSIST)
+  bool prew = false;     // W8A8_INT8 Swap-AB on activations widened once per launch (QG_CONFIG_I8_PREWIDEN)
+  int64_t prew_bytes = 0;  // their fp16 copy in the workspace (after the Split-K part)
   int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64 (mma.sync: 8 / 16 / 24 / 32)
   int ctr_tiles = 0;   // Split-K arrival counters of one group: enough for every kernel's token blocks
   int n_tiles = 0, m_tiles = 0, kt = 0, splits = 1;
@@ -208,6 +227,9 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->dp4a;
   p->mma = (config_id & QG_CONFIG_MMA_SYNC) != 0;
   p->persist = (config_id & QG_CONFIG_PERSIST) != 0;
+  p->prew = (config_id & QG_CONFIG_I8_PREWIDEN) != 0;
+  if (p->prew && (fmt != QG_W8A8_INT8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->mma))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_I8_PREWIDEN is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
   if (p->persist && (fmt != QG_FP8_DYNAMIC || variant != QG_STANDARD))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PERSIST is for FP8_Dynamic with QG_STANDARD");
   if (p->dp4a && (fmt != QG_W8A8_INT8 || M > qg::kDpMaxTokens))
@@ -227,6 +249,11 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   if (p->mma) {
     // token groups of 8 on the MMA N side; more than 32 tokens run as blocks of 32
     p->mpad = M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 24 ? 24 : 32));
+    p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
+    if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
+  } else if (p->prew) {
+    // blocks of 64 tokens, or of 128 above 64 tokens
+    p->mpad = M <= 64 ? 64 : 128;
     p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else if (p->swap) {
@@ -265,9 +292,15 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
 
 // rows: the token rows of A_q / Y (all groups' tokens for grouped launches).
 // The counters are those of 128-row tiles (see gemm_entry).
-int64_t workspace_bytes(const Plan& p, int64_t rows, int64_t N) {
+// PREW adds the fp16 copy of the activations (rows x K), 256-byte aligned,
+// after the Split-K part.
+int64_t split_workspace_bytes(const Plan& p, int64_t rows, int64_t N) {
   if (p.reduce != qg::kReduceGlobal) return 0;
   return ws_counter_bytes(static_cast<int64_t>(p.groups) * p.ctr_tiles) + static_cast<int64_t>(p.splits) * rows * N * 4;
+}
+int64_t prew_offset(const Plan& p, int64_t rows, int64_t N) { return cdiv(split_workspace_bytes(p, rows, N), 256) * 256; }
+int64_t workspace_bytes(const Plan& p, int64_t rows, int64_t N, int64_t K) {
+  return p.prew ? prew_offset(p, rows, N) + cdiv(rows * K * 2, 256) * 256 : split_workspace_bytes(p, rows, N);
 }
 
 // config_id = ring | distance << 5 (see qgemm.h).  Ring depth: ring > 0
@@ -340,14 +373,17 @@ int run_f8_swap_fmt(int fmt, bool fused, const Plan& p, const CUtensorMap& tmW, 
   return run_f8_swap<qg::kFmtBlock, MPAD, false>(p, tmW, tmA, g, config_id, stream);
 }
 
-template <int MPAD, bool FUSED>
+template <int MPAD, bool FUSED, bool PREW = false>
 int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
            cudaStream_t stream) {
   const int rb = g.recv_bytes;
-  int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD>(st, rb); }, &g.stages);
+  // PREW runs one CTA per SM (its TMEM takes all 512 columns): the default
+  // ring is the deepest that fits
+  if (PREW && (config_id & QG_CONFIG_RING_MASK) == 0) config_id |= kMaxStages;
+  int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD, PREW>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::kI8Threads,
-                     qg::gemm_i8_smem_bytes<MPAD>(g.stages, rb), tmW, tmA, g, stream);
+  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED, PREW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
+                     qg::i8_threads(PREW), qg::gemm_i8_smem_bytes<MPAD, PREW>(g.stages, rb), tmW, tmA, g, stream);
 }
 
 template <int NG, int TPW, int DPW, bool S8 = false>
@@ -452,7 +488,7 @@ int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
                      QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_PAIR_MMA |
-                     QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -468,6 +504,11 @@ int check_config_bits(int fmt, int variant, int config_id) {
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_DP4A needs QG_CONFIG_MMA_NARROW and at most 4 groups of 16 rows");
   if ((config_id & QG_CONFIG_MMA_S8) && !(config_id & QG_CONFIG_MMA_SYNC))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_MMA_S8 needs QG_CONFIG_MMA_SYNC");
+  if ((config_id & QG_CONFIG_I8_PREWIDEN) &&
+      (fmt != QG_W8A8_INT8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) ||
+       (config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_WIDE | QG_CONFIG_PERSIST))))
+    return fail(QG_ERR_INVALID_ARG,
+                "QG_CONFIG_I8_PREWIDEN is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernel");
   if ((config_id & QG_CONFIG_PAIR_MMA) && !(config_id & QG_CONFIG_PERSIST))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PAIR_MMA is a form of the QG_CONFIG_PERSIST kernel");
   if ((config_id & QG_CONFIG_PERSIST) &&
@@ -624,7 +665,7 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
   if (rc != QG_OK) return rc;
   if (grouped) p.groups = grouped->groups;
   if (wide) p.n_tiles = static_cast<int>(cdiv(N, 256));
-  const int64_t need = workspace_bytes(p, rows, N);
+  const int64_t need = workspace_bytes(p, rows, N, K);
   if (need > 0) {
     if (!workspace_dev) return fail(QG_ERR_WORKSPACE_TOO_SMALL, "split_k=%d needs a %lld-byte workspace", split_k, (long long)need);
     if (static_cast<int64_t>(ws_bytes) < need)
@@ -638,6 +679,15 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     tmA = tmW;  // unused: the kernel reads the bf16 activations directly
   } else {
     rc = make_map(&tmA, A_q_dev, rows, K, K, p.swap ? static_cast<uint32_t>(p.mpad) : 128u);
+    if (rc != QG_OK) return rc;
+  }
+  // PREW: the GEMM reads the fp16 copy of the activations in the workspace
+  uint8_t* a16 = nullptr;
+  if (p.prew) {
+    if (grouped || fused)
+      return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_I8_PREWIDEN takes the quantized activations of one group");
+    a16 = static_cast<uint8_t*>(workspace_dev) + prew_offset(p, rows, N);
+    rc = make_map_f16(&tmA, a16, rows, K, static_cast<uint32_t>(p.mpad));
     if (rc != QG_OK) return rc;
   }
 
@@ -698,6 +748,16 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (p.mpad == 16) return run_i8_mma<2>(p, tmW, tmA, g, config_id, s);
     if (p.mpad == 24) return run_i8_mma<3>(p, tmW, tmA, g, config_id, s);
     return run_i8_mma<4>(p, tmW, tmA, g, config_id, s);
+  }
+  if (p.prew) {
+    // the activations widened once (no timing slot: its time falls to the GEMM)
+    const int64_t n16 = rows * K / 16;
+    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(n16, 256), 4 * dev_info().sms)));
+    cudaError_t e = launch_cluster_xy(qg::widen_i8_kernel, dim3(blocks), dim3(256), 0, s, 1u, 1u,
+                                      static_cast<const uint8_t*>(A_q_dev), reinterpret_cast<uint4*>(a16), n16);
+    if (e != cudaSuccess) return cuda_fail(e, "widen launch");
+    return p.mpad == 64 ? run_i8<64, false, true>(p, tmW, tmA, g, config_id, s)
+                        : run_i8<128, false, true>(p, tmW, tmA, g, config_id, s);
   }
   if (fmt == QG_W8A8_INT8) {
     if (p.mpad == 16) return fz ? run_i8<16, true>(p, tmW, tmA, g, config_id, s) : run_i8<16, false>(p, tmW, tmA, g, config_id, s);
@@ -974,11 +1034,15 @@ int qg_quant_weight(int fmt, const float* W_dev, int64_t N, int64_t K, void* W_q
   return QG_OK;
 }
 
-size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k) {
+size_t qg_workspace_bytes_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, int config_id) {
   Plan p;
   if (fmt < 0 || fmt > 2 || M <= 0 || N <= 0 || K <= 0 || variant < 0 || variant > QG_SWAPAB_DP4A_SPLITK) return 0;
-  if (make_plan(fmt, M, N, K, variant, split_k, 0, &p) != QG_OK) return 0;
-  return static_cast<size_t>(workspace_bytes(p, M, N));
+  if (check_config_bits(fmt, variant, config_id) != QG_OK) return 0;
+  if (make_plan(fmt, M, N, K, variant, split_k, config_id, &p) != QG_OK) return 0;
+  return static_cast<size_t>(workspace_bytes(p, M, N, K));
+}
+size_t qg_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k) {
+  return qg_workspace_bytes_config(fmt, M, N, K, variant, split_k, 0);
 }
 
 int qg_check_config(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k, int config_id) {
@@ -1018,7 +1082,7 @@ size_t qg_workspace_bytes_grouped(int fmt, int groups, int64_t total_tokens, int
     return 0;
   if (make_plan(fmt, max_tokens, N, K, variant, split_k, 0, &p) != QG_OK) return 0;
   p.groups = groups;
-  return static_cast<size_t>(workspace_bytes(p, total_tokens, N));
+  return static_cast<size_t>(workspace_bytes(p, total_tokens, N, K));
 }
 
 int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, int64_t lda, const void* W_q_dev,
@@ -1026,7 +1090,8 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
                    void* workspace_dev, size_t ws_bytes, void* A_q_dev, float* s_a_dev, int32_t* debug_acc_dev,
                    void* stream) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
-  const bool fusable = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) && !(config_id & QG_CONFIG_MMA_SYNC);
+  const bool fusable = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) &&
+                       !(config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_I8_PREWIDEN));
   const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
   if (fusable && (!buffers || (config_id & QG_CONFIG_FUSED_QUANT) ||
                   (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {
@@ -1050,7 +1115,7 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
 int qg_gemm_w8a8_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, const float* s_a_dev,
                          const void* W_q_dev, const float* s_w_dev, void* Y_dev, int64_t ldy, int variant,
                          int split_k, int config_id, int32_t* debug_acc_dev, void* stream) {
-  const size_t need = qg_workspace_bytes(fmt, M, N, K, variant, split_k);
+  const size_t need = qg_workspace_bytes_config(fmt, M, N, K, variant, split_k, config_id);
   if (need > QG_NOALLOC_SCRATCH_BYTES)
     return fail(QG_ERR_WORKSPACE_TOO_SMALL,
                 "qg_gemm_w8a8_noalloc: this shape needs %zu bytes of Split-K scratch, more than the %u-byte static "

@@ -38,7 +38,7 @@ def main(argv=None) -> int:
     sa = torch.ones(a.M * ((a.K + 127) // 128) + 1, dtype=torch.float32, device=dev)
     sw = torch.ones(max(a.N, ((a.N + 127) // 128) * ((a.K + 127) // 128)), dtype=torch.float32, device=dev)
     Y = torch.empty(a.M * a.N, dtype=torch.bfloat16, device=dev)
-    need = q.qg_workspace_bytes(a.fmt, a.M, a.N, a.K, a.variant, a.split_k)
+    need = q.qg_workspace_bytes_config(a.fmt, a.M, a.N, a.K, a.variant, a.split_k, a.config_id)
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     for r in range(a.reps):
         W = pool[(r % copies) * wb:(r % copies + 1) * wb]

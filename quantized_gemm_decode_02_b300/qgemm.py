@@ -38,11 +38,12 @@ QG_CONFIG_PERSIST = 1 << 16
 QG_CONFIG_MMA_DP4A_SHIFT = 17
 QG_CONFIG_MMA_S8 = 1 << 20
 QG_CONFIG_PAIR_MMA = 1 << 21
+QG_CONFIG_I8_PREWIDEN = 1 << 22
 
 
 def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False, mma_sync: bool = False,
               narrow: bool = False, fused: bool = False, persist: bool = False, dp4a_rows16: int = 0,
-              s8: bool = False, pair_mma: bool = False) -> int:
+              s8: bool = False, pair_mma: bool = False, prewiden: bool = False) -> int:
     """config_id of a ring depth (0 = default), an L2 prefetch distance,
     (FP8_Dynamic Standard / Split-K) 256-row weight tiles, (W8A8_INT8
     Swap-AB) the mma.sync kernel with eight narrow MMA warps if `narrow`,
@@ -51,16 +52,18 @@ def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False, mma_sync: bo
     of 16 weight rows on dp4a warps (implies the narrow mma.sync kernel);
     `s8`: the mma.sync kernel on the int8 form of the instruction (implies
     mma_sync); `pair_mma`: the persistent kernel with tcgen05.mma.cta_group::2
-    (implies persist)."""
+    (implies persist); `prewiden`: W8A8_INT8 Swap-AB on activations widened
+    once per launch into the workspace (QG_CONFIG_I8_PREWIDEN)."""
     narrow = narrow or dp4a_rows16 > 0
     return (ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT) | (QG_CONFIG_WIDE if wide else 0)
             | (QG_CONFIG_MMA_SYNC if mma_sync or narrow or s8 else 0) | (QG_CONFIG_MMA_NARROW if narrow else 0)
             | (QG_CONFIG_MMA_S8 if s8 else 0)
             | (QG_CONFIG_FUSED_QUANT if fused else 0) | (QG_CONFIG_PERSIST if persist or pair_mma else 0)
-            | (QG_CONFIG_PAIR_MMA if pair_mma else 0)
+            | (QG_CONFIG_PAIR_MMA if pair_mma else 0) | (QG_CONFIG_I8_PREWIDEN if prewiden else 0)
             | (dp4a_rows16 << QG_CONFIG_MMA_DP4A_SHIFT))
 
-EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_check_config", "qg_workspace_init", "qg_gemm_w8a8",
+EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_workspace_bytes_config",
+           "qg_check_config", "qg_workspace_init", "qg_gemm_w8a8",
            "qg_linear_w8a8", "qg_gemm_w8a8_noalloc", "qg_gemm_w8a8_grouped", "qg_workspace_bytes_grouped",
            "qg_select", "qg_load_table", "qg_set_allow_default", "qg_set_launch_flags", "qg_set_wait_limit_ns",
            "qg_set_force_timeout", "qg_set_timing_log", "qg_timing_log_count", "qg_device_error", "qg_last_error",
@@ -83,6 +86,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qg_pack_weight.argtypes = [I, P, I64, I64, P, P]
     lib.qg_workspace_bytes.argtypes = [I, I64, I64, I64, I, I]
     lib.qg_workspace_bytes.restype = SZ
+    lib.qg_workspace_bytes_config.argtypes = [I, I64, I64, I64, I, I, I]
+    lib.qg_workspace_bytes_config.restype = SZ
     lib.qg_check_config.argtypes = [I, I64, I64, I64, I, I, I]
     lib.qg_workspace_init.argtypes = [P, SZ, P]
     lib.qg_gemm_w8a8.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, I, I, I, P, SZ, P, P]
@@ -159,6 +164,10 @@ def qg_pack_weight(fmt, W, N, K, W_q, s_w) -> None:
 
 def qg_workspace_bytes(fmt, M, N, K, variant, split_k) -> int:
     return int(_lib.qg_workspace_bytes(_fmt(fmt), M, N, K, variant, split_k))
+
+
+def qg_workspace_bytes_config(fmt, M, N, K, variant, split_k, config_id=0) -> int:
+    return int(_lib.qg_workspace_bytes_config(_fmt(fmt), M, N, K, variant, split_k, config_id))
 
 
 def qg_check_config(fmt, M, N, K, variant, split_k, config_id=0) -> int:

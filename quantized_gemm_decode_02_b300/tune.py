@@ -71,7 +71,8 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     and without Split-K (reduced in a cluster, up to 16 ranges) for every M
     (in blocks of 64 tokens above 64); for W8A8_INT8 at M <= 8 also their
     CUDA-core (dp4a) forms, and for W8A8_INT8 at every M the mma.sync forms
-    (QG_CONFIG_MMA_SYNC, widened or QG_CONFIG_MMA_S8); above 32 tokens also the Standard variant of the
+    (QG_CONFIG_MMA_SYNC, widened or QG_CONFIG_MMA_S8), and from 64 tokens on
+    its pre-widened form (QG_CONFIG_I8_PREWIDEN); above 32 tokens also the Standard variant of the
     E4M3 formats (FP8_Dynamic also with 256-row weight tiles).  Ring depth:
     0 = two CTAs per SM, 12 = one deep ring per SM (6 for Standard, whose
     stages are twice as large)."""
@@ -106,6 +107,17 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
             out.append((q.QG_SWAPAB, 1, cfg))
             for s in range(2, min(16, kt) + 1):
                 if mma_tiles * s > 12 * sms or kt // s < 1:
+                    continue
+                out.append((q.QG_SWAPAB_SPLITK, s, cfg))
+    if fmt == "W8A8_INT8" and M >= 64:
+        # activations widened once per launch (QG_CONFIG_I8_PREWIDEN), token
+        # blocks of 64 / 128: the compute-bound regime
+        pw_tiles = n_tiles * -(-M // (64 if M <= 64 else 128))
+        for ring in (0, 3):
+            cfg = q.config_id(ring, 0, prewiden=True)
+            out.append((q.QG_SWAPAB, 1, cfg))
+            for s in range(2, min(16, kt) + 1):
+                if pw_tiles * s > 4 * sms or kt // s < 1:
                     continue
                 out.append((q.QG_SWAPAB_SPLITK, s, cfg))
     if M > 32 and fmt != "W8A8_INT8":
@@ -150,6 +162,9 @@ class Bench:
         self.sw = torch.ones(65536 * 4, dtype=torch.float32, device=device)
         self.Y = torch.empty(512 * 51200, dtype=torch.bfloat16, device=device)
         self.ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
+        # QG_CONFIG_I8_PREWIDEN candidates write their fp16 activation copy into
+        # the workspace: a separate one keeps it off the Split-K counters
+        self.ws_prew = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device=device)
 
     def time_config(self, fmt, M, N, K, variant, split, cfg, min_bytes=3 * 126e6, reps=5, linear=False):
@@ -160,7 +175,8 @@ class Bench:
         step = (wbytes + 255) // 256 * 256
         if step * R > POOL_BYTES:
             R = max(2, POOL_BYTES // step)
-        need = q.qg_workspace_bytes(fmt, M, N, K, variant, split)
+        need = q.qg_workspace_bytes_config(fmt, M, N, K, variant, split, cfg)
+        ws = self.ws_prew if cfg & q.QG_CONFIG_I8_PREWIDEN else self.ws
         q.qg_set_launch_flags(q.QG_LAUNCH_PDL)
         try:
             graph = torch.cuda.CUDAGraph()
@@ -169,12 +185,12 @@ class Bench:
                     W = self.pool[r * step:r * step + wbytes]
                     if not linear:
                         q.qg_gemm_w8a8(fmt, M, N, K, self.Aq, self.sa, W, self.sw, self.Y, N, variant, split, cfg,
-                                       self.ws if need else None, need, None, stream=self.stream)
+                                       ws if need else None, need, None, stream=self.stream)
                         continue
                     # the linear call's two-kernel form (quantization into
                     # Aq / sa, then the GEMM), as bench.py runs it
                     q.qg_linear_w8a8(fmt, M, N, K, self.A, K, W, self.sw, self.Y, N, variant, split, cfg,
-                                     self.ws if need else None, need, self.Aq, self.sa, None, stream=self.stream)
+                                     ws if need else None, need, self.Aq, self.sa, None, stream=self.stream)
         finally:
             q.qg_set_launch_flags(0)
         for _ in range(2):
@@ -220,10 +236,11 @@ def time_layer_chain(bench, fmt, M, layers, cfgs, passes=3, reps=5):
             for _ in range(passes):
                 for w in range(windows):
                     for (K, N), off, (v, sp, c) in zip(layers, offs[w], cfgs):
-                        need = q.qg_workspace_bytes(fmt, M, N, K, v, sp)
+                        need = q.qg_workspace_bytes_config(fmt, M, N, K, v, sp, c)
                         W = bench.pool[off:off + N * K]
+                        ws = bench.ws_prew if c & q.QG_CONFIG_I8_PREWIDEN else bench.ws
                         q.qg_linear_w8a8(fmt, M, N, K, bench.A, K, W, bench.sw, bench.Y, N, v, sp, c,
-                                         bench.ws if need else None, need, bench.Aq, bench.sa, None,
+                                         ws if need else None, need, bench.Aq, bench.sa, None,
                                          stream=bench.stream)
     finally:
         q.qg_set_launch_flags(0)

@@ -60,7 +60,7 @@ def gemm_gpu(fmt, Aq, sa, Wq, sw, N, variant, split_k, config_id=0, debug=False,
     M, K = Aq.shape
     if Y is None:
         Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=Aq.device)
-    need = q.qg_workspace_bytes(fmt, M, N, K, variant, split_k)
+    need = q.qg_workspace_bytes_config(fmt, M, N, K, variant, split_k, config_id)
     if need and ws is None:
         ws = torch.zeros(need, dtype=torch.uint8, device=Aq.device)
     dbg = torch.full((M, N), -7, dtype=torch.int32, device=Aq.device) if debug else None

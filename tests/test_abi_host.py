@@ -137,6 +137,21 @@ def _grouped(q, fmt=0, groups=4, offs=OK16, total=8, max_tokens=4, N=256, K=256,
                                         variant, split, cfg, None, 0, None, None)
 
 
+def test_workspace_bytes_config(q):
+    pw = q.QG_CONFIG_I8_PREWIDEN
+    # the fp16 activation copy after the (256-byte aligned) Split-K part
+    assert q.qg_workspace_bytes_config(1, 300, 640, 4096, q.QG_SWAPAB_SPLITK, 3, pw) == 300 * 4096 * 2
+    split_part = ((5 * 19 * 4 + 255) // 256) * 256 + 18 * 300 * 640 * 4
+    assert q.qg_workspace_bytes(1, 300, 640, 4096, q.QG_SWAPAB_SPLITK, 18) == split_part
+    assert q.qg_workspace_bytes_config(1, 300, 640, 4096, q.QG_SWAPAB_SPLITK, 18, pw) == \
+        (split_part + 255) // 256 * 256 + 300 * 4096 * 2
+    assert q.qg_workspace_bytes_config(1, 7, 640, 4112, q.QG_SWAPAB, 1, pw) == (7 * 4112 * 2 + 255) // 256 * 256
+    # other configs: as qg_workspace_bytes; invalid ones: 0
+    assert q.qg_workspace_bytes_config(0, 16, 640, 4096, q.QG_SWAPAB_SPLITK, 18, 0) == \
+        q.qg_workspace_bytes(0, 16, 640, 4096, q.QG_SWAPAB_SPLITK, 18)
+    assert q.qg_workspace_bytes_config(0, 16, 640, 4096, q.QG_SWAPAB, 1, pw) == 0
+
+
 def test_grouped_validation(q):
     # every check below returns before any device work
     assert _grouped(q, groups=0) == q.QG_ERR_UNSUPPORTED_SHAPE
@@ -228,7 +243,10 @@ def test_check_config_returns_the_gemm_status(q):
              dict(fmt=1, M=8, cfg=q.QG_CONFIG_MMA_S8),                               # s8 without mma.sync
              dict(fmt=0, M=8, cfg=q.config_id(s8=True)),
              dict(fmt=0, M=300, variant=0, cfg=q.QG_CONFIG_PAIR_MMA),                # pair MMA without persist
-             dict(fmt=2, M=300, variant=0, cfg=q.config_id(pair_mma=True))]
+             dict(fmt=2, M=300, variant=0, cfg=q.config_id(pair_mma=True)),
+             dict(fmt=0, M=300, cfg=q.QG_CONFIG_I8_PREWIDEN),                          # prewiden: INT8 only
+             dict(fmt=1, M=300, cfg=q.QG_CONFIG_I8_PREWIDEN | q.QG_CONFIG_MMA_SYNC),
+             dict(fmt=1, M=300, variant=q.QG_SWAPAB_DP4A, cfg=q.QG_CONFIG_I8_PREWIDEN)]
     for c in cases:
         fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
         v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)

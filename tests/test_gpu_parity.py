@@ -326,6 +326,63 @@ def test_w8a8_int8_mma_sync_s8_ragged_k(orc, q, gc, M, K, ring):
                 config_id=q.config_id(ring, 0, s8=True))
 
 
+@pytest.mark.parametrize("M", [1, 17, 64, 65, 100, 128, 200, 300, 513])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 7), (SWS, 18)])
+def test_w8a8_int8_prewidened_activations(orc, q, gc, M, variant, split):
+    # QG_CONFIG_I8_PREWIDEN: activations widened once per launch into the
+    # workspace and loaded by TMA; token blocks of 64 (M <= 64) or 128 with
+    # a ragged last block; three exact 1024-K segments; cluster and
+    # workspace reductions; ragged N; int32 bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=1900 + M + split, outliers=True,
+                config_id=q.config_id(0, 0, prewiden=True))
+
+
+@pytest.mark.parametrize("M,K", [(130, 2320), (64, 144)])
+@pytest.mark.parametrize("ring", [2, 3])
+def test_w8a8_int8_prewidened_ragged_k_and_rings(orc, q, gc, M, K, ring):
+    # K not a multiple of 64 (the last fp16 atom partly past K) and shallow rings
+    gc.run_case(orc, "W8A8_INT8", M, 256, K, SWS, 2, seed=1950 + M + ring, outliers=True,
+                config_id=q.config_id(ring, 0, prewiden=True))
+
+
+def test_int8_prewidened_identical_to_other_kernels(gc, q):
+    # the same int32 accumulators and Y as the tcgen05 kernel that widens the
+    # activations itself, and through qg_linear_w8a8 (quantization, widening
+    # and GEMM: three kernels)
+    import seeded_inputs as si
+    M, N, K = 300, 640, 4096
+    A = si.activations(M, K, seed=61, outliers=True).to(gc.DEV)
+    W = torch.from_numpy(si.weights(N, K, seed=61)).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("W8A8_INT8", W)
+    Aq, sa = gc.quant_act_gpu("W8A8_INT8", A)
+    Y0, d0 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 3, debug=True)
+    cfg = q.config_id(0, 0, prewiden=True)
+    Y1, d1 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 3, config_id=cfg, debug=True)
+    Y2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=gc.DEV)
+    need = q.qg_workspace_bytes_config("W8A8_INT8", M, N, K, SWS, 3, cfg)
+    assert need >= M * K * 2 and need > q.qg_workspace_bytes("W8A8_INT8", M, N, K, SWS, 3)
+    ws = torch.zeros(need, dtype=torch.uint8, device=gc.DEV)
+    Aq2, sa2 = torch.empty_like(Aq), torch.empty_like(sa)
+    q.qg_linear_w8a8("W8A8_INT8", M, N, K, A, K, Wq, sw, Y2, N, SWS, 3, cfg, ws, need, Aq2, sa2, None)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    assert torch.equal(d0, d1) and torch.equal(Y0, Y1) and torch.equal(Y0, Y2)
+
+
+def test_prewidened_config_rejected_elsewhere(q, gc):
+    d = torch.zeros(1 << 20, dtype=torch.uint8, device=gc.DEV)
+    f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
+    pw = q.QG_CONFIG_I8_PREWIDEN
+    for fmt, v, s, cfg in (("FP8_Dynamic", SW, 1, pw), ("Block_FP8", SW, 1, pw), ("W8A8_INT8", DP, 1, pw),
+                           ("W8A8_INT8", SW, 1, pw | q.QG_CONFIG_MMA_SYNC), ("W8A8_INT8", SW, 1, pw | q.QG_CONFIG_FUSED_QUANT)):
+        with pytest.raises(q.QGError) as e:
+            q.qg_gemm_w8a8(fmt, 64, 256, 256, d, f, d, f, d, 256, v, s, cfg, d, d.numel())
+        assert e.value.code == q.QG_ERR_INVALID_ARG
+    with pytest.raises(q.QGError) as e:  # the fp16 copy needs the workspace
+        q.qg_gemm_w8a8("W8A8_INT8", 64, 256, 256, d, f, d, f, d, 256, SW, 1, pw)
+    assert e.value.code == q.QG_ERR_WORKSPACE_TOO_SMALL
+
+
 @pytest.mark.parametrize("M", [3, 12, 32])
 @pytest.mark.parametrize("ring", [2, 3, 6])
 def test_w8a8_int8_mma_sync_ring_depths(orc, q, gc, M, ring):
