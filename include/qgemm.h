@@ -87,6 +87,7 @@ typedef enum {
 #define QG_CONFIG_MMA_S8 (1 << 20)
 #define QG_CONFIG_PAIR_MMA (1 << 21)
 #define QG_CONFIG_I8_PREWIDEN (1 << 22)
+#define QG_CONFIG_I8_CONV16 (1 << 23)
 
 typedef enum {
   QG_OK = 0,
@@ -224,6 +225,13 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      that copy, which may cover where another call keeps
  *                      its Split-K arrival counters: give such calls a
  *                      workspace of their own;
+ *                      plus QG_CONFIG_I8_CONV16 for W8A8_INT8 with QG_SWAPAB /
+ *                      QG_SWAPAB_SPLITK on the tcgen05 kernel (with or
+ *                      without QG_CONFIG_I8_PREWIDEN): sixteen weight
+ *                      converter warps instead of eight and one CTA per SM
+ *                      with the deepest ring that fits, so that more weight
+ *                      bytes are in flight per SM while they are widened;
+ *                      not for the one-kernel form of qg_linear_w8a8;
  *   workspace_dev      qg_workspace_bytes_config() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

@@ -95,8 +95,23 @@ __host__ __device__ constexpr size_t gemm_i8_smem_bytes(int stages, int recv_byt
               : 1024 + static_cast<size_t>(stages) * I8Shape<MPAD>::kStageBytes +
                     static_cast<size_t>(kI8OpBufs) * I8Shape<MPAD>::kOpBBytes + recv_bytes + sizeof(CtrlI8);
 }
+// CW weight converter warps (warps 2 .. 2+CW-1; 8, or 16 in the form that
+// runs one CTA per SM with the deepest ring, QG_CONFIG_I8_CONV16): the
+// converters of a row quarter (warp % 4, the TMEM lanes a warp may reach)
+// split each k-tile into CW/4 parts of 8/(CW/4) 16-byte chunks, and drain
+// the accumulator in CW/4 token parts.
+template <int CW>
+struct I8Conv {
+  static constexpr int kWarps = CW;
+  static constexpr int kThreads = 32 * CW;
+  static constexpr int kAWarp = 2 + CW;     // first activation converter warp
+  static constexpr int kParts = CW / 4;     // K parts / token parts of a row quarter
+  static constexpr int kChunks = 8 / kParts;
+};
 // threads of the kernel: the PREW form has no activation converter warps
-__host__ __device__ constexpr int i8_threads(bool prew) { return prew ? 32 * kI8AWarp : kI8Threads; }
+__host__ __device__ constexpr int i8_threads(bool prew, int cw = kI8ConvWarps) {
+  return 32 * (2 + cw + (prew ? 0 : kI8AWarps));
+}
 
 // 4 int8 (one 32-bit word, element 0 in the low byte) -> two fp16x2 words:
 // bias each byte by 128 into an unsigned byte u, form the fp16 1024 + u by
@@ -111,6 +126,13 @@ __device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
   __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
   lo = *reinterpret_cast<uint32_t*>(&ha);
   hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// TMEM -> registers: this warp's 32 lanes x 4 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr));
 }
 
 // int8 activation codes -> their exact fp16 values (the B operand of the
@@ -135,11 +157,15 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const uint8_t* __restrict
 // FUSED: the activation warps read bf16 activations (g.A) and quantize them
 // to int8 codes themselves (qg_linear_w8a8): no quantization kernel and no
 // int8 activation tensor in between; tmA is unused.
-template <int MPAD, bool FUSED, bool PREW = false>
-__global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
+template <int MPAD, bool FUSED, bool PREW = false, int CW = kI8ConvWarps>
+__global__ void __launch_bounds__(i8_threads(PREW, CW), (PREW || CW > kI8ConvWarps) ? 1 : 2)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = I8Shape<MPAD>;
-  constexpr int kHalf = S::kHalf;
+  using C = I8Conv<CW>;
+  constexpr int kHalf = MPAD / C::kParts;  // tokens drained per converter thread
+  static_assert(CW == 8 || CW == 16, "8 or 16 weight converter warps");
+  static_assert(!(FUSED && CW != kI8ConvWarps), "the fused form keeps 8 converter warps");
+  static_assert(kHalf % 4 == 0, "token parts of at least 4");
   static_assert(!(PREW && FUSED), "the pre-widened form takes quantized activations");
   static_assert(MPAD <= 128, "token blocks of at most 128");
   constexpr uint32_t kStage = PREW ? S::kPrewStageBytes : S::kStageBytes;
@@ -173,15 +199,15 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->full_a[i], 1);
       // PREW: the MMAs read the stage's activations, so their commit releases it too
-      mbar_init(&ctl->empty[i], kI8ConvWarps + (PREW ? 1 : (FUSED ? 0 : kI8AWarps)));
+      mbar_init(&ctl->empty[i], C::kWarps + (PREW ? 1 : (FUSED ? 0 : kI8AWarps)));
     }
     for (int b = 0; b < kI8OpBufs; ++b) {
-      mbar_init(&ctl->op_full[b], kI8ConvWarps + (PREW ? 0 : kI8AWarps));
+      mbar_init(&ctl->op_full[b], C::kWarps + (PREW ? 0 : kI8AWarps));
       mbar_init(&ctl->op_empty[b], 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&ctl->d_full[d], 1);
-      mbar_init(&ctl->d_empty[d], kI8ConvWarps);
+      mbar_init(&ctl->d_empty[d], C::kWarps);
     }
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->done, 1);
@@ -211,7 +237,7 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
 #pragma unroll
   for (int m = 0; m < kHalf; ++m) iacc[m] = 0;
   const int cw = warp - 2;        // converter warp 0..7 (negative for warps 0, 1)
-  const int h = cw >> 2;          // K half of the weight row / token half of the accumulator
+  const int h = cw >> 2;          // K part of the weight row / token part of the accumulator
   const uint32_t row = (warp & 3) * 32u + lane;
 
   if (warp == 0) {
@@ -266,7 +292,7 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
   } else {
     if (warp == 1) tmem_alloc(&ctl->tmem_base, S::kTmemCols);
     tc_fence_before();
-    named_bar_sync(2, i8_threads(PREW) - 32);
+    named_bar_sync(2, i8_threads(PREW, CW) - 32);
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t tmem_a = tmem;                                   // kI8OpBufs x 64 columns
@@ -315,10 +341,10 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
         }
         tc_commit(&ctl->done);  // all issued MMAs complete
       }
-    } else if (FUSED && warp >= kI8AWarp) {
+    } else if (FUSED && warp >= C::kAWarp) {
       // ---------------------------------------- activation quantizers (fused)
       pdl_wait();  // the activations are written by the kernel this one depends on
-      const int at = threadIdx.x - 32 * kI8AWarp;  // 0..63
+      const int at = threadIdx.x - 32 * C::kAWarp;  // 0..63
       const bool whole_row = !clustered && g.splits > 1;  // workspace Split-K: scale over the whole row
       const int k0 = whole_row ? 0 : kb0 * kBK, k1 = whole_row ? g.K : min(g.K, kb1 * kBK);
       fused_token_scales(g, m_base, Mb, k0, k1, clustered, clustered ? split : 0, 127.0f, ctl->amax_s, ctl->sa_s,
@@ -377,10 +403,10 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
         if (lane == 0) mbar_arrive(&ctl->op_full[buf]);
       }
       if (!ok) *abort_flag = 1;
-    } else if (warp >= kI8AWarp) {
+    } else if (warp >= C::kAWarp) {
       // -------------------------------------------- activation converters
       pdl_wait();  // s_a is written by the kernel this one depends on
-      const int at = threadIdx.x - 32 * kI8AWarp;  // 0..63
+      const int at = threadIdx.x - 32 * C::kAWarp;  // 0..63
       if (at < MPAD) ctl->sa_s[at] = at < Mb ? __ldg(g.s_a + m_base + at) : 0.0f;
       bool ok = true;
       for (int i = 0; i < nk; ++i) {
@@ -440,13 +466,24 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
         bool w = mbar_wait(&ctl->d_full[d], static_cast<uint32_t>(seg / 2) & 1u, g.wait_ns);
         if (!__all_sync(0xffffffffu, w && !*abort_flag)) return false;
         tc_fence_after();
+        if constexpr (kHalf % 8 == 0) {
 #pragma unroll
-        for (int c = 0; c < kHalf; c += 8) {
-          uint32_t t[8];
-          tmem_ld_x8(tmem_d + lane_base + d * S::kDCols + h * kHalf + c, t);
-          tmem_ld_wait();
+          for (int c = 0; c < kHalf; c += 8) {
+            uint32_t t[8];
+            tmem_ld_x8(tmem_d + lane_base + d * S::kDCols + h * kHalf + c, t);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) iacc[c + j] += __float2int_rn(__uint_as_float(t[j]));
+            for (int j = 0; j < 8; ++j) iacc[c + j] += __float2int_rn(__uint_as_float(t[j]));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 4) {
+            uint32_t t[4];
+            tmem_ld_x4(tmem_d + lane_base + d * S::kDCols + h * kHalf + c, t);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) iacc[c + j] += __float2int_rn(__uint_as_float(t[j]));
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -470,7 +507,7 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
         const uint8_t* st = smem + static_cast<size_t>(s) * kStage;
         // this thread's 64 weight bytes -> fp16 -> TMEM operand buffer
 #pragma unroll
-        for (int c = 4 * h; c < 4 * h + 4; ++c) {
+        for (int c = C::kChunks * h; c < C::kChunks * (h + 1); ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(st + sw128_chunk(row, c));
           uint32_t o[8];
           int8x4_to_f16x4(v.x, o[0], o[1]);
@@ -517,26 +554,26 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
     store_bf16(g.Y + static_cast<int64_t>(m_base + m) * g.ldy + nn, y);
   };
 
-  const bool holds_acc = warp >= 2 && warp < kI8AWarp;
+  const bool holds_acc = warp >= 2 && warp < C::kAWarp;
   if (PREW && holds_acc) {
     // no activation warps staged the token scales: the accumulator threads do
     if (ct < MPAD) ctl->sa_s[ct] = ct < Mb ? __ldg(g.s_a + m_base + ct) : 0.0f;
-    named_bar_sync(1, kI8ConvThreads);
+    named_bar_sync(1, C::kThreads);
   }
   if (clustered) {
     if (holds_acc) {
       cluster_wait();  // every peer's receive barrier is initialized
       // rows go out even after an abort, so that every owner's wait completes
       cluster_push_row(iacc, h * kHalf, static_cast<int>(row), split, g.splits, Mb, recv, &ctl->recv_bar);
-      named_bar_sync(1, kI8ConvThreads);  // this CTA's own rows, stored locally, are visible
+      named_bar_sync(1, C::kThreads);  // this CTA's own rows, stored locally, are visible
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
       if (got && !abort) {
-        cluster_sum_rows<int32_t>(recv, split, g.splits, Mb, ct, kI8ConvThreads, [&](int m, int r, int32_t sum) {
+        cluster_sum_rows<int32_t>(recv, split, g.splits, Mb, ct, C::kThreads, [&](int m, int r, int32_t sum) {
           const int nn = n_tile * kBN + r;
           if (nn < g.N) finish(m, r, nn, sum);
         });
       }
-    } else if (!(FUSED && warp >= kI8AWarp)) {
+    } else if (!(FUSED && warp >= C::kAWarp)) {
       // the other warps pair their early arrive with a wait too (every peer
       // arrived right after its set-up, so this returns at once); the fused
       // quantizer warps waited before their row-maximum exchange
@@ -560,10 +597,10 @@ __global__ void __launch_bounds__(i8_threads(PREW), PREW ? 1 : 2)
         }
       }
       __threadfence();
-      named_bar_sync(1, kI8ConvThreads);
+      named_bar_sync(1, C::kThreads);
       const int tile_id = blockIdx.x + blockIdx.z * gridDim.x;
       if (ct == 0) ctl->last_flag = (atomicAdd(g.ws_count + tile_id, 1) == g.splits - 1);
-      named_bar_sync(1, kI8ConvThreads);
+      named_bar_sync(1, C::kThreads);
       if (ctl->last_flag) {
         __threadfence();
         if (n_ok) {

@@ -373,17 +373,17 @@ int run_f8_swap_fmt(int fmt, bool fused, const Plan& p, const CUtensorMap& tmW, 
   return run_f8_swap<qg::kFmtBlock, MPAD, false>(p, tmW, tmA, g, config_id, stream);
 }
 
-template <int MPAD, bool FUSED, bool PREW = false>
+template <int MPAD, bool FUSED, bool PREW = false, int CW = qg::kI8ConvWarps>
 int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
            cudaStream_t stream) {
   const int rb = g.recv_bytes;
-  // PREW runs one CTA per SM (its TMEM takes all 512 columns): the default
-  // ring is the deepest that fits
-  if (PREW && (config_id & QG_CONFIG_RING_MASK) == 0) config_id |= kMaxStages;
+  // PREW (its TMEM takes all 512 columns) and the 16-converter form run one
+  // CTA per SM: the default ring is the deepest that fits
+  if ((PREW || CW > qg::kI8ConvWarps) && (config_id & QG_CONFIG_RING_MASK) == 0) config_id |= kMaxStages;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD, PREW>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED, PREW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
-                     qg::i8_threads(PREW), qg::gemm_i8_smem_bytes<MPAD, PREW>(g.stages, rb), tmW, tmA, g, stream);
+  return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED, PREW, CW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
+                     qg::i8_threads(PREW, CW), qg::gemm_i8_smem_bytes<MPAD, PREW>(g.stages, rb), tmW, tmA, g, stream);
 }
 
 template <int NG, int TPW, int DPW, bool S8 = false>
@@ -488,7 +488,7 @@ int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
                      QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_PAIR_MMA |
-                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -509,6 +509,11 @@ int check_config_bits(int fmt, int variant, int config_id) {
        (config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_WIDE | QG_CONFIG_PERSIST))))
     return fail(QG_ERR_INVALID_ARG,
                 "QG_CONFIG_I8_PREWIDEN is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernel");
+  if ((config_id & QG_CONFIG_I8_CONV16) &&
+      (fmt != QG_W8A8_INT8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) ||
+       (config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_WIDE | QG_CONFIG_PERSIST))))
+    return fail(QG_ERR_INVALID_ARG,
+                "QG_CONFIG_I8_CONV16 is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernel");
   if ((config_id & QG_CONFIG_PAIR_MMA) && !(config_id & QG_CONFIG_PERSIST))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PAIR_MMA is a form of the QG_CONFIG_PERSIST kernel");
   if ((config_id & QG_CONFIG_PERSIST) &&
@@ -756,8 +761,17 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     cudaError_t e = launch_cluster_xy(qg::widen_i8_kernel, dim3(blocks), dim3(256), 0, s, 1u, 1u,
                                       static_cast<const uint8_t*>(A_q_dev), reinterpret_cast<uint4*>(a16), n16);
     if (e != cudaSuccess) return cuda_fail(e, "widen launch");
+    if (config_id & QG_CONFIG_I8_CONV16)
+      return p.mpad == 64 ? run_i8<64, false, true, 16>(p, tmW, tmA, g, config_id, s)
+                          : run_i8<128, false, true, 16>(p, tmW, tmA, g, config_id, s);
     return p.mpad == 64 ? run_i8<64, false, true>(p, tmW, tmA, g, config_id, s)
                         : run_i8<128, false, true>(p, tmW, tmA, g, config_id, s);
+  }
+  if (fmt == QG_W8A8_INT8 && (config_id & QG_CONFIG_I8_CONV16)) {
+    if (fz) return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_I8_CONV16 takes quantized activations");
+    if (p.mpad == 16) return run_i8<16, false, false, 16>(p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return run_i8<32, false, false, 16>(p, tmW, tmA, g, config_id, s);
+    return run_i8<64, false, false, 16>(p, tmW, tmA, g, config_id, s);
   }
   if (fmt == QG_W8A8_INT8) {
     if (p.mpad == 16) return fz ? run_i8<16, true>(p, tmW, tmA, g, config_id, s) : run_i8<16, false>(p, tmW, tmA, g, config_id, s);
@@ -1091,7 +1105,7 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
                    void* stream) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
   const bool fusable = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) &&
-                       !(config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_I8_PREWIDEN));
+                       !(config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16));
   const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
   if (fusable && (!buffers || (config_id & QG_CONFIG_FUSED_QUANT) ||
                   (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {

@@ -84,8 +84,14 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     swap_forms = [(q.QG_SWAPAB, q.QG_SWAPAB_SPLITK)]
     if fmt == "W8A8_INT8" and M <= 8:
         swap_forms.append((q.QG_SWAPAB_DP4A, q.QG_SWAPAB_DP4A_SPLITK))
-    for cfg in (0, 12):
+    cfgs = [0, 12]
+    if fmt == "W8A8_INT8" and M > 8:
+        # sixteen converter warps, one CTA per SM, the deepest ring
+        cfgs.append(q.config_id(0, 0, conv16=True))
+    for cfg in cfgs:
         for single, split in swap_forms:
+            if cfg & q.QG_CONFIG_I8_CONV16 and single != q.QG_SWAPAB:
+                continue
             out.append((single, 1, cfg))
             for s in range(2, min(16, kt) + 1):
                 if tiles * s > 12 * sms or kt // s < 1:
@@ -113,8 +119,8 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
         # activations widened once per launch (QG_CONFIG_I8_PREWIDEN), token
         # blocks of 64 / 128: the compute-bound regime
         pw_tiles = n_tiles * -(-M // (64 if M <= 64 else 128))
-        for ring in (0, 3):
-            cfg = q.config_id(ring, 0, prewiden=True)
+        for ring, c16 in ((0, False), (3, False), (0, True)):
+            cfg = q.config_id(ring, 0, prewiden=True, conv16=c16)
             out.append((q.QG_SWAPAB, 1, cfg))
             for s in range(2, min(16, kt) + 1):
                 if pw_tiles * s > 4 * sms or kt // s < 1:

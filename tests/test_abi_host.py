@@ -246,7 +246,9 @@ def test_check_config_returns_the_gemm_status(q):
              dict(fmt=2, M=300, variant=0, cfg=q.config_id(pair_mma=True)),
              dict(fmt=0, M=300, cfg=q.QG_CONFIG_I8_PREWIDEN),                          # prewiden: INT8 only
              dict(fmt=1, M=300, cfg=q.QG_CONFIG_I8_PREWIDEN | q.QG_CONFIG_MMA_SYNC),
-             dict(fmt=1, M=300, variant=q.QG_SWAPAB_DP4A, cfg=q.QG_CONFIG_I8_PREWIDEN)]
+             dict(fmt=1, M=300, variant=q.QG_SWAPAB_DP4A, cfg=q.QG_CONFIG_I8_PREWIDEN),
+             dict(fmt=2, M=32, cfg=q.QG_CONFIG_I8_CONV16),                              # conv16: INT8 only
+             dict(fmt=1, M=32, cfg=q.QG_CONFIG_I8_CONV16 | q.QG_CONFIG_FUSED_QUANT)]
     for c in cases:
         fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
         v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)
@@ -262,6 +264,8 @@ def test_check_config_returns_the_gemm_status(q):
                              q.config_id(dp4a_rows16=1, s8=True)) == q.QG_ERR_UNSUPPORTED_SHAPE
     assert q.qg_check_config(0, 300, 4096, 4096, q.QG_SPLITK, 3, q.config_id(4, 0, True)) == q.QG_OK
     assert q.qg_check_config(0, 512, 24576, 4096, q.QG_STANDARD, 1, q.config_id(3, 8, pair_mma=True)) == q.QG_OK
+    assert q.qg_check_config(1, 16, 4096, 4096, q.QG_SWAPAB_SPLITK, 4, q.config_id(conv16=True)) == q.QG_OK
+    assert q.qg_check_config(1, 300, 4096, 4096, q.QG_SWAPAB, 1, q.config_id(prewiden=True, conv16=True)) == q.QG_OK
     assert q.qg_check_config(2, 32, 4096, 12288, q.QG_SWAPAB_SPLITK, 96, q.config_id(12, 64)) == q.QG_OK
     assert q.qg_check_config(0, 0, 256, 256, 2, 1, 0) == q.QG_ERR_INVALID_ARG   # a configuration has M >= 1
 

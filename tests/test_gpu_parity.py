@@ -217,7 +217,7 @@ def test_graph_capture_and_pdl_replay(orc, gc, q):
 
 
 @pytest.mark.parametrize("fmt,mma_sync", [("FP8_Dynamic", False), ("W8A8_INT8", False), ("W8A8_INT8", True),
-                                          ("W8A8_INT8", "s8"), ("Block_FP8", False)])
+                                          ("W8A8_INT8", "s8"), ("W8A8_INT8", "conv16"), ("Block_FP8", False)])
 def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt, mma_sync):
     import seeded_inputs as si
     M, N, K = 4, 256, 1024
@@ -230,7 +230,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt, mma_
     assert q.qg_device_error() == 0
     q.qg_set_wait_limit_ns(2_000_000)  # 2 ms
     q.qg_set_force_timeout(True)
-    cfg = q.config_id(0, 0, mma_sync=mma_sync is True, s8=mma_sync == "s8")
+    cfg = q.config_id(0, 0, mma_sync=mma_sync is True, s8=mma_sync == "s8", conv16=mma_sync == "conv16")
     try:
         gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, SW, 1, config_id=cfg)
         assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
@@ -345,6 +345,23 @@ def test_w8a8_int8_prewidened_ragged_k_and_rings(orc, q, gc, M, K, ring):
                 config_id=q.config_id(ring, 0, prewiden=True))
 
 
+@pytest.mark.parametrize("M", [9, 16, 17, 32, 33, 64, 70])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 7), (SWS, 18)])
+def test_w8a8_int8_sixteen_converter_warps(orc, q, gc, M, variant, split):
+    # QG_CONFIG_I8_CONV16: sixteen weight converter warps (k-tiles in four
+    # parts, accumulators drained in four token parts: 4 tokens each at
+    # M <= 16), one CTA per SM with the deepest ring; int32 bit-exact
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=2000 + M + split, outliers=True,
+                config_id=q.config_id(0, 0, conv16=True))
+
+
+@pytest.mark.parametrize("M", [64, 100, 300])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 3), (SWS, 18)])
+def test_w8a8_int8_prewidened_sixteen_converter_warps(orc, q, gc, M, variant, split):
+    gc.run_case(orc, "W8A8_INT8", M, 300, 2304, variant, split, seed=2100 + M + split, outliers=True,
+                config_id=q.config_id(0, 0, prewiden=True, conv16=True))
+
+
 def test_int8_prewidened_identical_to_other_kernels(gc, q):
     # the same int32 accumulators and Y as the tcgen05 kernel that widens the
     # activations itself, and through qg_linear_w8a8 (quantization, widening
@@ -358,6 +375,9 @@ def test_int8_prewidened_identical_to_other_kernels(gc, q):
     Y0, d0 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 3, debug=True)
     cfg = q.config_id(0, 0, prewiden=True)
     Y1, d1 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 3, config_id=cfg, debug=True)
+    Y3, d3 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 3, config_id=q.config_id(conv16=True), debug=True)
+    Y4, d4 = gc.gemm_gpu("W8A8_INT8", Aq, sa, Wq, sw, N, SWS, 3, config_id=q.config_id(prewiden=True, conv16=True),
+                         debug=True)
     Y2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=gc.DEV)
     need = q.qg_workspace_bytes_config("W8A8_INT8", M, N, K, SWS, 3, cfg)
     assert need >= M * K * 2 and need > q.qg_workspace_bytes("W8A8_INT8", M, N, K, SWS, 3)
@@ -367,6 +387,7 @@ def test_int8_prewidened_identical_to_other_kernels(gc, q):
     torch.cuda.synchronize()
     assert q.qg_device_error() == 0
     assert torch.equal(d0, d1) and torch.equal(Y0, Y1) and torch.equal(Y0, Y2)
+    assert torch.equal(d0, d3) and torch.equal(Y0, Y3) and torch.equal(d0, d4) and torch.equal(Y0, Y4)
 
 
 def test_prewidened_config_rejected_elsewhere(q, gc):
@@ -374,7 +395,9 @@ def test_prewidened_config_rejected_elsewhere(q, gc):
     f = torch.ones(4096, dtype=torch.float32, device=gc.DEV)
     pw = q.QG_CONFIG_I8_PREWIDEN
     for fmt, v, s, cfg in (("FP8_Dynamic", SW, 1, pw), ("Block_FP8", SW, 1, pw), ("W8A8_INT8", DP, 1, pw),
-                           ("W8A8_INT8", SW, 1, pw | q.QG_CONFIG_MMA_SYNC), ("W8A8_INT8", SW, 1, pw | q.QG_CONFIG_FUSED_QUANT)):
+                           ("W8A8_INT8", SW, 1, pw | q.QG_CONFIG_MMA_SYNC), ("W8A8_INT8", SW, 1, pw | q.QG_CONFIG_FUSED_QUANT),
+                           ("FP8_Dynamic", SW, 1, q.QG_CONFIG_I8_CONV16),
+                           ("W8A8_INT8", SW, 1, q.QG_CONFIG_I8_CONV16 | q.QG_CONFIG_MMA_SYNC)):
         with pytest.raises(q.QGError) as e:
             q.qg_gemm_w8a8(fmt, 64, 256, 256, d, f, d, f, d, 256, v, s, cfg, d, d.numel())
         assert e.value.code == q.QG_ERR_INVALID_ARG
