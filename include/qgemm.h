@@ -216,8 +216,8 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      activations once into an exact fp16 copy in the
  *                      workspace (a second kernel), and the GEMM loads that
  *                      copy by TMA instead of widening it in every CTA, in
- *                      token blocks of 64 (M <= 64) or 128 -- each weight
- *                      tile widened once per 128 tokens; only the ring
+ *                      token blocks of 16 / 32 / 64 (M <= 64) or 128 -- each
+ *                      weight tile widened once per 128 tokens; only the ring
  *                      depth and the L2 prefetch distance may be combined
  *                      with it, and it is not for grouped launches or the
  *                      one-kernel form of qg_linear_w8a8 (QG_ERR_INVALID_ARG);

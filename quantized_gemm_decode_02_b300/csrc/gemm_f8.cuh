@@ -97,8 +97,8 @@ struct alignas(8) Ctrl {
   uint64_t full[16];
   uint64_t empty[16];
   uint64_t acc_full;
-  uint64_t tfull[4];
-  uint64_t tempty[4];
+  uint64_t tfull[8];
+  uint64_t tempty[8];
   uint64_t never;
   uint64_t recv_bar;  // split-K: peers' partial rows have landed
   uint64_t amax_bar;  // fused quantization: peers' partial row maxima have landed
@@ -434,7 +434,10 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
   constexpr bool BLOCK = (FMT == kFmtBlock);
   constexpr bool QWARPS = BLOCK && FUSED;                // quantizer warps 6..9
   constexpr int kT = swap_threads(FMT, FUSED);
-  constexpr int NBUF = BLOCK ? 4 : 1;
+  // Block_FP8: as many k-tile partial buffers as the 256 TMEM columns of one
+  // of two CTAs per SM hold, up to 8 (the fused form keeps 4: its scale ring
+  // holds stages + 4 k-tiles)
+  constexpr int NBUF = BLOCK ? ((FUSED || MPAD > 32) ? 4 : 256 / MPAD > 8 ? 8 : 256 / MPAD) : 1;
   constexpr uint32_t kTmemCols = pow2_cols(NBUF * MPAD);
   static_assert(kTmemCols <= 256, "two CTAs per SM share the 512 TMEM columns");
 

@@ -108,6 +108,11 @@ struct I8Conv {
   static constexpr int kParts = CW / 4;     // K parts / token parts of a row quarter
   static constexpr int kChunks = 8 / kParts;
 };
+// one CTA per SM: the PREW form beyond 32 tokens (its TMEM takes all 512
+// columns) and the sixteen-converter form
+__host__ __device__ constexpr bool i8_one_per_sm(int mpad, bool prew, int cw) {
+  return (prew && mpad > 32) || cw > kI8ConvWarps;
+}
 // threads of the kernel: the PREW form has no activation converter warps
 __host__ __device__ constexpr int i8_threads(bool prew, int cw = kI8ConvWarps) {
   return 32 * (2 + cw + (prew ? 0 : kI8AWarps));
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const uint8_t* __restrict
 // to int8 codes themselves (qg_linear_w8a8): no quantization kernel and no
 // int8 activation tensor in between; tmA is unused.
 template <int MPAD, bool FUSED, bool PREW = false, int CW = kI8ConvWarps>
-__global__ void __launch_bounds__(i8_threads(PREW, CW), (PREW || CW > kI8ConvWarps) ? 1 : 2)
+__global__ void __launch_bounds__(i8_threads(PREW, CW), i8_one_per_sm(MPAD, PREW, CW) ? 1 : 2)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using S = I8Shape<MPAD>;
   using C = I8Conv<CW>;

@@ -252,8 +252,8 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
     p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else if (p->prew) {
-    // blocks of 64 tokens, or of 128 above 64 tokens
-    p->mpad = M <= 64 ? 64 : 128;
+    // tokens padded to 16 / 32 / 64, blocks of 128 above 64 tokens
+    p->mpad = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
     p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else if (p->swap) {
@@ -377,9 +377,8 @@ template <int MPAD, bool FUSED, bool PREW = false, int CW = qg::kI8ConvWarps>
 int run_i8(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
            cudaStream_t stream) {
   const int rb = g.recv_bytes;
-  // PREW (its TMEM takes all 512 columns) and the 16-converter form run one
-  // CTA per SM: the default ring is the deepest that fits
-  if ((PREW || CW > qg::kI8ConvWarps) && (config_id & QG_CONFIG_RING_MASK) == 0) config_id |= kMaxStages;
+  // the forms that run one CTA per SM take the deepest ring that fits by default
+  if (qg::i8_one_per_sm(MPAD, PREW, CW) && (config_id & QG_CONFIG_RING_MASK) == 0) config_id |= kMaxStages;
   int rc = pick_stages(config_id, [rb](int st) { return qg::gemm_i8_smem_bytes<MPAD, PREW>(st, rb); }, &g.stages);
   if (rc != QG_OK) return rc;
   return launch_gemm(qg::gemm_i8_kernel<MPAD, FUSED, PREW, CW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
@@ -761,9 +760,14 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     cudaError_t e = launch_cluster_xy(qg::widen_i8_kernel, dim3(blocks), dim3(256), 0, s, 1u, 1u,
                                       static_cast<const uint8_t*>(A_q_dev), reinterpret_cast<uint4*>(a16), n16);
     if (e != cudaSuccess) return cuda_fail(e, "widen launch");
-    if (config_id & QG_CONFIG_I8_CONV16)
+    if (config_id & QG_CONFIG_I8_CONV16) {
+      if (p.mpad == 16) return run_i8<16, false, true, 16>(p, tmW, tmA, g, config_id, s);
+      if (p.mpad == 32) return run_i8<32, false, true, 16>(p, tmW, tmA, g, config_id, s);
       return p.mpad == 64 ? run_i8<64, false, true, 16>(p, tmW, tmA, g, config_id, s)
                           : run_i8<128, false, true, 16>(p, tmW, tmA, g, config_id, s);
+    }
+    if (p.mpad == 16) return run_i8<16, false, true>(p, tmW, tmA, g, config_id, s);
+    if (p.mpad == 32) return run_i8<32, false, true>(p, tmW, tmA, g, config_id, s);
     return p.mpad == 64 ? run_i8<64, false, true>(p, tmW, tmA, g, config_id, s)
                         : run_i8<128, false, true>(p, tmW, tmA, g, config_id, s);
   }
