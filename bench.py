@@ -73,6 +73,10 @@ def _items(fmts, model, layers, ms):
 WORKLOADS = {
     "int8_qwen3_1.7b": dict(items=_items(["W8A8_INT8"], "Qwen3-1.7B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),
     "fp8_qwen3_1.7b_o_m1": dict(items=_items(["FP8_Dynamic"], "Qwen3-1.7B", ("o",), (1,)), shared=False, bound="hbm"),
+    # the same linear 64 times in one graph (distinct weights, 268 MB): its cost
+    # inside a chain, without one graph launch per linear
+    "fp8_qwen3_1.7b_o_m1_chain64": dict(items=_items(["FP8_Dynamic"], "Qwen3-1.7B", ("o",), (1,)) * 64, shared=False,
+                                        bound="hbm"),
     "blockfp8_qwen3_8b": dict(items=_items(["Block_FP8"], "Qwen3-8B", LAYERS, range(1, 33)), shared=False,
                               bound="hbm"),
     "fp8_qwen3_32b": dict(items=_items(["FP8_Dynamic"], "Qwen3-32B", LAYERS, si.TUNED_M), shared=False, bound="hbm"),

@@ -286,9 +286,13 @@ def layer_context_pass(bench, table_in, out_path, fmts, models, ms, sms, log=Non
                 base = time_layer_chain(bench, fmt, M, shapes, cfgs)
                 best_total = base
                 for li, (layer, (K, N)) in enumerate(layers):
-                    # (the one-kernel Block_FP8 form was never faster in a layer
-                    # chain and is not swept)
                     cands = candidates(fmt, M, N, K, sms)
+                    if M <= 8:
+                        # the one-kernel form of the linear (quantization inside the
+                        # GEMM): every CTA reads whole activation rows, cheap at a few
+                        # tokens, and the linear has one kernel boundary instead of two
+                        cands += [(v, sp, c | q.QG_CONFIG_FUSED_QUANT) for (v, sp, c) in cands
+                                  if v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK) and not c & q.QG_CONFIG_MMA_SYNC]
                     for cand in cands:
                         if cand == cfgs[li]:
                             continue
