@@ -231,7 +231,8 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      converter warps instead of eight and one CTA per SM
  *                      with the deepest ring that fits, so that more weight
  *                      bytes are in flight per SM while they are widened;
- *                      not for the one-kernel form of qg_linear_w8a8;
+ *                      not for grouped launches or the one-kernel form of
+ *                      qg_linear_w8a8 (QG_ERR_INVALID_ARG);
  *   workspace_dev      qg_workspace_bytes_config() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

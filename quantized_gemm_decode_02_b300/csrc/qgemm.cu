@@ -660,6 +660,8 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (fused || wide || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK || variant == QG_SWAPAB_DP4A ||
                            variant == QG_SWAPAB_DP4A_SPLITK))
       return fail(QG_ERR_INVALID_ARG, "grouped launches run the Swap-AB variants");
+    if (config_id & (QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16))
+      return fail(QG_ERR_INVALID_ARG, "grouped launches take neither QG_CONFIG_I8_PREWIDEN nor QG_CONFIG_I8_CONV16");
     if (rows < 0 || rows > 0x7FFFFFFF || static_cast<int64_t>(grouped->groups) * N > 0x7FFFFFFF)
       return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
     if (rows == 0) return QG_OK;

@@ -164,6 +164,8 @@ def test_grouped_validation(q):
     assert _grouped(q, K=200) == q.QG_ERR_UNSUPPORTED_SHAPE
     assert _grouped(q, total=-1) == q.QG_ERR_INVALID_ARG
     assert _grouped(q, split=17, K=4096, variant=3) == q.QG_ERR_WORKSPACE_TOO_SMALL
+    assert _grouped(q, fmt=1, cfg=q.QG_CONFIG_I8_PREWIDEN) == q.QG_ERR_INVALID_ARG   # not for grouped launches
+    assert _grouped(q, fmt=1, cfg=q.QG_CONFIG_I8_CONV16) == q.QG_ERR_INVALID_ARG
     assert _grouped(q, total=0) == q.QG_OK                               # no tokens: nothing to do
     assert _grouped(q, max_tokens=0) == q.QG_OK
 

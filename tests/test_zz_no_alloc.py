@@ -90,6 +90,25 @@ def test_noalloc_without_split_k(orc, gc, q):
     _close(orc, gc, fmt, Aq, sa, Wq, sw, Y, Y_ref, dbg, dbg_ref)
 
 
+def test_noalloc_prewidened_activations(orc, gc, q):
+    # QG_CONFIG_I8_PREWIDEN keeps its fp16 activation copy in the static
+    # array too: the same accumulators as the workspace entry point, twice
+    fmt, M, N, K = "W8A8_INT8", 100, 384, 2304
+    cfg = q.config_id(prewiden=True)
+    need = q.qg_workspace_bytes_config(fmt, M, N, K, q.QG_SWAPAB_SPLITK, 3, cfg)
+    assert 0 < need <= q.QG_NOALLOC_SCRATCH_BYTES
+    Aq, sa, Wq, sw = _inputs(gc, fmt, M, N, K, seed=33)
+    Y_ref, dbg_ref = gc.gemm_gpu(fmt, Aq, sa, Wq, sw, N, q.QG_SWAPAB_SPLITK, 3, config_id=cfg, debug=True)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=gc.DEV)
+        dbg = torch.full((M, N), -7, dtype=torch.int32, device=gc.DEV)
+        q.qg_gemm_w8a8_noalloc(fmt, M, N, K, Aq, sa, Wq, sw, Y, N, q.QG_SWAPAB_SPLITK, 3, cfg, dbg)
+        torch.cuda.synchronize()
+        _close(orc, gc, fmt, Aq, sa, Wq, sw, Y, Y_ref, dbg, dbg_ref)
+    assert q.qg_device_error() == 0
+
+
 def test_noalloc_rejects_scratch_beyond_the_array(gc, q):
     M, N, K, S = 32, 12288, 4096, 17          # 17 * 32 * 12288 * 4 bytes = 25.5 MiB of partials
     need = q.qg_workspace_bytes("FP8_Dynamic", M, N, K, q.QG_SWAPAB_SPLITK, S)
