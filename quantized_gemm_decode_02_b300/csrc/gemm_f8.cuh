@@ -93,7 +93,7 @@ __host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
 }
 
 // Shared-memory control block that follows the ring.
-struct alignas(8) Ctrl {
+struct alignas(16) Ctrl {
   uint64_t full[16];
   uint64_t empty[16];
   uint64_t acc_full;
@@ -109,8 +109,9 @@ struct alignas(8) Ctrl {
   int abort_flag;
   float sa_s[64];   // per-token scales, staged for the epilogue
   float sw_s[128];  // per-channel scales of the tile's rows
-  float amax_s[kMaxClusterSplits * 64];  // fused quantization: [source rank][token] partial row maxima
-                                         // (Block_FP8 fused: [ring slot][token] activation scales)
+  alignas(16) float amax_s[kMaxClusterSplits * 64];  // fused quantization: [source rank][token] partial row maxima
+                                         // (Block_FP8 fused: [ring slot][token] activation scales;
+                                         // Block_FP8 two-kernel form: [k-tile][token] scale products)
 };
 
 template <bool SWAP, int MPAD>
@@ -688,67 +689,93 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
       }
       if constexpr (BLOCK) {
         const int nb = n_tile;  // 128-row tile == weight block row
-        // Two-kernel form: the products s_a[m,kb] * s_w[nb,kb] of the CTA's
-        // whole K range are loaded with every request in flight right after
-        // the dependency wait, into amax_s (unused by this form) when they
-        // fit, so no k-tile's promotion waits on a load; otherwise each
-        // k-tile's scales are fetched one k-tile ahead.
+        // Two-kernel form: the products s_a[m,kb] * s_w[nb,kb] (the k-tile's
+        // coefficient for each token) are staged in amax_s (unused by this
+        // form), so the promotion reads them as shared-memory broadcasts and
+        // spends one paired FMA per two tokens:
+        //   staged   the CTA's whole K range fits: loaded with every request
+        //            in flight right after the dependency wait;
+        //   chunked  otherwise: two halves of kChunkTiles k-tiles each, the
+        //            next chunk loaded into registers one chunk ahead and
+        //            stored at the chunk boundary (one barrier of the 128
+        //            promotion threads per chunk).
+        constexpr int kHalfCoefs = kMaxClusterSplits * 32;  // floats in one half of amax_s
+        constexpr int kChunkTiles = kHalfCoefs / MPAD;
+        constexpr int kCoefPer = kHalfCoefs / 128;          // per promotion thread and chunk
         const bool staged = !FUSED && nk * MPAD <= kMaxClusterSplits * 64;
-        if (staged) {
-          for (int e = threadIdx.x - 64; e < nk * MPAD; e += 128) {
-            const int i = e / MPAD, t = e - i * MPAD;
-            ctl->amax_s[e] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) *
+        const bool chunked = !FUSED && !staged;
+        const int et = threadIdx.x - 64;  // promotion thread 0..127
+        auto coef_of = [&](int i, int t) -> float {
+          return (i < nk && t < Mb) ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) *
                                           __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
                                     : 0.0f;
+        };
+        float cpre[kCoefPer];
+        auto load_chunk = [&](int c) {
+#pragma unroll
+          for (int j = 0; j < kCoefPer; ++j) {
+            const int e = et + 128 * j;
+            cpre[j] = coef_of(c * kChunkTiles + e / MPAD, e % MPAD);
+          }
+        };
+        auto store_chunk = [&](int c) {
+#pragma unroll
+          for (int j = 0; j < kCoefPer; ++j) ctl->amax_s[(c & 1) * kHalfCoefs + et + 128 * j] = cpre[j];
+        };
+        if (staged) {
+          for (int e = et; e < nk * MPAD; e += 128) {
+            const int i = e / MPAD;
+            ctl->amax_s[e] = coef_of(i, e - i * MPAD);
           }
           named_bar_sync(1, 128);
+        } else if (chunked) {
+          load_chunk(0);
+          store_chunk(0);
+          if (nk > kChunkTiles) load_chunk(1);
+          named_bar_sync(1, 128);
         }
-        // lane l holds s_a of tokens l, l + 32, ... for the current k-tile
+        // fused form: lane l holds s_a of tokens l, l + 32, ... for the
+        // current k-tile
         constexpr int kSaw = (MPAD + 31) / 32;
-        float sa_next[kSaw], sa_cur[kSaw];
-        if (!FUSED && !staged) {
-#pragma unroll
-          for (int j = 0; j < kSaw; ++j) {
-            const int t = lane + 32 * j;
-            sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0) : 0.0f;
-          }
-        }
-        float sw_next = staged ? 0.0f : __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0);
+        float sa_cur[kSaw];
+        float sw_next = FUSED ? __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0) : 0.0f;
+        // After a failed wait a warp stays in the loop without working, so
+        // that every promotion thread reaches every chunk barrier.
+        bool dead = false;
         for (int i = 0; i < nk; ++i) {
           const int buf = i % NBUF;
+          if (chunked && i > 0 && i % kChunkTiles == 0) {
+            // chunk c's half was last read in chunk c - 2, which every
+            // promotion thread left before the previous barrier
+            const int c = i / kChunkTiles;
+            store_chunk(c);
+            if ((c + 1) * kChunkTiles < nk) load_chunk(c + 1);
+            named_bar_sync(1, 128);
+          }
+          if (dead) continue;
+          float sw_cur = 0.0f;
           if constexpr (FUSED) {
             // this k-tile's scales, from the quantizer warps through the ring
             const int slot = i % kSaRing;
             if (!__all_sync(0xffffffffu, mbar_wait(&ctl->sfull[slot], static_cast<uint32_t>(i / kSaRing) & 1u,
                                                    g.wait_ns) && !*abort_flag)) {
               *abort_flag = 1;
-              break;
+              dead = true;
+              continue;
             }
 #pragma unroll
             for (int j = 0; j < kSaw; ++j) {
               const int t = lane + 32 * j;
               sa_cur[j] = t < MPAD ? ctl->amax_s[slot * 64 + t] : 0.0f;
             }
-          } else if (!staged) {
-#pragma unroll
-            for (int j = 0; j < kSaw; ++j) sa_cur[j] = sa_next[j];
-          }
-          const float sw_cur = sw_next;
-          if (i + 1 < nk && !staged) {
-            if constexpr (!FUSED) {
-#pragma unroll
-              for (int j = 0; j < kSaw; ++j) {
-                const int t = lane + 32 * j;
-                sa_next[j] = t < Mb ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i + 1)
-                                    : 0.0f;
-              }
-            }
-            sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
+            sw_cur = sw_next;
+            if (i + 1 < nk) sw_next = __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i + 1);
           }
           const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
           if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
             *abort_flag = 1;
-            break;
+            dead = true;
+            continue;
           }
           tc_fence_after();
           uint32_t v[MPAD];
@@ -762,10 +789,24 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&ctl->tempty[buf]);
-          if (staged) {
-            const float* coefs = ctl->amax_s + i * MPAD;
+          if constexpr (!FUSED) {
+            const float* coefs =
+                staged ? ctl->amax_s + i * MPAD
+                       : ctl->amax_s + ((i / kChunkTiles) & 1) * kHalfCoefs + (i % kChunkTiles) * MPAD;
 #pragma unroll
-            for (int m = 0; m < MPAD; ++m) acc[m] = fmaf(coefs[m], __uint_as_float(v[m]), acc[m]);
+            for (int m = 0; m < MPAD; m += 4) {
+              const float4 c4 = *reinterpret_cast<const float4*>(coefs + m);
+              const float2 r0 = __ffma2_rn(make_float2(c4.x, c4.y),
+                                           make_float2(__uint_as_float(v[m]), __uint_as_float(v[m + 1])),
+                                           make_float2(acc[m], acc[m + 1]));
+              const float2 r1 = __ffma2_rn(make_float2(c4.z, c4.w),
+                                           make_float2(__uint_as_float(v[m + 2]), __uint_as_float(v[m + 3])),
+                                           make_float2(acc[m + 2], acc[m + 3]));
+              acc[m] = r0.x;
+              acc[m + 1] = r0.y;
+              acc[m + 2] = r1.x;
+              acc[m + 3] = r1.y;
+            }
           } else {
 #pragma unroll
             for (int m = 0; m < MPAD; ++m) {

@@ -57,6 +57,46 @@ def test_block_fp8(orc, gc, M, variant, split):
     gc.run_case(orc, "Block_FP8", M, 392, 768, variant, split, seed=100 + M)
 
 
+@pytest.mark.parametrize("M", [5, 20, 48])
+@pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2)])
+def test_block_fp8_long_k_ranges(orc, gc, M, variant, split):
+    # K ranges whose scale products (k-tiles x token block) exceed the
+    # staged table of 1024: the promotion stages them in chunks of 32, 16 or
+    # 8 k-tiles (blocks of 16, 32, 64 tokens), 73 k-tiles per range, so the
+    # last chunk is ragged and both halves of the table are reused; split 2
+    # reduces in a cluster
+    K = 73 * 128 * split
+    gc.run_case(orc, "Block_FP8", M, 264, K, variant, split, seed=4100 + M + split)
+
+
+def test_block_fp8_chunked_promotion_timeout(orc, gc, q):
+    # a forced wait time-out on the chunked promotion path: the warps that
+    # gave up still pass every chunk barrier, the time-out is reported, and
+    # the context stays usable
+    import seeded_inputs as si
+    M, N, K = 20, 256, 4608  # 36 k-tiles x a 32-token block > 1024 products
+    A = si.activations(M, K, seed=3)
+    W = si.weights(N, K, seed=3)
+    Ad, Wd = A.to(gc.DEV), torch.from_numpy(W).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu("Block_FP8", Wd)
+    Aq, sa = gc.quant_act_gpu("Block_FP8", Ad)
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    q.qg_set_wait_limit_ns(2_000_000)  # 2 ms
+    q.qg_set_force_timeout(True)
+    try:
+        gc.gemm_gpu("Block_FP8", Aq, sa, Wq, sw, N, SW, 1)
+        assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
+    finally:
+        q.qg_set_force_timeout(False)
+        q.qg_set_wait_limit_ns(0)
+    assert q.qg_device_error() == 0
+    Y, _ = gc.gemm_gpu("Block_FP8", Aq, sa, Wq, sw, N, SW, 1)
+    torch.cuda.synchronize()
+    oAq, osa, oWq, osw = gc.check_quant(orc, "Block_FP8", A, W, Aq, sa, Wq, sw)
+    gc.check_gemm(orc, "Block_FP8", oAq, osa, oWq, osw, Y)
+
+
 @pytest.mark.parametrize("M", [1, 3, 16, 20, 32, 48])
 @pytest.mark.parametrize("variant,split", [(SW, 1), (SWS, 2), (SWS, 7)])
 def test_w8a8_int8(orc, gc, M, variant, split):
