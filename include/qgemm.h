@@ -88,6 +88,7 @@ typedef enum {
 #define QG_CONFIG_PAIR_MMA (1 << 21)
 #define QG_CONFIG_I8_PREWIDEN (1 << 22)
 #define QG_CONFIG_I8_CONV16 (1 << 23)
+#define QG_CONFIG_BLOCK_PROMO8 (1 << 24)
 
 typedef enum {
   QG_OK = 0,
@@ -233,6 +234,14 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      bytes are in flight per SM while they are widened;
  *                      not for grouped launches or the one-kernel form of
  *                      qg_linear_w8a8 (QG_ERR_INVALID_ARG);
+ *                      plus QG_CONFIG_BLOCK_PROMO8 for Block_FP8 with
+ *                      QG_SWAPAB / QG_SWAPAB_SPLITK: eight warps instead of
+ *                      four promote each k-tile's partial with its block
+ *                      scales (two per TMEM lane quarter, each taking half
+ *                      of the token block); same result; not for grouped
+ *                      launches nor with QG_CONFIG_FUSED_QUANT
+ *                      (QG_ERR_INVALID_ARG); qg_linear_w8a8 runs it as two
+ *                      kernels (A_q / s_a buffers required);
  *   workspace_dev      qg_workspace_bytes_config() bytes (may be NULL when 0);
  *   debug_acc_dev      W8A8_INT8 only, optional: int32 [M][N] receives the
  *                      exact integer accumulators (NULL to skip).

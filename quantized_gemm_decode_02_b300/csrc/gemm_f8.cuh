@@ -83,9 +83,13 @@ constexpr int kThreadsBlockFused = 320;
 // quantizer warps to the promotion warps (slots >= stages + 4 TMEM buffers)
 constexpr int kSaRing = 16;
 constexpr int kMaxStagesBlockFused = kSaRing - 4;
-__host__ __device__ constexpr int swap_threads(int fmt, bool fused) {
-  return (fmt == 2 && fused) ? kThreadsBlockFused : kThreads;
+// pw: promotion / epilogue warps of the two-kernel form (4, or 8 for the
+// Block_FP8 form with two warps per TMEM lane quarter)
+__host__ __device__ constexpr int swap_threads(int fmt, bool fused, int pw = 4) {
+  return (fmt == 2 && fused) ? kThreadsBlockFused : 64 + 32 * pw;
 }
+// Standard kernel: Block_FP8 promotes with eight epilogue warps
+__host__ __device__ constexpr int std_threads(int fmt) { return fmt == 2 ? 320 : kThreads; }
 constexpr uint64_t kDrainNs = 200000000ull;  // bound for draining in-flight copies on exit
 
 __host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
@@ -427,14 +431,21 @@ __device__ __forceinline__ void block_fused_quantize(const GemmArgs& g, Ctrl* ct
 //     waits for another -- write the stage's activation tile, and pass the
 //     k-tile's scales to the promotion warps through a ring in shared
 //     memory (amax_s, barriers sfull).
-template <int FMT, int MPAD, bool FUSED>
-__global__ void __launch_bounds__(swap_threads(FMT, FUSED),
+// PW (Block_FP8, two-kernel form): 4 promotion warps (2..5), or 8 (2..9):
+// two per TMEM lane quarter, warp w taking the token half (w - 2) / 4 of
+// every k-tile's partial, so each promotes half as many products per k-tile.
+template <int FMT, int MPAD, bool FUSED, int PW = 4>
+__global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
                                   (FMT == kFmtBlock && FUSED && MPAD > 32) ? 1 : 2)  // (64-token blocks: registers)
     gemm_f8_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using TS = TileShape<true, MPAD>;
   constexpr bool BLOCK = (FMT == kFmtBlock);
   constexpr bool QWARPS = BLOCK && FUSED;                // quantizer warps 6..9
-  constexpr int kT = swap_threads(FMT, FUSED);
+  constexpr int kT = swap_threads(FMT, FUSED, PW);
+  constexpr int kEpi = 32 * PW;                          // promotion / epilogue threads
+  constexpr int kTP = MPAD * 4 / PW;                     // tokens of each such thread
+  static_assert(PW == 4 || (PW == 8 && BLOCK && !FUSED), "eight promotion warps: Block_FP8, two-kernel form");
+  static_assert(kTP % 8 == 0, "token parts of whole 8-column TMEM loads");
   // Block_FP8: as many k-tile partial buffers as the 256 TMEM columns of one
   // of two CTAs per SM hold, up to 8 (the fused form keeps 4: its scale ring
   // holds stages + 4 k-tiles)
@@ -474,7 +485,7 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
     mbar_init(&ctl->acc_full, 1);
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], 128);
+      mbar_init(&ctl->tempty[b], kEpi);
     }
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->recv_bar, 1);
@@ -505,9 +516,10 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
   }
   pdl_launch_dependents();
   volatile int* abort_flag = &ctl->abort_flag;
-  float acc[MPAD];  // epilogue threads: weight row n of the tile x every token
+  float acc[kTP];  // epilogue threads: weight row n of the tile x tokens [t0, t0 + kTP)
 #pragma unroll
-  for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
+  for (int m = 0; m < kTP; ++m) acc[m] = 0.0f;
+  const int t0 = warp >= 2 ? ((warp - 2) >> 2) * kTP : 0;  // first token of this thread's part
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -701,10 +713,10 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
         //            promotion threads per chunk).
         constexpr int kHalfCoefs = kMaxClusterSplits * 32;  // floats in one half of amax_s
         constexpr int kChunkTiles = kHalfCoefs / MPAD;
-        constexpr int kCoefPer = kHalfCoefs / 128;          // per promotion thread and chunk
+        constexpr int kCoefPer = kHalfCoefs / kEpi;         // per promotion thread and chunk
         const bool staged = !FUSED && nk * MPAD <= kMaxClusterSplits * 64;
         const bool chunked = !FUSED && !staged;
-        const int et = threadIdx.x - 64;  // promotion thread 0..127
+        const int et = threadIdx.x - 64;  // promotion thread 0 .. kEpi-1
         auto coef_of = [&](int i, int t) -> float {
           return (i < nk && t < Mb) ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) *
                                           __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
@@ -714,25 +726,25 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
         auto load_chunk = [&](int c) {
 #pragma unroll
           for (int j = 0; j < kCoefPer; ++j) {
-            const int e = et + 128 * j;
+            const int e = et + kEpi * j;
             cpre[j] = coef_of(c * kChunkTiles + e / MPAD, e % MPAD);
           }
         };
         auto store_chunk = [&](int c) {
 #pragma unroll
-          for (int j = 0; j < kCoefPer; ++j) ctl->amax_s[(c & 1) * kHalfCoefs + et + 128 * j] = cpre[j];
+          for (int j = 0; j < kCoefPer; ++j) ctl->amax_s[(c & 1) * kHalfCoefs + et + kEpi * j] = cpre[j];
         };
         if (staged) {
-          for (int e = et; e < nk * MPAD; e += 128) {
+          for (int e = et; e < nk * MPAD; e += kEpi) {
             const int i = e / MPAD;
             ctl->amax_s[e] = coef_of(i, e - i * MPAD);
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(1, kEpi);
         } else if (chunked) {
           load_chunk(0);
           store_chunk(0);
           if (nk > kChunkTiles) load_chunk(1);
-          named_bar_sync(1, 128);
+          named_bar_sync(1, kEpi);
         }
         // fused form: lane l holds s_a of tokens l, l + 32, ... for the
         // current k-tile
@@ -750,7 +762,7 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
             const int c = i / kChunkTiles;
             store_chunk(c);
             if ((c + 1) * kChunkTiles < nk) load_chunk(c + 1);
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kEpi);
           }
           if (dead) continue;
           float sw_cur = 0.0f;
@@ -778,23 +790,17 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
             continue;
           }
           tc_fence_after();
-          uint32_t v[MPAD];
-#pragma unroll
-          for (int c = 0; c < MPAD; c += 8) {
-            uint32_t t[8];
-            tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(buf * MPAD + c), t);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[c + j] = t[j];
-          }
+          uint32_t v[kTP];
+          tmem_ld_cols(tmem + lane_base + static_cast<uint32_t>(buf * MPAD + t0), v);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&ctl->tempty[buf]);
           if constexpr (!FUSED) {
             const float* coefs =
-                staged ? ctl->amax_s + i * MPAD
-                       : ctl->amax_s + ((i / kChunkTiles) & 1) * kHalfCoefs + (i % kChunkTiles) * MPAD;
+                (staged ? ctl->amax_s + i * MPAD
+                        : ctl->amax_s + ((i / kChunkTiles) & 1) * kHalfCoefs + (i % kChunkTiles) * MPAD) + t0;
 #pragma unroll
-            for (int m = 0; m < MPAD; m += 4) {
+            for (int m = 0; m < kTP; m += 4) {
               const float4 c4 = *reinterpret_cast<const float4*>(coefs + m);
               const float2 r0 = __ffma2_rn(make_float2(c4.x, c4.y),
                                            make_float2(__uint_as_float(v[m]), __uint_as_float(v[m + 1])),
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
   const bool abort = ctl->abort_flag != 0;  // stable after the barrier: uniform
   const int row = (warp & 3) * 32 + lane;   // epilogue threads: weight row in the tile
   const int n = n_tile * kBN + row;
-  const int et = threadIdx.x - 64;          // 0..127 for the epilogue warps
+  const int et = threadIdx.x - 64;          // 0 .. kEpi-1 for the epilogue warps
   // m: token of this block; r: row of the tile (scales staged in shared
   // memory); nn = n_tile*128 + r
   auto out = [&](int m, int r, int nn, float sum) {
@@ -849,16 +855,16 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
     store_bf16(g.Y + static_cast<int64_t>(m_base + m) * g.ldy + nn, y);
   };
 
-  const bool epi = warp >= 2 && warp < 6;   // the epilogue warps hold the accumulators
+  const bool epi = warp >= 2 && warp < 2 + PW;  // the epilogue warps hold the accumulators
   if (clustered) {
     if (epi) {
       if (!FUSED || BLOCK) cluster_wait();  // every peer's receive barrier is initialized (fused FP8: waited already)
       // rows go out even after an abort, so that every owner's wait completes
-      cluster_push_row(acc, 0, row, split, g.splits, Mb, recv, &ctl->recv_bar);
-      named_bar_sync(1, 128);  // this CTA's own rows, stored locally, are visible
+      cluster_push_row(acc, t0, row, split, g.splits, Mb, recv, &ctl->recv_bar);
+      named_bar_sync(1, kEpi);  // this CTA's own rows, stored locally, are visible
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&ctl->recv_bar, 0, g.wait_ns));
       if (got && !abort) {
-        cluster_sum_rows<float>(recv, split, g.splits, Mb, et, 128, [&](int m, int r, float sum) {
+        cluster_sum_rows<float>(recv, split, g.splits, Mb, et, kEpi, [&](int m, int r, float sum) {
           const int nn = n_tile * kBN + r;
           if (nn < g.N) out(m, r, nn, sum);
         });
@@ -874,28 +880,28 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
     if (g.reduce == kReduceNone) {
       if (n_ok) {
 #pragma unroll
-        for (int m = 0; m < MPAD; ++m)
-          if (m < Mb) out(m, row, n, acc[m]);
+        for (int m = 0; m < kTP; ++m)
+          if (t0 + m < Mb) out(t0 + m, row, n, acc[m]);
       }
     } else {
       float* part = static_cast<float*>(g.ws_part);
       if (n_ok) {
 #pragma unroll
-        for (int m = 0; m < MPAD; ++m)
-          if (m < Mb) part[(static_cast<int64_t>(split) * g.M + m_base + m) * g.N + n] = acc[m];
+        for (int m = 0; m < kTP; ++m)
+          if (t0 + m < Mb) part[(static_cast<int64_t>(split) * g.M + m_base + t0 + m) * g.N + n] = acc[m];
       }
       __threadfence();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpi);
       const int tile_id = blockIdx.x + blockIdx.z * gridDim.x;
       if (et == 0) {
         const int old = atomicAdd(g.ws_count + tile_id, 1);
         ctl->last_flag = (old == g.splits - 1);
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpi);
       if (ctl->last_flag) {
         __threadfence();
         if (n_ok) {
-          for (int m = 0; m < Mb; ++m) {
+          for (int m = t0; m < min(Mb, t0 + kTP); ++m) {
             float sum = 0.0f;
             for (int s = 0; s < g.splits; ++s)
               sum += ld_cg_f32(part + (static_cast<int64_t>(s) * g.M + m_base + m) * g.N + n);
@@ -916,17 +922,23 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED),
 // BNW: weight rows per tile and MMA N (128; 256 for FP8_Dynamic's wide
 // tiles, which halve the MMA instructions and the activation-tile loads per
 // output).
+// Block_FP8: each k-tile's partial lands in one of four TMEM buffers (all
+// 512 columns: one CTA per SM) and eight promotion warps (two per TMEM lane
+// quarter, each owning 64 of the tile's weight rows) add it, times the
+// k-tile's coefficient s_a[m,kb] * s_w[nb,kb], into register accumulators.
 template <int FMT, int BNW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(std_threads(FMT), 1)
     gemm_f8_std_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
   using TS = StdShape<BNW>;
   constexpr bool BLOCK = (FMT == kFmtBlock);
   static_assert(BNW == 128 || (BNW == 256 && !BLOCK), "wide tiles are FP8_Dynamic only");
-  constexpr int NBUF = BLOCK ? 2 : 1;
-  // D is 128 lanes x BNW cols per buffer, plus (Block) a 128-col running sum.
+  constexpr int NBUF = BLOCK ? 4 : 1;
+  // D is 128 lanes x BNW cols per buffer
   constexpr uint32_t kBufCols = BNW;
-  constexpr uint32_t kTmemCols = pow2_cols(NBUF * kBufCols + (BLOCK ? kBN : 0));
+  constexpr uint32_t kTmemCols = pow2_cols(NBUF * kBufCols);
   static_assert(kTmemCols <= 512, "TMEM budget");
+  constexpr int kEpi = std_threads(FMT) - 64;        // epilogue threads (2 or 4 per TMEM lane)
+  constexpr int kCols = BLOCK ? kBN / 2 : BNW;        // weight rows (TMEM columns) of each
 
   stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
@@ -952,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->acc_full, 1);
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], 128);
+      mbar_init(&ctl->tempty[b], kEpi);
     }
     mbar_init(&ctl->never, 1);
     ctl->last_flag = 0;
@@ -1048,42 +1060,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // TMEM lane = token row m, columns = weight rows n.
+    // TMEM lane = token row m, columns = weight rows n; this thread's
+    // columns are [c0, c0 + kCols).
     pdl_wait();
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const int et = threadIdx.x - 64;  // 0..127
+    const int et = threadIdx.x - 64;  // 0 .. kEpi-1
+    const int c0 = ((warp - 2) >> 2) * kCols;
     const int m = m_tile * 128 + q * 32 + lane;
     const bool m_ok = m < g.M;
-    const uint32_t run_col = NBUF * kBufCols;  // Block: running sum columns
+    float acc[BLOCK ? kCols : 1];  // Block: the promoted sums of this thread's columns
+#pragma unroll
+    for (int c = 0; c < (BLOCK ? kCols : 1); ++c) acc[c] = 0.0f;
     if constexpr (BLOCK) {
       const int nb = n_tile;
-      for (int i = 0; i < nk; ++i) {
+      // the k-tiles' coefficients, requested kAhead k-tiles ahead into a
+      // register ring (an L2 round trip is several k-tiles of promotion)
+      constexpr int kAhead = 8;
+      auto coef_of = [&](int i) -> float {
+        return (m_ok && i < nk) ? __ldg(g.s_a + static_cast<int64_t>(m) * g.kt_total + kb0 + i) *
+                                      __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
+                                : 0.0f;
+      };
+      float cring[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) cring[u] = coef_of(u);
+      bool ok = true;
+      for (int i0 = 0; ok && i0 < nk; i0 += kAhead)
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        const int i = i0 + u;
+        if (i >= nk) break;
         const int buf = i % NBUF;
-        const float sa = m_ok ? __ldg(g.s_a + static_cast<int64_t>(m) * g.kt_total + kb0 + i) : 0.0f;
-        const float coef = sa * __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i);
+        const float coef = cring[u];
+        cring[u] = coef_of(i + kAhead);
         const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
         if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
           *abort_flag = 1;
+          ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < kBN; c += 8) {
-          uint32_t p[8], r[8];
-          tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c), p);
-          if (i > 0) tmem_ld_x8(tmem + lane_base + run_col + c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float prev = i > 0 ? __uint_as_float(r[j]) : 0.0f;
-            r[j] = __float_as_uint(fmaf(coef, __uint_as_float(p[j]), prev));
-          }
-          tmem_st_x8(tmem + lane_base + run_col + c, r);
-        }
-        tmem_st_wait();
+        uint32_t v[kCols];
+        tmem_ld_cols(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c0), v);
+        tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&ctl->tempty[buf]);
+        const float2 cc = make_float2(coef, coef);
+#pragma unroll
+        for (int c = 0; c < kCols; c += 2) {
+          const float2 r = __ffma2_rn(cc, make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                      make_float2(acc[c], acc[c + 1]));
+          acc[c] = r.x;
+          acc[c + 1] = r.y;
+        }
       }
       mbar_wait(&ctl->acc_full, 0, g.wait_ns);
     } else {
@@ -1092,15 +1122,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const bool abort = __any_sync(0xffffffffu, *abort_flag != 0);
     const float sa = (!BLOCK && m_ok) ? __ldg(g.s_a + m) : 1.0f;
-    const uint32_t src_col = BLOCK ? run_col : 0;
     float* part = static_cast<float*>(g.ws_part);
-#pragma unroll 1
-    for (int c = 0; c < BNW && !abort; c += 8) {
-      uint32_t t[8];
-      tmem_ld_x8(tmem + lane_base + src_col + c, t);
-      tmem_ld_wait();
-      const int n0 = n_tile * BNW + c;
-      if (!m_ok) continue;
+    // this thread's 8 results of columns [c0 + c, c0 + c + 8) to Y (or to
+    // its Split-K partial)
+    auto emit = [&](int c, const uint32_t (&t)[8]) {
+      const int n0 = n_tile * BNW + c0 + c;
+      if (!m_ok) return;
       if (g.splits == 1) {
         if (n0 + 8 <= g.N) {
           uint32_t packed[4];
@@ -1132,20 +1159,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8 && n0 + j < g.N; ++j)
           part[(static_cast<int64_t>(split) * g.M + m) * g.N + n0 + j] = __uint_as_float(t[j]);
       }
+    };
+    if (!abort) {
+      if constexpr (BLOCK) {
+#pragma unroll
+        for (int c = 0; c < kCols; c += 8) {
+          uint32_t t[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t[j] = __float_as_uint(acc[c + j]);
+          emit(c, t);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < kCols; c += 8) {
+          uint32_t t[8];
+          tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(c), t);
+          tmem_ld_wait();
+          emit(c, t);
+        }
+      }
     }
     if (g.splits > 1 && !abort) {
       __threadfence();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpi);
       const int tile_id = blockIdx.x;
       if (et == 0) {
         const int old = atomicAdd(g.ws_count + tile_id, 1);
         ctl->last_flag = (old == g.splits - 1);
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpi);
       if (ctl->last_flag) {
         __threadfence();
         if (m_ok) {
-          for (int c = 0; c < BNW; ++c) {
+          for (int c = c0; c < c0 + kCols; ++c) {
             const int n = n_tile * BNW + c;
             if (n >= g.N) break;
             float sum = 0.0f;

@@ -340,7 +340,7 @@ int launch_gemm(Kernel kernel, const Plan& p, dim3 grid, unsigned threads, size_
   return QG_OK;
 }
 
-template <int FMT, int MPAD, bool FUSED>
+template <int FMT, int MPAD, bool FUSED, int PW = 4>
 int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                 cudaStream_t stream) {
   const int rb = g.recv_bytes;
@@ -348,18 +348,21 @@ int run_f8_swap(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, q
   if (rc != QG_OK) return rc;
   // Block_FP8 fused: the scale ring holds stages + 4 k-tiles
   if (FMT == qg::kFmtBlock && FUSED && g.stages > qg::kMaxStagesBlockFused) g.stages = qg::kMaxStagesBlockFused;
-  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
-                     qg::swap_threads(FMT, FUSED), qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g,
-                     stream);
+  return launch_gemm(qg::gemm_f8_swap_kernel<FMT, MPAD, FUSED, PW>, p,
+                     dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::swap_threads(FMT, FUSED, PW),
+                     qg::gemm_f8_smem_bytes<true, MPAD>(g.stages, rb), tmW, tmA, g, stream);
 }
 
 template <int FMT, int BNW>
 int run_f8_std(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                cudaStream_t stream) {
+  // Block_FP8's four partial buffers take all the TMEM (one CTA per SM):
+  // the deepest ring that fits by default
+  if (FMT == qg::kFmtBlock && (config_id & QG_CONFIG_RING_MASK) == 0) config_id |= kMaxStages;
   int rc = pick_stages(config_id, [](int st) { return qg::gemm_f8_std_smem_bytes<BNW>(st); }, &g.stages);
   if (rc != QG_OK) return rc;
-  return launch_gemm(qg::gemm_f8_std_kernel<FMT, BNW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups), qg::kThreads,
-                     qg::gemm_f8_std_smem_bytes<BNW>(g.stages), tmW, tmA, g, stream);
+  return launch_gemm(qg::gemm_f8_std_kernel<FMT, BNW>, p, dim3(p.n_tiles * p.m_tiles, p.splits, p.groups),
+                     qg::std_threads(FMT), qg::gemm_f8_std_smem_bytes<BNW>(g.stages), tmW, tmA, g, stream);
 }
 
 template <int MPAD>
@@ -370,6 +373,8 @@ int run_f8_swap_fmt(int fmt, bool fused, const Plan& p, const CUtensorMap& tmW, 
     return run_f8_swap<qg::kFmtFP8, MPAD, false>(p, tmW, tmA, g, config_id, stream);
   }
   if (fused) return run_f8_swap<qg::kFmtBlock, MPAD, true>(p, tmW, tmA, g, config_id, stream);
+  // QG_CONFIG_BLOCK_PROMO8: eight promotion warps
+  if (config_id & QG_CONFIG_BLOCK_PROMO8) return run_f8_swap<qg::kFmtBlock, MPAD, false, 8>(p, tmW, tmA, g, config_id, stream);
   return run_f8_swap<qg::kFmtBlock, MPAD, false>(p, tmW, tmA, g, config_id, stream);
 }
 
@@ -487,7 +492,8 @@ int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
                      QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_PAIR_MMA |
-                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 | QG_CONFIG_BLOCK_PROMO8 | QG_CONFIG_RING_MASK |
+                     QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -513,6 +519,11 @@ int check_config_bits(int fmt, int variant, int config_id) {
        (config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_WIDE | QG_CONFIG_PERSIST))))
     return fail(QG_ERR_INVALID_ARG,
                 "QG_CONFIG_I8_CONV16 is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernel");
+  if ((config_id & QG_CONFIG_BLOCK_PROMO8) &&
+      (fmt != QG_BLOCK_FP8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) ||
+       (config_id & (QG_CONFIG_FUSED_QUANT | QG_CONFIG_WIDE | QG_CONFIG_PERSIST | QG_CONFIG_MMA_SYNC))))
+    return fail(QG_ERR_INVALID_ARG,
+                "QG_CONFIG_BLOCK_PROMO8 is for Block_FP8 with QG_SWAPAB / QG_SWAPAB_SPLITK, two-kernel form");
   if ((config_id & QG_CONFIG_PAIR_MMA) && !(config_id & QG_CONFIG_PERSIST))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PAIR_MMA is a form of the QG_CONFIG_PERSIST kernel");
   if ((config_id & QG_CONFIG_PERSIST) &&
@@ -660,8 +671,9 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (fused || wide || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK || variant == QG_SWAPAB_DP4A ||
                            variant == QG_SWAPAB_DP4A_SPLITK))
       return fail(QG_ERR_INVALID_ARG, "grouped launches run the Swap-AB variants");
-    if (config_id & (QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16))
-      return fail(QG_ERR_INVALID_ARG, "grouped launches take neither QG_CONFIG_I8_PREWIDEN nor QG_CONFIG_I8_CONV16");
+    if (config_id & (QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 | QG_CONFIG_BLOCK_PROMO8))
+      return fail(QG_ERR_INVALID_ARG,
+                  "grouped launches take none of QG_CONFIG_I8_PREWIDEN, QG_CONFIG_I8_CONV16, QG_CONFIG_BLOCK_PROMO8");
     if (rows < 0 || rows > 0x7FFFFFFF || static_cast<int64_t>(grouped->groups) * N > 0x7FFFFFFF)
       return fail(QG_ERR_UNSUPPORTED_SHAPE, "sizes too large");
     if (rows == 0) return QG_OK;
@@ -1111,7 +1123,8 @@ int qg_linear_w8a8(int fmt, int64_t M, int64_t N, int64_t K, const void* A_dev, 
                    void* stream) {
   if (fmt < 0 || fmt > 2) return fail(QG_ERR_INVALID_ARG, "unknown format %d", fmt);
   const bool fusable = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) &&
-                       !(config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16));
+                       !(config_id & (QG_CONFIG_MMA_SYNC | QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 |
+                                      QG_CONFIG_BLOCK_PROMO8));
   const bool buffers = A_q_dev != nullptr && s_a_dev != nullptr;
   if (fusable && (!buffers || (config_id & QG_CONFIG_FUSED_QUANT) ||
                   (g_launch_flags.load(std::memory_order_relaxed) & QG_LAUNCH_FUSED_QUANT))) {

@@ -64,6 +64,8 @@ TUNED_M = (1, 2, 4, 8, 16, 24, 32)
 FMT_ID = {"FP8_Dynamic": 0, "W8A8_INT8": 1, "Block_FP8": 2}
 POOL_BYTES = 512 << 20
 PREFETCH_DISTANCES = (1, 2, 4)  # weight k-tiles each CTA keeps requested into L2 ahead of its ring
+# kernel forms that qg_linear_w8a8 runs only as quantization kernel + GEMM
+NOT_FUSABLE = (q.QG_CONFIG_MMA_SYNC | q.QG_CONFIG_I8_PREWIDEN | q.QG_CONFIG_I8_CONV16 | q.QG_CONFIG_BLOCK_PROMO8)
 
 
 def candidates(fmt: str, M: int, N: int, K: int, sms: int):
@@ -72,7 +74,8 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     (in blocks of 64 tokens above 64); for W8A8_INT8 at M <= 8 also their
     CUDA-core (dp4a) forms, and for W8A8_INT8 at every M the mma.sync forms
     (QG_CONFIG_MMA_SYNC, widened or QG_CONFIG_MMA_S8), and from 64 tokens on
-    its pre-widened form (QG_CONFIG_I8_PREWIDEN); above 32 tokens also the Standard variant of the
+    its pre-widened form (QG_CONFIG_I8_PREWIDEN); for Block_FP8 Swap-AB with
+    eight promotion warps (QG_CONFIG_BLOCK_PROMO8); above 32 tokens also the Standard variant of the
     E4M3 formats (FP8_Dynamic also with 256-row weight tiles).  Ring depth:
     0 = two CTAs per SM, 12 = one deep ring per SM (6 for Standard, whose
     stages are twice as large)."""
@@ -88,6 +91,9 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
     if fmt == "W8A8_INT8" and M > 8:
         # sixteen converter warps, one CTA per SM, the deepest ring
         cfgs.append(q.config_id(0, 0, conv16=True))
+    if fmt == "Block_FP8":
+        # eight promotion warps (QG_CONFIG_BLOCK_PROMO8)
+        cfgs += [q.config_id(0, promo8=True), q.config_id(12, promo8=True)]
     for cfg in cfgs:
         for single, split in swap_forms:
             if cfg & q.QG_CONFIG_I8_CONV16 and single != q.QG_SWAPAB:
@@ -292,7 +298,7 @@ def layer_context_pass(bench, table_in, out_path, fmts, models, ms, sms, log=Non
                         # GEMM): every CTA reads whole activation rows, cheap at a few
                         # tokens, and the linear has one kernel boundary instead of two
                         cands += [(v, sp, c | q.QG_CONFIG_FUSED_QUANT) for (v, sp, c) in cands
-                                  if v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK) and not c & q.QG_CONFIG_MMA_SYNC]
+                                  if v in (q.QG_SWAPAB, q.QG_SWAPAB_SPLITK) and not c & NOT_FUSABLE]
                     for cand in cands:
                         if cand == cfgs[li]:
                             continue

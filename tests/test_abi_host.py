@@ -166,6 +166,7 @@ def test_grouped_validation(q):
     assert _grouped(q, split=17, K=4096, variant=3) == q.QG_ERR_WORKSPACE_TOO_SMALL
     assert _grouped(q, fmt=1, cfg=q.QG_CONFIG_I8_PREWIDEN) == q.QG_ERR_INVALID_ARG   # not for grouped launches
     assert _grouped(q, fmt=1, cfg=q.QG_CONFIG_I8_CONV16) == q.QG_ERR_INVALID_ARG
+    assert _grouped(q, fmt=2, cfg=q.QG_CONFIG_BLOCK_PROMO8) == q.QG_ERR_INVALID_ARG
     assert _grouped(q, total=0) == q.QG_OK                               # no tokens: nothing to do
     assert _grouped(q, max_tokens=0) == q.QG_OK
 
@@ -250,7 +251,11 @@ def test_check_config_returns_the_gemm_status(q):
              dict(fmt=1, M=300, cfg=q.QG_CONFIG_I8_PREWIDEN | q.QG_CONFIG_MMA_SYNC),
              dict(fmt=1, M=300, variant=q.QG_SWAPAB_DP4A, cfg=q.QG_CONFIG_I8_PREWIDEN),
              dict(fmt=2, M=32, cfg=q.QG_CONFIG_I8_CONV16),                              # conv16: INT8 only
-             dict(fmt=1, M=32, cfg=q.QG_CONFIG_I8_CONV16 | q.QG_CONFIG_FUSED_QUANT)]
+             dict(fmt=1, M=32, cfg=q.QG_CONFIG_I8_CONV16 | q.QG_CONFIG_FUSED_QUANT),
+             dict(fmt=0, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8),                           # promo8: Block_FP8 only
+             dict(fmt=1, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8),
+             dict(fmt=2, M=300, variant=0, cfg=q.QG_CONFIG_BLOCK_PROMO8),               # Swap-AB only
+             dict(fmt=2, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8 | q.QG_CONFIG_FUSED_QUANT)]
     for c in cases:
         fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
         v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)
@@ -268,6 +273,7 @@ def test_check_config_returns_the_gemm_status(q):
     assert q.qg_check_config(0, 512, 24576, 4096, q.QG_STANDARD, 1, q.config_id(3, 8, pair_mma=True)) == q.QG_OK
     assert q.qg_check_config(1, 16, 4096, 4096, q.QG_SWAPAB_SPLITK, 4, q.config_id(conv16=True)) == q.QG_OK
     assert q.qg_check_config(1, 300, 4096, 4096, q.QG_SWAPAB, 1, q.config_id(prewiden=True, conv16=True)) == q.QG_OK
+    assert q.qg_check_config(2, 512, 4096, 4096, q.QG_SWAPAB_SPLITK, 2, q.config_id(6, promo8=True)) == q.QG_OK
     assert q.qg_check_config(2, 32, 4096, 12288, q.QG_SWAPAB_SPLITK, 96, q.config_id(12, 64)) == q.QG_OK
     assert q.qg_check_config(0, 0, 256, 256, 2, 1, 0) == q.QG_ERR_INVALID_ARG   # a configuration has M >= 1
 

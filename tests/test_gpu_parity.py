@@ -69,12 +69,37 @@ def test_block_fp8_long_k_ranges(orc, gc, M, variant, split):
     gc.run_case(orc, "Block_FP8", M, 264, K, variant, split, seed=4100 + M + split)
 
 
-def test_block_fp8_chunked_promotion_timeout(orc, gc, q):
-    # a forced wait time-out on the chunked promotion path: the warps that
-    # gave up still pass every chunk barrier, the time-out is reported, and
-    # the context stays usable
+@pytest.mark.parametrize("M,N,K,split", [(33, 264, 4608, 1), (200, 392, 2560, 1), (130, 264, 3840, 3),
+                                           (300, 136, 1280, 6)])
+def test_block_fp8_standard_register_promotion(orc, gc, M, N, K, split):
+    # the Standard kernel's Block_FP8 promotion: four partial buffers, eight
+    # promotion warps with register accumulators; ragged token and weight
+    # tiles, long K ranges, Split-K through the workspace
+    gc.run_case(orc, "Block_FP8", M, N, K, ST if split == 1 else STS, split, seed=4500 + M)
+
+
+@pytest.mark.parametrize("M,K,variant,split", [(1, 768, SW, 1), (7, 768, SWS, 2), (16, 768, SWS, 5),
+                                               (24, 3840, SWS, 20), (32, 768, SW, 1), (5, 9344, SW, 1),
+                                               (20, 9344, SW, 1), (48, 18688, SWS, 2), (65, 2560, SW, 1),
+                                               (130, 2560, SWS, 3), (200, 2560, SWS, 20), (257, 4096, SW, 1)])
+def test_block_fp8_eight_promotion_warps(orc, gc, q, M, K, variant, split):
+    # QG_CONFIG_BLOCK_PROMO8: two promotion warps per TMEM lane quarter, each
+    # with half of the token block (blocks of 16, 32, 64), through every
+    # reduction (none, cluster, workspace), staged and chunked scale
+    # products, ragged token blocks and weight tiles
+    gc.run_case(orc, "Block_FP8", M, 264, K, variant, split, seed=4300 + M,
+                config_id=q.config_id(promo8=True))
+
+
+@pytest.mark.parametrize("variant,promo8", [(SW, False), (SW, True), (ST, False)])
+def test_block_fp8_chunked_promotion_timeout(orc, gc, q, variant, promo8):
+    # a forced wait time-out on the chunked promotion path (four or eight
+    # promotion warps; and the Standard kernel's eight promotion warps): the
+    # warps that gave up still pass every chunk barrier, the time-out is
+    # reported, and the context stays usable
     import seeded_inputs as si
     M, N, K = 20, 256, 4608  # 36 k-tiles x a 32-token block > 1024 products
+    cfg = q.config_id(promo8=promo8)
     A = si.activations(M, K, seed=3)
     W = si.weights(N, K, seed=3)
     Ad, Wd = A.to(gc.DEV), torch.from_numpy(W).to(gc.DEV)
@@ -85,13 +110,13 @@ def test_block_fp8_chunked_promotion_timeout(orc, gc, q):
     q.qg_set_wait_limit_ns(2_000_000)  # 2 ms
     q.qg_set_force_timeout(True)
     try:
-        gc.gemm_gpu("Block_FP8", Aq, sa, Wq, sw, N, SW, 1)
+        gc.gemm_gpu("Block_FP8", Aq, sa, Wq, sw, N, variant, 1, config_id=cfg)
         assert q.qg_device_error() == q.QG_ERR_DEVICE_TIMEOUT
     finally:
         q.qg_set_force_timeout(False)
         q.qg_set_wait_limit_ns(0)
     assert q.qg_device_error() == 0
-    Y, _ = gc.gemm_gpu("Block_FP8", Aq, sa, Wq, sw, N, SW, 1)
+    Y, _ = gc.gemm_gpu("Block_FP8", Aq, sa, Wq, sw, N, variant, 1, config_id=cfg)
     torch.cuda.synchronize()
     oAq, osa, oWq, osw = gc.check_quant(orc, "Block_FP8", A, W, Aq, sa, Wq, sw)
     gc.check_gemm(orc, "Block_FP8", oAq, osa, oWq, osw, Y)
