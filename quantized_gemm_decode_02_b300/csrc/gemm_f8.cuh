@@ -717,17 +717,15 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
         const bool staged = !FUSED && nk * MPAD <= kMaxClusterSplits * 64;
         const bool chunked = !FUSED && !staged;
         const int et = threadIdx.x - 64;  // promotion thread 0 .. kEpi-1
-        auto coef_of = [&](int i, int t) -> float {
-          return (i < nk && t < Mb) ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) *
-                                          __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
-                                    : 0.0f;
-        };
         float cpre[kCoefPer];
         auto load_chunk = [&](int c) {
 #pragma unroll
           for (int j = 0; j < kCoefPer; ++j) {
             const int e = et + kEpi * j;
-            cpre[j] = coef_of(c * kChunkTiles + e / MPAD, e % MPAD);
+            const int i = c * kChunkTiles + e / MPAD, t = e % MPAD;
+            cpre[j] = (i < nk && t < Mb) ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) *
+                                               __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
+                                         : 0.0f;
           }
         };
         auto store_chunk = [&](int c) {
@@ -735,9 +733,23 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
           for (int j = 0; j < kCoefPer; ++j) ctl->amax_s[(c & 1) * kHalfCoefs + et + kEpi * j] = cpre[j];
         };
         if (staged) {
-          for (int e = et; e < nk * MPAD; e += kEpi) {
-            const int i = e / MPAD;
-            ctl->amax_s[e] = coef_of(i, e - i * MPAD);
+          // loads issued in rounds of up to four before their products
+          constexpr int kPer = kMaxClusterSplits * 64 / kEpi;
+          constexpr int kRound = kPer > 4 ? 4 : kPer;
+#pragma unroll
+          for (int r0 = 0; r0 < kPer; r0 += kRound) {
+            float ra[kRound], rw[kRound];
+#pragma unroll
+            for (int j = 0; j < kRound; ++j) {
+              const int e = et + kEpi * (r0 + j);
+              const int i = e / MPAD, t = e % MPAD;
+              const bool ok_e = e < nk * MPAD && t < Mb;
+              ra[j] = ok_e ? __ldg(g.s_a + static_cast<int64_t>(m_base + t) * g.kt_total + kb0 + i) : 0.0f;
+              rw[j] = ok_e ? __ldg(s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < kRound; ++j)
+              if (et + kEpi * (r0 + j) < nk * MPAD) ctl->amax_s[et + kEpi * (r0 + j)] = ra[j] * rw[j];
           }
           named_bar_sync(1, kEpi);
         } else if (chunked) {
@@ -1074,17 +1086,18 @@ __global__ void __launch_bounds__(std_threads(FMT), 1)
     for (int c = 0; c < (BLOCK ? kCols : 1); ++c) acc[c] = 0.0f;
     if constexpr (BLOCK) {
       const int nb = n_tile;
-      // the k-tiles' coefficients, requested kAhead k-tiles ahead into a
-      // register ring (an L2 round trip is several k-tiles of promotion)
-      constexpr int kAhead = 8;
-      auto coef_of = [&](int i) -> float {
-        return (m_ok && i < nk) ? __ldg(g.s_a + static_cast<int64_t>(m) * g.kt_total + kb0 + i) *
-                                      __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i)
-                                : 0.0f;
+      // the k-tiles' scales, requested kAhead k-tiles ahead into a register
+      // ring (an L2 round trip is several k-tiles of promotion) and
+      // multiplied only when used, so no warp waits on a load it issued
+      constexpr int kAhead = 4;
+      float ring_a[kAhead], ring_w[kAhead];
+      auto fetch = [&](int u, int i) {
+        const bool ok_i = m_ok && i < nk;
+        ring_a[u] = ok_i ? __ldg(g.s_a + static_cast<int64_t>(m) * g.kt_total + kb0 + i) : 0.0f;
+        ring_w[u] = ok_i ? __ldg(g.s_w + static_cast<int64_t>(nb) * g.kt_total + kb0 + i) : 0.0f;
       };
-      float cring[kAhead];
 #pragma unroll
-      for (int u = 0; u < kAhead; ++u) cring[u] = coef_of(u);
+      for (int u = 0; u < kAhead; ++u) fetch(u, u);
       bool ok = true;
       for (int i0 = 0; ok && i0 < nk; i0 += kAhead)
 #pragma unroll
@@ -1092,8 +1105,8 @@ __global__ void __launch_bounds__(std_threads(FMT), 1)
         const int i = i0 + u;
         if (i >= nk) break;
         const int buf = i % NBUF;
-        const float coef = cring[u];
-        cring[u] = coef_of(i + kAhead);
+        const float sa_i = ring_a[u], sw_i = ring_w[u];
+        fetch(u, i + kAhead);
         const bool w = mbar_wait(&ctl->tfull[buf], static_cast<uint32_t>(i / NBUF) & 1u, g.wait_ns);
         if (!__all_sync(0xffffffffu, w && !*abort_flag)) {
           *abort_flag = 1;
@@ -1101,18 +1114,25 @@ __global__ void __launch_bounds__(std_threads(FMT), 1)
           break;
         }
         tc_fence_after();
-        uint32_t v[kCols];
-        tmem_ld_cols(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c0), v);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&ctl->tempty[buf]);
+        const float coef = sa_i * sw_i;
         const float2 cc = make_float2(coef, coef);
+        // the buffer's columns in two halves of 32 (registers)
 #pragma unroll
-        for (int c = 0; c < kCols; c += 2) {
-          const float2 r = __ffma2_rn(cc, make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                                      make_float2(acc[c], acc[c + 1]));
-          acc[c] = r.x;
-          acc[c + 1] = r.y;
+        for (int h = 0; h < kCols; h += 32) {
+          uint32_t v[32];
+          tmem_ld_cols(tmem + lane_base + static_cast<uint32_t>(buf * kBufCols + c0 + h), v);
+          tmem_ld_wait();
+          if (h + 32 >= kCols) {
+            tc_fence_before();
+            mbar_arrive(&ctl->tempty[buf]);
+          }
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 r = __ffma2_rn(cc, make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                        make_float2(acc[h + c], acc[h + c + 1]));
+            acc[h + c] = r.x;
+            acc[h + c + 1] = r.y;
+          }
         }
       }
       mbar_wait(&ctl->acc_full, 0, g.wait_ns);
