@@ -89,6 +89,8 @@ typedef enum {
 #define QG_CONFIG_I8_PREWIDEN (1 << 22)
 #define QG_CONFIG_I8_CONV16 (1 << 23)
 #define QG_CONFIG_BLOCK_PROMO8 (1 << 24)
+#define QG_CONFIG_PERSIST_ROWS_SHIFT 25
+#define QG_CONFIG_PERSIST_ROWS_MASK (3 << 25)
 
 typedef enum {
   QG_OK = 0,
@@ -203,14 +205,19 @@ QG_API int qg_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream)
  *                      tiles of one 256-row weight tile, each loading half
  *                      of the weight tile by TMA multicast into both CTAs,
  *                      with two TMEM accumulators so that a tile's epilogue
- *                      overlaps the next tile's MMAs; only the ring depth
- *                      and the L2 prefetch distance (weight k-tiles of the
- *                      CTA's half requested ahead, across tiles) may be
- *                      combined with it (QG_ERR_INVALID_ARG else); with it
+ *                      overlaps the next tile's MMAs; only the ring depth,
+ *                      the L2 prefetch distance (weight k-tiles of the
+ *                      CTA's half requested ahead, across tiles) and the
+ *                      fields below may be combined with it
+ *                      (QG_ERR_INVALID_ARG else); with it
  *                      also QG_CONFIG_PAIR_MMA: the pair runs each MMA as one
  *                      tcgen05.mma.cta_group::2 (M = 256 tokens, each CTA
  *                      holding only its own half of the weight tile, no
- *                      multicast), issued by the pair's even CTA;
+ *                      multicast), issued by the pair's even CTA; and
+ *                      r << QG_CONFIG_PERSIST_ROWS_SHIFT: weight tiles of
+ *                      256 (r = 0), 224, 192 or 160 rows (r = 1..3; MMA N),
+ *                      so that a shape's tile count fills the last round of
+ *                      the resident pairs better;
  *                      plus QG_CONFIG_I8_PREWIDEN for W8A8_INT8 with
  *                      QG_SWAPAB / QG_SWAPAB_SPLITK on the tcgen05 kernel
  *                      (the compute-bound regime): the call first widens the

@@ -7,19 +7,21 @@
 // tokens on the MMA M side; the pages send token counts beyond their tuned
 // range to other kernels ("Hybrid Dispatch"), here this library's own.
 //
-// Tiles: 128 tokens x 256 weight rows per CTA, D[128 x 256] fp32 in TMEM
-// (tcgen05.mma.kind::f8f6f4, M = 128, N = 256, K = 32 per instruction).
+// Tiles: 128 tokens x RW weight rows per CTA (RW = 256, or 224 / 192 / 160
+// so that a shape's tile count fills the resident clusters' last round
+// better), D[128 x RW] fp32 in TMEM (tcgen05.mma.kind::f8f6f4, M = 128,
+// N = RW, K = 32 per instruction).
 // Pairs: the two CTAs of a thread-block cluster take the two 128-token
-// halves of a 256-token pair tile and the same 256-row weight tile; CTA r
-// loads weight rows [128 r, 128 r + 128) of the tile with TMA multicast into
-// both CTAs' shared memory, so each weight k-tile crosses from L2 to the SMs
-// once per pair (each CTA loads 16 KB of weights and 16 KB of activations per
-// k-tile instead of 32 + 16).  A stage is refilled only when the MMAs of both
+// halves of a 256-token pair tile and the same RW-row weight tile; CTA r
+// loads weight rows [RW/2 r, RW/2 (r + 1)) of the tile with TMA multicast
+// into both CTAs' shared memory, so each weight k-tile crosses from L2 to the
+// SMs once per pair (at RW = 256 each CTA loads 16 KB of weights and 16 KB of
+// activations per k-tile instead of 32 + 16).  A stage is refilled only when the MMAs of both
 // CTAs are done with it (their commits arrive on both CTAs' empty barrier).
 // Persistent: gridDim.x = 2 x clusters (at most one CTA per SM); cluster c
 // takes pair tiles c, c + clusters, ..., token pair fastest, so the clusters
 // running at the same time share weight tiles in L2.
-// Double-buffered accumulator: two 256-column TMEM buffers; the MMA thread
+// Double-buffered accumulator: two RW-column TMEM buffers; the MMA thread
 // fills one tile's buffer while the epilogue warps drain the previous one.
 //
 // CTA = 6 warps: warp 0 TMA producer, warp 1 TMEM owner and MMA issuer,
@@ -30,10 +32,10 @@
 // PAIR (QG_CONFIG_PAIR_MMA): the pair runs one tcgen05.mma.cta_group::2 per
 // K step instead of one cta_group::1 MMA in each CTA: M = 256 tokens (128
 // from each CTA's shared memory, each CTA's TMEM receiving its own 128
-// rows), N = 256 weight rows of which each CTA holds only its own half (the
-// tensor cores of the pair exchange the halves), so a stage is 16 KB of
-// activations + 16 KB of weights per CTA (32 KB instead of 48: deeper ring)
-// and no multicast is needed.  The even CTA (the leader) issues every MMA;
+// rows), N = RW weight rows of which each CTA holds only its own half (the
+// tensor cores of the pair exchange the halves), so at RW = 256 a stage is
+// 16 KB of activations + 16 KB of weights per CTA (32 KB instead of 48:
+// deeper ring) and no multicast is needed.  The even CTA (the leader) issues every MMA;
 // both CTAs' TMA loads complete on the leader's full barrier (cta_group::2
 // copies), its commits arrive on the barriers of both CTAs (multicast), the
 // epilogue warps of both CTAs release an accumulator buffer by arriving on
@@ -46,16 +48,14 @@
 namespace qg {
 
 constexpr int kPsTok = 128;                       // tokens per CTA (MMA M)
-constexpr int kPsRows = 256;                      // weight rows per tile (MMA N)
+constexpr int kPsRows = 256;                      // the largest weight-row tile (MMA N)
 constexpr uint32_t kPsABytes = kPsTok * kBK;      // 16 KB
-constexpr uint32_t kPsWBytes = kPsRows * kBK;     // 32 KB (two multicast halves)
-constexpr uint32_t kPsStageBytes = kPsABytes + kPsWBytes;
-constexpr uint32_t kPsTmemCols = 2 * kPsRows;     // two accumulator buffers
-constexpr uint32_t kPs2WBytes = kPsTok * kBK;     // PAIR: this CTA's 128-row weight half, 16 KB
 
-template <bool PAIR>
+// A stage: the activation tile, then the weight rows of the tile (both
+// multicast halves) or, PAIR, this CTA's half of them.
+template <bool PAIR, int RW>
 __host__ __device__ constexpr uint32_t ps_stage_bytes() {
-  return PAIR ? kPsABytes + kPs2WBytes : kPsStageBytes;
+  return kPsABytes + static_cast<uint32_t>(PAIR ? RW / 2 : RW) * kBK;
 }
 
 struct alignas(8) CtrlPs {
@@ -71,9 +71,9 @@ struct alignas(8) CtrlPs {
   float sw_s[2][kPsRows];  // per-channel scales of the buffer's weight tile
 };
 
-template <bool PAIR = false>
+template <bool PAIR = false, int RW = kPsRows>
 __host__ __device__ constexpr size_t gemm_f8_persist_smem_bytes(int stages) {
-  return 1024 + static_cast<size_t>(stages) * ps_stage_bytes<PAIR>() + sizeof(CtrlPs);
+  return 1024 + static_cast<size_t>(stages) * ps_stage_bytes<PAIR, RW>() + sizeof(CtrlPs);
 }
 
 // 2-D TMA load multicast to the CTAs of ctaMask: the box lands at the same
@@ -150,11 +150,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 }
 
 // One CTA of a pair.  g.m_tiles = pair tiles along the tokens (ceil(M/256)),
-// g.kt_total = k-tiles; tiles = g.m_tiles * ceil(N/256).
-template <bool PAIR>
+// g.kt_total = k-tiles; tiles = g.m_tiles * ceil(N/RW).  tmW's box is RW/2
+// rows.
+template <bool PAIR, int RW = kPsRows>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f8_persist_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, GemmArgs g) {
-  constexpr uint32_t kStage = ps_stage_bytes<PAIR>();
+  static_assert(RW % 32 == 0 && RW >= 128 && RW <= kPsRows, "weight-row tiles of 128..256, halves of whole 16-row groups");
+  constexpr uint32_t kStage = ps_stage_bytes<PAIR, RW>();
+  constexpr int kHalfRows = RW / 2;                       // rows of one CTA's weight half
+  constexpr uint32_t kTmemCols = pow2_cols(2 * RW);       // two accumulator buffers
   stamp_start(g.tstamp);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();           // 0 or 1: token half of the pair tile
   const bool leader = rank == 0;
   const int cluster = static_cast<int>(blockIdx.x >> 1), clusters = static_cast<int>(gridDim.x >> 1);
-  const int tp_count = g.m_tiles, wn_count = (g.N + kPsRows - 1) / kPsRows;
+  const int tp_count = g.m_tiles, wn_count = (g.N + RW - 1) / RW;
   const int tiles = tp_count * wn_count;
   const int nk = g.kt_total;
 
@@ -190,8 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // them (and, PAIR, before the collective TMEM allocation)
   cluster_sync();
   if (warp == 1) {
-    if constexpr (PAIR) tmem_alloc_pair(&ctl->tmem_base, kPsTmemCols);
-    else tmem_alloc(&ctl->tmem_base, kPsTmemCols);
+    if constexpr (PAIR) tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+    else tmem_alloc(&ctl->tmem_base, kTmemCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -213,12 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stage's activation tile
       auto load_w = [&](int s, int wn, int kk) {
         uint8_t* st = smem + static_cast<size_t>(s) * kStage;
-        const int w_row = wn * kPsRows + static_cast<int>(rank) * kPsTok;
+        const int w_row = wn * RW + static_cast<int>(rank) * kHalfRows;
         if constexpr (PAIR)
           tma_load_2d_pair(st + kPsABytes, &tmW, kk * kBK, w_row, full0 + 8u * static_cast<uint32_t>(s), pol_w);
         else
-          tma_load_2d_multicast(st + kPsABytes + rank * (kPsWBytes / 2), &tmW, kk * kBK, w_row, &ctl->full[s], both,
-                                pol_w);
+          tma_load_2d_multicast(st + kPsABytes + rank * (kHalfRows * kBK), &tmW, kk * kBK, w_row, &ctl->full[s],
+                                both, pol_w);
       };
       auto load_a = [&](int s, int a_row, int kk) {
         uint8_t* st = smem + static_cast<size_t>(s) * kStage;
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           k2 -= nk;
           t2 += clusters;
         }
-        if (t2 < tiles) tma_prefetch_l2_2d(&tmW, k2 * kBK, (t2 / tp_count) * kPsRows + static_cast<int>(rank) * kPsTok);
+        if (t2 < tiles) tma_prefetch_l2_2d(&tmW, k2 * kBK, (t2 / tp_count) * RW + static_cast<int>(rank) * kHalfRows);
       };
       if (ahead > 0 && first >= 0)
         for (int kk = pre; kk < pre + ahead; ++kk) prefetch_ahead(first, kk - ahead);
@@ -290,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && (!PAIR || leader)) {
-      // E4M3 x E4M3 -> F32: 128 x 256 per CTA, or 256 x 256 for the pair
-      constexpr uint32_t idesc = make_idesc(PAIR ? 2 * kPsTok : kPsTok, kPsRows, 0, 0);
+      // E4M3 x E4M3 -> F32: 128 x RW per CTA, or 256 x RW for the pair
+      constexpr uint32_t idesc = make_idesc(PAIR ? 2 * kPsTok : kPsTok, RW, 0, 0);
       bool ok = !g.force_timeout || mbar_wait(&ctl->never, 0, g.wait_ns);
       int i = 0, lt = 0;
       for (int t = cluster; ok && t < tiles; t += clusters, ++lt) {
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(b * kPsRows);
+        const uint32_t d = tmem + static_cast<uint32_t>(b * RW);
         for (int kk = 0; kk < nk; ++kk, ++i) {
           const int s = i % stages;
           if (!mbar_wait(&ctl->full[s], static_cast<uint32_t>(i / stages) & 1u, g.wait_ns) || *abort_flag) {
@@ -354,10 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tp = t % tp_count, wn = t / tp_count, b = lt & 1;
       const int m = tp * 2 * kPsTok + static_cast<int>(rank) * kPsTok + q * 32 + lane;
       const bool m_ok = m < g.M;
-      // the tile's 256 weight scales into the buffer's slot (the slot's
+      // the tile's RW weight scales into the buffer's slot (the slot's
       // previous tile was drained before the barrier closing its iteration)
-      for (int j = et; j < kPsRows; j += 128) {
-        const int n = wn * kPsRows + j;
+      for (int j = et; j < RW; j += 128) {
+        const int n = wn * RW + j;
         ctl->sw_s[b][j] = n < g.N ? __ldg(g.s_w + n) : 0.0f;
       }
       const float sa = m_ok ? __ldg(g.s_a + m) : 0.0f;
@@ -371,11 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < kPsRows; c += 8) {
+      for (int c = 0; c < RW; c += 8) {
         uint32_t v[8];
-        tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(b * kPsRows + c), v);
+        tmem_ld_x8(tmem + lane_base + static_cast<uint32_t>(b * RW + c), v);
         tmem_ld_wait();
-        const int n0 = wn * kPsRows + c;
+        const int n0 = wn * RW + c;
         if (!m_ok || n0 >= g.N) continue;
         __nv_bfloat16* dst = g.Y + static_cast<int64_t>(m) * g.ldy + n0;
         if (n0 + 8 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
@@ -411,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (PAIR) tmem_dealloc_pair(tmem, kPsTmemCols);
-    else tmem_dealloc(tmem, kPsTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
   // every copy this CTA issued into its peer, and the peer's into this CTA,
   // has been consumed (or the CTA gave up after a bounded wait) before

@@ -212,6 +212,7 @@ struct Plan {
   bool dp4a = false;   // W8A8_INT8 Swap-AB on the CUDA cores (M <= 8)
   bool mma = false;    // W8A8_INT8 Swap-AB on mma.sync (QG_CONFIG_MMA_SYNC)
   bool persist = false;  // FP8_Dynamic Standard as the persistent pair kernel (QG_CONFIG_PERSIST)
+  int persist_rows = 256;  // its weight rows per tile (QG_CONFIG_PERSIST_ROWS_MASK)
   bool prew = false;     // W8A8_INT8 Swap-AB on activations widened once per launch (QG_CONFIG_I8_PREWIDEN)
   int64_t prew_bytes = 0;  // their fp16 copy in the workspace (after the Split-K part)
   int mpad = 0;        // swap: MMA N (tokens padded), 16 / 32 / 64 (mma.sync: 8 / 16 / 24 / 32)
@@ -227,6 +228,7 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
   p->swap = (variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->dp4a;
   p->mma = (config_id & QG_CONFIG_MMA_SYNC) != 0;
   p->persist = (config_id & QG_CONFIG_PERSIST) != 0;
+  p->persist_rows = 256 - 32 * ((config_id & QG_CONFIG_PERSIST_ROWS_MASK) >> QG_CONFIG_PERSIST_ROWS_SHIFT);
   p->prew = (config_id & QG_CONFIG_I8_PREWIDEN) != 0;
   if (p->prew && (fmt != QG_W8A8_INT8 || !(variant == QG_SWAPAB || variant == QG_SWAPAB_SPLITK) || p->mma))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_I8_PREWIDEN is for W8A8_INT8 with QG_SWAPAB / QG_SWAPAB_SPLITK");
@@ -262,9 +264,9 @@ int make_plan(int fmt, int64_t M, int64_t N, int64_t K, int variant, int split_k
     p->m_tiles = static_cast<int>(cdiv(M, p->mpad));
     if (p->m_tiles > 65535) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else if (p->persist) {
-    // pair tiles of 256 tokens x 256 weight rows
+    // pair tiles of 256 tokens x persist_rows weight rows
     p->m_tiles = static_cast<int>(cdiv(M, 256));
-    p->n_tiles = static_cast<int>(cdiv(N, 256));
+    p->n_tiles = static_cast<int>(cdiv(N, p->persist_rows));
     if (static_cast<int64_t>(p->m_tiles) * p->n_tiles > 0x7FFFFFFF) return fail(QG_ERR_UNSUPPORTED_SHAPE, "M too large");
   } else {
     p->m_tiles = static_cast<int>(cdiv(M, 128));
@@ -428,17 +430,17 @@ int run_i8_mma(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg
 // ring takes the deepest depth that fits one CTA's shared memory unless
 // config_id asks for fewer stages.  PAIR: the cta_group::2 form
 // (QG_CONFIG_PAIR_MMA).
-template <bool PAIR>
+template <bool PAIR, int RW>
 int run_f8_persist_t(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                      cudaStream_t stream) {
   const DevInfo d = dev_info();
   int st = 8;
-  while (st > 2 && qg::gemm_f8_persist_smem_bytes<PAIR>(st) > d.smem_optin) --st;
+  while (st > 2 && qg::gemm_f8_persist_smem_bytes<PAIR, RW>(st) > d.smem_optin) --st;
   const int want = config_id & QG_CONFIG_RING_MASK;
   if (want >= 2 && want < st) st = want;
   g.stages = st;
-  const size_t smem = qg::gemm_f8_persist_smem_bytes<PAIR>(st);
-  cudaError_t e = set_smem(qg::gemm_f8_persist_kernel<PAIR>, smem);
+  const size_t smem = qg::gemm_f8_persist_smem_bytes<PAIR, RW>(st);
+  cudaError_t e = set_smem(qg::gemm_f8_persist_kernel<PAIR, RW>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   // the tile schedule is static, so only clusters that can all be resident
@@ -456,7 +458,7 @@ int run_f8_persist_t(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& t
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&resident, qg::gemm_f8_persist_kernel<PAIR>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&resident, qg::gemm_f8_persist_kernel<PAIR, RW>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // clear the query's error; fall back to one pair per two SMs
       resident = 0;
     }
@@ -465,15 +467,25 @@ int run_f8_persist_t(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& t
   if (resident <= 0 || resident > sms / 2) resident = sms / 2;
   const int clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, resident)));
   g.reduce = qg::kReduceNone;
-  e = launch_cluster_xy(qg::gemm_f8_persist_kernel<PAIR>, dim3(2 * clusters), dim3(qg::kThreads), smem, stream, 2u, 1u,
-                        tmW, tmA, g);
+  e = launch_cluster_xy(qg::gemm_f8_persist_kernel<PAIR, RW>, dim3(2 * clusters), dim3(qg::kThreads), smem, stream, 2u,
+                        1u, tmW, tmA, g);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return QG_OK;
 }
+template <int RW>
+int run_f8_persist_rw(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
+                      cudaStream_t stream) {
+  return (config_id & QG_CONFIG_PAIR_MMA) ? run_f8_persist_t<true, RW>(p, tmW, tmA, g, config_id, stream)
+                                          : run_f8_persist_t<false, RW>(p, tmW, tmA, g, config_id, stream);
+}
 int run_f8_persist(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmA, qg::GemmArgs& g, int config_id,
                    cudaStream_t stream) {
-  return (config_id & QG_CONFIG_PAIR_MMA) ? run_f8_persist_t<true>(p, tmW, tmA, g, config_id, stream)
-                                          : run_f8_persist_t<false>(p, tmW, tmA, g, config_id, stream);
+  switch (p.persist_rows) {
+    case 224: return run_f8_persist_rw<224>(p, tmW, tmA, g, config_id, stream);
+    case 192: return run_f8_persist_rw<192>(p, tmW, tmA, g, config_id, stream);
+    case 160: return run_f8_persist_rw<160>(p, tmW, tmA, g, config_id, stream);
+    default: return run_f8_persist_rw<256>(p, tmW, tmA, g, config_id, stream);
+  }
 }
 
 template <int MT>
@@ -492,8 +504,8 @@ int check_config_bits(int fmt, int variant, int config_id) {
   if (config_id < 0 ||
       (config_id & ~(QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_MMA_NARROW | QG_CONFIG_FUSED_QUANT |
                      QG_CONFIG_PERSIST | QG_CONFIG_MMA_DP4A_MASK | QG_CONFIG_MMA_S8 | QG_CONFIG_PAIR_MMA |
-                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 | QG_CONFIG_BLOCK_PROMO8 | QG_CONFIG_RING_MASK |
-                     QG_CONFIG_PREFETCH_MASK)) ||
+                     QG_CONFIG_I8_PREWIDEN | QG_CONFIG_I8_CONV16 | QG_CONFIG_BLOCK_PROMO8 |
+                     QG_CONFIG_PERSIST_ROWS_MASK | QG_CONFIG_RING_MASK | QG_CONFIG_PREFETCH_MASK)) ||
       (config_id & QG_CONFIG_RING_MASK) > kMaxStages ||
       ((config_id & QG_CONFIG_PREFETCH_MASK) >> QG_CONFIG_PREFETCH_SHIFT) > QG_CONFIG_MAX_PREFETCH)
     return fail(QG_ERR_INVALID_ARG, "config_id %d: unknown bits, ring depth above %d or prefetch distance above %d",
@@ -526,6 +538,8 @@ int check_config_bits(int fmt, int variant, int config_id) {
                 "QG_CONFIG_BLOCK_PROMO8 is for Block_FP8 with QG_SWAPAB / QG_SWAPAB_SPLITK, two-kernel form");
   if ((config_id & QG_CONFIG_PAIR_MMA) && !(config_id & QG_CONFIG_PERSIST))
     return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PAIR_MMA is a form of the QG_CONFIG_PERSIST kernel");
+  if ((config_id & QG_CONFIG_PERSIST_ROWS_MASK) && !(config_id & QG_CONFIG_PERSIST))
+    return fail(QG_ERR_INVALID_ARG, "QG_CONFIG_PERSIST_ROWS_MASK is a field of the QG_CONFIG_PERSIST kernel");
   if ((config_id & QG_CONFIG_PERSIST) &&
       (fmt != QG_FP8_DYNAMIC || variant != QG_STANDARD ||
        (config_id & (QG_CONFIG_WIDE | QG_CONFIG_MMA_SYNC | QG_CONFIG_FUSED_QUANT | QG_CONFIG_MMA_DP4A_MASK |
@@ -691,7 +705,9 @@ int gemm_entry(int fmt, int64_t M, int64_t N, int64_t K, const void* A_q_dev, co
     if (!aligned(workspace_dev, 256)) return fail(QG_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   }
   CUtensorMap tmW, tmA;
-  rc = make_map(&tmW, W_q_dev, static_cast<int64_t>(p.groups) * N, K, K, wide ? 256u : 128u);
+  // the persistent kernel loads weight tiles in halves of persist_rows / 2 rows
+  const uint32_t w_box = p.persist ? static_cast<uint32_t>(p.persist_rows / 2) : (wide ? 256u : 128u);
+  rc = make_map(&tmW, W_q_dev, static_cast<int64_t>(p.groups) * N, K, K, w_box);
   if (rc != QG_OK) return rc;
   if (fused) {
     tmA = tmW;  // unused: the kernel reads the bf16 activations directly

@@ -41,12 +41,15 @@ QG_CONFIG_PAIR_MMA = 1 << 21
 QG_CONFIG_I8_PREWIDEN = 1 << 22
 QG_CONFIG_I8_CONV16 = 1 << 23
 QG_CONFIG_BLOCK_PROMO8 = 1 << 24
+QG_CONFIG_PERSIST_ROWS_SHIFT = 25
+QG_CONFIG_PERSIST_ROWS_MASK = 3 << 25
+PERSIST_ROWS = (256, 224, 192, 160)
 
 
 def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False, mma_sync: bool = False,
               narrow: bool = False, fused: bool = False, persist: bool = False, dp4a_rows16: int = 0,
               s8: bool = False, pair_mma: bool = False, prewiden: bool = False, conv16: bool = False,
-              promo8: bool = False) -> int:
+              promo8: bool = False, persist_rows: int = 256) -> int:
     """config_id of a ring depth (0 = default), an L2 prefetch distance,
     (FP8_Dynamic Standard / Split-K) 256-row weight tiles, (W8A8_INT8
     Swap-AB) the mma.sync kernel with eight narrow MMA warps if `narrow`,
@@ -59,7 +62,13 @@ def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False, mma_sync: bo
     once per launch into the workspace (QG_CONFIG_I8_PREWIDEN); `conv16`:
     its tcgen05 kernel with sixteen converter warps, one CTA per SM
     (QG_CONFIG_I8_CONV16); `promo8`: Block_FP8 Swap-AB with eight promotion
-    warps (QG_CONFIG_BLOCK_PROMO8)."""
+    warps (QG_CONFIG_BLOCK_PROMO8); `persist_rows`: the persistent kernel's
+    weight rows per tile, one of 256, 224, 192, 160 (not 256 implies
+    persist)."""
+    if persist_rows not in PERSIST_ROWS:
+        raise ValueError(f"persist_rows must be one of {PERSIST_ROWS}")
+    rows_code = PERSIST_ROWS.index(persist_rows)
+    persist = persist or rows_code > 0
     narrow = narrow or dp4a_rows16 > 0
     return (ring | (prefetch << QG_CONFIG_PREFETCH_SHIFT) | (QG_CONFIG_WIDE if wide else 0)
             | (QG_CONFIG_MMA_SYNC if mma_sync or narrow or s8 else 0) | (QG_CONFIG_MMA_NARROW if narrow else 0)
@@ -67,6 +76,7 @@ def config_id(ring: int = 0, prefetch: int = 0, wide: bool = False, mma_sync: bo
             | (QG_CONFIG_FUSED_QUANT if fused else 0) | (QG_CONFIG_PERSIST if persist or pair_mma else 0)
             | (QG_CONFIG_PAIR_MMA if pair_mma else 0) | (QG_CONFIG_I8_PREWIDEN if prewiden else 0)
             | (QG_CONFIG_I8_CONV16 if conv16 else 0) | (QG_CONFIG_BLOCK_PROMO8 if promo8 else 0)
+            | (rows_code << QG_CONFIG_PERSIST_ROWS_SHIFT)
             | (dp4a_rows16 << QG_CONFIG_MMA_DP4A_SHIFT))
 
 EXPORTS = ("qg_quant_act", "qg_quant_weight", "qg_pack_weight", "qg_workspace_bytes", "qg_workspace_bytes_config",

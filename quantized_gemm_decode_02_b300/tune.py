@@ -147,6 +147,10 @@ def candidates(fmt: str, M: int, N: int, K: int, sms: int):
             for pair in (False, True):
                 for ring in (0, 3, 4):
                     out.append((q.QG_STANDARD, 1, q.config_id(ring, 0, persist=True, pair_mma=pair)))
+            # narrower weight tiles, so that the tile count fills the last
+            # round of the resident pairs better (cta_group::2 form)
+            for rows in q.PERSIST_ROWS[1:]:
+                out.append((q.QG_STANDARD, 1, q.config_id(0, 0, pair_mma=True, persist_rows=rows)))
             # 256-row weight tiles: ring of 2 (two CTAs per SM) or 4 (one)
             wide_tiles = -(-N // 256) * -(-M // 128)
             for cfg in (q.config_id(0, 0, True), q.config_id(4, 0, True)):

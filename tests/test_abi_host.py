@@ -255,7 +255,8 @@ def test_check_config_returns_the_gemm_status(q):
              dict(fmt=0, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8),                           # promo8: Block_FP8 only
              dict(fmt=1, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8),
              dict(fmt=2, M=300, variant=0, cfg=q.QG_CONFIG_BLOCK_PROMO8),               # Swap-AB only
-             dict(fmt=2, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8 | q.QG_CONFIG_FUSED_QUANT)]
+             dict(fmt=2, M=32, cfg=q.QG_CONFIG_BLOCK_PROMO8 | q.QG_CONFIG_FUSED_QUANT),
+             dict(fmt=0, M=300, variant=0, cfg=1 << q.QG_CONFIG_PERSIST_ROWS_SHIFT)]  # rows without persist
     for c in cases:
         fmt, M, K = c.get("fmt", 0), c.get("M", 4), c.get("K", 256)
         v, s, cfg = c.get("variant", 2), c.get("split", 1), c.get("cfg", 0)
@@ -274,6 +275,11 @@ def test_check_config_returns_the_gemm_status(q):
     assert q.qg_check_config(1, 16, 4096, 4096, q.QG_SWAPAB_SPLITK, 4, q.config_id(conv16=True)) == q.QG_OK
     assert q.qg_check_config(1, 300, 4096, 4096, q.QG_SWAPAB, 1, q.config_id(prewiden=True, conv16=True)) == q.QG_OK
     assert q.qg_check_config(2, 512, 4096, 4096, q.QG_SWAPAB_SPLITK, 2, q.config_id(6, promo8=True)) == q.QG_OK
+    for rows in (224, 192, 160):
+        assert q.qg_check_config(0, 512, 24576, 4096, q.QG_STANDARD, 1,
+                                 q.config_id(pair_mma=True, persist_rows=rows)) == q.QG_OK
+    with pytest.raises(ValueError):
+        q.config_id(persist_rows=200)
     assert q.qg_check_config(2, 32, 4096, 12288, q.QG_SWAPAB_SPLITK, 96, q.config_id(12, 64)) == q.QG_OK
     assert q.qg_check_config(0, 0, 256, 256, 2, 1, 0) == q.QG_ERR_INVALID_ARG   # a configuration has M >= 1
 

@@ -530,6 +530,18 @@ def test_fp8_persistent_pairs(orc, q, gc, M, N, K, pair_mma):
 
 
 @pytest.mark.parametrize("pair_mma", [False, True])
+@pytest.mark.parametrize("rows", [224, 192, 160])
+@pytest.mark.parametrize("M,N,K", [(100, 424, 656), (513, 1000, 1024), (300, 4096, 512)])
+def test_fp8_persistent_narrow_weight_tiles(orc, q, gc, M, N, K, rows, pair_mma):
+    # weight tiles of 224 / 192 / 160 rows (QG_CONFIG_PERSIST_ROWS_MASK):
+    # TMA boxes of rows/2, MMA N = rows, the last tile ragged (424, 1000 and
+    # 4096 are not multiples of any of them; for 4096 the last tile's second
+    # half lies wholly past N), ragged K and token pairs
+    gc.run_case(orc, "FP8_Dynamic", M, N, K, ST, 1, seed=860 + M + rows, outliers=True,
+                config_id=q.config_id(persist=True, pair_mma=pair_mma, persist_rows=rows))
+
+
+@pytest.mark.parametrize("pair_mma", [False, True])
 @pytest.mark.parametrize("ring", [2, 3])
 def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring, pair_mma):
     # 3 x 80 = 240 pair tiles: every cluster takes several tiles, so both
