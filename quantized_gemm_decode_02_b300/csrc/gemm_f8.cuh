@@ -389,12 +389,13 @@ __device__ __forceinline__ void block_fused_quantize(const GemmArgs& g, Ctrl* ct
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float sc = scale_from_amax(mx, 448.0f);
       if (piece < MPAD * 4) {
-        const Divider dv(sc);
+        float qv[32];
+        Divider(sc).divide(x, qv);
         uint32_t w[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          w[j] = static_cast<uint32_t>(e4m3x2(dv(x[4 * j]), dv(x[4 * j + 1]))) |
-                 (static_cast<uint32_t>(e4m3x2(dv(x[4 * j + 2]), dv(x[4 * j + 3]))) << 16);
+          w[j] = static_cast<uint32_t>(e4m3x2(qv[4 * j], qv[4 * j + 1])) |
+                 (static_cast<uint32_t>(e4m3x2(qv[4 * j + 2], qv[4 * j + 3])) << 16);
         *reinterpret_cast<uint4*>(at + sw128_chunk(r, 2 * p)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(at + sw128_chunk(r, 2 * p + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
         if (p == 0) ctl->amax_s[slot * 64 + r] = r < Mb ? sc : 0.0f;
@@ -407,9 +408,11 @@ __device__ __forceinline__ void block_fused_quantize(const GemmArgs& g, Ctrl* ct
       }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile is read by the MMA (async proxy)
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->full_a[s]);
-    mbar_arrive(&ctl->sfull[slot]);  // every lane: its scales are written (release)
+    __syncwarp();  // every lane's codes and scales are written
+    if (lane == 0) {
+      mbar_arrive(&ctl->full_a[s]);
+      mbar_arrive(&ctl->sfull[slot]);
+    }
 #pragma unroll
     for (int q = 0; q < kPP; ++q)
 #pragma unroll
@@ -485,7 +488,7 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
     mbar_init(&ctl->acc_full, 1);
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], kEpi);
+      mbar_init(&ctl->tempty[b], kEpi / 32);  // one arrive per promotion warp
     }
     mbar_init(&ctl->never, 1);
     mbar_init(&ctl->recv_bar, 1);
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
     if (FUSED)
       for (int i = 0; i < stages; ++i) mbar_init(&ctl->full_a[i], 4);
     if (QWARPS)
-      for (int j = 0; j < kSaRing; ++j) mbar_init(&ctl->sfull[j], 128);
+      for (int j = 0; j < kSaRing; ++j) mbar_init(&ctl->sfull[j], 4);  // one arrive per quantizer warp
     ctl->last_flag = 0;
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -671,11 +674,12 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
             if (r < Mb) {
               float x[32];
               unpack_act32(cur[q], x);
-              const Divider dv(ctl->sa_s[r]);
+              float qv[32];
+              Divider(ctl->sa_s[r]).divide(x, qv);
 #pragma unroll
               for (int j = 0; j < 8; ++j)
-                w[j] = static_cast<uint32_t>(e4m3x2(dv(x[4 * j]), dv(x[4 * j + 1]))) |
-                       (static_cast<uint32_t>(e4m3x2(dv(x[4 * j + 2]), dv(x[4 * j + 3]))) << 16);
+                w[j] = static_cast<uint32_t>(e4m3x2(qv[4 * j], qv[4 * j + 1])) |
+                       (static_cast<uint32_t>(e4m3x2(qv[4 * j + 2], qv[4 * j + 3])) << 16);
               if (write_codes) {
                 uint8_t* dst = g.a_q_out + static_cast<int64_t>(m_base + r) * g.K + kt0 + 32 * p;
 #pragma unroll
@@ -806,7 +810,8 @@ __global__ void __launch_bounds__(swap_threads(FMT, FUSED, PW),
           tmem_ld_cols(tmem + lane_base + static_cast<uint32_t>(buf * MPAD + t0), v);
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&ctl->tempty[buf]);
+          __syncwarp();  // the warp's TMEM reads of the buffer are done
+          if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
           if constexpr (!FUSED) {
             const float* coefs =
                 (staged ? ctl->amax_s + i * MPAD
@@ -976,7 +981,7 @@ __global__ void __launch_bounds__(std_threads(FMT), 1)
     mbar_init(&ctl->acc_full, 1);
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], kEpi);
+      mbar_init(&ctl->tempty[b], kEpi / 32);  // one arrive per promotion warp
     }
     mbar_init(&ctl->never, 1);
     ctl->last_flag = 0;
@@ -1124,7 +1129,8 @@ __global__ void __launch_bounds__(std_threads(FMT), 1)
           tmem_ld_wait();
           if (h + 32 >= kCols) {
             tc_fence_before();
-            mbar_arrive(&ctl->tempty[buf]);
+            __syncwarp();  // the warp's TMEM reads of the buffer are done
+            if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
           }
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {

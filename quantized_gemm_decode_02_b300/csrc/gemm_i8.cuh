@@ -373,12 +373,13 @@ __global__ void __launch_bounds__(i8_threads(PREW, CW), i8_one_per_sm(MPAD, PREW
           if (r < Mb) {
             float x[32];
             load_act32(g, m_base + r, kt0 + 32 * p, x);
-            const Divider dv(ctl->sa_s[r]);
+            float qv[32];
+            Divider(ctl->sa_s[r]).divide(x, qv);
             uint32_t codes[8];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int q0 = max(-127, min(127, __float2int_rn(dv(x[2 * j]))));
-              const int q1 = max(-127, min(127, __float2int_rn(dv(x[2 * j + 1]))));
+              const int q0 = max(-127, min(127, __float2int_rn(qv[2 * j])));
+              const int q1 = max(-127, min(127, __float2int_rn(qv[2 * j + 1])));
               __half2 hh = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
               o[j] = *reinterpret_cast<uint32_t*>(&hh);
               const uint32_t pair = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8);

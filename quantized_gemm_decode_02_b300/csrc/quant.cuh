@@ -17,8 +17,21 @@ namespace qg {
 
 enum : int { kFmtFP8 = 0, kFmtINT8 = 1, kFmtBlock = 2 };
 
+// s = amax / qmax, correctly rounded, for the two format maxima (448 for
+// E4M3, 127 for INT8), by Markstein's method (see Divider below) with the
+// correctly rounded reciprocals of the constants written out: RN(1/448) has
+// the bits 0x3b124925 and RN(1/127) 0x3c010204.  The quotient of a positive
+// amax >= 2^-100 is normal, so two residual steps return it correctly
+// rounded; smaller amax (and any other qmax) divide with __fdiv_rn.  A
+// per-group or per-row scale costs a few fma, not a division routine.
 __device__ __forceinline__ float scale_from_amax(float amax, float qmax) {
-  return amax > 0.0f ? __fdiv_rn(amax, qmax) : 1.0f;
+  if (!(amax > 0.0f)) return 1.0f;
+  const bool known = qmax == 448.0f || qmax == 127.0f;
+  if (!known || amax < 0x1p-100f) return __fdiv_rn(amax, qmax);
+  const float r = __uint_as_float(qmax == 448.0f ? 0x3b124925u : 0x3c010204u);
+  const float q1 = __fmul_rn(amax, r);
+  const float q2 = __fmaf_rn(__fmaf_rn(-q1, qmax, amax), r, q1);
+  return __fmaf_rn(__fmaf_rn(-q2, qmax, amax), r, q2);
 }
 
 // Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448);
@@ -87,14 +100,28 @@ struct Divider {
     r = __frcp_rn(scale);
     exact = scale >= 0x1p-100f && scale <= 0x1p100f;
   }
-  __device__ __forceinline__ float operator()(float x) const {
-    if (!exact) return __fdiv_rn(x, s);
+  // x / s when `exact` (no branch, no division routine)
+  __device__ __forceinline__ float fast(float x) const {
     const float q1 = __fmul_rn(x, r);
     const float q2 = __fmaf_rn(__fmaf_rn(-q1, s, x), r, q1);
     const float q3 = __fmaf_rn(__fmaf_rn(-q2, s, x), r, q2);
     // the residual steps turn -0 into +0; the quotient of +-0 is +-0 (E4M3
     // keeps the sign of zero)
     return x == 0.0f ? x : q3;
+  }
+  __device__ __forceinline__ float operator()(float x) const { return exact ? fast(x) : __fdiv_rn(x, s); }
+  // q[i] = x[i] / s for a whole piece with one branch: a branch per value,
+  // each with a division routine on its other side, made the quantizers
+  // several times slower than the arithmetic itself
+  template <int N>
+  __device__ __forceinline__ void divide(const float (&x)[N], float (&q)[N]) const {
+    if (exact) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) q[i] = fast(x[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; ++i) q[i] = __fdiv_rn(x[i], s);
+    }
   }
 };
 
@@ -195,17 +222,19 @@ __global__ void __launch_bounds__(512) quant_rows_reg_kernel(const __nv_bfloat16
     const int k = (c * kThreads + static_cast<int>(threadIdx.x)) * 8;
     if (k >= K) break;
     uint32_t w[2];
+    float qv[8];
+    dv.divide(v[c], qv);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if constexpr (OUT == kFmtFP8) {
-        const uint16_t lo = e4m3x2(dv(v[c][4 * h + 0]), dv(v[c][4 * h + 1]));
-        const uint16_t hi = e4m3x2(dv(v[c][4 * h + 2]), dv(v[c][4 * h + 3]));
+        const uint16_t lo = e4m3x2(qv[4 * h + 0], qv[4 * h + 1]);
+        const uint16_t hi = e4m3x2(qv[4 * h + 2], qv[4 * h + 3]);
         w[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
       } else {
-        w[h] = static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 0]))) |
-               (static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 1]))) << 8) |
-               (static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 2]))) << 16) |
-               (static_cast<uint32_t>(int8_sym(dv(v[c][4 * h + 3]))) << 24);
+        w[h] = static_cast<uint32_t>(int8_sym(qv[4 * h + 0])) |
+               (static_cast<uint32_t>(int8_sym(qv[4 * h + 1])) << 8) |
+               (static_cast<uint32_t>(int8_sym(qv[4 * h + 2])) << 16) |
+               (static_cast<uint32_t>(int8_sym(qv[4 * h + 3])) << 24);
       }
     }
     *reinterpret_cast<uint2*>(q + k) = make_uint2(w[0], w[1]);
@@ -241,8 +270,10 @@ __global__ void __launch_bounds__(WARPS * 32) quant_groups_kernel(const __nv_bfl
     amax = warp_max(amax);
     const float s = scale_from_amax(amax, 448.0f);
     if (lane == 0) S[r * groups + g] = s;
-    uint16_t lo = e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
-    uint16_t hi = e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
+    float qv[4];
+    Divider(s).divide(v, qv);
+    uint16_t lo = e4m3x2(qv[0], qv[1]);
+    uint16_t hi = e4m3x2(qv[2], qv[3]);
     *reinterpret_cast<uint32_t*>(Q + r * static_cast<int64_t>(K) + g * 128 + lane * 4) =
         static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }

@@ -309,6 +309,37 @@ def test_bounded_wait_reports_timeout_and_context_survives(orc, gc, q, fmt, mma_
     gc.check_gemm(orc, fmt, oAq, osa, oWq, osw, Y, dbg)
 
 
+@pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])
+def test_scales_exact_across_binades(orc, gc, q, fmt):
+    # every scale amax / qmax (448 or 127; Markstein's method with the
+    # constant's reciprocal, __fdiv_rn below amax = 2^-100) equals the oracle's
+    # IEEE quotient, and so do the codes: fp32 weight rows / 128x128 blocks
+    # (full 24-bit mantissas) and bf16 activation rows / 1x128 groups whose
+    # maxima span 2^-126 .. 2^125, across the 2^-100 threshold
+    import seeded_inputs as si
+    rng = np.random.default_rng(11)
+    R, K = 512, 256
+    exps = np.concatenate([rng.integers(-126, 126, R - 16), np.arange(-104, -96, 0.5)])
+    amax = (1.0 + rng.random(R)) * np.exp2(exps)
+    amax = amax.astype(np.float32)
+    W = (rng.uniform(-1.0, 1.0, (R, K)) * amax[:, None]).astype(np.float32)
+    W[np.arange(R), rng.integers(0, K, R)] = amax * np.where(rng.random(R) < 0.5, -1.0, 1.0).astype(np.float32)
+    if fmt == "Block_FP8":
+        # one binade per 128x128 block: scale whole blocks by their own factor
+        blk = np.exp2(rng.integers(-120, 120, (R // 128, K // 128))).astype(np.float32)
+        W = (W / amax[:, None] * np.repeat(np.repeat(blk, 128, 0), 128, 1)).astype(np.float32)
+    Wd = torch.from_numpy(W).to(gc.DEV)
+    Wq, sw = gc.quant_weight_gpu(fmt, Wd)
+    # activations: bf16 rows (groups) with maxima over the bf16 exponent range
+    A32 = (rng.uniform(-1.0, 1.0, (R, K)) * amax[:, None]).astype(np.float32)
+    A32[np.arange(R), rng.integers(0, K, R)] = amax
+    A = torch.from_numpy(A32).to(torch.bfloat16)
+    Aq, sa = gc.quant_act_gpu(fmt, A.to(gc.DEV))
+    torch.cuda.synchronize()
+    assert q.qg_device_error() == 0
+    gc.check_quant(orc, fmt, A, W, Aq, sa, Wq, sw)
+
+
 def test_quant_act_row_stride(orc, gc, q):
     import seeded_inputs as si
     M, K, lda = 5, 512, 640
