@@ -8,8 +8,9 @@ weights on the CPU (bit-exact codes and scales), recomputes the activations'
 quantization (bit-exact) and the exact GEMM: INT8 accumulators bit-exact and
 Y within one bf16 ulp; FP8 formats within 8e-3 * s_a*s_w*sum|a_q*w_q|.
 
-Also covered: the M = 64..512 regime (Standard variant for the FP8 formats,
-Swap-AB in blocks of 64 tokens for INT8), with sampled rows."""
+Also covered: the M = 64..512 regime of every Qwen3-8B layer in the tuned
+table's configuration, and the Standard variant with and without Split-K for
+the E4M3 formats, with sampled rows."""
 from __future__ import annotations
 
 import os
@@ -102,6 +103,20 @@ def test_large_token_counts(orc, gc, q, fmt, M):
     if fmt != "W8A8_INT8":
         for v, sp in ((q.QG_STANDARD, 1), (q.QG_SPLITK, 3)):
             run_sampled(orc, gc, q, fmt, M, N, K, v, sp, 0, seed=2100 + M, outliers=True)
+
+
+LARGE_M = [(f, layer, M) for f in ("FP8_Dynamic", "W8A8_INT8", "Block_FP8") for layer in ("qkv", "o", "gate_up", "down")
+           for M in (64, 128, 256, 384, 512) if not (layer == "o" and M in (64, 256, 512))]
+
+
+@pytest.mark.parametrize("fmt,layer,M", LARGE_M)
+def test_large_m_table_configs(orc, gc, q, fmt, layer, M):
+    # every Qwen3-8B layer at M = 64..512 in the configuration the tuned
+    # table selects (persistent FP8 tiles of 192..256 weight rows, CTA pairs,
+    # Block_FP8 promotion with eight warps, Swap-AB token blocks for INT8)
+    K, N = si.QWEN3_LINEARS["Qwen3-8B"][layer]
+    variant, split, cfg = q.qg_select(fmt, M, N, K)
+    run_sampled(orc, gc, q, fmt, M, N, K, variant, split, cfg, seed=4000 + M, outliers=(fmt == "Block_FP8"))
 
 
 @pytest.mark.parametrize("fmt", ["FP8_Dynamic", "W8A8_INT8", "Block_FP8"])

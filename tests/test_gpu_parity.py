@@ -596,8 +596,9 @@ def test_fp8_persistent_many_tiles_per_pair(orc, q, gc, ring, pair_mma):
     assert not torch.isnan(Y.float()).any()
 
 
+@pytest.mark.parametrize("rows", [256, 160])
 @pytest.mark.parametrize("pair_mma", [False, True])
-def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc, pair_mma):
+def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc, pair_mma, rows):
     import seeded_inputs as si
     M, N, K = 300, 1024, 1024
     A = si.activations(M, K, seed=830)
@@ -606,7 +607,7 @@ def test_fp8_persistent_bounded_wait_and_recovery(orc, q, gc, pair_mma):
     Aq, sa = gc.quant_act_gpu("FP8_Dynamic", A.to(gc.DEV))
     torch.cuda.synchronize()
     assert q.qg_device_error() == 0
-    cfg = q.config_id(persist=True, pair_mma=pair_mma)
+    cfg = q.config_id(persist=True, pair_mma=pair_mma, persist_rows=rows)
     q.qg_set_wait_limit_ns(2_000_000)
     q.qg_set_force_timeout(True)
     try:
